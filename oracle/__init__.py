@@ -1,0 +1,202 @@
+"""CPU oracle for the W8A8 quantized linear layer -- TEST INFRASTRUCTURE.
+
+Plain, slow, obviously correct: a C file (q8_oracle.c, built with gcc
+-O2 -ffp-contract=off) wrapped with ctypes over numpy arrays. It shares no
+code with the CUDA library and never imports it. Only tests/, the smoke check
+and bench.py's CPU-baseline leg may call it; the product path never does.
+
+Every function follows a passage of the pages (cited in q8_oracle.c):
+  quantize_sym / quantize_asym   "100 Days of GPU, Day 98" (What a scale
+                                 actually promises); "Write Int8 Quantized
+                                 Kernel" step 1; "Activation Quantization
+                                 Architecture" (The quantizer itself; numpy
+                                 reference; Fusion pseudocode for the guard)
+  colsum                         Day 98 (zero-point paragraph after the kernel)
+  gemm_acc                       Day 98 (accumulate loop); "Activation
+                                 Quantization Architecture" (The integer GEMM)
+  linear_codes / linear_codes_at Day 98 (epilogue listing)
+All of them are pinned by tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libq8oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, BAD_ARG, INT32_OVERFLOW = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile q8_oracle.c with gcc (OpenMP if available). Returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC",
+            "-shared", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.q8o_quantize_sym.argtypes = [p, i64, i64, i32, p, p]
+        lib.q8o_quantize_sym.restype = i32
+        lib.q8o_quantize_asym.argtypes = [p, i64, i64, i32, p, p, p]
+        lib.q8o_quantize_asym.restype = i32
+        lib.q8o_colsum.argtypes = [p, i64, i64, p]
+        lib.q8o_colsum.restype = None
+        lib.q8o_dot.argtypes = [p, p, i64]
+        lib.q8o_dot.restype = i64
+        lib.q8o_gemm_acc.argtypes = [p, p, i64, i64, i64, p, i32]
+        lib.q8o_gemm_acc.restype = None
+        lib.q8o_linear_codes.argtypes = [p, p, p, i32, p, p, i32, i64, i64, i64, p, i32]
+        lib.q8o_linear_codes.restype = i32
+        lib.q8o_linear_codes_at.argtypes = [p, p, p, i32, p, p, i32, i64, p, p, i64, p, p]
+        lib.q8o_linear_codes_at.restype = i32
+        lib.q8o_sym_scale.argtypes = [ctypes.c_float]
+        lib.q8o_sym_scale.restype = ctypes.c_float
+        lib.q8o_openmp_max_threads.argtypes = []
+        lib.q8o_openmp_max_threads.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return int(_load().q8o_openmp_max_threads())
+
+
+def quantize_sym(x: np.ndarray, per_row: bool):
+    """Symmetric int8 codes of a 2-D fp32 array; returns (q int8, s fp32[rows or 1])."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.int8)
+    s = np.empty(rows if per_row else 1, np.float32)
+    st = _load().q8o_quantize_sym(_ptr(x), rows, cols, int(per_row), _ptr(q), _ptr(s))
+    assert st == OK
+    return q, s
+
+
+def quantize_asym(x: np.ndarray, per_row: bool):
+    """Asymmetric int8 codes; returns (q int8, s fp32, z int32) with s, z [rows or 1]."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.int8)
+    n = rows if per_row else 1
+    s = np.empty(n, np.float32)
+    z = np.empty(n, np.int32)
+    st = _load().q8o_quantize_asym(_ptr(x), rows, cols, int(per_row), _ptr(q), _ptr(s), _ptr(z))
+    assert st == OK
+    return q, s, z
+
+
+def sym_scale(amax: float) -> np.float32:
+    return np.float32(_load().q8o_sym_scale(ctypes.c_float(amax)))
+
+
+def colsum(qw: np.ndarray) -> np.ndarray:
+    """int64 column sums of a K-major W[N, K] of codes."""
+    qw = _c(qw, np.int8)
+    N, K = qw.shape
+    out = np.empty(N, np.int64)
+    _load().q8o_colsum(_ptr(qw), N, K, _ptr(out))
+    return out
+
+
+def dot(a: np.ndarray, b: np.ndarray) -> int:
+    a = _c(a, np.int8)
+    b = _c(b, np.int8)
+    assert a.shape == b.shape and a.ndim == 1
+    return int(_load().q8o_dot(_ptr(a), _ptr(b), a.shape[0]))
+
+
+def gemm_acc(qa: np.ndarray, qw: np.ndarray, threads: int = 1) -> np.ndarray:
+    """int64 acc[M, N] = qa[M, K] . qw[N, K]^T."""
+    qa = _c(qa, np.int8)
+    qw = _c(qw, np.int8)
+    M, K = qa.shape
+    N, K2 = qw.shape
+    assert K == K2
+    acc = np.empty((M, N), np.int64)
+    _load().q8o_gemm_acc(_ptr(qa), _ptr(qw), M, N, K, _ptr(acc), threads)
+    return acc
+
+
+def linear_codes(qa, sa, za, qw, sw, a_per_row: bool, w_per_row: bool, threads: int = 1):
+    """fp32 y[M, N] from codes and scales; returns (y, status)."""
+    qa = _c(qa, np.int8)
+    qw = _c(qw, np.int8)
+    sa = _c(sa, np.float32)
+    sw = _c(sw, np.float32)
+    za = None if za is None else _c(za, np.int32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    y = np.empty((M, N), np.float32)
+    st = _load().q8o_linear_codes(_ptr(qa), _ptr(sa), _ptr(za), int(a_per_row),
+                                  _ptr(qw), _ptr(sw), int(w_per_row), M, N, K, _ptr(y), threads)
+    return y, st
+
+
+def linear_codes_at(qa, sa, za, qw, sw, ms, ns, a_per_row: bool, w_per_row: bool):
+    """y and int64 acc at the (ms[i], ns[i]) pairs only; returns (y, acc, status)."""
+    qa = _c(qa, np.int8)
+    qw = _c(qw, np.int8)
+    sa = _c(sa, np.float32)
+    sw = _c(sw, np.float32)
+    za = None if za is None else _c(za, np.int32)
+    ms = _c(ms, np.int64)
+    ns = _c(ns, np.int64)
+    K = qa.shape[1]
+    y = np.empty(ms.size, np.float32)
+    acc = np.empty(ms.size, np.int64)
+    st = _load().q8o_linear_codes_at(_ptr(qa), _ptr(sa), _ptr(za), int(a_per_row), _ptr(qw), _ptr(sw),
+                                     int(w_per_row), K, _ptr(ms), _ptr(ns), ms.size, _ptr(y), _ptr(acc))
+    return y, acc, st
+
+
+def linear(a: np.ndarray, w: np.ndarray, act_per_row: bool, act_symmetric: bool,
+           w_per_row: bool, threads: int = 1):
+    """Whole layer from fp32 A[M, K] and W[N, K]: quantize both, integer GEMM, epilogue.
+
+    Returns a dict with qa, sa, za (None if symmetric), qw, sw, colsum, y, status.
+    """
+    if act_symmetric:
+        qa, sa = quantize_sym(a, act_per_row)
+        za = None
+    else:
+        qa, sa, za = quantize_asym(a, act_per_row)
+    qw, sw = quantize_sym(w, w_per_row)
+    M, N = a.shape[0], w.shape[0]
+    y = np.empty((M, N), np.float32)
+    lib = _load()
+    st = lib.q8o_linear_codes(_ptr(qa), _ptr(sa), _ptr(za), int(act_per_row), _ptr(qw), _ptr(sw),
+                              int(w_per_row), M, N, a.shape[1], _ptr(y), threads)
+    return dict(qa=qa, sa=sa, za=za, qw=qw, sw=sw, colsum=colsum(qw), y=y, status=st)

@@ -1,0 +1,252 @@
+/*
+ * q8_oracle.c -- plain, slow CPU oracle for the W8A8 quantized linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the independent reference that the
+ * CUDA path is checked against. It shares no code, header, table or helper
+ * with the library under int8_quantized_gemm_gb300/. Only tests/, the smoke
+ * check in __graft_entry__.py and the cpu_baseline leg of bench.py may load
+ * it. The product never calls it.
+ *
+ * Build: gcc -O2 -ffp-contract=off (no -ffast-math) so that every fp32
+ * operation below is one IEEE-754 single-precision operation, rounded to
+ * nearest-even, in exactly the order written. Integer dot products
+ * accumulate in int64, so they cannot overflow for any K this file accepts.
+ *
+ * Steps and the passages they follow:
+ *  - symmetric scale s = max|x| / 127, codes clamp(rint(x/s), -127, 127):
+ *      "100 Days of GPU, Day 98" (What a scale actually promises);
+ *      "Write Int8 Quantized Kernel" (Required reasoning process, step 1);
+ *      "Activation Quantization Architecture" (The quantizer itself, and the
+ *      numpy reference quantize_per_token / quantize_per_channel).
+ *    The zero-row guard is applied to amax before the divide, as in the fused
+ *    norm+quantize pseudocode of "Activation Quantization Architecture"
+ *    (Fusion): s = max(amax, 1e-8) / 127.
+ *  - asymmetric scale and zero point: Day 98 (z is the code that dequantizes
+ *    to zero) and "Write Int8 Quantized Kernel" step 1 (s = (max-min)/255,
+ *    z = round(-min/s)), stored in the int8 range [-128, 127]:
+ *      lo = min(min x, 0), hi = max(max x, 0), s = max(hi - lo, 1e-8) / 255,
+ *      z  = clamp(-128 - rint(lo / s), -128, 127),
+ *      q  = clamp(rint(x / s) + z, -128, 127).
+ *  - integer dot product acc[m][n] = sum_k qa[m][k] * qw[n][k] (Day 98, the
+ *    accumulate loop; "Activation Quantization Architecture", The integer
+ *    GEMM, written out), here in int64.
+ *  - column sums colsum[n] = sum_k qw[n][k] (Day 98, the zero-point paragraph
+ *    after the kernel listing).
+ *  - epilogue corr = acc - z * colsum, y = (float)corr * (s_a * s_w), the
+ *    multiply order of the Day 98 epilogue listing.
+ * rint() is round-half-to-even in the default rounding mode, matching np.rint
+ * in the numpy reference of "Activation Quantization Architecture".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#define Q8O_ZERO_GUARD 1e-8f
+
+/* Status codes of the oracle (not the library's). */
+enum { Q8O_OK = 0, Q8O_BAD_ARG = 1, Q8O_INT32_OVERFLOW = 2 };
+
+static float q8o_absf(float v) { return v < 0.0f ? -v : v; }
+
+static int q8o_clampi(long v, int lo, int hi) {
+    if (v < lo) return lo;
+    if (v > hi) return hi;
+    return (int)v;
+}
+
+/* amax over n values (exact: comparisons only). */
+static float q8o_amax(const float* x, int64_t n) {
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = q8o_absf(x[i]);
+        if (a > m) m = a;
+    }
+    return m;
+}
+
+float q8o_sym_scale(float amax) {
+    float g = amax > Q8O_ZERO_GUARD ? amax : Q8O_ZERO_GUARD;
+    return g / 127.0f;
+}
+
+int q8o_sym_code(float x, float s) {
+    float r = rintf(x / s);
+    return q8o_clampi((long)r, -127, 127);
+}
+
+/*
+ * Symmetric quantization of a rows x cols fp32 matrix (row-major).
+ * per_row != 0: one scale per row (per token for A, per output channel for a
+ * K-major W[N, K]); s has `rows` entries. per_row == 0: one scale for the
+ * whole tensor; s has one entry.
+ */
+int q8o_quantize_sym(const float* x, int64_t rows, int64_t cols, int per_row,
+                     int8_t* q, float* s) {
+    if (rows < 0 || cols < 0) return Q8O_BAD_ARG;
+    if (!per_row) {
+        float amax = q8o_amax(x, rows * cols);
+        float sc = q8o_sym_scale(amax);
+        s[0] = sc;
+        for (int64_t i = 0; i < rows * cols; ++i) q[i] = (int8_t)q8o_sym_code(x[i], sc);
+        return Q8O_OK;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * cols;
+        float sc = q8o_sym_scale(q8o_amax(xr, cols));
+        s[r] = sc;
+        for (int64_t c = 0; c < cols; ++c) q[r * cols + c] = (int8_t)q8o_sym_code(xr[c], sc);
+    }
+    return Q8O_OK;
+}
+
+/* Range of a set of values, widened to include 0 so that 0 has a code. */
+static void q8o_range0(const float* x, int64_t n, float* lo, float* hi) {
+    float a = 0.0f, b = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        if (x[i] < a) a = x[i];
+        if (x[i] > b) b = x[i];
+    }
+    *lo = a;
+    *hi = b;
+}
+
+void q8o_asym_params(float lo, float hi, float* s, int* z) {
+    float span = hi - lo;
+    float g = span > Q8O_ZERO_GUARD ? span : Q8O_ZERO_GUARD;
+    float sc = g / 255.0f;
+    float r = rintf(lo / sc);
+    *s = sc;
+    *z = q8o_clampi(-128L - (long)r, -128, 127);
+}
+
+int q8o_asym_code(float x, float s, int z) {
+    float r = rintf(x / s);
+    return q8o_clampi((long)r + (long)z, -128, 127);
+}
+
+/* Asymmetric quantization; s and z have `rows` entries (per_row) or one. */
+int q8o_quantize_asym(const float* x, int64_t rows, int64_t cols, int per_row,
+                      int8_t* q, float* s, int32_t* z) {
+    if (rows < 0 || cols < 0) return Q8O_BAD_ARG;
+    if (!per_row) {
+        float lo, hi, sc;
+        int zp;
+        q8o_range0(x, rows * cols, &lo, &hi);
+        q8o_asym_params(lo, hi, &sc, &zp);
+        s[0] = sc;
+        z[0] = zp;
+        for (int64_t i = 0; i < rows * cols; ++i) q[i] = (int8_t)q8o_asym_code(x[i], sc, zp);
+        return Q8O_OK;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * cols;
+        float lo, hi, sc;
+        int zp;
+        q8o_range0(xr, cols, &lo, &hi);
+        q8o_asym_params(lo, hi, &sc, &zp);
+        s[r] = sc;
+        z[r] = zp;
+        for (int64_t c = 0; c < cols; ++c) q[r * cols + c] = (int8_t)q8o_asym_code(xr[c], sc, zp);
+    }
+    return Q8O_OK;
+}
+
+/* colsum[n] = sum_k qw[n][k], in int64. */
+void q8o_colsum(const int8_t* qw, int64_t N, int64_t K, int64_t* colsum) {
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t t = 0;
+        for (int64_t k = 0; k < K; ++k) t += qw[n * K + k];
+        colsum[n] = t;
+    }
+}
+
+/* One integer dot product of length K, in int64. */
+int64_t q8o_dot(const int8_t* a, const int8_t* b, int64_t K) {
+    int64_t t = 0;
+    for (int64_t k = 0; k < K; ++k) t += (int64_t)a[k] * (int64_t)b[k];
+    return t;
+}
+
+/* acc[m][n] = sum_k qa[m][k] * qw[n][k] for all m, n (int64 out). */
+void q8o_gemm_acc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                  int64_t* acc, int threads) {
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) acc[m * N + n] = q8o_dot(qa + m * K, qw + n * K, K);
+}
+
+/*
+ * Epilogue for one element: corr = acc - z * colsum (int64), must fit int32;
+ * y = (float)corr * (s_a * s_w). Returns Q8O_INT32_OVERFLOW if corr or acc
+ * leaves the int32 range (the value is still written).
+ */
+int q8o_epilogue_one(int64_t acc, int32_t z, int64_t colsum, float sa, float sw, float* y) {
+    int64_t corr = acc - (int64_t)z * colsum;
+    float scale = sa * sw;
+    *y = (float)corr * scale;
+    if (acc > INT32_MAX || acc < INT32_MIN || corr > INT32_MAX || corr < INT32_MIN)
+        return Q8O_INT32_OVERFLOW;
+    return Q8O_OK;
+}
+
+/*
+ * Full linear layer on codes already quantized: y[m][n] for all m, n.
+ * sa has M entries if a_per_row else 1; za is NULL (symmetric) or has M / 1
+ * entries; sw has N entries if w_per_row else 1. Returns the worst status.
+ */
+int q8o_linear_codes(const int8_t* qa, const float* sa, const int32_t* za, int a_per_row,
+                     const int8_t* qw, const float* sw, int w_per_row,
+                     int64_t M, int64_t N, int64_t K, float* y, int threads) {
+    int status = Q8O_OK;
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1) reduction(max : status)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        float a_s = sa[a_per_row ? m : 0];
+        int32_t a_z = za ? za[a_per_row ? m : 0] : 0;
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t acc = q8o_dot(qa + m * K, qw + n * K, K);
+            int64_t cs = 0;
+            if (za) {
+                for (int64_t k = 0; k < K; ++k) cs += qw[n * K + k];
+            }
+            int st = q8o_epilogue_one(acc, a_z, cs, a_s, sw[w_per_row ? n : 0], &y[m * N + n]);
+            if (st > status) status = st;
+        }
+    }
+    return status;
+}
+
+/* y at a list of (m, n) pairs; same arguments as q8o_linear_codes. */
+int q8o_linear_codes_at(const int8_t* qa, const float* sa, const int32_t* za, int a_per_row,
+                        const int8_t* qw, const float* sw, int w_per_row, int64_t K,
+                        const int64_t* ms, const int64_t* ns, int64_t count,
+                        float* y, int64_t* acc_out) {
+    int status = Q8O_OK;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = ms[i], n = ns[i];
+        int64_t acc = q8o_dot(qa + m * K, qw + n * K, K);
+        int64_t cs = 0;
+        if (za) {
+            for (int64_t k = 0; k < K; ++k) cs += qw[n * K + k];
+        }
+        if (acc_out) acc_out[i] = acc;
+        int st = q8o_epilogue_one(acc, za ? za[a_per_row ? m : 0] : 0, cs,
+                                  sa[a_per_row ? m : 0], sw[w_per_row ? n : 0], &y[i]);
+        if (st > status) status = st;
+    }
+    return status;
+}
+
+int q8o_openmp_max_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
