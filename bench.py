@@ -1,0 +1,418 @@
+"""Benchmark of the W8A8 quantized linear layer on GB300.
+
+One step = the run-time hot path on one batch: dynamic per-token activation
+quantization (q8_quantize_act) followed by the INT8 GEMM with the fused
+dequantization epilogue (q8_gemm_dequant). Weight quantization and column sums
+are offline (done once, timed separately as `weight_prep_ms`).
+
+Metric: TOPS = 2*M*N*K / step time (integer multiply-adds counted as 2 ops,
+activation quantization included), on the large-prefill workload
+(A [8192, 16384] x W [8192, 16384]^T, per-token x per-channel, fp32 out).
+Inputs are synthetic and resident in HBM; L2 is flushed (256 MiB write)
+before every timed step; each step is timed with CUDA events on the launching
+stream, and the quantizer and the GEMM separately for the roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, int64 accumulation) on the
+host cores on a bounded row sample of the same workload. Under torchrun each
+rank runs an independent replica (the path shards by tokens with no
+exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = "prefill16k"
+DECODE = "decode"
+METRIC = "W8A8 GEMM TOPS (2MNK/s incl. act quantize)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ our arm
+
+def layer_inputs(name, device):
+    import torch
+    wl = workloads.WORKLOADS[name]
+    a = torch.from_numpy(workloads.make_activations(wl)).to(device)
+    w = torch.from_numpy(workloads.make_weights(wl)).to(device)
+    return wl, a, w
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import int8_quantized_gemm_gb300 as q8
+    from int8_quantized_gemm_gb300 import build
+
+    build.build()
+    q8.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream()
+    hbm_peak, tc_peak, peak_kind = peaks()
+
+    wl, a, w = layer_inputs(HEADLINE, device)
+    M, N, K = wl.M, wl.N, wl.K
+    apr, wpr, sym = wl.act_granularity == "row", wl.w_granularity == "row", wl.act_symmetric
+
+    # offline: weight quantization and column sums (timed once, not part of a step)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    qw, s_w = q8.q8_quantize_weight(w, per_row=wpr)
+    colsum = q8.q8_colsum(qw)
+    t1.record()
+    torch.cuda.synchronize()
+    weight_prep_ms = t0.elapsed_time(t1)
+    del w
+
+    qa = torch.empty((M, K), dtype=torch.int8, device=device)
+    s_a = torch.empty(M if apr else 1, dtype=torch.float32, device=device)
+    z_a = None if sym else torch.empty(M if apr else 1, dtype=torch.int32, device=device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    kernel = q8.q8_gemm_pick(M, N, K)
+
+    def step():
+        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches0 = q8.q8_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+            evs[i][1].record(stream)
+            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+            evs[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    barrier(world)
+    launches = q8.q8_launch_count() - launches0
+    assert q8.q8_device_error() == 0
+    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [q + g for q, g in zip(quant_ms, gemm_ms)]
+    ms_step = max_over_ranks(statistics.mean(step_ms), world)
+
+    ops = 2.0 * M * N * K
+    value = ops * world / (ms_step * 1e-3) / 1e12
+    gemm_avg = statistics.mean(gemm_ms)
+    quant_avg = statistics.mean(quant_ms)
+    gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
+    quant_bytes = M * K * 5 + 4 * M
+    quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
+    gemm_bytes = M * K + N * K + 4 * N + 4 * M + 4 * M * N
+
+    # ---- end to end through the public API: pinned host A in, y back to pinned host
+    a_host = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
+    a_host.copy_(a.cpu())
+    y_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(2):
+        a.copy_(a_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    ee0 = torch.cuda.Event(enable_timing=True)
+    ee1 = torch.cuda.Event(enable_timing=True)
+    ee0.record(stream)
+    for _ in range(e2e_steps):
+        a.copy_(a_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    ee1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(ee0.elapsed_time(ee1) / e2e_steps, world)
+    e2e_value = ops * world / (e2e_ms * 1e-3) / 1e12
+
+    # ---- decode-shaped workload (HBM-bound): same step, reported beside the headline
+    decode = measure_decode(q8, device, args, hbm_peak, flush)
+
+    cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": f"{HEADLINE}: A fp32 [{M},{K}] per-token sym x W int8 [{N},{K}] per-channel"
+                                   f" sym -> y fp32 [{M},{N}]",
+                       "M": M, "N": N, "K": K, "gemm_kernel": kernel, "l2": "flushed before every step (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "kernel": f"gemm_{kernel}", "achieved": round(gemm_tops, 1),
+                         "peak": tc_peak, "unit": "TFLOP/s", "frac": round(gemm_tops / tc_peak, 4),
+                         "peak_source": f"{peak_kind} bf16 dense burst (the GEMM runs tcgen05 kind::f16; fp16 = bf16 rate)",
+                         "traffic": None,
+                         "algorithmic_bytes_per_launch": gemm_bytes, "ms_per_launch": round(gemm_avg, 4)},
+            "quantizer": {"ms": round(quant_avg, 4), "GB/s": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
+                          "bytes": quant_bytes},
+            "decode": decode,
+            "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K * 4,
+                    "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": int(launches),
+            "weight_prep_ms": round(weight_prep_ms, 3),
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+            "wall_s_timed": round(wall1 - wall0, 3),
+        }
+        print(json.dumps(line))
+
+
+def measure_decode(q8, device, args, hbm_peak, flush):
+    import torch
+    wl, a, w = layer_inputs(DECODE, device)
+    M, N, K = wl.M, wl.N, wl.K
+    qw, s_w = q8.q8_quantize_weight(w, per_row=True)
+    del w
+    qa = torch.empty((M, K), dtype=torch.int8, device=device)
+    s_a = torch.empty(M, dtype=torch.float32, device=device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    kernel = q8.q8_gemm_pick(M, N, K)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+    torch.cuda.synchronize()
+    q_ms, g_ms = [], []
+    for _ in range(max(10, args.steps)):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+        e[1].record()
+        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+        e[2].record()
+        torch.cuda.synchronize()
+        q_ms.append(e[0].elapsed_time(e[1]))
+        g_ms.append(e[1].elapsed_time(e[2]))
+    gq = statistics.mean(g_ms)
+    step = statistics.mean(q_ms) + gq
+    gemm_bytes = N * K + M * K + 4 * N + 4 * M + 4 * M * N
+    return {"workload": f"{DECODE}: A [{M},{K}] x W int8 [{N},{K}]", "gemm_kernel": kernel,
+            "ms_per_step": round(step, 4), "TOPS": round(2.0 * M * N * K / (step * 1e-3) / 1e12, 2),
+            "gemm_ms": round(gq, 4), "gemm_GB/s": round(gemm_bytes / (gq * 1e-3) / 1e9, 1),
+            "gemm_frac_hbm": round(gemm_bytes / (gq * 1e-3) / 1e9 / hbm_peak, 4),
+            "algorithmic_bytes": gemm_bytes}
+
+
+# ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
+
+class OracleSample:
+    """The headline workload's inputs, with W quantized offline, for timing the oracle on row samples."""
+
+    def __init__(self):
+        import oracle
+        self.oracle = oracle
+        self.wl = workloads.WORKLOADS[HEADLINE]
+        self.a = workloads.make_activations(self.wl)
+        self.qw, self.sw = oracle.quantize_sym(workloads.make_weights(self.wl), True)
+        self.cores = len(os.sched_getaffinity(0))
+
+    def step(self, rows: int, start: int = 0):
+        o = self.oracle
+        a = self.a[start:start + rows]
+        qa, sa = o.quantize_sym(a, True)
+        y, st = o.linear_codes(qa, sa, None, self.qw, self.sw, True, True, threads=self.cores)
+        assert st == o.OK
+        return y
+
+    def ops(self, rows):
+        return 2.0 * rows * self.wl.N * self.wl.K
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    s = OracleSample()
+    rows = max(1, s.cores)
+    t = time.perf_counter()
+    s.step(rows)
+    dt = time.perf_counter() - t
+    rows = int(max(1, min(s.wl.M, rows * budget_s / max(dt, 1e-3))))
+    rows = max(s.cores, (rows // s.cores) * s.cores)
+    t = time.perf_counter()
+    s.step(rows, start=rows)
+    dt = time.perf_counter() - t
+    return {"value": round(s.ops(rows) / dt / 1e12, 6), "unit": "TOPS", "cores": s.cores, "kind": "oracle",
+            "sample": f"{rows} of {s.wl.M} token rows of {HEADLINE} (quantize rows + int64 dot products "
+                      f"against all {s.wl.N} channels, K={s.wl.K}), {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    s = OracleSample()
+    rows = s.cores
+    t = time.perf_counter()
+    s.step(rows)
+    dt = time.perf_counter() - t
+    per_step_target = min(8.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = int(max(s.cores, min(s.wl.M // 2, rows * per_step_target / max(dt, 1e-3))))
+    for i in range(args.warmup):
+        s.step(rows, start=(i * rows) % (s.wl.M - rows))
+    times = []
+    for i in range(args.steps):
+        t = time.perf_counter()
+        s.step(rows, start=((i + args.warmup) * rows) % (s.wl.M - rows))
+        times.append(time.perf_counter() - t)
+    ms = statistics.mean(times) * 1e3
+    value = s.ops(rows) / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": f"{HEADLINE} (row sample per step: {rows} tokens)", "M": s.wl.M, "N": s.wl.N,
+                   "K": s.wl.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": s.cores, "kind": "oracle",
+                         "sample": f"{rows} token rows per step"},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

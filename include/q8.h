@@ -1,0 +1,182 @@
+/*
+ * q8.h -- C ABI of the GB300 W8A8 quantized linear layer.
+ *
+ * The layer is the datapath the pages describe as "dequantize after integer
+ * accumulation": activations are quantized at run time, weights offline, the
+ * dot products are exact integer arithmetic accumulated in INT32, and the
+ * scales (and the zero-point correction) are applied once per output element
+ * in the epilogue:
+ *
+ *   y[m][n] = (float)(acc[m][n] - z_a[m] * colsum[n]) * (s_a[m] * s_w[n]),
+ *   acc[m][n] = sum_k qa[m][k] * qw[n][k],   colsum[n] = sum_k qw[n][k].
+ *
+ * ("100 Days of GPU, Day 98: Quantization and sparsity", sections "What a
+ * scale actually promises" and "The program, and the gate that has to be per
+ * column"; "Activation Quantization Architecture", section "The integer GEMM,
+ * written out"; "Write Int8 Quantized Kernel", reasoning steps 1, 2 and 4.)
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers (memory the caller allocated on
+ *    the current CUDA device) unless stated otherwise. The caller owns every
+ *    buffer; the library keeps no pointer after a call returns and allocates
+ *    no device memory.
+ *  - Matrices are row-major and dense. A is [M, K]; the weight is stored
+ *    K-major as W[N, K] (row n holds output channel n), the (N, K) layout of
+ *    "Write Int8 Quantized Kernel" (Common failure modes); y is [M, N].
+ *  - Every array base must be 16-byte aligned and K must be a multiple of 16
+ *    (rows are then 16-byte aligned for vector loads and TMA tiles).
+ *  - Calls are asynchronous and ordered on `stream` (NULL = the legacy default
+ *    stream). A returned Q8_OK means the work was enqueued; errors that
+ *    happen on the device surface at the next synchronising call.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    rejected call enqueues nothing and touches no memory.
+ *  - Inputs must be finite: NaN and Inf are not checked and give unspecified
+ *    codes (the pages do not define them).
+ *  - M, N or K equal to 0 are valid empty problems.
+ */
+#ifndef Q8_H_
+#define Q8_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* q8_stream_t;
+
+typedef enum q8_status {
+    Q8_OK = 0,
+    Q8_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, misaligned base */
+    Q8_ERR_UNSUPPORTED = 2,  /* K not a multiple of 16, or K beyond the INT32 range limit */
+    Q8_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    Q8_ERR_TIMEOUT = 4       /* a bounded device-side wait gave up (see q8_device_error) */
+} q8_status;
+
+/* One scale for the whole tensor, or one per row: per token for A (rows of
+ * A), per output channel for W (rows of the K-major W[N, K]). Day 98, "What
+ * a scale actually promises"; "Write Int8 Quantized Kernel", inputs to gather. */
+typedef enum q8_granularity { Q8_PER_TENSOR = 0, Q8_PER_ROW = 1 } q8_granularity;
+
+typedef enum q8_symmetry { Q8_SYMMETRIC = 0, Q8_ASYMMETRIC = 1 } q8_symmetry;
+
+/* GEMM kernel choice for q8_gemm_dequant_ex / q8_gemm_s32_ex. */
+typedef enum q8_gemm_kernel {
+    Q8_GEMM_AUTO = 0,     /* pick by shape (what q8_gemm_dequant does) */
+    Q8_GEMM_TCGEN05 = 1,  /* tcgen05 tensor-core kernel (fp32 TMEM chunks drained to INT32) */
+    Q8_GEMM_MMA_S8 = 2,   /* warp-level mma.sync s8 kernel, 128x128 tiles */
+    Q8_GEMM_SKINNY = 3    /* warp-level mma.sync s8 kernel for M <= 16 rows per tile */
+} q8_gemm_kernel;
+
+/*
+ * Dynamic activation quantization (one call per forward pass).
+ *
+ * Symmetric: s = max(amax, 1e-8) / 127 with amax = max|a| over the row (or
+ * tensor), q = clamp(rint(a / s), -127, 127), z not used. ("Activation
+ * Quantization Architecture", The quantizer itself and the Fusion pseudocode;
+ * Day 98, What a scale actually promises.)
+ * Asymmetric: lo = min(min a, 0), hi = max(max a, 0), s = max(hi - lo, 1e-8)
+ * / 255, z = clamp(-128 - rint(lo / s), -128, 127), q = clamp(rint(a / s) + z,
+ * -128, 127): the uint8 codes 0..255 of "Write Int8 Quantized Kernel" step 1
+ * stored as int8 (code - 128), with z the code that dequantizes to zero (Day 98).
+ * Divisions are IEEE fp32, rint is round-half-to-even.
+ *
+ * a   : fp32 [M, K], read only.
+ * qa  : int8 [M, K], written.
+ * s_a : fp32 [M] (Q8_PER_ROW) or [1] (Q8_PER_TENSOR), written.
+ * z_a : int32 [M] or [1], written; must be NULL for Q8_SYMMETRIC and non-NULL
+ *       for Q8_ASYMMETRIC.
+ * Per-tensor granularity uses s_a[0] (and z_a[0]) as its reduction cell, so no
+ * extra workspace is needed; their contents on entry are ignored.
+ */
+q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g,
+                          q8_symmetry sym, int8_t* qa, float* s_a, int32_t* z_a,
+                          q8_stream_t stream);
+
+/*
+ * Offline symmetric weight quantization, per output channel or per tensor,
+ * with the symmetric rule above ("Activation Quantization Architecture", the
+ * numpy reference quantize_per_channel; Day 98, one scale per column of B).
+ *
+ * w   : fp32 W[N, K] (K-major), read only.
+ * qw  : int8 [N, K], written.
+ * s_w : fp32 [N] (Q8_PER_ROW) or [1] (Q8_PER_TENSOR), written.
+ */
+q8_status q8_quantize_weight(const float* w, int64_t N, int64_t K, q8_granularity g,
+                             int8_t* qw, float* s_w, q8_stream_t stream);
+
+/*
+ * Column sums of the quantized weights, colsum[n] = sum_k qw[n][k] (exact
+ * int32; |colsum| <= 128 K). Computed once, offline, next to the weights; the
+ * epilogue needs them only when A is asymmetric (Day 98, the paragraph after
+ * the kernel listing).
+ *
+ * qw     : int8 [N, K], read only.
+ * colsum : int32 [N], written.
+ */
+q8_status q8_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum,
+                    q8_stream_t stream);
+
+/*
+ * Integer GEMM with the fused dequantization epilogue:
+ *   acc  = sum_k qa[m][k] * qw[n][k]                  (exact, INT32)
+ *   corr = acc - z_a[m] * colsum[n]                   (INT32; 0 when z_a == NULL)
+ *   y    = (float)corr * (s_a[m] * s_w[n])            (two fp32 roundings)
+ * The multiply order is that of the Day 98 epilogue listing; the zero-point
+ * correction is applied before the scales ("Write Int8 Quantized Kernel",
+ * correctness requirements).
+ *
+ * qa, qw   : int8 [M, K], int8 [N, K]; any codes in [-128, 127] are accepted.
+ * s_a      : fp32 [M] if ga == Q8_PER_ROW, else [1].
+ * z_a      : NULL (symmetric A) or int32 [M] / [1] following ga.
+ * s_w      : fp32 [N] if gw == Q8_PER_ROW, else [1].
+ * colsum   : int32 [N]; required iff z_a != NULL (ignored otherwise).
+ * y        : fp32 [M, N], written.
+ * Limits   : K <= 131056 when z_a == NULL (128*128*K < 2^31) and K <= 65792
+ *            otherwise (255*128*K < 2^31), so acc and corr never leave INT32;
+ *            larger K returns Q8_ERR_UNSUPPORTED.
+ */
+q8_status q8_gemm_dequant(const int8_t* qa, const float* s_a, const int32_t* z_a,
+                          q8_granularity ga, const int8_t* qw, const float* s_w,
+                          q8_granularity gw, const int32_t* colsum, int64_t M, int64_t N,
+                          int64_t K, float* y, q8_stream_t stream);
+
+/* q8_gemm_dequant with an explicit kernel choice. A kernel that cannot run
+ * the given shape returns Q8_ERR_UNSUPPORTED (Q8_GEMM_AUTO never does). */
+q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* z_a,
+                             q8_granularity ga, const int8_t* qw, const float* s_w,
+                             q8_granularity gw, const int32_t* colsum, int64_t M, int64_t N,
+                             int64_t K, float* y, q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
+ * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),
+ * computed by the same main loop as q8_gemm_dequant_ex with the same kernel
+ * choice. Used to check the integer GEMM bit for bit.
+ * acc : int32 [M, N], written. K <= 131056.
+ */
+q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                         int32_t* acc, q8_gemm_kernel kernel, q8_stream_t stream);
+
+/* The kernel q8_gemm_dequant would run for this shape (never Q8_GEMM_AUTO). */
+q8_gemm_kernel q8_gemm_pick(int64_t M, int64_t N, int64_t K);
+
+/* Static description of a status code. Never NULL. */
+const char* q8_status_string(q8_status status);
+
+/*
+ * Device-side error word of the current device: 0 if every bounded wait of a
+ * tensor-core kernel completed, otherwise a nonzero code naming the wait that
+ * gave up. Synchronises the device. Reading it resets it to 0. A nonzero
+ * value means the outputs of the kernel that set it are invalid.
+ */
+q8_status q8_device_error(uint32_t* code_out);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t q8_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8_H_ */

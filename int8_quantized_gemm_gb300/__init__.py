@@ -1,0 +1,206 @@
+"""GB300 W8A8 quantized linear layer: Python binding of the C ABI in include/q8.h.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+libq8.so. PyTorch supplies device memory and the current stream. There is no
+CPU fallback; if the library is missing or a call fails, an exception says so.
+
+  q8_quantize_act(a, per_row=True, symmetric=True)   -> qa, s_a, z_a
+  q8_quantize_weight(w, per_row=True)                 -> qw, s_w
+  q8_colsum(qw)                                       -> colsum
+  q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum)      -> y
+  q8_gemm_s32(qa, qw)                                 -> acc (raw INT32 accumulators)
+  q8_linear(a, qw, s_w, colsum)                       -> y   (quantize A, then GEMM)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "Q8Error", "load", "q8_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
+    "q8_gemm_s32", "q8_linear", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+]
+
+LIB_PATH = _build.LIB
+Q8_OK, Q8_ERR_INVALID_ARG, Q8_ERR_UNSUPPORTED, Q8_ERR_CUDA, Q8_ERR_TIMEOUT = range(5)
+Q8_PER_TENSOR, Q8_PER_ROW = 0, 1
+Q8_SYMMETRIC, Q8_ASYMMETRIC = 0, 1
+KERNELS = {"auto": 0, "tcgen05": 1, "mma_s8": 2, "skinny": 3}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+
+_lib = None
+
+
+class Q8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libq8.so (built in-tree by build.py). Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libq8.so is not built ({path}); run int8_quantized_gemm_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.q8_quantize_act.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
+    lib.q8_quantize_weight.argtypes = [p, i64, i64, i32, p, p, p]
+    lib.q8_colsum.argtypes = [p, i64, i64, p, p]
+    lib.q8_gemm_dequant.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, p]
+    lib.q8_gemm_dequant_ex.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32, p]
+    lib.q8_gemm_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
+    lib.q8_gemm_pick.argtypes = [i64, i64, i64]
+    lib.q8_status_string.argtypes = [i32]
+    lib.q8_status_string.restype = ctypes.c_char_p
+    lib.q8_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.q8_launch_count.argtypes = []
+    lib.q8_launch_count.restype = ctypes.c_uint64
+    for name in ("q8_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
+                 "q8_gemm_dequant_ex", "q8_gemm_s32_ex", "q8_gemm_pick", "q8_device_error"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().q8_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != Q8_OK:
+        raise Q8Error(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def q8_quantize_act(a: torch.Tensor, per_row: bool = True, symmetric: bool = True, qa=None, s_a=None,
+                    z_a=None, stream=None):
+    """Dynamic activation quantization of fp32 a[M, K]; returns (qa int8, s_a fp32, z_a int32 or None)."""
+    _need(a, torch.float32, "a", 2)
+    M, K = a.shape
+    n = M if per_row else 1
+    qa = torch.empty((M, K), dtype=torch.int8, device=a.device) if qa is None else qa
+    s_a = torch.empty(n, dtype=torch.float32, device=a.device) if s_a is None else s_a
+    if not symmetric and z_a is None:
+        z_a = torch.empty(n, dtype=torch.int32, device=a.device)
+    if symmetric:
+        z_a = None
+    _check(load().q8_quantize_act(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
+                                  Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(s_a),
+                                  _ptr(z_a), _stream(stream)), "q8_quantize_act")
+    return qa, s_a, z_a
+
+
+def q8_quantize_weight(w: torch.Tensor, per_row: bool = True, qw=None, s_w=None, stream=None):
+    """Symmetric quantization of fp32 W[N, K] (K-major); returns (qw int8, s_w fp32)."""
+    _need(w, torch.float32, "w", 2)
+    N, K = w.shape
+    qw = torch.empty((N, K), dtype=torch.int8, device=w.device) if qw is None else qw
+    s_w = torch.empty(N if per_row else 1, dtype=torch.float32, device=w.device) if s_w is None else s_w
+    _check(load().q8_quantize_weight(_ptr(w), N, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR, _ptr(qw),
+                                     _ptr(s_w), _stream(stream)), "q8_quantize_weight")
+    return qw, s_w
+
+
+def q8_colsum(qw: torch.Tensor, out=None, stream=None):
+    _need(qw, torch.int8, "qw", 2)
+    N, K = qw.shape
+    out = torch.empty(N, dtype=torch.int32, device=qw.device) if out is None else out
+    _check(load().q8_colsum(_ptr(qw), N, K, _ptr(out), _stream(stream)), "q8_colsum")
+    return out
+
+
+def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "auto", stream=None):
+    """y[M, N] = (acc - z_a*colsum) * (s_a * s_w) from int8 codes; per-row scales are inferred
+    from the lengths of s_a (M entries) and s_w (N entries)."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw, torch.int8, "qw", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qa and qw disagree on K")
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    ga = Q8_PER_ROW if (s_a.numel() == M and M != 1) else Q8_PER_TENSOR
+    gw = Q8_PER_ROW if (s_w.numel() == N and N != 1) else Q8_PER_TENSOR
+    if s_a.numel() not in (1, M) or s_w.numel() not in (1, N):
+        raise ValueError("s_a must have 1 or M entries and s_w 1 or N entries")
+    if z_a is not None:
+        _need(z_a, torch.int32, "z_a", 1)
+        if z_a.numel() != s_a.numel():
+            raise ValueError("z_a must have as many entries as s_a")
+        if colsum is None:
+            raise ValueError("an asymmetric A needs the weight column sums")
+        _need(colsum, torch.int32, "colsum", 1)
+    y = torch.empty((M, N), dtype=torch.float32, device=qa.device) if y is None else y
+    _need(y, torch.float32, "y", 2)
+    _check(load().q8_gemm_dequant_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
+                                     _ptr(colsum if z_a is not None else None), M, N, K, _ptr(y),
+                                     KERNELS[kernel], _stream(stream)), "q8_gemm_dequant")
+    return y
+
+
+def q8_gemm_s32(qa, qw, out=None, kernel: str = "auto", stream=None):
+    """Raw INT32 accumulators acc[M, N] = qa . qw^T (diagnostic export of the integer GEMM)."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw, torch.int8, "qw", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    out = torch.empty((M, N), dtype=torch.int32, device=qa.device) if out is None else out
+    _need(out, torch.int32, "out", 2)
+    _check(load().q8_gemm_s32_ex(_ptr(qa), _ptr(qw), M, N, K, _ptr(out), KERNELS[kernel], _stream(stream)),
+           "q8_gemm_s32")
+    return out
+
+
+def q8_linear(a, qw, s_w, colsum=None, per_row: bool = True, symmetric: bool = True, kernel: str = "auto",
+              stream=None):
+    """Whole W8A8 layer on fp32 activations: dynamic quantization of a, then the GEMM + epilogue."""
+    qa, s_a, z_a = q8_quantize_act(a, per_row=per_row, symmetric=symmetric, stream=stream)
+    return q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, kernel=kernel, stream=stream)
+
+
+def q8_gemm_pick(M: int, N: int, K: int) -> str:
+    return KERNEL_NAMES[load().q8_gemm_pick(M, N, K)]
+
+
+def q8_launch_count() -> int:
+    return int(load().q8_launch_count())
+
+
+def q8_device_error() -> int:
+    """Device error word of the tensor-core kernel (0 = every bounded wait completed); resets it."""
+    code = ctypes.c_uint32(0)
+    st = load().q8_device_error(ctypes.byref(code))
+    if st not in (Q8_OK, Q8_ERR_TIMEOUT):
+        _check(st, "q8_device_error")
+    return int(code.value)

@@ -1,0 +1,177 @@
+// C ABI of the library: host-side argument validation, kernel choice and the
+// mapping of CUDA errors to q8_status. Validation runs before any CUDA call, so
+// a rejected call enqueues nothing (and can be exercised without a GPU).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "q8_internal.h"
+
+namespace q8 {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace q8
+
+namespace {
+
+// 128*128*K < 2^31 for any int8 codes; (255*128)*K < 2^31 once a zero point
+// (|qa - z| <= 255) enters the correction.
+constexpr int64_t kMaxKSym = 131056;
+constexpr int64_t kMaxKAsym = 65792;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_gran(q8_granularity g) { return g == Q8_PER_TENSOR || g == Q8_PER_ROW; }
+
+q8_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return Q8_OK;
+    if (e == cudaErrorNotSupported) return Q8_ERR_UNSUPPORTED;
+    return Q8_ERR_CUDA;
+}
+
+q8_status check_k(int64_t K, bool asym) {
+    if (K < 0) return Q8_ERR_INVALID_ARG;
+    if (K % 16 != 0) return Q8_ERR_UNSUPPORTED;
+    if (K > (asym ? kMaxKAsym : kMaxKSym)) return Q8_ERR_UNSUPPORTED;
+    return Q8_OK;
+}
+
+q8_status check_quant_args(const float* x, int64_t rows, int64_t cols, q8_granularity g, const int8_t* q,
+                           const float* s, bool need_matrix_ptrs) {
+    if (rows < 0 || cols < 0 || !valid_gran(g)) return Q8_ERR_INVALID_ARG;
+    if (!s || !aligned(s, 4)) return Q8_ERR_INVALID_ARG;
+    if (need_matrix_ptrs) {
+        if (!x || !q || !aligned(x, 16) || !aligned(q, 16)) return Q8_ERR_INVALID_ARG;
+    }
+    if (cols % 16 != 0) return Q8_ERR_UNSUPPORTED;
+    return Q8_OK;
+}
+
+q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                      const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                      int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
+                      q8_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+    if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
+        kernel != Q8_GEMM_SKINNY)
+        return Q8_ERR_INVALID_ARG;
+    const bool epilogue = (out_i32 == nullptr);
+    if (epilogue) {
+        if (!valid_gran(ga) || !valid_gran(gw)) return Q8_ERR_INVALID_ARG;
+        if (!s_a || !s_w || !y) return Q8_ERR_INVALID_ARG;
+        if (!aligned(s_a, 4) || !aligned(s_w, 4) || !aligned(y, 16)) return Q8_ERR_INVALID_ARG;
+        if (z_a && (!colsum || !aligned(z_a, 4) || !aligned(colsum, 4))) return Q8_ERR_INVALID_ARG;
+    } else if (!aligned(out_i32, 16)) {
+        return Q8_ERR_INVALID_ARG;
+    }
+    if (M > 0 && N > 0 && K > 0) {
+        if (!qa || !qw || !aligned(qa, 16) || !aligned(qw, 16)) return Q8_ERR_INVALID_ARG;
+    }
+    q8_status st = check_k(K, epilogue && z_a != nullptr);
+    if (st != Q8_OK) return st;
+    if (M > INT32_MAX || N > INT32_MAX) return Q8_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return Q8_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        // Empty dot products: acc = 0, colsum = 0, so y = 0 * scale = +0.0f.
+        const size_t bytes = (size_t)M * (size_t)N * 4;
+        return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
+    }
+    q8::Epilogue ep{s_a, z_a, s_w, colsum, ga == Q8_PER_ROW, gw == Q8_PER_ROW, y, out_i32};
+    if (kernel == Q8_GEMM_AUTO) kernel = q8_gemm_pick(M, N, K);
+    switch (kernel) {
+        case Q8_GEMM_TCGEN05:
+            if (!q8::gemm_tc_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
+            return from_cuda(q8::launch_gemm_tc(qa, qw, M, N, K, ep, s));
+        case Q8_GEMM_SKINNY:
+            return from_cuda(q8::launch_gemm_mma(qa, qw, M, N, K, ep, true, s));
+        case Q8_GEMM_MMA_S8:
+        default:
+            return from_cuda(q8::launch_gemm_mma(qa, qw, M, N, K, ep, false, s));
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym,
+                          int8_t* qa, float* s_a, int32_t* z_a, q8_stream_t stream) {
+    if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
+    if ((sym == Q8_ASYMMETRIC) != (z_a != nullptr)) return Q8_ERR_INVALID_ARG;
+    if (z_a && !aligned(z_a, 4)) return Q8_ERR_INVALID_ARG;
+    q8_status st = check_quant_args(a, M, K, g, qa, s_a, M > 0 && K > 0);
+    if (st != Q8_OK) return st;
+    if (g == Q8_PER_ROW && M == 0) return Q8_OK;
+    return from_cuda(q8::launch_quantize(a, M, K, g == Q8_PER_ROW, qa, s_a, z_a,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_quantize_weight(const float* w, int64_t N, int64_t K, q8_granularity g, int8_t* qw, float* s_w,
+                             q8_stream_t stream) {
+    q8_status st = check_quant_args(w, N, K, g, qw, s_w, N > 0 && K > 0);
+    if (st != Q8_OK) return st;
+    if (g == Q8_PER_ROW && N == 0) return Q8_OK;
+    return from_cuda(q8::launch_quantize(w, N, K, g == Q8_PER_ROW, qw, s_w, nullptr,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum, q8_stream_t stream) {
+    if (N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+    if (K % 16 != 0 || K > kMaxKSym) return Q8_ERR_UNSUPPORTED;
+    if (N == 0) return Q8_OK;
+    if (!colsum || !aligned(colsum, 4)) return Q8_ERR_INVALID_ARG;
+    if (K > 0 && (!qw || !aligned(qw, 16))) return Q8_ERR_INVALID_ARG;
+    return from_cuda(q8::launch_colsum(qw, N, K, colsum, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_gemm_dequant(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                          const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                          int64_t M, int64_t N, int64_t K, float* y, q8_stream_t stream) {
+    return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream);
+}
+
+q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                             const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                             int64_t M, int64_t N, int64_t K, float* y, q8_gemm_kernel kernel,
+                             q8_stream_t stream) {
+    return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, kernel, stream);
+}
+
+q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,
+                         q8_gemm_kernel kernel, q8_stream_t stream) {
+    if (!acc && M > 0 && N > 0) return Q8_ERR_INVALID_ARG;
+    return gemm_common(qa, nullptr, nullptr, Q8_PER_TENSOR, qw, nullptr, Q8_PER_TENSOR, nullptr, M, N, K,
+                       nullptr, acc, kernel, stream);
+}
+
+q8_gemm_kernel q8_gemm_pick(int64_t M, int64_t N, int64_t K) {
+    if (q8::gemm_tc_supports(M, N, K)) return Q8_GEMM_TCGEN05;
+    if (M <= 16) return Q8_GEMM_SKINNY;
+    return Q8_GEMM_MMA_S8;
+}
+
+const char* q8_status_string(q8_status status) {
+    switch (status) {
+        case Q8_OK: return "ok";
+        case Q8_ERR_INVALID_ARG: return "invalid argument";
+        case Q8_ERR_UNSUPPORTED: return "unsupported shape or size";
+        case Q8_ERR_CUDA: return "CUDA error";
+        case Q8_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+q8_status q8_device_error(uint32_t* code_out) {
+    if (!code_out) return Q8_ERR_INVALID_ARG;
+    cudaError_t e = q8::read_and_clear_device_error(code_out);
+    if (e != cudaSuccess) return Q8_ERR_CUDA;
+    return *code_out ? Q8_ERR_TIMEOUT : Q8_OK;
+}
+
+uint64_t q8_launch_count(void) { return q8::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

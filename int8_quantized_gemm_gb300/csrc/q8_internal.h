@@ -1,0 +1,52 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/q8.h"
+
+namespace q8 {
+
+// Every kernel launch of the library goes through note_launch() so that
+// q8_launch_count() can report how many of our kernels ran.
+void note_launch(int n = 1);
+
+// Symmetric rule: s = max(amax, 1e-8) / 127; codes clamp(rint(x / s), -127, 127).
+// Asymmetric rule: lo = min(min, 0), hi = max(max, 0), s = max(hi - lo, 1e-8) / 255,
+// z = clamp(-128 - rint(lo / s), -128, 127), q = clamp(rint(x / s) + z, -128, 127).
+constexpr float kZeroGuard = 1e-8f;
+
+// Quantize rows of x (rows x cols, row-major); per_row selects one scale per row
+// or one for the whole tensor. z == nullptr selects the symmetric rule.
+cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row,
+                            int8_t* q, float* s, int32_t* z, cudaStream_t stream);
+
+cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum,
+                          cudaStream_t stream);
+
+// Epilogue operands shared by every GEMM kernel. When out_i32 != nullptr the
+// kernel writes the raw accumulators there instead of y.
+struct Epilogue {
+    const float* s_a;
+    const int32_t* z_a;      // nullptr: symmetric A
+    const float* s_w;
+    const int32_t* colsum;   // used iff z_a != nullptr
+    bool a_per_row;
+    bool w_per_row;
+    float* y;
+    int32_t* out_i32;
+};
+
+cudaError_t launch_gemm_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                            const Epilogue& ep, bool skinny, cudaStream_t stream);
+
+// tcgen05 kernel; returns cudaErrorNotSupported when the shape is outside its range.
+cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                           const Epilogue& ep, cudaStream_t stream);
+bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
+
+// Device error word (bounded waits that gave up), one per device.
+cudaError_t read_and_clear_device_error(uint32_t* code);
+
+}  // namespace q8

@@ -1,0 +1,335 @@
+// Activation / weight quantizers and weight column sums.
+//
+// These kernels are HBM-bound streams: each fp32 element is read once from
+// HBM (4 bytes) and its code written once (1 byte). Per-row quantization keeps
+// the whole row in registers between the range reduction and the code pass,
+// so the row is never re-read. Arithmetic follows the rules in q8.h exactly:
+// IEEE fp32 division (__fdiv_rn), round-half-to-even (__float2int_rn), and no
+// contraction of multiplies into FMAs (the file is built with -fmad=false).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8_internal.h"
+
+namespace q8 {
+namespace {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v, lo), hi); }
+
+// Symmetric scale from the absolute maximum.
+__device__ __forceinline__ float sym_scale(float amax) {
+    return __fdiv_rn(fmaxf(amax, kZeroGuard), 127.0f);
+}
+
+__device__ __forceinline__ void asym_params(float lo, float hi, float* s, int* z) {
+    float span = __fsub_rn(hi, lo);
+    float sc = __fdiv_rn(fmaxf(span, kZeroGuard), 255.0f);
+    *s = sc;
+    *z = clampi(-128 - __float2int_rn(__fdiv_rn(lo, sc)), -128, 127);
+}
+
+__device__ __forceinline__ int sym_code(float x, float s) {
+    return clampi(__float2int_rn(__fdiv_rn(x, s)), -127, 127);
+}
+
+__device__ __forceinline__ int asym_code(float x, float s, int z) {
+    return clampi(__float2int_rn(__fdiv_rn(x, s)) + z, -128, 127);
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
+           ((uint32_t)(d & 0xFF) << 24);
+}
+
+// Block-wide max of two values (hi, and nlo = -lo for the asymmetric range).
+// All threads receive the results.
+template <bool ASYM>
+__device__ __forceinline__ void block_max2(float& hi, float& nlo, float* red) {
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) {
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        if (ASYM) nlo = fmaxf(nlo, __shfl_xor_sync(0xffffffffu, nlo, o));
+    }
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nwarps = blockDim.x / kWarp;
+    if (lane == 0) {
+        red[warp] = hi;
+        if (ASYM) red[32 + warp] = nlo;
+    }
+    __syncthreads();
+    hi = lane < nwarps ? red[lane] : 0.0f;
+    if (ASYM) nlo = lane < nwarps ? red[32 + lane] : 0.0f;
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) {
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        if (ASYM) nlo = fmaxf(nlo, __shfl_xor_sync(0xffffffffu, nlo, o));
+    }
+}
+
+// One CTA per row; each thread keeps up to VPT float4 of the row in registers.
+// Requires cols % 4 == 0 and cols / 4 <= VPT * blockDim.x.
+template <int VPT, bool ASYM>
+__global__ void __launch_bounds__(512) quantize_rows_kernel(const float* __restrict__ x, int64_t cols,
+                                                            int8_t* __restrict__ q,
+                                                            float* __restrict__ s,
+                                                            int32_t* __restrict__ z) {
+    __shared__ float red[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
+    float4 v[VPT];
+    float hi = 0.0f, nlo = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4) {
+            v[j] = __ldcs(xr + i);   // streamed once: evict-first
+            if (ASYM) {
+                hi = fmaxf(hi, fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w)));
+                nlo = fmaxf(nlo, -fminf(fminf(v[j].x, v[j].y), fminf(v[j].z, v[j].w)));
+            } else {
+                hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)),
+                                     fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+            }
+        }
+    }
+    block_max2<ASYM>(hi, nlo, red);
+    float sc;
+    int zp = 0;
+    if (ASYM) {
+        asym_params(-nlo, hi, &sc, &zp);
+    } else {
+        sc = sym_scale(hi);
+    }
+    if (threadIdx.x == 0) {
+        s[row] = sc;
+        if (ASYM) z[row] = zp;
+    }
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4) {
+            uint32_t w;
+            if (ASYM)
+                w = pack4(asym_code(v[j].x, sc, zp), asym_code(v[j].y, sc, zp),
+                          asym_code(v[j].z, sc, zp), asym_code(v[j].w, sc, zp));
+            else
+                w = pack4(sym_code(v[j].x, sc), sym_code(v[j].y, sc), sym_code(v[j].z, sc),
+                          sym_code(v[j].w, sc));
+            qr[i] = w;
+        }
+    }
+}
+
+// Rows longer than the register budget: reduce in one sweep, code in a second
+// sweep (the second read of the row is served mostly by L2).
+template <bool ASYM>
+__global__ void __launch_bounds__(512) quantize_long_rows_kernel(const float* __restrict__ x, int64_t cols,
+                                                                 int8_t* __restrict__ q,
+                                                                 float* __restrict__ s,
+                                                                 int32_t* __restrict__ z) {
+    __shared__ float red[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
+    float hi = 0.0f, nlo = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        float4 v = xr[i];
+        if (ASYM) {
+            hi = fmaxf(hi, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            nlo = fmaxf(nlo, -fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+        } else {
+            hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    }
+    block_max2<ASYM>(hi, nlo, red);
+    float sc;
+    int zp = 0;
+    if (ASYM) {
+        asym_params(-nlo, hi, &sc, &zp);
+    } else {
+        sc = sym_scale(hi);
+    }
+    if (threadIdx.x == 0) {
+        s[row] = sc;
+        if (ASYM) z[row] = zp;
+    }
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        float4 v = __ldcs(xr + i);
+        qr[i] = ASYM ? pack4(asym_code(v.x, sc, zp), asym_code(v.y, sc, zp), asym_code(v.z, sc, zp),
+                             asym_code(v.w, sc, zp))
+                     : pack4(sym_code(v.x, sc), sym_code(v.y, sc), sym_code(v.z, sc), sym_code(v.w, sc));
+    }
+}
+
+// Per-tensor range: every block reduces its share and folds it into the cells
+// with an integer atomic max on the fp32 bit pattern (non-negative floats
+// order like their bits, so the result does not depend on block order).
+// cell_hi holds max|x| (symmetric) or max(max x, 0); cell_nlo holds -min(min x, 0).
+template <bool ASYM>
+__global__ void __launch_bounds__(512) tensor_range_kernel(const float* __restrict__ x, int64_t n4,
+                                                           unsigned int* cell_hi,
+                                                           unsigned int* cell_nlo) {
+    __shared__ float red[64];
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    float hi = 0.0f, nlo = 0.0f;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 v = x4[i];
+        if (ASYM) {
+            hi = fmaxf(hi, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            nlo = fmaxf(nlo, -fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+        } else {
+            hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    }
+    block_max2<ASYM>(hi, nlo, red);
+    if (threadIdx.x == 0) {
+        atomicMax(cell_hi, __float_as_uint(hi));
+        if (ASYM) atomicMax(cell_nlo, __float_as_uint(nlo));
+    }
+}
+
+// Turns the reduced range in the cells into the tensor's scale (and zero point),
+// written over the same cells.
+template <bool ASYM>
+__global__ void tensor_params_kernel(float* s, int32_t* z) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const float hi = __uint_as_float(*reinterpret_cast<unsigned int*>(s));
+    if (ASYM) {
+        const float nlo = __uint_as_float(*reinterpret_cast<unsigned int*>(z));
+        float sc;
+        int zp;
+        asym_params(-nlo, hi, &sc, &zp);
+        s[0] = sc;
+        z[0] = zp;
+    } else {
+        s[0] = sym_scale(hi);
+    }
+}
+
+template <bool ASYM>
+__global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restrict__ x, int64_t n4,
+                                                           const float* __restrict__ s,
+                                                           const int32_t* __restrict__ z,
+                                                           int8_t* __restrict__ q) {
+    const float sc = s[0];
+    const int zp = ASYM ? z[0] : 0;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 v = __ldcs(x4 + i);
+        q4[i] = ASYM ? pack4(asym_code(v.x, sc, zp), asym_code(v.y, sc, zp), asym_code(v.z, sc, zp),
+                             asym_code(v.w, sc, zp))
+                     : pack4(sym_code(v.x, sc), sym_code(v.y, sc), sym_code(v.z, sc), sym_code(v.w, sc));
+    }
+}
+
+// colsum[n] = sum_k qw[n][k]: one warp per weight row, 16-byte loads, dp4a
+// against ones (four signed bytes summed into an int32 per instruction).
+__global__ void __launch_bounds__(256) colsum_kernel(const int8_t* __restrict__ qw, int64_t N,
+                                                     int64_t K, int32_t* __restrict__ colsum) {
+    const int64_t n = blockIdx.x * (int64_t)(blockDim.x / kWarp) + threadIdx.x / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    if (n >= N) return;
+    const int4* r = reinterpret_cast<const int4*>(qw + n * K);
+    const int64_t n16 = K / 16;
+    int acc = 0;
+    for (int64_t i = lane; i < n16; i += kWarp) {
+        int4 v = r[i];
+        acc = __dp4a(v.x, 0x01010101, acc);
+        acc = __dp4a(v.y, 0x01010101, acc);
+        acc = __dp4a(v.z, 0x01010101, acc);
+        acc = __dp4a(v.w, 0x01010101, acc);
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) colsum[n] = acc;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return sms;
+}
+
+template <int VPT, bool ASYM>
+cudaError_t launch_rows(const float* x, int64_t rows, int64_t cols, int threads, int8_t* q, float* s,
+                        int32_t* z, cudaStream_t st) {
+    quantize_rows_kernel<VPT, ASYM><<<(unsigned)rows, threads, 0, st>>>(x, cols, q, s, z);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <bool ASYM>
+cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, int8_t* q, float* s, int32_t* z,
+                          cudaStream_t st) {
+    const int64_t n4 = cols / 4;
+    // Smallest block that covers the row with the per-thread register budget.
+    auto threads_for = [&](int vpt) {
+        int64_t t = (n4 + vpt - 1) / vpt;
+        t = ((t + kWarp - 1) / kWarp) * kWarp;
+        return (int)(t < kWarp ? kWarp : t);
+    };
+    if (n4 <= 128 * 1) return launch_rows<1, ASYM>(x, rows, cols, threads_for(1), q, s, z, st);
+    if (n4 <= 256 * 2) return launch_rows<2, ASYM>(x, rows, cols, threads_for(2), q, s, z, st);
+    if (n4 <= 256 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
+    if (n4 <= 512 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
+    if (n4 <= 512 * 8) return launch_rows<8, ASYM>(x, rows, cols, threads_for(8), q, s, z, st);
+    if (n4 <= 512 * 16) return launch_rows<16, ASYM>(x, rows, cols, threads_for(16), q, s, z, st);
+    quantize_long_rows_kernel<ASYM><<<(unsigned)rows, 512, 0, st>>>(x, cols, q, s, z);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <bool ASYM>
+cudaError_t dispatch_tensor(const float* x, int64_t n, int8_t* q, float* s, int32_t* z, cudaStream_t st) {
+    const int64_t n4 = n / 4;
+    cudaError_t e = cudaMemsetAsync(s, 0, sizeof(float), st);
+    if (e == cudaSuccess && ASYM) e = cudaMemsetAsync(z, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+    int64_t blocks = (n4 + 511) / 512;
+    const int64_t cap = (int64_t)num_sms() * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    tensor_range_kernel<ASYM><<<(unsigned)blocks, 512, 0, st>>>(
+        x, n4, reinterpret_cast<unsigned int*>(s), reinterpret_cast<unsigned int*>(z));
+    tensor_params_kernel<ASYM><<<1, 32, 0, st>>>(s, z);
+    tensor_codes_kernel<ASYM><<<(unsigned)blocks, 512, 0, st>>>(x, n4, s, z, q);
+    note_launch(3);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row, int8_t* q,
+                            float* s, int32_t* z, cudaStream_t stream) {
+    if (per_row) {
+        if (rows == 0) return cudaSuccess;
+        return z ? dispatch_rows<true>(x, rows, cols, q, s, z, stream)
+                 : dispatch_rows<false>(x, rows, cols, q, s, z, stream);
+    }
+    return z ? dispatch_tensor<true>(x, rows * cols, q, s, z, stream)
+             : dispatch_tensor<false>(x, rows * cols, q, s, z, stream);
+}
+
+cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
+    colsum_kernel<<<(unsigned)blocks, warps_per_block * kWarp, 0, stream>>>(qw, N, K, colsum);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace q8

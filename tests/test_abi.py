@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU. These
+calls never launch a kernel (validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int8_quantized_gemm_gb300 import build
+    build.build()
+    import int8_quantized_gemm_gb300 as q8
+    return q8.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\*?\s+\**(q8_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("q8_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
+                     "q8_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in q8.h but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.q8_status_string(s)
+    assert lib.q8_status_string(99) == b"unknown status"
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)          # 16-byte aligned, never dereferenced: validation fails first
+MISALIGNED = P(0x10004)
+
+
+def gemm(lib, qa=FAKE, sa=FAKE, za=None, ga=1, qw=FAKE, sw=FAKE, gw=1, cs=None, M=8, N=8, K=16,
+         y=FAKE, kernel=0):
+    return lib.q8_gemm_dequant_ex(qa, sa, za, ga, qw, sw, gw, cs, M, N, K, y, kernel, None)
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    assert gemm(lib, qa=None) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, y=None) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, sa=None) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, M=-1) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, ga=7) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, kernel=9) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, qa=MISALIGNED) == q8.Q8_ERR_INVALID_ARG
+    assert gemm(lib, za=FAKE, cs=None) == q8.Q8_ERR_INVALID_ARG     # asymmetric A needs colsum
+    assert gemm(lib, K=24) == q8.Q8_ERR_UNSUPPORTED                # K % 16
+    assert gemm(lib, K=131072) == q8.Q8_ERR_UNSUPPORTED            # 128*128*K would leave int32
+    assert gemm(lib, K=65808, za=FAKE, cs=FAKE) == q8.Q8_ERR_UNSUPPORTED
+    # empty problems are valid and launch nothing
+    before = lib.q8_launch_count()
+    assert gemm(lib, M=0) == q8.Q8_OK
+    assert gemm(lib, N=0) == q8.Q8_OK
+    assert lib.q8_launch_count() == before
+
+
+def test_k_limits_are_the_int32_bounds():
+    # 128*128*K < 2^31 for raw codes; 255*128*K < 2^31 with a zero point.
+    assert 128 * 128 * 131056 < 2 ** 31 <= 128 * 128 * (131056 + 16)
+    assert 255 * 128 * 65792 < 2 ** 31 <= 255 * 128 * (65792 + 16)
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    q = lib.q8_quantize_act
+    assert q(FAKE, 4, 32, 1, 0, FAKE, FAKE, FAKE, None) == q8.Q8_ERR_INVALID_ARG   # z_a given for symmetric
+    assert q(FAKE, 4, 32, 1, 1, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG   # z_a missing for asymmetric
+    assert q(FAKE, 4, 32, 1, 2, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG   # bad symmetry
+    assert q(FAKE, 4, 32, 5, 0, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG   # bad granularity
+    assert q(None, 4, 32, 1, 0, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert q(FAKE, 4, 24, 1, 0, FAKE, FAKE, None, None) == q8.Q8_ERR_UNSUPPORTED
+    assert q(MISALIGNED, 4, 32, 1, 0, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert q(FAKE, 0, 32, 1, 0, FAKE, FAKE, None, None) == q8.Q8_OK
+    w = lib.q8_quantize_weight
+    assert w(FAKE, 4, 32, 1, None, FAKE, None) == q8.Q8_ERR_INVALID_ARG
+    assert w(FAKE, 4, 40, 1, FAKE, FAKE, None) == q8.Q8_ERR_UNSUPPORTED
+    assert lib.q8_colsum(FAKE, 4, 32, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert lib.q8_colsum(FAKE, 4, 20, FAKE, None) == q8.Q8_ERR_UNSUPPORTED
+
+
+def test_kernel_pick_is_a_concrete_kernel(lib):
+    import int8_quantized_gemm_gb300 as q8
+    for shape in ((16, 28672, 8192), (8192, 8192, 16384), (1, 1, 16), (513, 100, 48)):
+        assert q8.q8_gemm_pick(*shape) in ("tcgen05", "mma_s8", "skinny")
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import int8_quantized_gemm_gb300 as q8
+    with pytest.raises(ValueError):
+        q8.q8_quantize_act(torch.zeros(4, 32))

@@ -1,0 +1,293 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer results (codes, zero points, column sums, INT32 accumulators) and the
+fp32 scales must be bit-identical; y must be within 2 ulp (the kernels use the
+oracle's operation order, so 0 ulp is expected). Inputs are seeded, synthetic
+and shaped like the workloads in workloads.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gates
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ("tcgen05", "mma_s8", "skinny")
+
+
+@pytest.fixture(scope="module")
+def q8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import int8_quantized_gemm_gb300 as q8mod
+    from int8_quantized_gemm_gb300 import build
+    build.build()
+    q8mod.load()
+    return q8mod
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def assert_no_device_error(q8):
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+
+
+def max_ulp(a, b):
+    return int(gates.ulp_distance(a, b).max()) if a.size else 0
+
+
+# ---------------------------------------------------------------- quantizers
+
+QUANT_CASES = [
+    # (M, K, per_row, symmetric, maker)
+    (16, 256, False, True, "tiny"),
+    (512, 2048, True, True, "prefill2k"),
+    (2048, 4096, True, False, "relu4k"),
+    (16, 8192, True, True, "decode"),
+    (64, 16384, True, True, "prefill16k"),
+    (37, 528, True, False, "prefill2k"),       # ragged K per thread block
+    (5, 40000, True, True, "prefill2k"),       # rows longer than the register budget
+    (3, 40000, True, False, "relu4k"),
+    (300, 48, False, False, "relu4k"),         # per-tensor asymmetric
+    (1, 16, True, True, "tiny"),
+    (7, 1040, False, True, "prefill2k"),
+]
+
+
+@pytest.mark.parametrize("M,K,per_row,sym,name", QUANT_CASES)
+def test_quantize_act_bit_exact(q8, M, K, per_row, sym, name):
+    a = workloads.make_activations(workloads.WORKLOADS[name], M=M, K=K)
+    a[M // 2] = 0.0                                     # an all-zero row (padding token)
+    if M > 2:
+        a[1] = -np.abs(a[1])                            # a non-positive row
+    qa, s_a, z_a = q8.q8_quantize_act(dev(a), per_row=per_row, symmetric=sym)
+    if sym:
+        rq, rs = oracle.quantize_sym(a, per_row)
+    else:
+        rq, rs, rz = oracle.quantize_asym(a, per_row)
+        np.testing.assert_array_equal(host(z_a), rz)
+    np.testing.assert_array_equal(host(s_a), rs)
+    np.testing.assert_array_equal(host(qa), rq)
+
+
+def test_rounding_ties_on_gpu(q8):
+    x = np.array([[127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, -1.5, -127.0] + [0.0] * 7,
+                  [0.881577730178833, 0.7115095853805542] + [0.0] * 14,
+                  [3.754473924636841, 0.10346975177526474] + [0.0] * 14], np.float32)
+    qa, s_a, _ = q8.q8_quantize_act(dev(x), per_row=True)
+    q = host(qa)
+    assert q[0, :9].tolist() == [127, 2, 4, -2, 0, 2, 0, -2, -127]
+    assert q[1, 1] == 102 and q[2, 1] == 4
+
+
+@pytest.mark.parametrize("per_row", [True, False])
+@pytest.mark.parametrize("N,K", [(128, 256), (2048, 2048), (1000, 4112)])
+def test_quantize_weight_and_colsum_bit_exact(q8, per_row, N, K):
+    w = workloads.make_weights(workloads.WORKLOADS["prefill2k"], N=N, K=K)
+    qw, s_w = q8.q8_quantize_weight(dev(w), per_row=per_row)
+    cs = q8.q8_colsum(qw)
+    rq, rs = oracle.quantize_sym(w, per_row)
+    np.testing.assert_array_equal(host(s_w), rs)
+    np.testing.assert_array_equal(host(qw), rq)
+    np.testing.assert_array_equal(host(cs).astype(np.int64), oracle.colsum(rq))
+
+
+def test_colsum_extreme_codes(q8):
+    qw = np.full((9, 131056), -128, np.int8)
+    qw[3] = 127
+    cs = q8.q8_colsum(dev(qw))
+    np.testing.assert_array_equal(host(cs).astype(np.int64), oracle.colsum(qw))
+
+
+# ---------------------------------------------------------------- integer GEMM
+
+GEMM_SHAPES = [
+    (1, 1, 16), (16, 128, 256), (128, 256, 1024), (200, 264, 1088), (129, 257, 1040),
+    (300, 520, 2064), (17, 1000, 4096), (256, 512, 3072), (64, 96, 48),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_s32_bit_exact(q8, kernel, M, N, K):
+    qa = workloads.random_codes((M, K), seed=M * 7 + K)
+    qw = workloads.random_codes((N, K), seed=N * 11 + K)
+    acc = q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(host(acc).astype(np.int64), oracle.gemm_acc(qa, qw, threads=8))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gemm_s32_extreme_codes(q8, kernel):
+    """-128 * -128 products everywhere: every fp32 chunk sum sits exactly on 2^24."""
+    M, N, K = 160, 300, 16384
+    qa = np.full((M, K), -128, np.int8)
+    qw = np.full((N, K), -128, np.int8)
+    qw[1::2] = 127
+    acc = host(q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)).astype(np.int64)
+    assert_no_device_error(q8)
+    expect = np.where(np.arange(N) % 2 == 0, K * 16384, -K * 128 * 127)
+    np.testing.assert_array_equal(acc, np.broadcast_to(expect, (M, N)))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gemm_s32_small_terms_next_to_large_partial_sums(q8, kernel):
+    """Each 1024-deep chunk first climbs to ~2^24 with -128*-128 products, then adds +-1
+    and +-127 terms: an accumulator that kept fewer than 24 significant bits would drop them."""
+    M, N, K = 130, 260, 4096
+    rng = np.random.Generator(np.random.PCG64(5))
+    qa = np.zeros((M, K), np.int8)
+    qw = np.zeros((N, K), np.int8)
+    for c0 in range(0, K, 1024):
+        big = 1000
+        qa[:, c0:c0 + big] = -128
+        qw[:, c0:c0 + big] = -128
+        qa[:, c0 + big:c0 + 1024] = rng.integers(-128, 128, size=(M, 1024 - big))
+        qw[:, c0 + big:c0 + 1024] = rng.choice(np.array([-1, 1, 127, -127], np.int8), size=(N, 1024 - big))
+    acc = host(q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)).astype(np.int64)
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(acc, oracle.gemm_acc(qa, qw, threads=8))
+
+
+# ---------------------------------------------------------------- GEMM + epilogue
+
+LAYER_CASES = [
+    # name, M, N, K, act_per_row, act_sym, w_per_row
+    ("tiny", 16, 128, 256, False, True, False),
+    ("prefill2k", 200, 264, 1088, True, True, True),
+    ("relu4k", 333, 520, 2048, True, False, True),
+    ("decode", 16, 1000, 8192, True, True, True),
+    ("relu4k", 129, 256, 1040, False, False, True),
+    ("prefill2k", 64, 300, 528, True, True, False),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name,M,N,K,apr,asym_is_sym,wpr", LAYER_CASES)
+def test_linear_layer_matches_oracle(q8, kernel, name, M, N, K, apr, asym_is_sym, wpr):
+    wl = workloads.WORKLOADS[name]
+    a = workloads.make_activations(wl, M=M, K=K)
+    w = workloads.make_weights(wl, N=N, K=K)
+    ref = oracle.linear(a, w, apr, asym_is_sym, wpr, threads=8)
+    assert ref["status"] == oracle.OK
+    qw, s_w = q8.q8_quantize_weight(dev(w), per_row=wpr)
+    cs = q8.q8_colsum(qw)
+    qa, s_a, z_a = q8.q8_quantize_act(dev(a), per_row=apr, symmetric=asym_is_sym)
+    y = host(q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, cs, kernel=kernel))
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(host(qa), ref["qa"])
+    assert max_ulp(y, ref["y"]) <= 2
+    # and the layer still honours the page's per-column gate against fp64
+    if wpr:
+        err = np.abs(y - gates.reference_fp64(a, w))
+        assert gates.first_violation(err, gates.column_gate_atol(a, w, apr)) is None
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_epilogue_with_random_scales_and_zero_points(q8, kernel):
+    M, N, K = 150, 280, 1536
+    qa = workloads.random_codes((M, K), seed=40)
+    qw = workloads.random_codes((N, K), seed=41, lo=-127)
+    sa = workloads.random_scales(M, seed=42)
+    sw = workloads.random_scales(N, seed=43)
+    za = workloads.random_zero_points(M, seed=44)
+    cs = oracle.colsum(qw).astype(np.int32)
+    y = host(q8.q8_gemm_dequant(dev(qa), dev(sa), dev(za), dev(qw), dev(sw), dev(cs), kernel=kernel))
+    ry, st = oracle.linear_codes(qa, sa, za, qw, sw, True, True, threads=8)
+    assert st == oracle.OK
+    assert max_ulp(y, ry) <= 2
+
+
+def test_empty_problems(q8):
+    z = torch.zeros(0, 32, dtype=torch.int8, device="cuda")
+    w = torch.zeros(8, 32, dtype=torch.int8, device="cuda")
+    s = torch.ones(8, dtype=torch.float32, device="cuda")
+    y = q8.q8_gemm_dequant(z, torch.ones(1, device="cuda"), None, w, s)
+    assert y.shape == (0, 8)
+    qa0 = torch.zeros(4, 0, dtype=torch.int8, device="cuda")
+    qw0 = torch.zeros(8, 0, dtype=torch.int8, device="cuda")
+    y0 = q8.q8_gemm_dequant(qa0, torch.ones(4, device="cuda"), None, qw0, s)
+    assert torch.count_nonzero(y0).item() == 0 and not torch.signbit(y0).any()
+    qa, s_a, _ = q8.q8_quantize_act(torch.zeros(3, 0, device="cuda"))
+    assert torch.all(s_a == torch.tensor(np.float32(np.float32(1e-8) / np.float32(127)), device="cuda"))
+
+
+def test_launch_counter_counts_our_kernels(q8):
+    before = q8.q8_launch_count()
+    a = torch.randn(64, 256, device="cuda")
+    qa, s_a, _ = q8.q8_quantize_act(a)
+    qw, s_w = q8.q8_quantize_weight(torch.randn(128, 256, device="cuda"))
+    q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, kernel="tcgen05")
+    assert q8.q8_launch_count() - before == 3
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+FULL = ["tiny", "prefill2k", "relu4k", "decode", "prefill16k"]
+
+
+def _sample_pairs(M, N, count, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ms = np.concatenate([rng.integers(0, M, count), [0, M - 1, 0, M - 1, min(127, M - 1), min(128, M - 1)]])
+    ns = np.concatenate([rng.integers(0, N, count), [0, N - 1, N - 1, 0, min(255, N - 1), min(256, N - 1)]])
+    return ms.astype(np.int64), ns.astype(np.int64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(q8, name):
+    """The bench's launch configuration (kernel chosen by q8_gemm_pick) at the workload's full
+    size: every code, scale and zero point bit-exact, y and INT32 acc on sampled outputs."""
+    wl = workloads.WORKLOADS[name]
+    a = workloads.make_activations(wl)
+    w = workloads.make_weights(wl)
+    apr, wpr = wl.act_granularity == "row", wl.w_granularity == "row"
+    if wl.act_symmetric:
+        (rqa, rsa), rza = oracle.quantize_sym(a, apr), None
+    else:
+        rqa, rsa, rza = oracle.quantize_asym(a, apr)
+    rqw, rsw = oracle.quantize_sym(w, wpr)
+    a_d, w_d = dev(a), dev(w)
+    del a
+    qw, s_w = q8.q8_quantize_weight(w_d, per_row=wpr)
+    del w_d
+    cs = q8.q8_colsum(qw)
+    qa, s_a, z_a = q8.q8_quantize_act(a_d, per_row=apr, symmetric=wl.act_symmetric)
+    y = q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, cs)
+    acc = q8.q8_gemm_s32(qa, qw)
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(host(s_a), rsa)
+    np.testing.assert_array_equal(host(qa), rqa)
+    if rza is not None:
+        np.testing.assert_array_equal(host(z_a), rza)
+    np.testing.assert_array_equal(host(s_w), rsw)
+    np.testing.assert_array_equal(host(qw), rqw)
+    np.testing.assert_array_equal(host(cs).astype(np.int64), oracle.colsum(rqw))
+    ms, ns = _sample_pairs(wl.M, wl.N, 3000, seed=wl.seed)
+    ry, racc, st = oracle.linear_codes_at(rqa, rsa, rza, rqw, rsw, ms, ns, apr, wpr)
+    assert st == oracle.OK
+    yt, acct = torch.as_tensor(ms).cuda(), torch.as_tensor(ns).cuda()
+    np.testing.assert_array_equal(host(acc[yt, acct]).astype(np.int64), racc)
+    assert max_ulp(host(y[yt, acct]), ry) <= 2
+
+
+@pytest.mark.slow
+def test_full_size_worst_case_codes(q8):
+    """Large prefill shape with raw codes at the int8 extremes: every acc equals the closed
+    form, K * (-128) * (-127), the accumulator bound of Day 98."""
+    wl = workloads.WORKLOADS["prefill16k"]
+    qa = torch.full((wl.M, wl.K), -128, dtype=torch.int8, device="cuda")
+    qw = torch.full((wl.N, wl.K), -127, dtype=torch.int8, device="cuda")
+    acc = q8.q8_gemm_s32(qa, qw)
+    assert_no_device_error(q8)
+    assert torch.all(acc == wl.K * 16256).item()
+    assert wl.K * 16256 == 266338304
