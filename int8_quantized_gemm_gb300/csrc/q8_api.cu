@@ -58,8 +58,13 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         kernel != Q8_GEMM_SKINNY)
         return Q8_ERR_INVALID_ARG;
     const bool epilogue = (out_i32 == nullptr);
+    if (epilogue && (!valid_gran(ga) || !valid_gran(gw))) return Q8_ERR_INVALID_ARG;
+    {
+        q8_status kst = check_k(K, epilogue && z_a != nullptr);
+        if (kst != Q8_OK) return kst;
+    }
+    if (M == 0 || N == 0) return Q8_OK;   // empty output: nothing is read or written
     if (epilogue) {
-        if (!valid_gran(ga) || !valid_gran(gw)) return Q8_ERR_INVALID_ARG;
         if (!s_a || !s_w || !y) return Q8_ERR_INVALID_ARG;
         if (!aligned(s_a, 4) || !aligned(s_w, 4) || !aligned(y, 16)) return Q8_ERR_INVALID_ARG;
         if (z_a && (!colsum || !aligned(z_a, 4) || !aligned(colsum, 4))) return Q8_ERR_INVALID_ARG;
@@ -69,10 +74,7 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
     if (M > 0 && N > 0 && K > 0) {
         if (!qa || !qw || !aligned(qa, 16) || !aligned(qw, 16)) return Q8_ERR_INVALID_ARG;
     }
-    q8_status st = check_k(K, epilogue && z_a != nullptr);
-    if (st != Q8_OK) return st;
     if (M > INT32_MAX || N > INT32_MAX) return Q8_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0) return Q8_OK;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) {
@@ -144,6 +146,10 @@ q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* 
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,
                          q8_gemm_kernel kernel, q8_stream_t stream) {
     if (!acc && M > 0 && N > 0) return Q8_ERR_INVALID_ARG;
+    if (!acc) {  // empty output
+        if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+        return check_k(K, false);
+    }
     return gemm_common(qa, nullptr, nullptr, Q8_PER_TENSOR, qw, nullptr, Q8_PER_TENSOR, nullptr, M, N, K,
                        nullptr, acc, kernel, stream);
 }

@@ -342,8 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 in[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) in[j] = *reinterpret_cast<const uint4*>(st8 + (ct + kConv * j) * 16);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty8 + 8 * s8);
             if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty)) break;
             uint8_t* st16 = smem + s16 * kStage16;
 #pragma unroll
@@ -360,6 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(bar_full16 + 8 * s16);
+            // Release the staging slot only now: the converted values were built from
+            // every loaded register, so the shared-memory reads have completed. (An
+            // arrive right after issuing the loads let the next TMA write, which is
+            // not ordered after pending generic-proxy reads, land first.)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty8 + 8 * s8);
         }
       }
     } else {

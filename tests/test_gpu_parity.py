@@ -126,6 +126,21 @@ def test_gemm_s32_bit_exact(q8, kernel, M, N, K):
     np.testing.assert_array_equal(host(acc).astype(np.int64), oracle.gemm_acc(qa, qw, threads=8))
 
 
+@pytest.mark.parametrize("M,N,K,reps", [(1024, 1024, 4096, 10), (2048, 2048, 8192, 4)])
+def test_gemm_s32_repeatable_under_load(q8, M, N, K, reps):
+    """Many tiles per CTA and deep K: every repetition must be bit-exact. Pipeline races
+    (a staging slot refilled before its reads completed) show up here as whole tile rows
+    whose k-block was replaced by a later one."""
+    qa = workloads.random_codes((M, K), seed=M * 7 + K)
+    qw = workloads.random_codes((N, K), seed=N * 11 + K)
+    ref = oracle.gemm_acc(qa, qw, threads=16)
+    da, dw = dev(qa), dev(qw)
+    for _ in range(reps):
+        acc = host(q8.q8_gemm_s32(da, dw, kernel="tcgen05")).astype(np.int64)
+        assert_no_device_error(q8)
+        np.testing.assert_array_equal(acc, ref)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_gemm_s32_extreme_codes(q8, kernel):
     """-128 * -128 products everywhere: every fp32 chunk sum sits exactly on 2^24."""
