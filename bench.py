@@ -53,62 +53,74 @@ def peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """Samples the SM clock and the clock-event (throttle) reasons through NVML about every
+    millisecond while the timed region runs (reads only; nothing is set)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    def __init__(self, cuda_index: int):
+        self.samples = []
+        self.max_mhz = None
+        self.stop = threading.Event()
         self.thread = None
+        self.nvml = None
+        try:
+            import ctypes
+            import torch
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            ok = False
+            uuid = getattr(torch.cuda.get_device_properties(cuda_index), "uuid", None)
+            if uuid is not None:
+                ok = nvml.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(handle)) == 0
+            if not ok:
+                count = ctypes.c_uint()
+                nvml.nvmlDeviceGetCount_v2(ctypes.byref(count))
+                if count.value == 1:
+                    ok = nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) == 0
+            if not ok:
+                return
+            self.nvml, self.handle, self.ct = nvml, handle, ctypes
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except Exception:
+            self.nvml = None
+
+    def _run(self):
+        ct, nvml, h = self.ct, self.nvml, self.handle
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if nvml.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and get_reasons(h, ct.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.001)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
-        except Exception:
-            self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            if self.thread:
-                self.thread.join(timeout=2)
+        self.stop.set()
+        if self.thread:
+            self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 6:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[2:6]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
 
 
 def dist_setup():
@@ -226,30 +238,10 @@ def run_ours(args, world, rank, local):
     gemm_bytes = M * K + N * K + 4 * N + 4 * M + 4 * M * N
 
     # ---- end to end through the public API: pinned host A in, y back to pinned host
-    a_host = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
-    a_host.copy_(a.cpu())
-    y_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
-    e2e_steps = max(1, min(args.steps, 5))
-    for _ in range(2):
-        a.copy_(a_host, non_blocking=True)
-        step()
-        y_host.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    ee0 = torch.cuda.Event(enable_timing=True)
-    ee1 = torch.cuda.Event(enable_timing=True)
-    ee0.record(stream)
-    for _ in range(e2e_steps):
-        a.copy_(a_host, non_blocking=True)
-        step()
-        y_host.copy_(y, non_blocking=True)
-    ee1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(ee0.elapsed_time(ee1) / e2e_steps, world)
-    e2e_value = ops * world / (e2e_ms * 1e-3) / 1e12
+    e2e = None if args.no_e2e else measure_e2e(a, y, step, ops, world, args)
 
     # ---- decode-shaped workload (HBM-bound): same step, reported beside the headline
-    decode = measure_decode(q8, device, args, hbm_peak, flush)
+    decode = None if args.no_decode else measure_decode(q8, device, args, hbm_peak, flush)
 
     cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
@@ -270,8 +262,7 @@ def run_ours(args, world, rank, local):
             "quantizer": {"ms": round(quant_avg, 4), "GB/s": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
                           "bytes": quant_bytes},
             "decode": decode,
-            "e2e": {"value": round(e2e_value, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K * 4,
-                    "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 3)},
+            "e2e": e2e,
             "gpu_launches": int(launches),
             "weight_prep_ms": round(weight_prep_ms, 3),
             "clocks": clocks.summary(),
@@ -281,7 +272,39 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line))
 
 
+def measure_e2e(a, y, step, ops, world, args):
+    """The same step through the public API with the inputs in pinned host memory: the H2D
+    copy of A and the D2H copy of y are inside the timed region."""
+    import torch
+    M, K = a.shape
+    N = y.shape[1]
+    a_host = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
+    a_host.copy_(a.cpu())
+    y_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        a.copy_(a_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    steps = max(1, min(args.steps, 5))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        a.copy_(a_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return {"value": round(ops * world / (ms * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K * 4,
+            "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(ms, 3)}
+
+
 def measure_decode(q8, device, args, hbm_peak, flush):
+    """Decode-shaped workload (16 tokens, HBM-bound): the step with each GEMM kernel."""
     import torch
     wl, a, w = layer_inputs(DECODE, device)
     M, N, K = wl.M, wl.N, wl.K
@@ -290,32 +313,44 @@ def measure_decode(q8, device, args, hbm_peak, flush):
     qa = torch.empty((M, K), dtype=torch.int8, device=device)
     s_a = torch.empty(M, dtype=torch.float32, device=device)
     y = torch.empty((M, N), dtype=torch.float32, device=device)
-    kernel = q8.q8_gemm_pick(M, N, K)
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
-        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
-    torch.cuda.synchronize()
-    q_ms, g_ms = [], []
-    for _ in range(max(10, args.steps)):
-        flush.zero_()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record()
-        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
-        e[1].record()
-        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
-        e[2].record()
-        torch.cuda.synchronize()
-        q_ms.append(e[0].elapsed_time(e[1]))
-        g_ms.append(e[1].elapsed_time(e[2]))
-    gq = statistics.mean(g_ms)
-    step = statistics.mean(q_ms) + gq
+    pick = q8.q8_gemm_pick(M, N, K)
     gemm_bytes = N * K + M * K + 4 * N + 4 * M + 4 * M * N
-    return {"workload": f"{DECODE}: A [{M},{K}] x W int8 [{N},{K}]", "gemm_kernel": kernel,
+
+    def timed(kernel):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, kernel=kernel)
+        torch.cuda.synchronize()
+        q_ms, g_ms = [], []
+        for _ in range(max(10, args.steps)):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+            e[1].record()
+            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, kernel=kernel)
+            e[2].record()
+            torch.cuda.synchronize()
+            q_ms.append(e[0].elapsed_time(e[1]))
+            g_ms.append(e[1].elapsed_time(e[2]))
+        return statistics.mean(q_ms), statistics.mean(g_ms)
+
+    per_kernel = {}
+    quant_ms = gq = None
+    for kernel in ("tcgen05", "skinny", "mma_s8"):
+        qm, gm = timed(kernel)
+        per_kernel[kernel] = {"gemm_ms": round(gm, 4),
+                              "gemm_frac_hbm": round(gemm_bytes / (gm * 1e-3) / 1e9 / hbm_peak, 4)}
+        if kernel == pick:
+            quant_ms, gq = qm, gm
+    step = quant_ms + gq
+    return {"workload": f"{DECODE}: A [{M},{K}] x W int8 [{N},{K}]", "gemm_kernel": pick,
             "ms_per_step": round(step, 4), "TOPS": round(2.0 * M * N * K / (step * 1e-3) / 1e12, 2),
-            "gemm_ms": round(gq, 4), "gemm_GB/s": round(gemm_bytes / (gq * 1e-3) / 1e9, 1),
+            "quant_ms": round(quant_ms, 4), "gemm_ms": round(gq, 4),
+            "gemm_GB/s": round(gemm_bytes / (gq * 1e-3) / 1e9, 1),
             "gemm_frac_hbm": round(gemm_bytes / (gq * 1e-3) / 1e9 / hbm_peak, 4),
-            "algorithmic_bytes": gemm_bytes}
+            "algorithmic_bytes": gemm_bytes, "per_kernel": per_kernel}
 
 
 # ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
@@ -399,9 +434,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped workload")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
