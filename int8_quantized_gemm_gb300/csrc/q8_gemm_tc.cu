@@ -200,6 +200,21 @@ __device__ __forceinline__ void cvt_word(uint32_t w, uint32_t& lo, uint32_t& hi)
     hi = hsub_1152(((w >> 8) & 0x00FF00FFu) ^ 0x64806480u);
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 // Byte offset of fp16 16-byte chunk j (0..7) of row r in a 128B-swizzled K-major tile.
 __device__ __forceinline__ uint32_t sw128(int r, int j) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
@@ -335,26 +350,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [A | W] in one run of 128-byte swizzled rows, so row r of the
         // combined staging tile lands at sw128(r, .) for both operands.
         const int ct = threadIdx.x - 64;
+        // Chunk j of this thread is idx = ct + 192 j: staging byte idx * 16, fp16 row
+        // r = ct / 4 + 48 j with (r & 7) independent of j, so both addresses are a
+        // per-thread base plus a constant stride (3072 and 6144 bytes).
+        const int r0 = ct >> 2, c0 = ct & 3;
+        const uint32_t src0 = (uint32_t)(ct * 16);
+        const uint32_t dst0 = sw128(r0, 2 * c0);
+        const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
             if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull)) break;
-            const uint8_t* st8 = smem + kOffStage8 + s8 * kStage8;
+            const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
             uint4 in[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) in[j] = *reinterpret_cast<const uint4*>(st8 + (ct + kConv * j) * 16);
+            for (int j = 0; j < 8; ++j) in[j] = lds128(st8 + kConv * 16 * j);
             if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty)) break;
-            uint8_t* st16 = smem + s16 * kStage16;
+            const uint32_t st16 = sbase + s16 * kStage16;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int idx = ct + kConv * j;
-                const int r = idx >> 2, c = idx & 3;
                 uint4 o0, o1;
                 cvt_word(in[j].x, o0.x, o0.y);
                 cvt_word(in[j].y, o0.z, o0.w);
                 cvt_word(in[j].z, o1.x, o1.y);
                 cvt_word(in[j].w, o1.z, o1.w);
-                *reinterpret_cast<uint4*>(st16 + sw128(r, 2 * c)) = o0;
-                *reinterpret_cast<uint4*>(st16 + sw128(r, 2 * c + 1)) = o1;
+                sts128(st16 + dst0 + 6144 * j, o0);
+                sts128(st16 + dst1 + 6144 * j, o1);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar_full16 + 8 * s16);
@@ -413,16 +433,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
                     float* row = ep.y + (int64_t)m * N;
                     const bool vec = ((N & 3) == 0);
+                    // per-channel scales and column sums four at a time when they are 16-byte aligned
+                    const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
+                    const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
 #pragma unroll
                     for (int e4 = 0; e4 < 32; ++e4) {
                         const int n = nb + e4 * 4;
+                        const bool full = n + 3 < N;
+                        float sw4[4];
+                        int cs4[4] = {0, 0, 0, 0};
+                        if (vsw && full) {
+                            const float4 t = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
+                            sw4[0] = t.x; sw4[1] = t.y; sw4[2] = t.z; sw4[3] = t.w;
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
+                        }
+                        if (ep.z_a) {
+                            if (vcs && full) {
+                                const int4 t = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
+                                cs4[0] = t.x; cs4[1] = t.y; cs4[2] = t.z; cs4[3] = t.w;
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
+                            }
+                        }
                         float o[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const int nn = n + q < N ? n + q : 0;
-                            const int corr = ep.z_a ? acc[e4 * 4 + q] - za * __ldg(ep.colsum + nn) : acc[e4 * 4 + q];
-                            const float sc = __fmul_rn(sa, __ldg(ep.s_w + (ep.w_per_row ? nn : 0)));
-                            o[q] = __fmul_rn(__int2float_rn(corr), sc);
+                            const int corr = acc[e4 * 4 + q] - za * cs4[q];
+                            o[q] = __fmul_rn(__int2float_rn(corr), __fmul_rn(sa, sw4[q]));
                         }
                         if (vec && n + 3 < N) {
                             *reinterpret_cast<float4*>(row + n) = make_float4(o[0], o[1], o[2], o[3]);

@@ -71,7 +71,7 @@ __device__ __forceinline__ void block_max2(float& hi, float& nlo, float* red) {
 // One CTA per row; each thread keeps up to VPT float4 of the row in registers.
 // Requires cols % 4 == 0 and cols / 4 <= VPT * blockDim.x.
 template <int VPT, bool ASYM>
-__global__ void __launch_bounds__(512) quantize_rows_kernel(const float* __restrict__ x, int64_t cols,
+__global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel(const float* __restrict__ x, int64_t cols,
                                                             int8_t* __restrict__ q,
                                                             float* __restrict__ s,
                                                             int32_t* __restrict__ z) {
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(512) quantize_rows_kernel(const float* __restr
 // Rows longer than the register budget: reduce in one sweep, code in a second
 // sweep (the second read of the row is served mostly by L2).
 template <bool ASYM>
-__global__ void __launch_bounds__(512) quantize_long_rows_kernel(const float* __restrict__ x, int64_t cols,
+__global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* __restrict__ x, int64_t cols,
                                                                  int8_t* __restrict__ q,
                                                                  float* __restrict__ s,
                                                                  int32_t* __restrict__ z) {
@@ -281,13 +281,13 @@ cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, int8_t* q,
         t = ((t + kWarp - 1) / kWarp) * kWarp;
         return (int)(t < kWarp ? kWarp : t);
     };
-    if (n4 <= 128 * 1) return launch_rows<1, ASYM>(x, rows, cols, threads_for(1), q, s, z, st);
-    if (n4 <= 256 * 2) return launch_rows<2, ASYM>(x, rows, cols, threads_for(2), q, s, z, st);
-    if (n4 <= 256 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
-    if (n4 <= 512 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
-    if (n4 <= 512 * 8) return launch_rows<8, ASYM>(x, rows, cols, threads_for(8), q, s, z, st);
-    if (n4 <= 512 * 16) return launch_rows<16, ASYM>(x, rows, cols, threads_for(16), q, s, z, st);
-    quantize_long_rows_kernel<ASYM><<<(unsigned)rows, 512, 0, st>>>(x, cols, q, s, z);
+    // Up to 1024 threads per row and at most 4 float4 per thread keeps the kernel at
+    // <= 32 registers, so two 1024-thread blocks (a full SM) stay resident.
+    if (n4 <= 1024 * 1) return launch_rows<1, ASYM>(x, rows, cols, threads_for(1), q, s, z, st);
+    if (n4 <= 1024 * 2) return launch_rows<2, ASYM>(x, rows, cols, threads_for(2), q, s, z, st);
+    if (n4 <= 1024 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
+    if (n4 <= 1024 * 8) return launch_rows<8, ASYM>(x, rows, cols, threads_for(8), q, s, z, st);
+    quantize_long_rows_kernel<ASYM><<<(unsigned)rows, 1024, 0, st>>>(x, cols, q, s, z);
     note_launch();
     return cudaGetLastError();
 }
