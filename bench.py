@@ -338,7 +338,7 @@ def measure_decode(q8, device, args, hbm_peak, flush):
 
     per_kernel = {}
     quant_ms = gq = None
-    for kernel in ("tcgen05", "skinny", "mma_s8"):
+    for kernel in ("decode", "tcgen05", "skinny", "mma_s8"):
         qm, gm = timed(kernel)
         per_kernel[kernel] = {"gemm_ms": round(gm, 4),
                               "gemm_frac_hbm": round(gemm_bytes / (gm * 1e-3) / 1e9 / hbm_peak, 4)}

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libq8.so")
-SOURCES = ["q8_api.cu", "q8_quant.cu", "q8_gemm_mma.cu", "q8_gemm_tc.cu"]
+SOURCES = ["q8_api.cu", "q8_quant.cu", "q8_gemm_mma.cu", "q8_gemm_tc.cu", "q8_gemv_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,6 +40,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "q8_internal.h"),
+                                                      os.path.join(CSRC, "q8_tc_ptx.cuh"),
                                                       os.path.join(ROOT, "include", "q8.h"),
                                                       os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)

@@ -37,12 +37,16 @@
 #include <stdint.h>
 
 #include "q8_internal.h"
+#include "q8_tc_ptx.cuh"
 
 namespace q8 {
 
-__device__ unsigned int g_tc_error;
+// Device error word of this kernel (one per device): bits name the bounded wait that gave up.
+static __device__ unsigned int g_tc_error;
 
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
@@ -63,162 +67,8 @@ constexpr int kOffBar = kOffStage8 + S8 * kStage8;
 constexpr int kBarBytes = 8 * (2 * S8 + 2 * S16 + 4) + 16;
 constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
 
-constexpr long long kTimeoutCycles = 1LL << 31;    // about a second
-
-enum : unsigned {
-    kErrProducer = 1u,
-    kErrConvFull = 2u,
-    kErrConvEmpty = 4u,
-    kErrMmaFull = 8u,
-    kErrMmaAcc = 16u,
-    kErrDrain = 32u
-};
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity. Returns false if the
-// kernel is aborting (another role gave up) or this wait ran out of time.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned code) {
-    if (mbar_try(bar, parity)) return true;
-    long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
-                *abort_flag = 1;
-                atomicOr(&g_tc_error, code);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes in 8-row atoms of 1024 bytes (stride between atoms 1024 bytes).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;             // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;             // 128-byte swizzle
-    return d;
-}
-
 // Instruction descriptor of kind::f16: fp16 A and B, both K-major, fp32 D, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-}
-
-// int8 x 4 (one 32-bit word, bytes x0..x3) -> two fp16x2 words holding exactly
-// (x0, x2) and (x1, x3). The K order inside each group of four is permuted
-// the same way for A and W, which leaves every dot product unchanged.
-// Bits 0x64 | (x ^ 0x80) form the fp16 value 1024 + (x + 128); subtracting
-// 1152 (0x6480) leaves x exactly.
-__device__ __forceinline__ uint32_t hsub_1152(uint32_t v) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(v), "r"(0x64806480u));
-    return r;
-}
-__device__ __forceinline__ void cvt_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    lo = hsub_1152((w & 0x00FF00FFu) ^ 0x64806480u);
-    hi = hsub_1152(((w >> 8) & 0x00FF00FFu) ^ 0x64806480u);
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
-// Byte offset of fp16 16-byte chunk j (0..7) of row r in a 128B-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128(int r, int j) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
-}
+constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 
 struct TileGeom {
     int num_m, num_n, tiles;
@@ -273,10 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     }
     tc_fence_before();
     __syncthreads();
@@ -302,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kb == 0) tile_coords(tg, blockIdx.x + i * gridDim.x, m0, n0);
                 const int s = g % S8;
                 const uint32_t par = (uint32_t)((g / S8) & 1);
-                if (!mbar_wait(bar_empty8 + 8 * s, par ^ 1u, abort_flag, kErrProducer)) break;
+                if (!mbar_wait(bar_empty8 + 8 * s, par ^ 1u, abort_flag, kErrProducer, &g_tc_error)) break;
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
                 mbar_expect_tx(bar_full8 + 8 * s, kStage8);
                 tma_load_2d(dst, &tmap_a, kb * BK, m0, bar_full8 + 8 * s);
@@ -319,12 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool last = (kb % KB_PER_CHUNK) == KB_PER_CHUNK - 1 || kb == KB - 1;
                 const int buf = c & 1;
                 if (first) {
-                    if (!mbar_wait(bar_accempty + 8 * buf, (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag, kErrMmaAcc))
+                    if (!mbar_wait(bar_accempty + 8 * buf, (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag, kErrMmaAcc, &g_tc_error))
                         break;
                     tc_fence_after();
                 }
                 const int s = g % S16;
-                if (!mbar_wait(bar_full16 + 8 * s, (uint32_t)((g / S16) & 1), abort_flag, kErrMmaFull)) break;
+                if (!mbar_wait(bar_full16 + 8 * s, (uint32_t)((g / S16) & 1), abort_flag, kErrMmaFull, &g_tc_error)) break;
                 tc_fence_after();
                 const uint32_t a_addr = sbase + s * kStage16;
                 const uint64_t adesc = smem_desc_sw128(a_addr);
@@ -333,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // advance 16 fp16 = 32 bytes along K inside the swizzled rows
-                    mma_f16(d, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), (first && kk == 0) ? 0u : 1u);
+                    mma_f16(d, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), kIdesc, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(bar_empty16 + 8 * s);
                 if (last) {
@@ -359,12 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
-            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull)) break;
+            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc_error)) break;
             const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
             uint4 in[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) in[j] = lds128(st8 + kConv * 16 * j);
-            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty)) break;
+            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty, &g_tc_error)) break;
             const uint32_t st16 = sbase + s16 * kStage16;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -398,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ti = 0, cc = 0;    // tile (in this CTA's sequence) and chunk within it
         for (int c = 0; c < chunks_total; ++c, (++cc == CPT ? (cc = 0, ++ti) : 0)) {
             const int buf = c & 1;
-            if (!mbar_wait(bar_accfull + 8 * buf, (uint32_t)((c >> 1) & 1), abort_flag, kErrDrain)) break;
+            if (!mbar_wait(bar_accfull + 8 * buf, (uint32_t)((c >> 1) & 1), abort_flag, kErrDrain, &g_tc_error)) break;
             tc_fence_after();
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + col_half * 128);
@@ -489,11 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem_base), "r"(kTmemCols)
-                     : "memory");
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
+}  // namespace
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -507,14 +356,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// 2-D int8 tensor map over a row-major [rows, K] matrix, box [box_rows, BK],
+// 2-D int8 tensor map over a row-major [rows, K] matrix, box [box_rows, box_k],
 // no swizzle (the staging tile is read by ordinary loads), zero fill outside.
-bool make_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows) {
+bool make_map_impl(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -522,7 +371,7 @@ bool make_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int
     return r == CUDA_SUCCESS;
 }
 
-int sm_count() {
+int sm_count_impl() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -530,6 +379,12 @@ int sm_count() {
 }
 
 }  // namespace
+
+bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k) {
+    return make_map_impl(map, base, rows, K, box_rows, box_k);
+}
+
+int device_sm_count() { return sm_count_impl(); }
 
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K) {
     if (!(M >= 1 && N >= 1 && K >= 16 && (K % 16) == 0 && M < (1LL << 31) && N < (1LL << 31))) return false;
@@ -543,7 +398,7 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream) {
     if (!gemm_tc_supports(M, N, K)) return cudaErrorNotSupported;
     CUtensorMap ma, mw;
-    if (!make_map(&ma, qa, M, K, BM) || !make_map(&mw, qw, N, K, BN)) return cudaErrorInvalidValue;
+    if (!make_tma_map_i8(&ma, qa, M, K, BM, BK) || !make_tma_map_i8(&mw, qw, N, K, BN, BK)) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -551,13 +406,14 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
         attr_set = true;
     }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    const int sms = device_sm_count();
+    const int grid = (int)(tiles < sms ? tiles : sms);
     gemm_tc_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mw, (int)M, (int)N, (int)K, ep);
     note_launch();
     return cudaGetLastError();
 }
 
-cudaError_t read_and_clear_device_error(uint32_t* code) {
+cudaError_t read_and_clear_gemm_tc_error(uint32_t* code) {
     unsigned int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v));
     if (e != cudaSuccess) return e;

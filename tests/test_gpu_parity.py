@@ -15,7 +15,12 @@ from tests import gates
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ("tcgen05", "mma_s8", "skinny")
+KERNELS = ("tcgen05", "mma_s8", "skinny", "decode")
+
+
+def runs(kernel, M):
+    """Whether the kernel accepts M rows (the decode kernel takes M <= 16)."""
+    return kernel != "decode" or M <= 16
 
 
 @pytest.fixture(scope="module")
@@ -113,6 +118,7 @@ def test_colsum_extreme_codes(q8):
 GEMM_SHAPES = [
     (1, 1, 16), (16, 128, 256), (128, 256, 1024), (200, 264, 1088), (129, 257, 1040),
     (300, 520, 2064), (17, 1000, 4096), (256, 512, 3072), (64, 96, 48),
+    (16, 28672, 8192), (5, 1000, 1040), (16, 65, 16), (11, 4100, 3200),
 ]
 
 
@@ -121,6 +127,11 @@ GEMM_SHAPES = [
 def test_gemm_s32_bit_exact(q8, kernel, M, N, K):
     qa = workloads.random_codes((M, K), seed=M * 7 + K)
     qw = workloads.random_codes((N, K), seed=N * 11 + K)
+    if not runs(kernel, M):
+        with pytest.raises(q8.Q8Error) as ex:
+            q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)
+        assert ex.value.status == q8.Q8_ERR_UNSUPPORTED
+        return
     acc = q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)
     assert_no_device_error(q8)
     np.testing.assert_array_equal(host(acc).astype(np.int64), oracle.gemm_acc(qa, qw, threads=8))
@@ -144,7 +155,7 @@ def test_gemm_s32_repeatable_under_load(q8, M, N, K, reps):
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_gemm_s32_extreme_codes(q8, kernel):
     """-128 * -128 products everywhere: every fp32 chunk sum sits exactly on 2^24."""
-    M, N, K = 160, 300, 16384
+    M, N, K = (16 if kernel == "decode" else 160), 300, 16384
     qa = np.full((M, K), -128, np.int8)
     qw = np.full((N, K), -128, np.int8)
     qw[1::2] = 127
@@ -158,7 +169,7 @@ def test_gemm_s32_extreme_codes(q8, kernel):
 def test_gemm_s32_small_terms_next_to_large_partial_sums(q8, kernel):
     """Each 1024-deep chunk first climbs to ~2^24 with -128*-128 products, then adds +-1
     and +-127 terms: an accumulator that kept fewer than 24 significant bits would drop them."""
-    M, N, K = 130, 260, 4096
+    M, N, K = (16 if kernel == "decode" else 130), 260, 4096
     rng = np.random.Generator(np.random.PCG64(5))
     qa = np.zeros((M, K), np.int8)
     qw = np.zeros((N, K), np.int8)
@@ -178,6 +189,7 @@ def test_gemm_s32_small_terms_next_to_large_partial_sums(q8, kernel):
 LAYER_CASES = [
     # name, M, N, K, act_per_row, act_sym, w_per_row
     ("tiny", 16, 128, 256, False, True, False),
+    ("decode", 7, 3000, 2064, True, False, True),
     ("prefill2k", 200, 264, 1088, True, True, True),
     ("relu4k", 333, 520, 2048, True, False, True),
     ("decode", 16, 1000, 8192, True, True, True),
@@ -189,6 +201,8 @@ LAYER_CASES = [
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name,M,N,K,apr,asym_is_sym,wpr", LAYER_CASES)
 def test_linear_layer_matches_oracle(q8, kernel, name, M, N, K, apr, asym_is_sym, wpr):
+    if not runs(kernel, M):
+        pytest.skip("the decode kernel takes M <= 16")
     wl = workloads.WORKLOADS[name]
     a = workloads.make_activations(wl, M=M, K=K)
     w = workloads.make_weights(wl, N=N, K=K)
@@ -209,7 +223,7 @@ def test_linear_layer_matches_oracle(q8, kernel, name, M, N, K, apr, asym_is_sym
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_epilogue_with_random_scales_and_zero_points(q8, kernel):
-    M, N, K = 150, 280, 1536
+    M, N, K = (13 if kernel == "decode" else 150), 280, 1536
     qa = workloads.random_codes((M, K), seed=40)
     qw = workloads.random_codes((N, K), seed=41, lo=-127)
     sa = workloads.random_scales(M, seed=42)
