@@ -303,7 +303,7 @@ def measure_e2e(a, y, step, ops, world, args):
             "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(ms, 3)}
 
 
-def measure_decode(q8, device, args, hbm_peak, flush):
+def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "tcgen05", "skinny", "mma_s8")):
     """Decode-shaped workload (16 tokens, HBM-bound): the step with each GEMM kernel."""
     import torch
     wl, a, w = layer_inputs(DECODE, device)
@@ -338,7 +338,7 @@ def measure_decode(q8, device, args, hbm_peak, flush):
 
     per_kernel = {}
     quant_ms = gq = None
-    for kernel in ("decode", "tcgen05", "skinny", "mma_s8"):
+    for kernel in kernels:
         qm, gm = timed(kernel)
         per_kernel[kernel] = {"gemm_ms": round(gm, 4),
                               "gemm_frac_hbm": round(gemm_bytes / (gm * 1e-3) / 1e9 / hbm_peak, 4)}
@@ -436,6 +436,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped workload")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the decode-shaped workload (one JSON object, for profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -443,6 +445,17 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup()
+    if args.decode_only:
+        import torch
+        import int8_quantized_gemm_gb300 as q8
+        from int8_quantized_gemm_gb300 import build
+        build.build()
+        q8.load()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        print(json.dumps(measure_decode(q8, device, args, peaks()[0], flush, kernels=("decode",))))
+        return
     run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
