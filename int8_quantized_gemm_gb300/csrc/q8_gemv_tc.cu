@@ -9,11 +9,16 @@
 // 128 x 16 fp32 tile in tensor memory and y is written transposed. 64-row
 // tiles give 448 tiles for N = 28672, about three per SM on 152 SMs.
 //
-// Exactness is the same argument as the prefill kernel: int8 codes are exact
-// in fp16, products are exact, each fp32 accumulator holds at most 1024
-// products (|partial| <= 2^24), and chunk sums are added in INT32 registers.
+// An N = 16 MMA is short, so a chain of them into one accumulator is bound by
+// the MMA latency, not the tensor pipe. The eight K-steps of a stage therefore
+// accumulate into eight separate TMEM accumulators (independent chains); the
+// drain adds them. Exactness is the prefill kernel's argument: int8 codes are
+// exact in fp16, products are exact, every fp32 accumulator holds at most
+// 1024 products (|partial| <= 2^24; here 128 per chain), and chunk sums are
+// added in INT32 registers.
 //
-//   warp 0      TMA: W [64 x 128] and A [16 x 128] int8 boxes -> staging ring (6 x 10 KB)
+//   warp 0      TMA: W [64 x 128] and A [16 x 128] int8 boxes, 128-byte swizzled,
+//               -> staging ring (10 x 10 KB)
 //   warp 1      TMEM allocation, tcgen05.mma issue (one thread)
 //   warps 2..7  int8 -> fp16 conversion into the swizzled operand ring (3 x 36 KB)
 //   warps 8..9  drain the chunk accumulators into INT32 and run the epilogue
@@ -37,13 +42,14 @@ constexpr int RW = 64;             // real weight rows per tile
 constexpr int MM = 128;            // MMA M (rows RW..MM-1 are zero)
 constexpr int NT = 16;             // tokens: MMA N
 constexpr int BK = 128;            // K per stage
-constexpr int S8 = 6;              // int8 staging stages
+constexpr int S8 = 10;             // int8 staging stages
 constexpr int S16 = 3;             // fp16 operand stages
 constexpr int KB_PER_CHUNK = 8;    // 8 * 128 = 1024 K per exact fp32 chunk
 constexpr int kConv = 192;         // converter threads, warps 2..7
 constexpr int kDrainWarps = 2;     // warps 8..9: TMEM lane quarters 0 and 1 (weight rows 0..63)
 constexpr int kThreads = 320;
-constexpr int kTmemCols = 32;      // two 128 x 16 fp32 buffers
+constexpr int kChains = BK / 16;   // independent accumulators, one per K-step of a stage
+constexpr int kTmemCols = 2 * kChains * NT;   // two buffers of 8 chains x 16 columns = 256
 
 constexpr int kW8 = RW * BK;                       // 8 KB
 constexpr int kA8 = NT * BK;                       // 2 KB
@@ -153,13 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t st = sbase + s * kStage16;
-                const uint32_t d = tmem_base + (uint32_t)(buf * NT);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
+                for (int kk = 0; kk < kChains; ++kk) {
+                    const uint32_t d = tmem_base + (uint32_t)((buf * kChains + kk) * NT);
                     const uint32_t off = (uint32_t)((kk & 3) * 32);   // 16 fp16 along K inside a swizzle column
                     const uint64_t adesc = smem_desc_sw128(st + (kk >> 2) * kAtomW + off);
                     const uint64_t bdesc = smem_desc_sw128(st + kW16 + (kk >> 2) * kAtomA + off);
-                    mma_f16(d, adesc, bdesc, kIdesc, (first && kk == 0) ? 0u : 1u);
+                    mma_f16(d, adesc, bdesc, kIdesc, first ? 0u : 1u);
                 }
                 mma_commit(bar_empty16 + 8 * s);
                 if (last) {
@@ -171,9 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------------- converters
-        // Staging row r (0..63 weights, 64..79 tokens) is 128 bytes = 8 chunks of 16 K
-        // values; chunk c becomes fp16 chunks 2c, 2c+1 of the 256-byte fp16 row, which
-        // sit in swizzle column c / 4.
+        // Staging rows (0..63 weights, 64..79 tokens) are 128 bytes = 8 chunks of 16 K
+        // values, stored by TMA with the 128-byte swizzle (chunk c of row r at c ^ (r & 7)).
+        // Thread chunk idx covers row = idx % rows, chunk c = idx / rows of its operand, so
+        // eight neighbouring threads touch eight rows of one chunk column: conflict-free
+        // for the loads and for the fp16 stores. Chunk c becomes fp16 chunks 2c, 2c+1 of
+        // the 256-byte fp16 row, in swizzle column c / 4.
         const int ct = threadIdx.x - 64;
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
@@ -184,7 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int idx = ct + kConv * j;
-                in[j] = idx < kChunks8 ? lds128(st8 + idx * 16) : make_uint4(0, 0, 0, 0);
+                const bool is_w = idx < RW * 8;
+                const int li = is_w ? idx : idx - RW * 8;
+                const int r = is_w ? (li & (RW - 1)) : (li & (NT - 1));
+                const int c = is_w ? (li / RW) : (li / NT);
+                const uint32_t src = st8 + (is_w ? 0 : kW8) + sw128(r, c);
+                in[j] = idx < kChunks8 ? lds128(src) : make_uint4(0, 0, 0, 0);
             }
             if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
                            &g_gemv_error))
@@ -194,10 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) {
                 const int idx = ct + kConv * j;
                 if (idx < kChunks8) {
-                    const int rall = idx >> 3, c = idx & 7;
+                    const bool is_w = idx < RW * 8;
+                    const int li = is_w ? idx : idx - RW * 8;
+                    const int r = is_w ? (li & (RW - 1)) : (li & (NT - 1));
+                const int c = is_w ? (li / RW) : (li / NT);
                     const int atom = c >> 2, w0 = (2 * c) & 7;
-                    const bool is_w = rall < RW;
-                    const int r = is_w ? rall : rall - RW;
                     const uint32_t region = is_w ? st16 + atom * kAtomW : st16 + kW16 + atom * kAtomA;
                     uint4 o0, o1;
                     cvt_word(in[j].x, o0.x, o0.y);
@@ -226,11 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar_accfull + 8 * buf, (uint32_t)((c >> 1) & 1), abort_flag, kErrDrain, &g_gemv_error))
                 break;
             tc_fence_after();
-            uint32_t v[16];
-            tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * NT), v);
             const int keep = cc != 0;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) acc[j] = acc[j] * keep + __float2int_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < NT; ++j) acc[j] *= keep;
+#pragma unroll 1
+            for (int kk = 0; kk < kChains; ++kk) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kChains + kk) * NT), v);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) acc[j] += __float2int_rn(__uint_as_float(v[j]));
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_accempty + 8 * buf);
@@ -282,7 +302,7 @@ cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream) {
     if (!gemv_tc_supports(M, N, K)) return cudaErrorNotSupported;
     CUtensorMap mw, ma;
-    if (!make_tma_map_i8(&mw, qw, N, K, RW, BK) || !make_tma_map_i8(&ma, qa, M, K, NT, BK))
+    if (!make_tma_map_i8(&mw, qw, N, K, RW, BK, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BK, true))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;

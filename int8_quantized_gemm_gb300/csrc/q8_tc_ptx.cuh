@@ -193,8 +193,11 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }  // namespace tc
 
 // Host side: TMA descriptor of a row-major int8 [rows, K] matrix with box
-// [box_rows, box_k] and zero fill outside; false if the driver entry point is missing.
-bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k);
+// [box_rows, box_k] and zero fill outside; swizzle128 stores each 128-byte box
+// row with its 16-byte chunks XOR-permuted by (row % 8) (box_k must be 128).
+// False if the driver entry point is missing.
+bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k,
+                     bool swizzle128 = false);
 int device_sm_count();
 
 }  // namespace q8
