@@ -303,7 +303,7 @@ def measure_e2e(a, y, step, ops, world, args):
             "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(ms, 3)}
 
 
-def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "tcgen05", "skinny", "mma_s8")):
+def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode_tc", "tcgen05", "skinny")):
     """Decode-shaped workload (16 tokens, HBM-bound): the step with each GEMM kernel."""
     import torch
     wl, a, w = layer_inputs(DECODE, device)
@@ -454,7 +454,7 @@ def main():
         device = torch.device("cuda", local)
         torch.cuda.set_device(device)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        print(json.dumps(measure_decode(q8, device, args, peaks()[0], flush, kernels=("decode",))))
+        print(json.dumps(measure_decode(q8, device, args, peaks()[0], flush, kernels=("decode", "decode_tc"))))
         return
     run_ours(args, world, rank, local)
     if world > 1:

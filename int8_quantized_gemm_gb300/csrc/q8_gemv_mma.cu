@@ -1,0 +1,261 @@
+// Decode-shaped integer GEMM (M <= 16 tokens) + dequantization epilogue on the
+// warp-level fp16 tensor-core instruction mma.sync.m16n8k16 (fp32 accumulate).
+//
+// With a handful of tokens the layer is a stream of the int8 weights from HBM
+// with little arithmetic per byte. The weights go HBM -> shared memory by TMA
+// (a 16-stage ring per SM) and shared memory -> registers by ordinary loads;
+// each warp converts its int8 fragments to fp16 in registers and feeds them
+// straight to the MMA, so converted data never goes back through shared memory.
+// (The int8 MMA of this GPU runs at a fraction of the fp16 rate, too low for
+// this stream.)
+//
+// Exactness: int8 codes and their products are exact in fp16 / fp32; each
+// fp32 accumulator holds the sum of at most 1024 products (|sum| <= 2^24, an
+// exactly representable integer) before it is converted to int32 and added to
+// an INT32 total, so the result is the exact integer dot product.
+//
+// K order inside a stage: lane quad t of a warp owns the 16-byte segment
+// [64h + 16t, +16) of its rows; word i of the segment feeds MMA step i, its
+// bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3) as (8+2t, 9+2t). Weights and
+// activations use the same mapping, so the dot products are unchanged.
+//
+// Work: 64 weight rows (output channels) per tile, tiles dealt round-robin to
+// one CTA per SM. Warp w (1..8) handles rows 16r .. 16r+15 (two n8 groups,
+// r = (w-1) % 4) and K half h = (w-1) / 4 of every 128-wide stage; the two
+// halves are added through shared memory at the end of the tile.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8_internal.h"
+#include "q8_tc_ptx.cuh"
+
+namespace q8 {
+
+static __device__ unsigned int g_gemv_mma_error;
+
+namespace {
+
+using namespace tc;
+
+constexpr int RW = 64;             // weight rows per tile
+constexpr int NT = 16;             // token rows (MMA M)
+constexpr int BK = 128;            // K per stage
+constexpr int S8 = 16;             // stages in the ring
+constexpr int kW8 = RW * BK;       // 8 KB of weights per stage
+constexpr int kA8 = NT * BK;       // 2 KB of activations per stage
+constexpr int kStage = kW8 + kA8;
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = 32 * (1 + kComputeWarps);
+constexpr int kStagesPerChunk = 16;   // 16 stages x 64 K per warp = 1024 products per fp32 sum
+constexpr int kOffRed = S8 * kStage;                          // int32 [4 row groups][32 lanes][8] partials
+constexpr int kRedBytes = 4 * 32 * 8 * 4;
+constexpr int kOffBar = kOffRed + kRedBytes;
+constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
+
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                    int M, int N, int K, Epilogue ep) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sraw = smem_u32(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - sraw);
+    const uint32_t bar_full = sbase + kOffBar;
+    const uint32_t bar_empty = bar_full + 8 * S8;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 16 * S8);
+    int32_t* red = reinterpret_cast<int32_t*>(smem + kOffRed);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kComputeWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    }
+    __syncthreads();
+
+    const int tiles = (N + RW - 1) / RW;
+    const int KB = (K + BK - 1) / BK;
+    const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total_g = my_tiles * KB;
+    // each CTA starts its K sweep at its own block, spreading activation reads over L2
+    const int k_rot = (int)(((long long)blockIdx.x * KB) / gridDim.x);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int i = 0, kb = 0;
+            for (int g = 0; g < total_g; ++g) {
+                const int n0 = ((int)blockIdx.x + i * (int)gridDim.x) * RW;
+                const int s = g % S8;
+                if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
+                               &g_gemv_mma_error))
+                    break;
+                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
+                const uint32_t dst = sbase + s * kStage;
+                mbar_expect_tx(bar_full + 8 * s, kStage);
+                tma_load_2d(dst, &tmap_w, kx, n0, bar_full + 8 * s);
+                tma_load_2d(dst + kW8, &tmap_a, kx, 0, bar_full + 8 * s);
+                if (++kb == KB) { kb = 0; ++i; }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int wc = warp - 1;          // 0..7
+        const int rg = wc & 3;            // 16-row group of the tile
+        const int h = wc >> 2;            // K half of each stage
+        const int g8 = lane >> 2, t = lane & 3;
+        // staging rows are 128 bytes stored with the 128-byte TMA swizzle: chunk c of
+        // row r sits at chunk c ^ (r & 7); this lane reads chunk 4h + t of its rows
+        const int c = 4 * h + t;
+        const uint32_t w_off0 = sw128(16 * rg + g8, c);          // weight row of n8 group 0
+        const uint32_t w_off1 = sw128(16 * rg + 8 + g8, c);      // weight row of n8 group 1
+        const uint32_t a_off0 = kW8 + sw128(g8, c);              // token row g
+        const uint32_t a_off1 = kW8 + sw128(g8 + 8, c);          // token row g + 8
+        int tot[2][4];
+        float part[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tot[j][e] = 0, part[j][e] = 0.0f;
+        int kb = 0, ti = 0, in_chunk = 0;
+        for (int g = 0; g < total_g; ++g) {
+            const int s = g % S8;
+            if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_gemv_mma_error))
+                break;
+            const uint32_t st = sbase + s * kStage;
+            const uint4 wv0 = lds128(st + w_off0);
+            const uint4 wv1 = lds128(st + w_off1);
+            const uint4 av0 = lds128(st + a_off0);
+            const uint4 av1 = lds128(st + a_off1);
+            const uint32_t aw0[4] = {av0.x, av0.y, av0.z, av0.w}, aw1[4] = {av1.x, av1.y, av1.z, av1.w};
+            const uint32_t ww0[4] = {wv0.x, wv0.y, wv0.z, wv0.w}, ww1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t a[4], b0[2], b1[2];
+                cvt_word(aw0[i], a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
+                cvt_word(aw1[i], a[1], a[3]);     // token row g+8
+                cvt_word(ww0[i], b0[0], b0[1]);   // weight rows of group 0
+                cvt_word(ww1[i], b1[0], b1[1]);   // weight rows of group 1
+                mma_m16n8k16(part[0], a, b0[0], b0[1]);
+                mma_m16n8k16(part[1], a, b1[0], b1[1]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the loaded registers have been consumed
+            const bool tile_end = (kb == KB - 1);
+            if (++in_chunk == kStagesPerChunk || tile_end) {
+                in_chunk = 0;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        tot[j][e] += __float2int_rn(part[j][e]);
+                        part[j][e] = 0.0f;
+                    }
+            }
+            if (tile_end) {
+                // add the K half of warp (rg, 1) into warp (rg, 0), which writes the tile
+                int32_t* slot = red + (rg * 32 + lane) * 8;
+                if (h == 1) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) slot[j * 4 + e] = tot[j][e];
+                }
+                named_barrier(1 + rg, 64);
+                if (h == 0) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) tot[j][e] += slot[j * 4 + e];
+                    const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + 16 * rg;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int m = g8 + (e >> 1) * 8;          // c0,c1: token g; c2,c3: token g+8
+                            const int n = n0 + 8 * j + 2 * t + (e & 1);
+                            if (m < M && n < N) {
+                                if (ep.out_i32) {
+                                    ep.out_i32[(int64_t)m * N + n] = tot[j][e];
+                                } else {
+                                    const int r = ep.a_per_row ? m : 0;
+                                    const int corr = ep.z_a ? tot[j][e] - __ldg(ep.z_a + r) * __ldg(ep.colsum + n)
+                                                            : tot[j][e];
+                                    const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
+                                    ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
+                                }
+                            }
+                        }
+                    }
+                }
+                named_barrier(1 + rg, 64);   // the slot is free again for the next tile
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) tot[j][e] = 0;
+            }
+            if (++kb == KB) { kb = 0; ++ti; }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1LL << 22)) __nanosleep(1000);
+    }
+}
+
+}  // namespace
+
+bool gemv_mma_supports(int64_t M, int64_t N, int64_t K) {
+    if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % 16) == 0)) return false;
+    const int64_t tiles = (N + RW - 1) / RW;
+    const int64_t kb = (K + BK - 1) / BK;
+    return tiles * kb < (1LL << 31);
+}
+
+cudaError_t launch_gemv_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                            const Epilogue& ep, cudaStream_t stream) {
+    if (!gemv_mma_supports(M, N, K)) return cudaErrorNotSupported;
+    CUtensorMap mw, ma;
+    if (!make_tma_map_i8(&mw, qw, N, K, RW, BK, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BK, true))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (N + RW - 1) / RW;
+    const int sms = device_sm_count();
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    gemv_mma_kernel<<<grid, kThreads, kSmem, stream>>>(mw, ma, (int)M, (int)N, (int)K, ep);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_gemv_mma_error(uint32_t* code) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_mma_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *code = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_gemv_mma_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace q8

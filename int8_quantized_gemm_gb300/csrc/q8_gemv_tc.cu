@@ -17,11 +17,14 @@
 // 1024 products (|partial| <= 2^24; here 128 per chain), and chunk sums are
 // added in INT32 registers.
 //
-//   warp 0      TMA: W [64 x 128] and A [16 x 128] int8 boxes, 128-byte swizzled,
-//               -> staging ring (10 x 10 KB)
-//   warp 1      TMEM allocation, tcgen05.mma issue (one thread)
-//   warps 2..7  int8 -> fp16 conversion into the swizzled operand ring (3 x 36 KB)
-//   warps 8..9  drain the chunk accumulators into INT32 and run the epilogue
+//   warp 0          TMA: W [64 x 128] and A [16 x 128] int8 boxes, 128-byte swizzled,
+//                   -> staging ring (10 x 10 KB)
+//   warp 1          TMEM allocation, tcgen05.mma issue (one thread)
+//   warps 2..11,    int8 -> fp16 conversion into the swizzled operand ring (3 x 36 KB);
+//   14, 15          twelve warps, so each thread converts at most two 16-byte chunks a stage
+//   warps 12, 13    drain the chunk accumulators into INT32 and run the epilogue
+// setmaxnreg gives the last warpgroup (drain + two converter warps) 232 registers and
+// the other three 80: 3*128*80 + 128*232 = 60416 <= 512 threads x 128 at launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -45,9 +48,10 @@ constexpr int BK = 128;            // K per stage
 constexpr int S8 = 10;             // int8 staging stages
 constexpr int S16 = 3;             // fp16 operand stages
 constexpr int KB_PER_CHUNK = 8;    // 8 * 128 = 1024 K per exact fp32 chunk
-constexpr int kConv = 192;         // converter threads, warps 2..7
-constexpr int kDrainWarps = 2;     // warps 8..9: TMEM lane quarters 0 and 1 (weight rows 0..63)
-constexpr int kThreads = 320;
+constexpr int kConv = 384;         // converter threads: warps 2..11, 14, 15
+constexpr int kDrainWarps = 2;     // warps 12, 13: TMEM lane quarters 0 and 1 (weight rows 0..63)
+constexpr int kThreads = 512;
+constexpr int kRegsLow = 80, kRegsHigh = 232;
 constexpr int kChains = BK / 16;   // independent accumulators, one per K-step of a stage
 constexpr int kTmemCols = 2 * kChains * NT;   // two buffers of 8 chains x 16 columns = 256
 
@@ -122,9 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int CPT = (KB + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
     const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total_g = my_tiles * KB;
+    const int k_rot = (int)(((long long)blockIdx.x * KB) / gridDim.x);
 
+    const bool is_conv = (warp >= 2 && warp < 12) || warp >= 14;
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
         if (lane == 0) {
             int i = 0, kb = 0;
             for (int g = 0; g < total_g; ++g) {
@@ -134,14 +141,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                &g_gemv_error))
                     break;
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
+                // Each CTA walks K from its own starting block, so the SMs do not all read
+                // the same activation slice (a handful of L2 lines) at the same moment.
+                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
                 mbar_expect_tx(bar_full8 + 8 * s, kStage8);
-                tma_load_2d(dst, &tmap_w, kb * BK, n0, bar_full8 + 8 * s);
-                tma_load_2d(dst + kW8, &tmap_a, kb * BK, 0, bar_full8 + 8 * s);
+                tma_load_2d(dst, &tmap_w, kx, n0, bar_full8 + 8 * s);
+                tma_load_2d(dst + kW8, &tmap_a, kx, 0, bar_full8 + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
         if (lane == 0) {
             int kb = 0, c = 0;
             for (int g = 0; g < total_g; ++g) {
@@ -175,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++kb == KB) kb = 0;
             }
         }
-    } else if (warp < 8) {
+    } else if (is_conv) {
         // ---------------------------------------------------------------- converters
         // Staging rows (0..63 weights, 64..79 tokens) are 128 bytes = 8 chunks of 16 K
         // values, stored by TMA with the 128-byte swizzle (chunk c of row r at c ^ (r & 7)).
@@ -183,15 +194,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // eight neighbouring threads touch eight rows of one chunk column: conflict-free
         // for the loads and for the fp16 stores. Chunk c becomes fp16 chunks 2c, 2c+1 of
         // the 256-byte fp16 row, in swizzle column c / 4.
-        const int ct = threadIdx.x - 64;
+        if (warp < 12) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
+        } else {
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh));
+        }
+        const int ct = warp < 12 ? threadIdx.x - 64 : threadIdx.x - 128;   // 0 .. 383
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
             if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_gemv_error))
                 break;
             const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8;
-            uint4 in[4];
+            uint4 in[2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 const int idx = ct + kConv * j;
                 const bool is_w = idx < RW * 8;
                 const int li = is_w ? idx : idx - RW * 8;
@@ -205,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             const uint32_t st16 = sbase + s16 * kStage16;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 const int idx = ct + kConv * j;
                 if (idx < kChunks8) {
                     const bool is_w = idx < RW * 8;
@@ -230,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- drain + epilogue
-        const int quarter = warp & 3;   // 0 or 1: weight rows 0..31 / 32..63 of the tile
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh));
+        const int quarter = warp & 3;   // warps 12, 13: weight rows 0..31 / 32..63 of the tile
         int acc[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j] = 0;

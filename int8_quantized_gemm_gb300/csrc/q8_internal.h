@@ -51,8 +51,14 @@ cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream);
 bool gemv_tc_supports(int64_t M, int64_t N, int64_t K);
 
+// Warp-level fp16 MMA kernel for M <= 16 (decode), weights streamed by TMA.
+cudaError_t launch_gemv_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                            const Epilogue& ep, cudaStream_t stream);
+bool gemv_mma_supports(int64_t M, int64_t N, int64_t K);
+
 // Device error words (bounded waits that gave up), one per kernel file and device.
 cudaError_t read_and_clear_gemm_tc_error(uint32_t* code);
 cudaError_t read_and_clear_gemv_tc_error(uint32_t* code);
+cudaError_t read_and_clear_gemv_mma_error(uint32_t* code);
 
 }  // namespace q8

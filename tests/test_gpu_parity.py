@@ -15,12 +15,12 @@ from tests import gates
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ("tcgen05", "mma_s8", "skinny", "decode")
+KERNELS = ("tcgen05", "mma_s8", "skinny", "decode", "decode_tc")
 
 
 def runs(kernel, M):
     """Whether the kernel accepts M rows (the decode kernel takes M <= 16)."""
-    return kernel != "decode" or M <= 16
+    return not kernel.startswith("decode") or M <= 16
 
 
 @pytest.fixture(scope="module")
@@ -155,7 +155,7 @@ def test_gemm_s32_repeatable_under_load(q8, M, N, K, reps):
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_gemm_s32_extreme_codes(q8, kernel):
     """-128 * -128 products everywhere: every fp32 chunk sum sits exactly on 2^24."""
-    M, N, K = (16 if kernel == "decode" else 160), 300, 16384
+    M, N, K = (16 if kernel.startswith("decode") else 160), 300, 16384
     qa = np.full((M, K), -128, np.int8)
     qw = np.full((N, K), -128, np.int8)
     qw[1::2] = 127
@@ -169,7 +169,7 @@ def test_gemm_s32_extreme_codes(q8, kernel):
 def test_gemm_s32_small_terms_next_to_large_partial_sums(q8, kernel):
     """Each 1024-deep chunk first climbs to ~2^24 with -128*-128 products, then adds +-1
     and +-127 terms: an accumulator that kept fewer than 24 significant bits would drop them."""
-    M, N, K = (16 if kernel == "decode" else 130), 260, 4096
+    M, N, K = (16 if kernel.startswith("decode") else 130), 260, 4096
     rng = np.random.Generator(np.random.PCG64(5))
     qa = np.zeros((M, K), np.int8)
     qw = np.zeros((N, K), np.int8)
@@ -223,7 +223,7 @@ def test_linear_layer_matches_oracle(q8, kernel, name, M, N, K, apr, asym_is_sym
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_epilogue_with_random_scales_and_zero_points(q8, kernel):
-    M, N, K = (13 if kernel == "decode" else 150), 280, 1536
+    M, N, K = (13 if kernel.startswith("decode") else 150), 280, 1536
     qa = workloads.random_codes((M, K), seed=40)
     qw = workloads.random_codes((N, K), seed=41, lo=-127)
     sa = workloads.random_scales(M, seed=42)
