@@ -14,15 +14,16 @@
 // exactly representable integer) before it is converted to int32 and added to
 // an INT32 total, so the result is the exact integer dot product.
 //
-// K order inside a stage: lane quad t of a warp owns the 16-byte segment
-// [64h + 16t, +16) of its rows; word i of the segment feeds MMA step i, its
+// K order inside a stage: lane quad t of a warp owns the 8-byte segment
+// [32q + 8t, +8) of its rows; word i of the segment feeds MMA step i, its
 // bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3) as (8+2t, 9+2t). Weights and
 // activations use the same mapping, so the dot products are unchanged.
 //
 // Work: 64 weight rows (output channels) per tile, tiles dealt round-robin to
-// one CTA per SM. Warp w (1..8) handles rows 16r .. 16r+15 (two n8 groups,
-// r = (w-1) % 4) and K half h = (w-1) / 4 of every 128-wide stage; the two
-// halves are added through shared memory at the end of the tile.
+// one CTA per SM. Compute warp w (0..15) handles rows 16r .. 16r+15 (two n8
+// groups, r = w % 4) and K quarter q = w / 4 of every 128-wide stage, four
+// warps per SM sub-partition to hide the load -> convert -> MMA latency; the
+// quarters are added through shared memory at the end of the tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -45,11 +46,11 @@ constexpr int S8 = 16;             // stages in the ring
 constexpr int kW8 = RW * BK;       // 8 KB of weights per stage
 constexpr int kA8 = NT * BK;       // 2 KB of activations per stage
 constexpr int kStage = kW8 + kA8;
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 16;
 constexpr int kThreads = 32 * (1 + kComputeWarps);
-constexpr int kStagesPerChunk = 16;   // 16 stages x 64 K per warp = 1024 products per fp32 sum
-constexpr int kOffRed = S8 * kStage;                          // int32 [4 row groups][32 lanes][8] partials
-constexpr int kRedBytes = 4 * 32 * 8 * 4;
+constexpr int kStagesPerChunk = 32;   // 32 stages x 32 K per warp = 1024 products per fp32 sum
+constexpr int kOffRed = S8 * kStage;  // int32 [4 row groups][3 quarters][32 lanes][8] partials
+constexpr int kRedBytes = 4 * 3 * 32 * 8 * 4;
 constexpr int kOffBar = kOffRed + kRedBytes;
 constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 
@@ -59,6 +60,12 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
@@ -117,17 +124,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- compute warps
-        const int wc = warp - 1;          // 0..7
+        const int wc = warp - 1;          // 0..15
         const int rg = wc & 3;            // 16-row group of the tile
-        const int h = wc >> 2;            // K half of each stage
+        const int q = wc >> 2;            // K quarter of each stage
         const int g8 = lane >> 2, t = lane & 3;
         // staging rows are 128 bytes stored with the 128-byte TMA swizzle: chunk c of
-        // row r sits at chunk c ^ (r & 7); this lane reads chunk 4h + t of its rows
-        const int c = 4 * h + t;
-        const uint32_t w_off0 = sw128(16 * rg + g8, c);          // weight row of n8 group 0
-        const uint32_t w_off1 = sw128(16 * rg + 8 + g8, c);      // weight row of n8 group 1
-        const uint32_t a_off0 = kW8 + sw128(g8, c);              // token row g
-        const uint32_t a_off1 = kW8 + sw128(g8 + 8, c);          // token row g + 8
+        // row r sits at chunk c ^ (r & 7); this lane reads the 8 bytes at 32q + 8t
+        const int c = 2 * q + (t >> 1), half = 8 * (t & 1);
+        const uint32_t w_off0 = sw128(16 * rg + g8, c) + half;         // weight row of n8 group 0
+        const uint32_t w_off1 = sw128(16 * rg + 8 + g8, c) + half;     // weight row of n8 group 1
+        const uint32_t a_off0 = kW8 + sw128(g8, c) + half;             // token row g
+        const uint32_t a_off1 = kW8 + sw128(g8 + 8, c) + half;         // token row g + 8
         int tot[2][4];
         float part[2][4];
 #pragma unroll
@@ -140,14 +147,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_gemv_mma_error))
                 break;
             const uint32_t st = sbase + s * kStage;
-            const uint4 wv0 = lds128(st + w_off0);
-            const uint4 wv1 = lds128(st + w_off1);
-            const uint4 av0 = lds128(st + a_off0);
-            const uint4 av1 = lds128(st + a_off1);
-            const uint32_t aw0[4] = {av0.x, av0.y, av0.z, av0.w}, aw1[4] = {av1.x, av1.y, av1.z, av1.w};
-            const uint32_t ww0[4] = {wv0.x, wv0.y, wv0.z, wv0.w}, ww1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
+            const uint2 wv0 = lds64(st + w_off0);
+            const uint2 wv1 = lds64(st + w_off1);
+            const uint2 av0 = lds64(st + a_off0);
+            const uint2 av1 = lds64(st + a_off1);
+            const uint32_t aw0[2] = {av0.x, av0.y}, aw1[2] = {av1.x, av1.y};
+            const uint32_t ww0[2] = {wv0.x, wv0.y}, ww1[2] = {wv1.x, wv1.y};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 uint32_t a[4], b0[2], b1[2];
                 cvt_word(aw0[i], a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
                 cvt_word(aw1[i], a[1], a[3]);     // token row g+8
@@ -170,20 +177,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
             }
             if (tile_end) {
-                // add the K half of warp (rg, 1) into warp (rg, 0), which writes the tile
-                int32_t* slot = red + (rg * 32 + lane) * 8;
-                if (h == 1) {
+                // add the K quarters of warps (rg, 1..3) into warp (rg, 0), which writes the tile
+                if (q != 0) {
+                    int32_t* slot = red + ((rg * 3 + q - 1) * 32 + lane) * 8;
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) slot[j * 4 + e] = tot[j][e];
                 }
-                named_barrier(1 + rg, 64);
-                if (h == 0) {
+                named_barrier(1 + rg, 128);
+                if (q == 0) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
+                    for (int qq = 0; qq < 3; ++qq) {
+                        const int32_t* slot = red + ((rg * 3 + qq) * 32 + lane) * 8;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) tot[j][e] += slot[j * 4 + e];
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) tot[j][e] += slot[j * 4 + e];
+                    }
                     const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + 16 * rg;
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                named_barrier(1 + rg, 64);   // the slot is free again for the next tile
+                named_barrier(1 + rg, 128);   // the slots are free again for the next tile
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
