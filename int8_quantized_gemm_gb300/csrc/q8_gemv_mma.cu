@@ -14,16 +14,18 @@
 // exactly representable integer) before it is converted to int32 and added to
 // an INT32 total, so the result is the exact integer dot product.
 //
-// K order inside a stage: lane quad t of a warp owns the 8-byte segment
-// [32q + 8t, +8) of its rows; word i of the segment feeds MMA step i, its
-// bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3) as (8+2t, 9+2t). Weights and
-// activations use the same mapping, so the dot products are unchanged.
+// K order inside a stage: compute warp s owns the 16 K values [16s, 16s+16) of
+// every stage, one MMA K-step; lane quad t holds the 4 bytes [16s + 4t, +4) of
+// its rows, bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3) as (8+2t, 9+2t).
+// Weights and activations use the same mapping, so the dot products are
+// unchanged. With the 128-byte TMA swizzle these 4-byte loads hit 32 distinct
+// banks.
 //
 // Work: 64 weight rows (output channels) per tile, tiles dealt round-robin to
-// one CTA per SM. Compute warp w (0..15) handles rows 16r .. 16r+15 (two n8
-// groups, r = w % 4) and K quarter q = w / 4 of every 128-wide stage, four
-// warps per SM sub-partition to hide the load -> convert -> MMA latency; the
-// quarters are added through shared memory at the end of the tile.
+// one CTA per SM. Each compute warp covers all 64 rows (eight n8 groups, eight
+// independent accumulators) for its K-step, so a token fragment is converted
+// once per eight MMAs; at the end of a tile the eight K-step partials are
+// added in shared memory (integer adds, exact) and written out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -46,11 +48,11 @@ constexpr int S8 = 16;             // stages in the ring
 constexpr int kW8 = RW * BK;       // 8 KB of weights per stage
 constexpr int kA8 = NT * BK;       // 2 KB of activations per stage
 constexpr int kStage = kW8 + kA8;
-constexpr int kComputeWarps = 16;
+constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
 constexpr int kThreads = 32 * (1 + kComputeWarps);
-constexpr int kStagesPerChunk = 32;   // 32 stages x 32 K per warp = 1024 products per fp32 sum
-constexpr int kOffRed = S8 * kStage;  // int32 [4 row groups][3 quarters][32 lanes][8] partials
-constexpr int kRedBytes = 4 * 3 * 32 * 8 * 4;
+constexpr int kStagesPerChunk = 64;   // 64 stages x 16 K per warp = 1024 products per fp32 sum
+constexpr int kOffRed = S8 * kStage;  // int32 [16 tokens][64 rows] tile sums
+constexpr int kRedBytes = NT * RW * 4;
 constexpr int kOffBar = kOffRed + kRedBytes;
 constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 
@@ -62,9 +64,9 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 
@@ -124,21 +126,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- compute warps
-        const int wc = warp - 1;          // 0..15
-        const int rg = wc & 3;            // 16-row group of the tile
-        const int q = wc >> 2;            // K quarter of each stage
+        const int ks = warp - 1;          // K-step of each stage: bytes [16 ks, 16 ks + 16)
+        const int ct = threadIdx.x - 32;  // 0 .. 255
         const int g8 = lane >> 2, t = lane & 3;
-        // staging rows are 128 bytes stored with the 128-byte TMA swizzle: chunk c of
-        // row r sits at chunk c ^ (r & 7); this lane reads the 8 bytes at 32q + 8t
-        const int c = 2 * q + (t >> 1), half = 8 * (t & 1);
-        const uint32_t w_off0 = sw128(16 * rg + g8, c) + half;         // weight row of n8 group 0
-        const uint32_t w_off1 = sw128(16 * rg + 8 + g8, c) + half;     // weight row of n8 group 1
-        const uint32_t a_off0 = kW8 + sw128(g8, c) + half;             // token row g
-        const uint32_t a_off1 = kW8 + sw128(g8 + 8, c) + half;         // token row g + 8
-        int tot[2][4];
-        float part[2][4];
+        // weight row 8j + g and token rows g, g+8 at chunk ks (swizzled), word t
+        uint32_t w_off[8];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 8; ++j) w_off[j] = sw128(8 * j + g8, ks) + 4 * t;
+        const uint32_t a_off0 = kW8 + sw128(g8, ks) + 4 * t;
+        const uint32_t a_off1 = kW8 + sw128(g8 + 8, ks) + 4 * t;
+        for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) red[i] = 0;
+        named_barrier(1, 32 * kComputeWarps);
+        int tot[8][4];
+        float part[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) tot[j][e] = 0, part[j][e] = 0.0f;
         int kb = 0, ti = 0, in_chunk = 0;
@@ -147,21 +149,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_gemv_mma_error))
                 break;
             const uint32_t st = sbase + s * kStage;
-            const uint2 wv0 = lds64(st + w_off0);
-            const uint2 wv1 = lds64(st + w_off1);
-            const uint2 av0 = lds64(st + a_off0);
-            const uint2 av1 = lds64(st + a_off1);
-            const uint32_t aw0[2] = {av0.x, av0.y}, aw1[2] = {av1.x, av1.y};
-            const uint32_t ww0[2] = {wv0.x, wv0.y}, ww1[2] = {wv1.x, wv1.y};
+            uint32_t wq[8];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint32_t a[4], b0[2], b1[2];
-                cvt_word(aw0[i], a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
-                cvt_word(aw1[i], a[1], a[3]);     // token row g+8
-                cvt_word(ww0[i], b0[0], b0[1]);   // weight rows of group 0
-                cvt_word(ww1[i], b1[0], b1[1]);   // weight rows of group 1
-                mma_m16n8k16(part[0], a, b0[0], b0[1]);
-                mma_m16n8k16(part[1], a, b1[0], b1[1]);
+            for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_off[j]);
+            const uint32_t aq0 = lds32(st + a_off0), aq1 = lds32(st + a_off1);
+            uint32_t a[4];
+            cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
+            cvt_word(aq1, a[1], a[3]);     // token row g+8
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t b0, b1;
+                cvt_word(wq[j], b0, b1);   // weight row 8j + g
+                mma_m16n8k16(part[j], a, b0, b1);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the loaded registers have been consumed
@@ -169,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++in_chunk == kStagesPerChunk || tile_end) {
                 in_chunk = 0;
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < 8; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         tot[j][e] += __float2int_rn(part[j][e]);
@@ -177,50 +176,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
             }
             if (tile_end) {
-                // add the K quarters of warps (rg, 1..3) into warp (rg, 0), which writes the tile
-                if (q != 0) {
-                    int32_t* slot = red + ((rg * 3 + q - 1) * 32 + lane) * 8;
+                // add the eight K-step partials of the tile in shared memory (integer adds)
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < 8; ++j)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) slot[j * 4 + e] = tot[j][e];
-                }
-                named_barrier(1 + rg, 128);
-                if (q == 0) {
-#pragma unroll
-                    for (int qq = 0; qq < 3; ++qq) {
-                        const int32_t* slot = red + ((rg * 3 + qq) * 32 + lane) * 8;
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) tot[j][e] += slot[j * 4 + e];
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
+                        const int r = 8 * j + 2 * t + (e & 1);
+                        atomicAdd(red + m * RW + r, tot[j][e]);
+                        tot[j][e] = 0;
                     }
-                    const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + 16 * rg;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int m = g8 + (e >> 1) * 8;          // c0,c1: token g; c2,c3: token g+8
-                            const int n = n0 + 8 * j + 2 * t + (e & 1);
-                            if (m < M && n < N) {
-                                if (ep.out_i32) {
-                                    ep.out_i32[(int64_t)m * N + n] = tot[j][e];
-                                } else {
-                                    const int r = ep.a_per_row ? m : 0;
-                                    const int corr = ep.z_a ? tot[j][e] - __ldg(ep.z_a + r) * __ldg(ep.colsum + n)
-                                                            : tot[j][e];
-                                    const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
-                                    ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
-                                }
-                            }
+                named_barrier(1, 32 * kComputeWarps);
+                const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW;
+                for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) {
+                    const int m = i / RW, n = n0 + i % RW;
+                    const int v = red[i];
+                    red[i] = 0;
+                    if (m < M && n < N) {
+                        if (ep.out_i32) {
+                            ep.out_i32[(int64_t)m * N + n] = v;
+                        } else {
+                            const int r = ep.a_per_row ? m : 0;
+                            const int corr = ep.z_a ? v - __ldg(ep.z_a + r) * __ldg(ep.colsum + n) : v;
+                            const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
+                            ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
                         }
                     }
                 }
-                named_barrier(1 + rg, 128);   // the slots are free again for the next tile
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) tot[j][e] = 0;
+                named_barrier(1, 32 * kComputeWarps);   // the sums are zero again for the next tile
             }
             if (++kb == KB) { kb = 0; ++ti; }
         }
