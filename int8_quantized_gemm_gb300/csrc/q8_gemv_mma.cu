@@ -25,12 +25,7 @@
 // one CTA per SM. Each compute warp covers all 64 rows (eight n8 groups, eight
 // independent accumulators) for its K-step, so a token fragment is converted
 // once per eight MMAs; at the end of a tile the eight K-step partials are
-// added into one of two shared-memory sum buffers (integer adds, exact) and an
-// epilogue warp writes the tile out while the compute warps start the next.
-//
-//   warp 0       TMA producer (one thread)
-//   warps 1..8   compute (one K-step each)
-//   warp 9       epilogue: sums -> y, clears the buffer
+// added in shared memory (integer adds, exact) and written out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -54,14 +49,12 @@ constexpr int kW8 = RW * BK;       // 8 KB of weights per stage
 constexpr int kA8 = NT * BK;       // 2 KB of activations per stage
 constexpr int kStage = kW8 + kA8;
 constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
-constexpr int kEpiWarp = 1 + kComputeWarps;
-constexpr int kThreads = 32 * (2 + kComputeWarps);
+constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int kStagesPerChunk = 64;   // 64 stages x 16 K per warp = 1024 products per fp32 sum
-constexpr int kOffRed = S8 * kStage;  // two int32 [16 tokens][64 rows] tile sum buffers
-constexpr int kRedBytes = 2 * NT * RW * 4;
+constexpr int kOffRed = S8 * kStage;  // int32 [16 tokens][64 rows] tile sums
+constexpr int kRedBytes = NT * RW * 4;
 constexpr int kOffBar = kOffRed + kRedBytes;
-constexpr int kBarBytes = 16 * S8 + 32 + 16;   // full/empty per stage, tile_done/red_free per buffer, flag
-constexpr int kSmem = kOffBar + kBarBytes + 1024;
+constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -77,6 +70,10 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     int M, int N, int K, Epilogue ep) {
@@ -86,9 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + (sbase - sraw);
     const uint32_t bar_full = sbase + kOffBar;
     const uint32_t bar_empty = bar_full + 8 * S8;
-    const uint32_t bar_tile_done = bar_empty + 8 * S8;   // [2]: compute warps -> epilogue warp
-    const uint32_t bar_red_free = bar_tile_done + 16;    // [2]: epilogue warp -> compute warps
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 16 * S8 + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 16 * S8);
     int32_t* red = reinterpret_cast<int32_t*>(smem + kOffRed);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -97,16 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kComputeWarps);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar_tile_done + 8 * b, kComputeWarps);
-            mbar_init(bar_red_free + 8 * b, 1);
-        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     }
-    for (int i = threadIdx.x; i < 2 * NT * RW; i += kThreads) red[i] = 0;
     __syncthreads();
 
     const int tiles = (N + RW - 1) / RW;
@@ -134,35 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
-    } else if (warp == kEpiWarp) {
-        // ---------------------------------------------------------------- epilogue warp
-        for (int ti = 0; ti < my_tiles; ++ti) {
-            const int b = ti & 1;
-            if (!mbar_wait(bar_tile_done + 8 * b, (uint32_t)((ti >> 1) & 1), abort_flag, kErrDrain, &g_gemv_mma_error))
-                break;
-            int32_t* sums = red + b * NT * RW;
-            const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW;
-            for (int i = lane; i < NT * RW; i += 32) {
-                const int m = i / RW, n = n0 + i % RW;
-                const int v = sums[i];
-                sums[i] = 0;
-                if (m < M && n < N) {
-                    if (ep.out_i32) {
-                        ep.out_i32[(int64_t)m * N + n] = v;
-                    } else {
-                        const int r = ep.a_per_row ? m : 0;
-                        const int corr = ep.z_a ? v - __ldg(ep.z_a + r) * __ldg(ep.colsum + n) : v;
-                        const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
-                        ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_red_free + 8 * b);
-        }
     } else {
         // ---------------------------------------------------------------- compute warps
         const int ks = warp - 1;          // K-step of each stage: bytes [16 ks, 16 ks + 16)
+        const int ct = threadIdx.x - 32;  // 0 .. 255
         const int g8 = lane >> 2, t = lane & 3;
         // weight row 8j + g and token rows g, g+8 at chunk ks (swizzled), word t
         uint32_t w_off[8];
@@ -170,6 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) w_off[j] = sw128(8 * j + g8, ks) + 4 * t;
         const uint32_t a_off0 = kW8 + sw128(g8, ks) + 4 * t;
         const uint32_t a_off1 = kW8 + sw128(g8 + 8, ks) + 4 * t;
+        for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) red[i] = 0;
+        named_barrier(1, 32 * kComputeWarps);
         int tot[8][4];
         float part[8][4];
 #pragma unroll
@@ -209,24 +176,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
             }
             if (tile_end) {
-                // add the eight K-step partials of the tile into sum buffer ti % 2 (integer
-                // adds), once the epilogue warp has emptied it (it held tile ti - 2)
-                const int b = ti & 1;
-                if (ti >= 2 && !mbar_wait(bar_red_free + 8 * b, (uint32_t)(((ti - 2) >> 1) & 1), abort_flag,
-                                          kErrMmaAcc, &g_gemv_mma_error))
-                    break;
-                int32_t* sums = red + b * NT * RW;
+                // add the eight K-step partials of the tile in shared memory (integer adds)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
                         const int r = 8 * j + 2 * t + (e & 1);
-                        atomicAdd(sums + m * RW + r, tot[j][e]);
+                        atomicAdd(red + m * RW + r, tot[j][e]);
                         tot[j][e] = 0;
                     }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tile_done + 8 * b);
+                named_barrier(1, 32 * kComputeWarps);
+                const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW;
+                for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) {
+                    const int m = i / RW, n = n0 + i % RW;
+                    const int v = red[i];
+                    red[i] = 0;
+                    if (m < M && n < N) {
+                        if (ep.out_i32) {
+                            ep.out_i32[(int64_t)m * N + n] = v;
+                        } else {
+                            const int r = ep.a_per_row ? m : 0;
+                            const int corr = ep.z_a ? v - __ldg(ep.z_a + r) * __ldg(ep.colsum + n) : v;
+                            const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
+                            ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
+                        }
+                    }
+                }
+                named_barrier(1, 32 * kComputeWarps);   // the sums are zero again for the next tile
             }
             if (++kb == KB) { kb = 0; ++ti; }
         }
