@@ -192,43 +192,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // ---------------------------------------------------------------- converters
-        // A stage is 1536 16-byte int8 chunks ([A 128 rows | W 256 rows] x 4 chunks of
-        // each 64-byte staging row), split over 8 virtual warps of 32 lanes x 6 chunks:
-        // virtual lane v takes idx = v + 256 j, i.e. row v / 4 + 64 j, chunk v % 4. The
-        // fp16 stage is [A | W] in one run of 128-byte swizzled rows and (row & 7) does
-        // not change with j, so both addresses are a per-lane base plus a constant
-        // stride (4096 and 8192 bytes). Warps are spread over the four SM sub-partitions
-        // as warp % 4: warps 2, 6 and 3, 7 share sub-partitions 2 and 3 while warps 4
-        // and 5 are alone on 0 and 1, so warps 4 and 5 take two virtual warps each and
-        // every sub-partition converts a quarter of the stage.
-        const int vw0 = warp == 2 ? 0 : warp == 3 ? 1 : warp == 6 ? 2 : warp == 7 ? 3 : warp == 4 ? 4 : 6;
-        const int nvw = (warp == 4 || warp == 5) ? 2 : 1;
+        // 1536 16-byte int8 chunks per stage ([A 128 rows | W 256 rows] x 4
+        // chunks of each 64-byte staging row), 8 per thread. The fp16 stage is
+        // [A | W] in one run of 128-byte swizzled rows, so row r of the
+        // combined staging tile lands at sw128(r, .) for both operands.
+        const int ct = threadIdx.x - 64;
+        // Chunk j of this thread is idx = ct + 192 j: staging byte idx * 16, fp16 row
+        // r = ct / 4 + 48 j with (r & 7) independent of j, so both addresses are a
+        // per-thread base plus a constant stride (3072 and 6144 bytes).
+        const int r0 = ct >> 2, c0 = ct & 3;
+        const uint32_t src0 = (uint32_t)(ct * 16);
+        const uint32_t dst0 = sw128(r0, 2 * c0);
+        const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
             if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc_error)) break;
-            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty, &g_tc_error))
-                break;
-            const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8;
+            const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
+            uint4 in[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) in[j] = lds128(st8 + kConv * 16 * j);
+            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty, &g_tc_error)) break;
             const uint32_t st16 = sbase + s16 * kStage16;
-            for (int vv = 0; vv < nvw; ++vv) {
-                const int v = (vw0 + vv) * 32 + lane;        // virtual lane 0..255
-                const int r0 = v >> 2, c0 = v & 3;
-                const uint32_t src = st8 + (uint32_t)(v * 16);
-                const uint32_t dst0 = st16 + sw128(r0, 2 * c0);
-                const uint32_t dst1 = st16 + sw128(r0, 2 * c0 + 1);
-                uint4 in[6];
 #pragma unroll
-                for (int j = 0; j < 6; ++j) in[j] = lds128(src + 4096 * j);
-#pragma unroll
-                for (int j = 0; j < 6; ++j) {
-                    uint4 o0, o1;
-                    cvt_word(in[j].x, o0.x, o0.y);
-                    cvt_word(in[j].y, o0.z, o0.w);
-                    cvt_word(in[j].z, o1.x, o1.y);
-                    cvt_word(in[j].w, o1.z, o1.w);
-                    sts128(dst0 + 8192 * j, o0);
-                    sts128(dst1 + 8192 * j, o1);
-                }
+            for (int j = 0; j < 8; ++j) {
+                uint4 o0, o1;
+                cvt_word(in[j].x, o0.x, o0.y);
+                cvt_word(in[j].y, o0.z, o0.w);
+                cvt_word(in[j].z, o1.x, o1.y);
+                cvt_word(in[j].w, o1.z, o1.w);
+                sts128(st16 + dst0 + 6144 * j, o0);
+                sts128(st16 + dst1 + 6144 * j, o1);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar_full16 + 8 * s16);
