@@ -68,7 +68,8 @@ typedef enum q8_gemm_kernel {
     Q8_GEMM_MMA_S8 = 2,   /* warp-level mma.sync s8 kernel, 128x128 tiles */
     Q8_GEMM_SKINNY = 3,   /* warp-level mma.sync s8 kernel, 16x64 tiles */
     Q8_GEMM_DECODE = 4,   /* M <= 16: TMA weight stream, in-register int8->fp16, mma.sync f16 */
-    Q8_GEMM_DECODE_TC = 5 /* M <= 16 on tcgen05: weights as the MMA M side, tokens as N = 16 */
+    Q8_GEMM_DECODE_TC = 5, /* M <= 16 on tcgen05: weights as the MMA M side, tokens as N = 16 */
+    Q8_GEMM_TCGEN05_PAIR = 6 /* tcgen05 on CTA pairs (cta_group::2), 256 x 256 tiles */
 } q8_gemm_kernel;
 
 /*

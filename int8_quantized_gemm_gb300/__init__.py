@@ -29,7 +29,7 @@ LIB_PATH = _build.LIB
 Q8_OK, Q8_ERR_INVALID_ARG, Q8_ERR_UNSUPPORTED, Q8_ERR_CUDA, Q8_ERR_TIMEOUT = range(5)
 Q8_PER_TENSOR, Q8_PER_ROW = 0, 1
 Q8_SYMMETRIC, Q8_ASYMMETRIC = 0, 1
-KERNELS = {"auto": 0, "tcgen05": 1, "mma_s8": 2, "skinny": 3, "decode": 4, "decode_tc": 5}
+KERNELS = {"auto": 0, "tcgen05": 1, "mma_s8": 2, "skinny": 3, "decode": 4, "decode_tc": 5, "tcgen05_pair": 6}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
 _lib = None

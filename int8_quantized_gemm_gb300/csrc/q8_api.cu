@@ -55,7 +55,8 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
                       q8_stream_t stream) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
-        kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC)
+        kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
+        kernel != Q8_GEMM_TCGEN05_PAIR)
         return Q8_ERR_INVALID_ARG;
     const bool epilogue = (out_i32 == nullptr);
     if (epilogue && (!valid_gran(ga) || !valid_gran(gw))) return Q8_ERR_INVALID_ARG;
@@ -88,6 +89,9 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         case Q8_GEMM_TCGEN05:
             if (!q8::gemm_tc_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
             return from_cuda(q8::launch_gemm_tc(qa, qw, M, N, K, ep, s));
+        case Q8_GEMM_TCGEN05_PAIR:
+            if (!q8::gemm_tc2_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
+            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s));
         case Q8_GEMM_DECODE:
             if (!q8::gemv_mma_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
             return from_cuda(q8::launch_gemv_mma(qa, qw, M, N, K, ep, s));
@@ -180,12 +184,13 @@ const char* q8_status_string(q8_status status) {
 
 q8_status q8_device_error(uint32_t* code_out) {
     if (!code_out) return Q8_ERR_INVALID_ARG;
-    uint32_t a = 0, b = 0, c = 0;
+    uint32_t a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = q8::read_and_clear_gemm_tc_error(&a);
     if (e == cudaSuccess) e = q8::read_and_clear_gemv_tc_error(&b);
     if (e == cudaSuccess) e = q8::read_and_clear_gemv_mma_error(&c);
+    if (e == cudaSuccess) e = q8::read_and_clear_gemm_tc2_error(&d);
     if (e != cudaSuccess) return Q8_ERR_CUDA;
-    *code_out = a | (b << 8) | (c << 16);
+    *code_out = a | (b << 8) | (c << 16) | (d << 24);
     return *code_out ? Q8_ERR_TIMEOUT : Q8_OK;
 }
 

@@ -1,0 +1,396 @@
+// Integer GEMM + dequantization epilogue on CTA pairs (tcgen05 cta_group::2).
+//
+// The exactness argument is the one of the single-CTA kernel (q8_gemm_tc.cu):
+// int8 codes are exact in fp16, each fp32 TMEM accumulator holds at most 1024
+// products (|partial| <= 2^24), and chunk sums are added in INT32 registers.
+//
+// Why pairs: the single-CTA kernel streams every operand byte through shared
+// memory four times (TMA write, conversion read, fp16 write, MMA read) and is
+// bound by shared-memory bandwidth, not by the tensor core. Two CTAs of a
+// cluster share one 256 x 256 MMA tile: each CTA holds and converts 128 rows
+// of A and 128 rows (one half) of W, and the pair's tensor cores exchange the
+// W halves, so per SM the shared-memory traffic per FLOP drops by a third.
+//
+//   both CTAs   warp 0       TMA: int8 A [128 x 64] (own rows) and W [128 x 64]
+//                            (own half of the 256 columns) -> staging ring
+//               warps 2..7   int8 -> fp16 into the swizzled operand ring; each
+//                            warp then arrives on the even CTA's stage barrier
+//               warps 8..15  drain their own TMEM rows (128 x 256) per 1024-K chunk
+//                            into INT32 registers, epilogue, store y
+//   even CTA    warp 1       issues tcgen05.mma.cta_group::2 (M = 256, N = 256) and
+//                            commits to the barriers of both CTAs
+//   both CTAs   warp 1       allocates / frees TMEM collectively with the peer
+// setmaxnreg: 72 registers for warpgroups 0-1, 184 for the drain warpgroups.
+// Waits on mbarriers are bounded (device error word + abort flag).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8_internal.h"
+#include "q8_tc_ptx.cuh"
+
+namespace q8 {
+
+static __device__ unsigned int g_tc2_error;
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 256;             // rows of the pair tile (128 per CTA)
+constexpr int BMH = 128;
+constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per CTA)
+constexpr int BNH = 128;
+constexpr int BK = 64;
+constexpr int S8 = 6;               // int8 staging stages (16 KB)
+constexpr int S16 = 3;              // fp16 operand stages (32 KB)
+constexpr int KB_PER_CHUNK = 16;    // 1024 K per exact fp32 chunk
+constexpr int kConv = 192;          // converter threads, warps 2..7 of each CTA
+constexpr int kDrainWarps = 8;      // warps 8..15 of each CTA
+constexpr int kThreads = 512;
+constexpr int kRegsLow = 72, kRegsHigh = 184;
+constexpr int kTmemCols = 512;      // two 128 x 256 fp32 accumulator buffers per CTA
+
+constexpr int kA8 = BMH * BK, kB8 = BNH * BK, kStage8 = kA8 + kB8;                // 16 KB
+constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16;   // 32 KB
+constexpr int kChunks8 = kStage8 / 16;                                            // 1024
+constexpr int kOffStage8 = S16 * kStage16;
+constexpr int kOffBar = kOffStage8 + S8 * kStage8;
+constexpr int kBarBytes = 8 * (2 * S8 + 2 * S16 + 4) + 16;
+constexpr int kSmem = kOffBar + kBarBytes + 1024;
+constexpr uint32_t kIdesc = idesc_f16(BM, BN);
+constexpr uint16_t kPairMask = 0x3;
+
+static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages must keep 1024-byte alignment");
+
+struct PairGeom {
+    int num_m, num_n, tiles;
+};
+
+// Pair tiles in bands of 4 M-tiles (1024 rows), N swept inside a band.
+__device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, int& n0) {
+    constexpr int GM = 4;
+    const int band = t / (GM * tg.num_n);
+    const int within = t - band * GM * tg.num_n;
+    const int rows = min(GM, tg.num_m - band * GM);
+    m0 = (band * GM + within % rows) * BM;
+    n0 = (within / rows) * BN;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+                    int M, int N, int K, Epilogue ep) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sraw = smem_u32(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - sraw);
+    const uint32_t bar_full8 = sbase + kOffBar;
+    const uint32_t bar_empty8 = bar_full8 + 8 * S8;
+    const uint32_t bar_full16 = bar_empty8 + 8 * S8;     // used in the even CTA: 2 x 6 converter warps
+    const uint32_t bar_empty16 = bar_full16 + 8 * S16;   // both CTAs: the pair MMA's commit
+    const uint32_t bar_accfull = bar_empty16 + 8 * S16;  // both CTAs: the pair MMA's commit
+    const uint32_t bar_accempty = bar_accfull + 16;      // used in the even CTA: 2 x 8 drain warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * S8 + 2 * S16 + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();            // 0: issues the MMA; 1: peer
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(bar_full8 + 8 * s, 1);
+            mbar_init(bar_empty8 + 8 * s, kConv / 32);
+        }
+        for (int s = 0; s < S16; ++s) {
+            mbar_init(bar_full16 + 8 * s, 2 * (kConv / 32));
+            mbar_init(bar_empty16 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_accfull + 8 * b, 1);
+            mbar_init(bar_accempty + 8 * b, 2 * kDrainWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    PairGeom tg;
+    tg.num_m = (M + BM - 1) / BM;
+    tg.num_n = (N + BN - 1) / BN;
+    tg.tiles = tg.num_m * tg.num_n;
+    const int cluster = (int)(blockIdx.x >> 1), nclusters = (int)(gridDim.x >> 1);
+    const int KB = (K + BK - 1) / BK;
+    const int CPT = (KB + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
+    const int my_tiles = cluster < tg.tiles ? (tg.tiles - 1 - cluster) / nclusters + 1 : 0;
+    const int total_g = my_tiles * KB;
+
+    if (warp < 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
+      if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int i = 0, kb = 0, m0 = 0, n0 = 0;
+            for (int g = 0; g < total_g; ++g) {
+                if (kb == 0) pair_coords(tg, cluster + i * nclusters, m0, n0);
+                const int s = g % S8;
+                if (!mbar_wait(bar_empty8 + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
+                               &g_tc2_error))
+                    break;
+                const uint32_t dst = sbase + kOffStage8 + s * kStage8;
+                mbar_expect_tx(bar_full8 + 8 * s, kStage8);
+                tma_load_2d(dst, &tmap_a, kb * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
+                tma_load_2d(dst + kA8, &tmap_w, kb * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                if (++kb == KB) { kb = 0; ++i; }
+            }
+        }
+      } else if (warp == 1) {
+        // ---------------------------------------------------------------- pair MMA issuer
+        if (leader && lane == 0) {
+            int kb = 0, c = 0;
+            for (int g = 0; g < total_g; ++g) {
+                const bool first = (kb % KB_PER_CHUNK) == 0;
+                const bool last = (kb % KB_PER_CHUNK) == KB_PER_CHUNK - 1 || kb == KB - 1;
+                const int buf = c & 1;
+                if (first) {
+                    if (!mbar_wait_cluster(bar_accempty + 8 * buf, (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag,
+                                           kErrMmaAcc, &g_tc2_error))
+                        break;
+                    tc_fence_after();
+                }
+                const int s = g % S16;
+                if (!mbar_wait_cluster(bar_full16 + 8 * s, (uint32_t)((g / S16) & 1), abort_flag, kErrMmaFull,
+                                       &g_tc2_error))
+                    break;
+                tc_fence_after();
+                const uint32_t a_addr = sbase + s * kStage16;
+                const uint64_t adesc = smem_desc_sw128(a_addr);
+                const uint64_t bdesc = smem_desc_sw128(a_addr + kA16);
+                const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_f16_pair(d, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), kIdesc,
+                                 (first && kk == 0) ? 0u : 1u);
+                mma_commit_pair(bar_empty16 + 8 * s, kPairMask);
+                if (last) {
+                    mma_commit_pair(bar_accfull + 8 * buf, kPairMask);
+                    ++c;
+                }
+                if (++kb == KB) kb = 0;
+            }
+        }
+      } else {
+        // ---------------------------------------------------------------- converters
+        // 1024 16-byte int8 chunks per stage ([A 128 rows | W 128 rows] x 4 chunks of each
+        // 64-byte staging row); thread ct takes idx = ct + 192 j (j < 6, idx < 1024): row
+        // ct / 4 + 48 j, chunk ct % 4. (row & 7) does not change with j, so the swizzled
+        // fp16 address is a per-thread base plus 6144 j bytes.
+        const int ct = threadIdx.x - 64;
+        const int r0 = ct >> 2, c0 = ct & 3;
+        const uint32_t src0 = (uint32_t)(ct * 16);
+        const uint32_t dst0 = sw128(r0, 2 * c0);
+        const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
+        for (int g = 0; g < total_g; ++g) {
+            const int s8 = g % S8, s16 = g % S16;
+            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
+                break;
+            const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
+            uint4 in[6];
+#pragma unroll
+            for (int j = 0; j < 6; ++j)
+                in[j] = (ct + kConv * j < kChunks8) ? lds128(st8 + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
+                           &g_tc2_error))
+                break;
+            const uint32_t st16 = sbase + s16 * kStage16;
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                if (ct + kConv * j < kChunks8) {
+                    uint4 o0, o1;
+                    cvt_word(in[j].x, o0.x, o0.y);
+                    cvt_word(in[j].y, o0.z, o0.w);
+                    cvt_word(in[j].z, o1.x, o1.y);
+                    cvt_word(in[j].w, o1.z, o1.w);
+                    sts128(st16 + dst0 + 6144 * j, o0);
+                    sts128(st16 + dst1 + 6144 * j, o1);
+                }
+            }
+            // Every lane makes its fp16 stores visible to the tensor core, then one lane per
+            // warp arrives on the even CTA's barrier (which issues the pair MMA): locally
+            // there, with a cluster-scope release from the odd CTA.
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(bar_full16 + 8 * s16);
+                else
+                    mbar_arrive_cluster(mapa_shared(bar_full16 + 8 * s16, 0));
+                mbar_arrive(bar_empty8 + 8 * s8);   // after the loaded registers were consumed
+            }
+        }
+      }
+    } else {
+        // ---------------------------------------------------------------- drain + epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh));
+        const int quarter = warp & 3;
+        const int col_half = (warp - 8) >> 2;
+        int acc[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) acc[c] = 0;
+        const int chunks_total = my_tiles * CPT;
+        int ti = 0, cc = 0;
+        for (int c = 0; c < chunks_total; ++c, (++cc == CPT ? (cc = 0, ++ti) : 0)) {
+            const int buf = c & 1;
+            if (!mbar_wait(bar_accfull + 8 * buf, (uint32_t)((c >> 1) & 1), abort_flag, kErrDrain, &g_tc2_error))
+                break;
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + col_half * 128);
+            const int keep = cc != 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t v[32];
+                tmem_ld32(taddr + j * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    acc[j * 32 + e] = acc[j * 32 + e] * keep + __float2int_rn(__uint_as_float(v[e]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_accempty + 8 * buf, 0));
+            if (cc != CPT - 1) continue;
+            int m0, n0;
+            pair_coords(tg, cluster + ti * nclusters, m0, n0);
+            const int m = m0 + (int)rank * BMH + quarter * 32 + lane;
+            const int nb = n0 + col_half * 128;
+            if (m < M) {
+                if (ep.out_i32) {
+                    int32_t* row = ep.out_i32 + (int64_t)m * N;
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (nb + e < N) row[nb + e] = acc[e];
+                } else {
+                    const float sa = ep.s_a[ep.a_per_row ? m : 0];
+                    const int za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
+                    float* row = ep.y + (int64_t)m * N;
+                    const bool vec = ((N & 3) == 0);
+                    const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
+                    const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
+#pragma unroll
+                    for (int e4 = 0; e4 < 32; ++e4) {
+                        const int n = nb + e4 * 4;
+                        const bool full = n + 3 < N;
+                        float sw4[4];
+                        int cs4[4] = {0, 0, 0, 0};
+                        if (vsw && full) {
+                            const float4 t4 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
+                            sw4[0] = t4.x; sw4[1] = t4.y; sw4[2] = t4.z; sw4[3] = t4.w;
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
+                        }
+                        if (ep.z_a) {
+                            if (vcs && full) {
+                                const int4 t4 = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
+                                cs4[0] = t4.x; cs4[1] = t4.y; cs4[2] = t4.z; cs4[3] = t4.w;
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
+                            }
+                        }
+                        float o[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int corr = acc[e4 * 4 + q] - za * cs4[q];
+                            o[q] = __fmul_rn(__int2float_rn(corr), __fmul_rn(sa, sw4[q]));
+                        }
+                        if (vec && full) {
+                            *reinterpret_cast<float4*>(row + n) = make_float4(o[0], o[1], o[2], o[3]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (n + q < N) row[n + q] = o[q];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // Wind down: both CTAs finish (the even CTA's MMA reads the odd CTA's shared
+    // memory and the odd CTA arrives on the even CTA's barriers until the end).
+    if (*abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1LL << 22)) __nanosleep(1000);
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K) {
+    if (!(M >= 1 && N >= 1 && K >= 16 && (K % 16) == 0 && M < (1LL << 31) && N < (1LL << 31))) return false;
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t kb = (K + BK - 1) / BK;
+    return tiles < (1LL << 30) && tiles * kb < (1LL << 31);
+}
+
+// Clusters of two that fit on the device at once (a GPC with an odd number of
+// free SMs leaves one idle), so that the persistent grid runs in one wave.
+// Cached per device; SMs / 2 if the occupancy query fails.
+static int resident_pairs() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
+    if (cached[dev] > 0) return cached[dev];
+    int pairs = device_sm_count() / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) == cudaSuccess && n > 0 && n < pairs) pairs = n;
+    (void)cudaGetLastError();
+    cached[dev] = pairs;
+    return pairs;
+}
+
+cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                            const Epilogue& ep, cudaStream_t stream) {
+    if (!gemm_tc2_supports(M, N, K)) return cudaErrorNotSupported;
+    CUtensorMap ma, mw;
+    if (!make_tma_map_i8(&ma, qa, M, K, BMH, BK) || !make_tma_map_i8(&mw, qw, N, K, BNH, BK))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t pairs = resident_pairs();
+    const int clusters = (int)(tiles < pairs ? tiles : pairs);
+    gemm_tc2_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(ma, mw, (int)M, (int)N, (int)K, ep);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc2_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *code = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_tc2_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace q8

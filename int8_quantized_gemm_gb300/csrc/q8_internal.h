@@ -46,6 +46,11 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream);
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
 
+// tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles).
+cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                            const Epilogue& ep, cudaStream_t stream);
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K);
+
 // tcgen05 kernel for M <= 16 (decode): weight rows on the MMA's M side.
 cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
                            const Epilogue& ep, cudaStream_t stream);
@@ -60,5 +65,6 @@ bool gemv_mma_supports(int64_t M, int64_t N, int64_t K);
 cudaError_t read_and_clear_gemm_tc_error(uint32_t* code);
 cudaError_t read_and_clear_gemv_tc_error(uint32_t* code);
 cudaError_t read_and_clear_gemv_mma_error(uint32_t* code);
+cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code);
 
 }  // namespace q8

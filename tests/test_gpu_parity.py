@@ -15,7 +15,7 @@ from tests import gates
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ("tcgen05", "mma_s8", "skinny", "decode", "decode_tc")
+KERNELS = ("tcgen05", "tcgen05_pair", "mma_s8", "skinny", "decode", "decode_tc")
 
 
 def runs(kernel, M):
@@ -147,9 +147,10 @@ def test_gemm_s32_repeatable_under_load(q8, M, N, K, reps):
     ref = oracle.gemm_acc(qa, qw, threads=16)
     da, dw = dev(qa), dev(qw)
     for _ in range(reps):
-        acc = host(q8.q8_gemm_s32(da, dw, kernel="tcgen05")).astype(np.int64)
-        assert_no_device_error(q8)
-        np.testing.assert_array_equal(acc, ref)
+        for kernel in ("tcgen05", "tcgen05_pair"):
+            acc = host(q8.q8_gemm_s32(da, dw, kernel=kernel)).astype(np.int64)
+            assert_no_device_error(q8)
+            np.testing.assert_array_equal(acc, ref)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
