@@ -42,8 +42,8 @@ constexpr int BMH = 128;
 constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per CTA)
 constexpr int BNH = 128;
 constexpr int BK = 64;
-constexpr int S8 = 6;               // int8 staging stages (16 KB)
-constexpr int S16 = 3;              // fp16 operand stages (32 KB)
+constexpr int S8 = 4;               // int8 staging stages (16 KB)
+constexpr int S16 = 4;              // fp16 operand stages (32 KB)
 constexpr int KB_PER_CHUNK = 16;    // 1024 K per exact fp32 chunk
 constexpr int kConv = 192;          // converter threads, warps 2..7 of each CTA
 constexpr int kDrainWarps = 8;      // warps 8..15 of each CTA
@@ -56,7 +56,7 @@ constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16; 
 constexpr int kChunks8 = kStage8 / 16;                                            // 1024
 constexpr int kOffStage8 = S16 * kStage16;
 constexpr int kOffBar = kOffStage8 + S8 * kStage8;
-constexpr int kBarBytes = 8 * (2 * S8 + 2 * S16 + 4) + 16;
+constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
 constexpr int kSmem = kOffBar + kBarBytes + 1024;
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 constexpr uint16_t kPairMask = 0x3;
@@ -86,11 +86,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + (sbase - sraw);
     const uint32_t bar_full8 = sbase + kOffBar;
     const uint32_t bar_empty8 = bar_full8 + 8 * S8;
-    const uint32_t bar_full16 = bar_empty8 + 8 * S8;     // used in the even CTA: 2 x 6 converter warps
+    const uint32_t bar_full16 = bar_empty8 + 8 * S8;     // used in the even CTA: its 6 converter warps + relay
     const uint32_t bar_empty16 = bar_full16 + 8 * S16;   // both CTAs: the pair MMA's commit
     const uint32_t bar_accfull = bar_empty16 + 8 * S16;  // both CTAs: the pair MMA's commit
     const uint32_t bar_accempty = bar_accfull + 16;      // used in the even CTA: 2 x 8 drain warps
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * S8 + 2 * S16 + 4));
+    const uint32_t bar_conv16 = bar_accempty + 16;       // used in the odd CTA: its 6 converter warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * S8 + 3 * S16 + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -103,8 +104,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar_empty8 + 8 * s, kConv / 32);
         }
         for (int s = 0; s < S16; ++s) {
-            mbar_init(bar_full16 + 8 * s, 2 * (kConv / 32));
+            mbar_init(bar_full16 + 8 * s, kConv / 32 + 1);
             mbar_init(bar_empty16 + 8 * s, 1);
+            mbar_init(bar_conv16 + 8 * s, kConv / 32);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
@@ -184,6 +186,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (++kb == KB) kb = 0;
             }
+        } else if (!leader && lane == 0) {
+            // ---------------------------------------------------------------- relay (odd CTA)
+            // Forwards "stage converted" to the even CTA with one remote arrive per stage.
+            // The converted operands stay in this CTA's shared memory, fenced to the async
+            // proxy by the converters, and the pair MMA reads them from here.
+            for (int g = 0; g < total_g; ++g) {
+                const int s = g % S16;
+                if (!mbar_wait(bar_conv16 + 8 * s, (uint32_t)((g / S16) & 1), abort_flag, kErrRelay, &g_tc2_error))
+                    break;
+                mbar_arrive_remote(mapa_shared(bar_full16 + 8 * s, 0));
+            }
         }
       } else {
         // ---------------------------------------------------------------- converters
@@ -222,15 +235,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             // Every lane makes its fp16 stores visible to the tensor core, then one lane per
-            // warp arrives on the even CTA's barrier (which issues the pair MMA): locally
-            // there, with a cluster-scope release from the odd CTA.
+            // warp arrives: on the MMA barrier in the even CTA, on the relay's barrier in
+            // the odd one.
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (leader)
-                    mbar_arrive(bar_full16 + 8 * s16);
-                else
-                    mbar_arrive_cluster(mapa_shared(bar_full16 + 8 * s16, 0));
+                mbar_arrive((leader ? bar_full16 : bar_conv16) + 8 * s16);
                 mbar_arrive(bar_empty8 + 8 * s8);   // after the loaded registers were consumed
             }
         }

@@ -18,7 +18,8 @@ enum : unsigned {
     kErrConvEmpty = 4u,
     kErrMmaFull = 8u,
     kErrMmaAcc = 16u,
-    kErrDrain = 32u
+    kErrDrain = 32u,
+    kErrRelay = 64u     // CTA pairs: the odd CTA's forwarder of converted stages
 };
 
 
@@ -214,6 +215,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 // Arrive on an mbarrier of any CTA in the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster with the instruction's default
+// ordering (release at CTA scope). For announcing data that sits in the arriving CTA's
+// own shared memory, already made visible to the async proxy (the pair MMA reads each
+// CTA's operand half through that CTA's shared memory), or for handing back a buffer.
+// A cluster-scope release costs a memory fence of several hundred nanoseconds per
+// arrive, which serialises a per-stage hand-off.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {

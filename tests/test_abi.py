@@ -100,9 +100,12 @@ def test_quantize_rejects_bad_arguments(lib):
 def test_kernel_pick_is_a_concrete_kernel(lib):
     import int8_quantized_gemm_gb300 as q8
     for shape in ((16, 28672, 8192), (8192, 8192, 16384), (1, 1, 16), (513, 100, 48)):
-        assert q8.q8_gemm_pick(*shape) in ("tcgen05", "mma_s8", "skinny", "decode")
+        assert q8.q8_gemm_pick(*shape) in ("tcgen05", "tcgen05_pair", "mma_s8", "skinny", "decode")
     assert q8.q8_gemm_pick(16, 28672, 8192) == "decode"
-    assert q8.q8_gemm_pick(8192, 8192, 16384) == "tcgen05"
+    assert q8.q8_gemm_pick(8192, 8192, 16384) == "tcgen05_pair"
+    assert q8.q8_gemm_pick(2048, 4096, 4096) == "tcgen05_pair"
+    assert q8.q8_gemm_pick(17, 4096, 4096) == "skinny"
+    assert q8.q8_gemm_pick(300, 1000, 1024) == "skinny"
 
 
 def test_binding_refuses_cpu_tensors():
