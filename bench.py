@@ -276,7 +276,12 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "step_ms": {"mean": round(statistics.mean(step_ms), 4), "min": round(min(step_ms), 4),
+                        "median": round(statistics.median(step_ms), 4)},
+            "gemm_ms": {"mean": round(gemm_avg, 4), "min": round(min(gemm_ms), 4),
+                        "median": round(statistics.median(gemm_ms), 4)},
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": f"{HEADLINE}: A fp32 [{M},{K}] per-token sym x W int8 [{N},{K}] per-channel"
                                    f" sym -> y fp32 [{M},{N}]",
