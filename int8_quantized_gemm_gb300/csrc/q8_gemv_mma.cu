@@ -3,7 +3,9 @@
 //
 // With a handful of tokens the layer is a stream of the int8 weights from HBM
 // with little arithmetic per byte. The weights go HBM -> shared memory by TMA
-// (a 16-stage ring per SM) and shared memory -> registers by ordinary loads;
+// (an 8-stage ring per SM; a stage is 64 rows x 256 bytes of K, fetched as two
+// 128-byte boxes, which streams DRAM better than 128-byte row pieces) and shared
+// memory -> registers by ordinary loads;
 // each warp converts its int8 fragments to fp16 in registers and feeds them
 // straight to the MMA, so converted data never goes back through shared memory.
 // (The int8 MMA of this GPU runs at a fraction of the fp16 rate, too low for
@@ -14,9 +16,10 @@
 // exactly representable integer) before it is converted to int32 and added to
 // an INT32 total, so the result is the exact integer dot product.
 //
-// K order inside a stage: compute warp s owns the 16 K values [16s, 16s+16) of
-// every stage, one MMA K-step; lane quad t holds the 4 bytes [16s + 4t, +4) of
-// its rows, bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3) as (8+2t, 9+2t).
+// K order inside a stage: compute warp s (of 16) owns the 16 K values
+// [16s, 16s+16) of every stage, one MMA K-step; lane quad t holds the 4 bytes
+// [16s + 4t, +4) of its rows, bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3)
+// as (8+2t, 9+2t).
 // Weights and activations use the same mapping, so the dot products are
 // unchanged. With the 128-byte TMA swizzle these 4-byte loads hit 32 distinct
 // banks.
@@ -24,7 +27,7 @@
 // Work: 64 weight rows (output channels) per tile, tiles dealt round-robin to
 // one CTA per SM. Each compute warp covers all 64 rows (eight n8 groups, eight
 // independent accumulators) for its K-step, so a token fragment is converted
-// once per eight MMAs; at the end of a tile the eight K-step partials are
+// once per eight MMAs; at the end of a tile the sixteen K-step partials are
 // added in shared memory (integer adds, exact) and written out.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,16 +46,17 @@ using namespace tc;
 
 constexpr int RW = 64;             // weight rows per tile
 constexpr int NT = 16;             // token rows (MMA M)
-constexpr int BK = 128;            // K per stage
-constexpr int S8 = 16;             // stages in the ring
-constexpr int kW8 = RW * BK;       // 8 KB of weights per stage
-constexpr int kA8 = NT * BK;       // 2 KB of activations per stage
+constexpr int BK = 256;            // K per stage: two 128-byte swizzled boxes per operand
+constexpr int BKH = 128;
+constexpr int S8 = 10;             // stages in the ring
+constexpr int kW8 = RW * BK;       // 16 KB of weights per stage: [half 0 | half 1]
+constexpr int kA8 = NT * BK;       // 4 KB of activations per stage
 constexpr int kStage = kW8 + kA8;
 constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
 constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int kStagesPerChunk = 64;   // 64 stages x 16 K per warp = 1024 products per fp32 sum
-constexpr int kOffRed = S8 * kStage;  // int32 [16 tokens][64 rows] tile sums
-constexpr int kRedBytes = NT * RW * 4;
+constexpr int kOffRed = S8 * kStage;  // int32 [2][16 tokens][64 rows] tile sums (tile parity)
+constexpr int kRedBytes = 2 * NT * RW * 4;
 constexpr int kOffBar = kOffRed + kRedBytes;
 constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 
@@ -120,50 +124,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sbase + s * kStage;
                 mbar_expect_tx(bar_full + 8 * s, kStage);
                 tma_load_2d(dst, &tmap_w, kx, n0, bar_full + 8 * s);
+                tma_load_2d(dst + RW * BKH, &tmap_w, kx + BKH, n0, bar_full + 8 * s);
                 tma_load_2d(dst + kW8, &tmap_a, kx, 0, bar_full + 8 * s);
+                tma_load_2d(dst + kW8 + NT * BKH, &tmap_a, kx + BKH, 0, bar_full + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
     } else {
         // ---------------------------------------------------------------- compute warps
         const int ks = warp - 1;          // K-step of each stage: bytes [16 ks, 16 ks + 16)
-        const int ct = threadIdx.x - 32;  // 0 .. 255
+        const int ct = threadIdx.x - 32;  // 0 .. 511
         const int g8 = lane >> 2, t = lane & 3;
-        // weight row 8j + g and token rows g, g+8 at chunk ks (swizzled), word t
+        const int half = ks >> 3, kc = ks & 7;   // which 128-byte box, 16-byte chunk in its rows
+        // weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t
         uint32_t w_off[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w_off[j] = sw128(8 * j + g8, ks) + 4 * t;
-        const uint32_t a_off0 = kW8 + sw128(g8, ks) + 4 * t;
-        const uint32_t a_off1 = kW8 + sw128(g8 + 8, ks) + 4 * t;
-        for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) red[i] = 0;
+        for (int j = 0; j < 8; ++j) w_off[j] = half * (RW * BKH) + sw128(8 * j + g8, kc) + 4 * t;
+        const uint32_t a_off0 = kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
+        const uint32_t a_off1 = kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
+        for (int i = ct; i < 2 * NT * RW; i += 32 * kComputeWarps) red[i] = 0;
         named_barrier(1, 32 * kComputeWarps);
+        // Epilogue outputs of this thread: tokens em and em + 8, row er of each tile. The token
+        // scales are loaded once here; the channel scales at the tile's end (loading them at the
+        // tile's first stage measured slower).
+        const int em = ct / RW, er = ct % RW;
+        float esa0 = 0.0f, esa1 = 0.0f, esw = 0.0f;
+        int eza0 = 0, eza1 = 0, ecs = 0;
+        if (!ep.out_i32) {
+            if (em < M) {
+                esa0 = __ldg(ep.s_a + (ep.a_per_row ? em : 0));
+                if (ep.z_a) eza0 = __ldg(ep.z_a + (ep.a_per_row ? em : 0));
+            }
+            if (em + 8 < M) {
+                esa1 = __ldg(ep.s_a + (ep.a_per_row ? em + 8 : 0));
+                if (ep.z_a) eza1 = __ldg(ep.z_a + (ep.a_per_row ? em + 8 : 0));
+            }
+        }
         int tot[8][4];
         float part[8][4];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) tot[j][e] = 0, part[j][e] = 0.0f;
-        int kb = 0, ti = 0, in_chunk = 0;
-        for (int g = 0; g < total_g; ++g) {
+        int kb = 0, ti = 0, in_chunk = 0, g = 0;
+        for (; g < total_g; ++g) {
             const int s = g % S8;
-            if (!mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_gemv_mma_error))
+            // warp-uniform: the whole warp leaves together when a wait gives up (abort)
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag,
+                                                   kErrConvFull, &g_gemv_mma_error)))
                 break;
             const uint32_t st = sbase + s * kStage;
             uint32_t wq[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_off[j]);
             const uint32_t aq0 = lds32(st + a_off0), aq1 = lds32(st + a_off1);
-            uint32_t a[4];
+            uint32_t a[4], b[8][2];
             cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
             cvt_word(aq1, a[1], a[3]);     // token row g+8
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t b0, b1;
-                cvt_word(wq[j], b0, b1);   // weight row 8j + g
-                mma_m16n8k16(part[j], a, b0, b1);
-            }
+            for (int j = 0; j < 8; ++j) cvt_word(wq[j], b[j][0], b[j][1]);   // weight row 8j + g
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // the loaded registers have been consumed
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             const bool tile_end = (kb == KB - 1);
             if (++in_chunk == kStagesPerChunk || tile_end) {
                 in_chunk = 0;
@@ -176,36 +199,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
             }
             if (tile_end) {
-                // add the eight K-step partials of the tile in shared memory (integer adds)
+                // add the sixteen K-step partials of the tile in shared memory (integer adds),
+                // in the tile-sum buffer of this tile's parity
+                int32_t* rb = red + (ti & 1) * (NT * RW);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
                         const int r = 8 * j + 2 * t + (e & 1);
-                        atomicAdd(red + m * RW + r, tot[j][e]);
+                        atomicAdd(rb + m * RW + r, tot[j][e]);
                         tot[j][e] = 0;
                     }
                 named_barrier(1, 32 * kComputeWarps);
-                const int n0 = ((int)blockIdx.x + ti * (int)gridDim.x) * RW;
-                for (int i = ct; i < NT * RW; i += 32 * kComputeWarps) {
-                    const int m = i / RW, n = n0 + i % RW;
-                    const int v = red[i];
-                    red[i] = 0;
-                    if (m < M && n < N) {
-                        if (ep.out_i32) {
-                            ep.out_i32[(int64_t)m * N + n] = v;
-                        } else {
-                            const int r = ep.a_per_row ? m : 0;
-                            const int corr = ep.z_a ? v - __ldg(ep.z_a + r) * __ldg(ep.colsum + n) : v;
-                            const float sc = __fmul_rn(__ldg(ep.s_a + r), __ldg(ep.s_w + (ep.w_per_row ? n : 0)));
-                            ep.y[(int64_t)m * N + n] = __fmul_rn(__int2float_rn(corr), sc);
-                        }
+                // Read and re-zero this thread's two sums. The buffer is next written at tile
+                // ti + 2, after every thread has passed the tile barrier of tile ti + 1.
+                const int i0 = em * RW + er, i1 = i0 + 8 * RW;
+                const int v0 = rb[i0], v1 = rb[i1];
+                rb[i0] = 0;
+                rb[i1] = 0;
+                const int n = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + er;
+                if (n < N && !ep.out_i32) {
+                    esw = __ldg(ep.s_w + (ep.w_per_row ? n : 0));
+                    if (ep.z_a) ecs = __ldg(ep.colsum + n);
+                }
+                if (n < N) {
+                    if (ep.out_i32) {
+                        if (em < M) ep.out_i32[(int64_t)em * N + n] = v0;
+                        if (em + 8 < M) ep.out_i32[(int64_t)(em + 8) * N + n] = v1;
+                    } else {
+                        if (em < M)
+                            ep.y[(int64_t)em * N + n] =
+                                __fmul_rn(__int2float_rn(v0 - eza0 * ecs), __fmul_rn(esa0, esw));
+                        if (em + 8 < M)
+                            ep.y[(int64_t)(em + 8) * N + n] =
+                                __fmul_rn(__int2float_rn(v1 - eza1 * ecs), __fmul_rn(esa1, esw));
                     }
                 }
-                named_barrier(1, 32 * kComputeWarps);   // the sums are zero again for the next tile
             }
             if (++kb == KB) { kb = 0; ++ti; }
+        }
+        // After an abort: pass the tile-end barriers still ahead, so that no compute warp
+        // waits at one forever.
+        for (; g < total_g; ++g) {
+            if (kb == KB - 1) named_barrier(1, 32 * kComputeWarps);
+            if (++kb == KB) kb = 0;
         }
     }
     __syncthreads();
@@ -228,7 +266,7 @@ cudaError_t launch_gemv_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64
                             const Epilogue& ep, cudaStream_t stream) {
     if (!gemv_mma_supports(M, N, K)) return cudaErrorNotSupported;
     CUtensorMap mw, ma;
-    if (!make_tma_map_i8(&mw, qw, N, K, RW, BK, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BK, true))
+    if (!make_tma_map_i8(&mw, qw, N, K, RW, BKH, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BKH, true))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
