@@ -357,9 +357,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D int8 tensor map over a row-major [rows, K] matrix, box [box_rows, box_k],
-// optionally 128-byte swizzled, zero fill outside.
+// with the given shared-memory swizzle, zero fill outside.
 bool make_map_impl(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k,
-                   bool swizzle128) {
+                   CUtensorMapSwizzle swizzle) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -367,8 +367,7 @@ bool make_map_impl(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K
     cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -385,7 +384,25 @@ int sm_count_impl() {
 
 bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k,
                      bool swizzle128) {
-    return make_map_impl(map, base, rows, K, box_rows, box_k, swizzle128);
+    return make_map_impl(map, base, rows, K, box_rows, box_k,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows) {
+    return make_map_impl(map, base, rows, K, box_rows, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool make_tma_map_out32(CUtensorMap* map, void* base, bool is_float, int64_t rows, int64_t cols) {
+    auto enc = get_encode();
+    if (!enc || (cols % 4) != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 int device_sm_count() { return sm_count_impl(); }

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "q8_internal.h"
 #include "q8_tc_ptx.cuh"
@@ -55,7 +56,9 @@ constexpr int kA8 = BMH * BK, kB8 = BNH * BK, kStage8 = kA8 + kB8;              
 constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16;   // 32 KB
 constexpr int kChunks8 = kStage8 / 16;                                            // 1024
 constexpr int kOffStage8 = S16 * kStage16;
-constexpr int kOffBar = kOffStage8 + S8 * kStage8;
+constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 32 block of 4-byte outputs (TMA store source)
+constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
+constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
 constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
 constexpr int kSmem = kOffBar + kBarBytes + 1024;
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
@@ -79,7 +82,7 @@ __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-                    int M, int N, int K, Epilogue ep) {
+                    const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, Epilogue ep) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -277,61 +280,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (cc != CPT - 1) continue;
             int m0, n0;
             pair_coords(tg, cluster + ti * nclusters, m0, n0);
-            const int m = m0 + (int)rank * BMH + quarter * 32 + lane;
+            const int mrow0 = m0 + (int)rank * BMH + quarter * 32;
+            const int m = mrow0 + lane;
             const int nb = n0 + col_half * 128;
-            if (m < M) {
-                if (ep.out_i32) {
-                    int32_t* row = ep.out_i32 + (int64_t)m * N;
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (nb + e < N) row[nb + e] = acc[e];
+            float sa = 0.0f;
+            int za = 0;
+            if (!ep.out_i32 && m < M) {
+                sa = ep.s_a[ep.a_per_row ? m : 0];
+                za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
+            }
+            const bool vec = ((N & 3) == 0);
+            const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
+            const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
+            // outputs (m, n .. n + 3) of accumulator columns e .. e + 3, as 4-byte words
+            auto out4 = [&](int e, int n) -> uint4 {
+                if (ep.out_i32) return make_uint4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                const bool full = n + 3 < N;
+                float sw4[4];
+                int cs4[4] = {0, 0, 0, 0};
+                if (vsw && full) {
+                    const float4 t4 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
+                    sw4[0] = t4.x; sw4[1] = t4.y; sw4[2] = t4.z; sw4[3] = t4.w;
                 } else {
-                    const float sa = ep.s_a[ep.a_per_row ? m : 0];
-                    const int za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
-                    float* row = ep.y + (int64_t)m * N;
-                    const bool vec = ((N & 3) == 0);
-                    const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
-                    const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
 #pragma unroll
-                    for (int e4 = 0; e4 < 32; ++e4) {
-                        const int n = nb + e4 * 4;
-                        const bool full = n + 3 < N;
-                        float sw4[4];
-                        int cs4[4] = {0, 0, 0, 0};
-                        if (vsw && full) {
-                            const float4 t4 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
-                            sw4[0] = t4.x; sw4[1] = t4.y; sw4[2] = t4.z; sw4[3] = t4.w;
-                        } else {
+                    for (int q = 0; q < 4; ++q) sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
+                }
+                if (ep.z_a) {
+                    if (vcs && full) {
+                        const int4 t4 = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
+                        cs4[0] = t4.x; cs4[1] = t4.y; cs4[2] = t4.z; cs4[3] = t4.w;
+                    } else {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
-                        }
-                        if (ep.z_a) {
-                            if (vcs && full) {
-                                const int4 t4 = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
-                                cs4[0] = t4.x; cs4[1] = t4.y; cs4[2] = t4.z; cs4[3] = t4.w;
-                            } else {
+                        for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
+                    }
+                }
+                uint32_t o[4];
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
-                            }
-                        }
-                        float o[4];
+                for (int q = 0; q < 4; ++q)
+                    o[q] = __float_as_uint(__fmul_rn(__int2float_rn(acc[e + q] - za * cs4[q]), __fmul_rn(sa, sw4[q])));
+                return make_uint4(o[0], o[1], o[2], o[3]);
+            };
+            if (tma_out) {
+                // Each 32 x 32 block goes through this warp's shared buffer (128-byte swizzle: row
+                // `lane`, 16-byte chunk c at chunk c ^ (lane & 7)) and one TMA store, which writes
+                // whole lines and clips rows >= M and columns >= N.
+                const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - 8) * kEpiBytes);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int corr = acc[e4 * 4 + q] - za * cs4[q];
-                            o[q] = __fmul_rn(__int2float_rn(corr), __fmul_rn(sa, sw4[q]));
-                        }
-                        if (vec && full) {
-                            *reinterpret_cast<float4*>(row + n) = make_float4(o[0], o[1], o[2], o[3]);
-                        } else {
+                for (int j = 0; j < 4; ++j) {
+                    if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
+                    __syncwarp();
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (n + q < N) row[n + q] = o[q];
-                        }
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        sts128(ebuf + (uint32_t)(lane * 128 + ((c4 ^ (lane & 7)) << 4)),
+                               out4(j * 32 + c4 * 4, nb + j * 32 + c4 * 4));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_out, ebuf, nb + j * 32, mrow0);
+                        bulk_commit();
+                    }
+                }
+            } else if (m < M) {
+                uint32_t* row = ep.out_i32 ? reinterpret_cast<uint32_t*>(ep.out_i32) + (int64_t)m * N
+                                           : reinterpret_cast<uint32_t*>(ep.y) + (int64_t)m * N;
+#pragma unroll
+                for (int e4 = 0; e4 < 32; ++e4) {
+                    const int n = nb + e4 * 4;
+                    const uint4 o = out4(e4 * 4, n);
+                    if (vec && n + 3 < N) {
+                        *reinterpret_cast<uint4*>(row + n) = o;
+                    } else {
+                        if (n < N) row[n] = o.x;
+                        if (n + 1 < N) row[n + 1] = o.y;
+                        if (n + 2 < N) row[n + 2] = o.z;
+                        if (n + 3 < N) row[n + 3] = o.w;
                     }
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();   // stores done before the shared buffers go away
     }
 
     // Wind down: both CTAs finish (the even CTA's MMA reads the odd CTA's shared
@@ -386,7 +413,12 @@ cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t pairs = resident_pairs();
     const int clusters = (int)(tiles < pairs ? tiles : pairs);
-    gemm_tc2_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(ma, mw, (int)M, (int)N, (int)K, ep);
+    CUtensorMap mo;
+    const bool tma_out = ep.out_i32 ? make_tma_map_out32(&mo, ep.out_i32, false, M, N)
+                                    : make_tma_map_out32(&mo, ep.y, true, M, N);
+    if (!tma_out) memset(&mo, 0, sizeof(mo));
+    gemm_tc2_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N, (int)K,
+                                                                ep);
     note_launch();
     return cudaGetLastError();
 }

@@ -194,6 +194,20 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// TMA tensor store of a box from shared memory (bulk-group completion), and the waits on
+// the issuing thread's bulk groups: ".read" only until the shared-memory source has been read.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 // Two CTAs of a cluster share one MMA: the even CTA issues it, A rows and B rows
 // are split between the pair's shared memories, and each CTA's tensor memory
@@ -299,6 +313,13 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 // False if the driver entry point is missing.
 bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k,
                      bool swizzle128 = false);
+// Same with box [box_rows, 64] and the 64-byte swizzle: the 16-byte chunk c of row r
+// lands at chunk c ^ ((r >> 1) & 3) of its 64-byte row (shared-memory base 512-byte aligned).
+bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows);
+// Output map for TMA stores: 4-byte elements (fp32 or int32) of a row-major [rows, cols]
+// matrix, box [32 rows, 32 cols] with the 128-byte swizzle. False unless cols % 4 == 0 and
+// the base is 16-byte aligned (the row pitch must be a multiple of 16 bytes).
+bool make_tma_map_out32(CUtensorMap* map, void* base, bool is_float, int64_t rows, int64_t cols);
 int device_sm_count();
 
 }  // namespace q8
