@@ -55,8 +55,11 @@ constexpr int kStage = kW8 + kA8;
 constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
 constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int kStagesPerChunk = 64;   // 64 stages x 16 K per warp = 1024 products per fp32 sum
-constexpr int kOffRed = S8 * kStage;  // int32 [2][16 tokens][64 rows] tile sums (tile parity)
-constexpr int kRedBytes = 2 * NT * RW * 4;
+// int32 tile sums [2 (tile parity)][16 tokens][64 rows], token rows padded to 72 words so
+// that the eight tokens of one atomic instruction fall in different banks (2-way, not 8-way)
+constexpr int RWP = RW + 8;
+constexpr int kOffRed = S8 * kStage;
+constexpr int kRedBytes = 2 * NT * RWP * 4;
 constexpr int kOffBar = kOffRed + kRedBytes;
 constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) w_off[j] = half * (RW * BKH) + sw128(8 * j + g8, kc) + 4 * t;
         const uint32_t a_off0 = kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
         const uint32_t a_off1 = kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
-        for (int i = ct; i < 2 * NT * RW; i += 32 * kComputeWarps) red[i] = 0;
+        for (int i = ct; i < 2 * NT * RWP; i += 32 * kComputeWarps) red[i] = 0;
         named_barrier(1, 32 * kComputeWarps);
         // Epilogue outputs of this thread: tokens em and em + 8, row er of each tile. The token
         // scales are loaded once here; the channel scales at the tile's end (loading them at the
@@ -201,20 +204,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tile_end) {
                 // add the sixteen K-step partials of the tile in shared memory (integer adds),
                 // in the tile-sum buffer of this tile's parity
-                int32_t* rb = red + (ti & 1) * (NT * RW);
+                int32_t* rb = red + (ti & 1) * (NT * RWP);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
                         const int r = 8 * j + 2 * t + (e & 1);
-                        atomicAdd(rb + m * RW + r, tot[j][e]);
+                        atomicAdd(rb + m * RWP + r, tot[j][e]);
                         tot[j][e] = 0;
                     }
                 named_barrier(1, 32 * kComputeWarps);
                 // Read and re-zero this thread's two sums. The buffer is next written at tile
                 // ti + 2, after every thread has passed the tile barrier of tile ti + 1.
-                const int i0 = em * RW + er, i1 = i0 + 8 * RW;
+                const int i0 = em * RWP + er, i1 = i0 + 8 * RWP;
                 const int v0 = rb[i0], v1 = rb[i1];
                 rb[i0] = 0;
                 rb[i1] = 0;
