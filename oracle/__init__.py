@@ -15,7 +15,9 @@ Every function follows a passage of the pages (cited in q8_oracle.c):
   gemm_acc                       Day 98 (accumulate loop); "Activation
                                  Quantization Architecture" (The integer GEMM)
   linear_codes / linear_codes_at Day 98 (epilogue listing)
-All of them are pinned by tests/test_oracle_pins.py.
+  rmsnorm / rmsnorm_quantize     "Activation Quantization Architecture" (Fusion:
+                                 the fused norm-and-quantize pseudocode)
+All of them are pinned by tests/test_oracle_pins.py and tests/test_oracle_rmsnorm.py.
 """
 from __future__ import annotations
 
@@ -76,6 +78,8 @@ def _load():
         lib.q8o_linear_codes_at.restype = i32
         lib.q8o_sym_scale.argtypes = [ctypes.c_float]
         lib.q8o_sym_scale.restype = ctypes.c_float
+        lib.q8o_rmsnorm.argtypes = [p, p, i64, i64, ctypes.c_float, p, p]
+        lib.q8o_rmsnorm.restype = i32
         lib.q8o_openmp_max_threads.argtypes = []
         lib.q8o_openmp_max_threads.restype = i32
         _lib = lib
@@ -116,6 +120,28 @@ def quantize_asym(x: np.ndarray, per_row: bool):
     st = _load().q8o_quantize_asym(_ptr(x), rows, cols, int(per_row), _ptr(q), _ptr(s), _ptr(z))
     assert st == OK
     return q, s, z
+
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float):
+    """RMSNorm rows of fp32 x with weights gamma; returns (y fp32, exact sum of squares per row
+    as float64). The sum is exact and rounded once to fp32 (see q8o_rmsnorm)."""
+    x = _c(x, np.float32)
+    gamma = _c(gamma, np.float32)
+    rows, cols = x.shape
+    assert gamma.shape == (cols,)
+    y = np.empty((rows, cols), np.float32)
+    sumsq = np.empty(rows, np.float64)
+    st = _load().q8o_rmsnorm(_ptr(x), _ptr(gamma), rows, cols, ctypes.c_float(eps), _ptr(y), _ptr(sumsq))
+    assert st == OK
+    return y, sumsq
+
+
+def rmsnorm_quantize(x: np.ndarray, gamma: np.ndarray, eps: float) -> dict:
+    """Fused RMSNorm + per-token symmetric quantization: qa int8, sa fp32 [rows], plus the
+    normalised rows y and the per-row sums of squares."""
+    y, sumsq = rmsnorm(x, gamma, eps)
+    qa, sa = quantize_sym(y, per_row=True)
+    return {"qa": qa, "sa": sa, "y": y, "sumsq": sumsq}
 
 
 def sym_scale(amax: float) -> np.float32:

@@ -34,6 +34,10 @@
  *    after the kernel listing).
  *  - epilogue corr = acc - z * colsum, y = (float)corr * (s_a * s_w), the
  *    multiply order of the Day 98 epilogue listing.
+ *  - fused RMSNorm + per-token quantization ("Activation Quantization
+ *    Architecture", Fusion: the fused norm-and-quantize pseudocode):
+ *      rms = sqrt(mean(x * x) + eps), y = x / rms * gamma, then the symmetric
+ *    per-token quantizer above on y (see q8o_rmsnorm for the summation reading).
  * rint() is round-half-to-even in the default rounding mode, matching np.rint
  * in the numpy reference of "Activation Quantization Architecture".
  */
@@ -240,6 +244,39 @@ int q8o_linear_codes_at(const int8_t* qa, const float* sa, const int32_t* za, in
         if (st > status) status = st;
     }
     return status;
+}
+
+/*
+ * RMSNorm of each row of x[rows][cols] with per-column weights gamma[cols]
+ * ("Activation Quantization Architecture", Fusion pseudocode):
+ *   rms = sqrt(mean(x * x) + eps),  y = x / rms * gamma.
+ * The pages do not fix the order of the sum in mean(x * x). Reading taken: the
+ * sum S of the exact squares x_k^2 is formed exactly and rounded once to fp32,
+ * so that the value does not depend on any order. Here each square is exact in
+ * long double (a 24-bit significand squared needs 48 bits) and the running sum
+ * keeps at least 64 significand bits, far below one fp32 ulp of S for any row
+ * length this file is used with. After that every step is one fp32 operation in
+ * the order written: mean = fl(fl(S) / cols), r = sqrtf(fl(mean + eps)),
+ * y_k = fl(fl(x_k / r) * gamma_k). sumsq[row] (optional) receives S as a double.
+ */
+int q8o_rmsnorm(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps, float* y,
+                double* sumsq) {
+    if (rows < 0 || cols <= 0 || !(eps >= 0.0f)) return Q8O_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * cols;
+        long double acc = 0.0L;
+        for (int64_t k = 0; k < cols; ++k) {
+            const long double v = (long double)xr[k];
+            acc += v * v;
+        }
+        if (sumsq) sumsq[r] = (double)acc;
+        const float ms = (float)acc;                 /* one rounding of the exact sum */
+        const float mean = ms / (float)cols;
+        const float rms = sqrtf(mean + eps);
+        float* yr = y + r * cols;
+        for (int64_t k = 0; k < cols; ++k) yr[k] = (xr[k] / rms) * gamma[k];
+    }
+    return Q8O_OK;
 }
 
 int q8o_openmp_max_threads(void) {

@@ -73,3 +73,16 @@ def ulp_distance(x, y):
     xi = np.where(xi < 0, np.int64(-2**31) - xi, xi)
     yi = np.where(yi < 0, np.int64(-2**31) - yi, yi)
     return np.abs(xi - yi)
+
+
+def near_f32_midpoint(s, rel: float = 2.0 ** -36) -> np.ndarray:
+    """True where the value s (float64) lies within rel * |s| of a midpoint between two
+    adjacent fp32 values: there an accurate sum formed in another order may round to
+    either neighbour, so both are correct results of the reading "exact sum, rounded once"."""
+    s = np.asarray(s, np.float64)
+    f = s.astype(np.float32)
+    lo = np.nextafter(f, np.float32(-np.inf)).astype(np.float64)
+    hi = np.nextafter(f, np.float32(np.inf)).astype(np.float64)
+    f64 = f.astype(np.float64)
+    d = np.minimum(np.abs(s - (f64 + lo) / 2), np.abs(s - (f64 + hi) / 2))
+    return d <= rel * np.abs(s)
