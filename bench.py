@@ -271,6 +271,9 @@ def run_ours(args, world, rank, local):
     # ---- decode-shaped workload (HBM-bound): same step, reported beside the headline
     decode = None if args.no_decode else measure_decode(q8, device, args, hbm_peak, flush)
 
+    # ---- fused RMSNorm + per-token quantization of the same activations (HBM-bound)
+    rmsq = measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak)
+
     cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     if rank == 0:
@@ -295,6 +298,7 @@ def run_ours(args, world, rank, local):
             "quantizer": {"ms": round(quant_avg, 4), "GB/s": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
                           "bytes": quant_bytes},
             "decode": decode,
+            "rmsnorm_quantize": rmsq,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "weight_prep_ms": round(weight_prep_ms, 3),
@@ -401,6 +405,34 @@ def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode
             "gemm_GB/s": round(gemm_bytes / (gq * 1e-3) / 1e9, 1),
             "gemm_frac_hbm": round(gemm_bytes / (gq * 1e-3) / 1e9 / hbm_peak, 4),
             "algorithmic_bytes": gemm_bytes, "per_kernel": per_kernel}
+
+
+def measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak):
+    """The fused norm-and-quantize kernel on the headline activations, L2 flushed before
+    each launch; algorithmic bytes: read A (4 M K) and gamma (4 K), write codes (M K) and
+    scales (4 M)."""
+    import torch
+    M, K = a.shape
+    gamma = torch.from_numpy(workloads.make_norm_weights(K, seed=4)).to(a.device)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        q8.q8_rmsnorm_quantize_act(a, gamma, 1e-6, qa=qa, s_a=s_a)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(max(10, args.steps)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        q8.q8_rmsnorm_quantize_act(a, gamma, 1e-6, qa=qa, s_a=s_a)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    mean = statistics.mean(ms)
+    nbytes = 5 * M * K + 4 * M + 4 * K
+    return {"workload": f"{HEADLINE} activations [{M},{K}], gamma [{K}], eps 1e-6", "ms": round(mean, 4),
+            "GB/s": round(nbytes / (mean * 1e-3) / 1e9, 1), "frac_hbm": round(nbytes / (mean * 1e-3) / 1e9 / hbm_peak, 4),
+            "bytes": nbytes}
 
 
 # ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)

@@ -98,6 +98,33 @@ q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g
                           q8_stream_t stream);
 
 /*
+ * Fused RMSNorm + per-token symmetric activation quantization, the step before
+ * the GEMM when the layer input comes out of a normalisation ("Activation
+ * Quantization Architecture", Fusion: the kernel pseudocode for the fused norm
+ * and quantize step). Per row m of a:
+ *   rms = sqrt(mean_k a[m,k]^2 + eps),  y[m,k] = a[m,k] / rms * gamma[k],
+ *   then s_a[m] and qa[m,:] from y exactly as q8_quantize_act(Q8_PER_ROW,
+ *   Q8_SYMMETRIC) would compute them from y.
+ * Arithmetic: the sum of squares is the exact sum rounded once to fp32 (any
+ * order of summation gives it, up to sums within ~2^-40 of an fp32 rounding
+ * midpoint, where either neighbour is returned); then fp32 IEEE operations in
+ * the order written: mean = sum / K, rms = sqrt(mean + eps), y = (a / rms) *
+ * gamma. y itself is not stored: one pass reads a and writes the codes.
+ *
+ * a     : fp32 [M, K], read only, 16-byte aligned.
+ * gamma : fp32 [K], read only, 16-byte aligned.
+ * eps   : > 0 and finite.
+ * qa    : int8 [M, K], written, 16-byte aligned.
+ * s_a   : fp32 [M], written.
+ * Errors: Q8_ERR_INVALID_ARG for null or misaligned pointers (M > 0), M < 0,
+ * K <= 0 with M > 0, or eps not > 0; Q8_ERR_UNSUPPORTED for K % 16 != 0 or
+ * K > 2^24 (K must convert to fp32 exactly for the mean).
+ * M == 0 returns Q8_OK without touching the device.
+ */
+q8_status q8_rmsnorm_quantize_act(const float* a, const float* gamma, int64_t M, int64_t K, float eps,
+                                  int8_t* qa, float* s_a, q8_stream_t stream);
+
+/*
  * Offline symmetric weight quantization, per output channel or per tensor,
  * with the symmetric rule above ("Activation Quantization Architecture", the
  * numpy reference quantize_per_channel; Day 98, one scale per column of B).

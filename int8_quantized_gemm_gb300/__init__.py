@@ -5,6 +5,7 @@ libq8.so. PyTorch supplies device memory and the current stream. There is no
 CPU fallback; if the library is missing or a call fails, an exception says so.
 
   q8_quantize_act(a, per_row=True, symmetric=True)   -> qa, s_a, z_a
+  q8_rmsnorm_quantize_act(a, gamma, eps)             -> qa, s_a   (fused RMSNorm + per-token quantize)
   q8_quantize_weight(w, per_row=True)                 -> qw, s_w
   q8_colsum(qw)                                       -> colsum
   q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum)      -> y
@@ -21,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "Q8Error", "load", "q8_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
+    "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_s32", "q8_linear", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
@@ -52,6 +53,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.q8_quantize_act.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
+    lib.q8_rmsnorm_quantize_act.argtypes = [p, p, i64, i64, ctypes.c_float, p, p, p]
     lib.q8_quantize_weight.argtypes = [p, i64, i64, i32, p, p, p]
     lib.q8_colsum.argtypes = [p, i64, i64, p, p]
     lib.q8_gemm_dequant.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, p]
@@ -63,7 +65,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.q8_launch_count.argtypes = []
     lib.q8_launch_count.restype = ctypes.c_uint64
-    for name in ("q8_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
+    for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_s32_ex", "q8_gemm_pick", "q8_device_error"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -118,6 +120,22 @@ def q8_quantize_act(a: torch.Tensor, per_row: bool = True, symmetric: bool = Tru
                                   Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(s_a),
                                   _ptr(z_a), _stream(stream)), "q8_quantize_act")
     return qa, s_a, z_a
+
+
+def q8_rmsnorm_quantize_act(a: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, qa=None, s_a=None,
+                            stream=None):
+    """Fused RMSNorm (weights gamma[K], eps under the root) + per-token symmetric quantization
+    of fp32 a[M, K]; returns (qa int8 [M, K], s_a fp32 [M])."""
+    _need(a, torch.float32, "a", 2)
+    _need(gamma, torch.float32, "gamma", 1)
+    M, K = a.shape
+    if gamma.numel() != K:
+        raise ValueError("gamma must have K entries")
+    qa = torch.empty((M, K), dtype=torch.int8, device=a.device) if qa is None else qa
+    s_a = torch.empty(M, dtype=torch.float32, device=a.device) if s_a is None else s_a
+    _check(load().q8_rmsnorm_quantize_act(_ptr(a), _ptr(gamma), M, K, ctypes.c_float(eps), _ptr(qa), _ptr(s_a),
+                                          _stream(stream)), "q8_rmsnorm_quantize_act")
+    return qa, s_a
 
 
 def q8_quantize_weight(w: torch.Tensor, per_row: bool = True, qw=None, s_w=None, stream=None):

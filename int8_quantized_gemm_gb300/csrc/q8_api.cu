@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <math.h>
 
 #include "q8_internal.h"
 
@@ -120,6 +121,19 @@ q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g
     if (g == Q8_PER_ROW && M == 0) return Q8_OK;
     return from_cuda(q8::launch_quantize(a, M, K, g == Q8_PER_ROW, qa, s_a, z_a,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_rmsnorm_quantize_act(const float* a, const float* gamma, int64_t M, int64_t K, float eps, int8_t* qa,
+                                  float* s_a, q8_stream_t stream) {
+    if (M < 0 || !(eps > 0.0f) || !(eps < INFINITY)) return Q8_ERR_INVALID_ARG;
+    if (M == 0) return Q8_OK;
+    if (K <= 0) return Q8_ERR_INVALID_ARG;
+    if (!a || !gamma || !qa || !s_a || !aligned(a, 16) || !aligned(gamma, 16) || !aligned(qa, 16) ||
+        !aligned(s_a, 4))
+        return Q8_ERR_INVALID_ARG;
+    if (K % 16 != 0 || K > (int64_t(1) << 24)) return Q8_ERR_UNSUPPORTED;
+    return from_cuda(q8::launch_rmsnorm_quantize(a, gamma, M, K, eps, qa, s_a,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 q8_status q8_quantize_weight(const float* w, int64_t N, int64_t K, q8_granularity g, int8_t* qw, float* s_w,

@@ -22,6 +22,9 @@ constexpr float kZeroGuard = 1e-8f;
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row,
                             int8_t* q, float* s, int32_t* z, cudaStream_t stream);
 
+// Fused RMSNorm + per-token symmetric quantization of x[rows, cols] (cols % 4 == 0).
+cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps,
+                                   int8_t* q, float* s, cudaStream_t stream);
 cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum,
                           cudaStream_t stream);
 

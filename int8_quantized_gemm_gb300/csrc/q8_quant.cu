@@ -252,6 +252,159 @@ __global__ void __launch_bounds__(256) colsum_kernel(const int8_t* __restrict__ 
     if (lane == 0) colsum[n] = acc;
 }
 
+// ------------------------------------------------------------------ fused RMSNorm + quantize
+// rms = sqrt(mean(x * x) + eps), y = x / rms * gamma, then the per-token symmetric quantizer
+// on y. The sum of squares is the exact sum rounded once to fp32: every square is split into
+// its fp32 product and the exact remainder (one FMA), and the running sums are kept as
+// unevaluated pairs (hi, lo) combined with TwoSum (Knuth), about twice fp32's precision, so
+// the single final rounding fl(hi + lo) is the exactly rounded sum unless that sum lies
+// within ~2^-40 of an fp32 rounding midpoint (where either neighbour is a correct rounding).
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2) {
+    float s, e;
+    two_sum(hi, h2, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(l2, e));
+}
+
+__device__ __forceinline__ void pair_add_square(float& hi, float& lo, float v) {
+    const float p = __fmul_rn(v, v);
+    pair_add(hi, lo, p, __fmaf_rn(v, v, -p));   // v * v == p + remainder exactly
+}
+
+// Block-wide sum of the pairs; every thread receives lane 0's fl(hi + lo), so the whole
+// row uses the same bits (lanes of a butterfly may differ in the last bit of lo).
+__device__ __forceinline__ float block_sum_pairs(float hi, float lo, float* red) {
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nwarps = blockDim.x / kWarp;
+    hi = __shfl_sync(0xffffffffu, hi, 0);
+    lo = __shfl_sync(0xffffffffu, lo, 0);
+    if (lane == 0) {
+        red[warp] = hi;
+        red[32 + warp] = lo;
+    }
+    __syncthreads();
+    hi = lane < nwarps ? red[lane] : 0.0f;
+    lo = lane < nwarps ? red[32 + lane] : 0.0f;
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    return __shfl_sync(0xffffffffu, __fadd_rn(hi, lo), 0);
+}
+
+__device__ __forceinline__ float rms_of(float sumsq, int64_t cols, float eps) {
+    const float mean = __fdiv_rn(sumsq, (float)cols);
+    return __fsqrt_rn(__fadd_rn(mean, eps));
+}
+
+__device__ __forceinline__ float norm1(float x, float rms, float g) { return __fmul_rn(__fdiv_rn(x, rms), g); }
+
+// One CTA per row, the row in registers (VPT float4 per thread): one HBM read of x. Up to
+// four float4 per thread the kernel fits 32 registers, so two 1024-thread CTAs share an SM
+// (the row phases - load, reduce, normalise, reduce, store - of one CTA overlap the other's).
+template <int VPT>
+__global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1))
+    rmsnorm_quantize_rows_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int64_t cols,
+                                 float eps, int8_t* __restrict__ q, float* __restrict__ s) {
+    __shared__ float red[64];
+    __shared__ float red2[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
+    const float4* g4 = reinterpret_cast<const float4*>(gamma);
+    float4 v[VPT];
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4) {
+            v[j] = __ldcs(xr + i);
+            pair_add_square(hi, lo, v[j].x);
+            pair_add_square(hi, lo, v[j].y);
+            pair_add_square(hi, lo, v[j].z);
+            pair_add_square(hi, lo, v[j].w);
+        }
+    }
+    const float rms = rms_of(block_sum_pairs(hi, lo, red), cols, eps);
+    float amax = 0.0f, unused = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4) {
+            const float4 g = __ldg(g4 + i);
+            v[j] = make_float4(norm1(v[j].x, rms, g.x), norm1(v[j].y, rms, g.y), norm1(v[j].z, rms, g.z),
+                               norm1(v[j].w, rms, g.w));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+        }
+    }
+    block_max2<false>(amax, unused, red2);
+    const float sc = sym_scale(amax);
+    if (threadIdx.x == 0) s[row] = sc;
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4)
+            qr[i] = pack4(sym_code(v[j].x, sc), sym_code(v[j].y, sc), sym_code(v[j].z, sc), sym_code(v[j].w, sc));
+    }
+}
+
+// Rows longer than the register budget: three sweeps (sum of squares; y and its maximum;
+// codes), the later ones served mostly from L2.
+__global__ void __launch_bounds__(1024)
+    rmsnorm_quantize_long_rows_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                      int64_t cols, float eps, int8_t* __restrict__ q, float* __restrict__ s) {
+    __shared__ float red[64];
+    __shared__ float red2[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
+    const float4* g4 = reinterpret_cast<const float4*>(gamma);
+    float hi = 0.0f, lo = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = xr[i];
+        pair_add_square(hi, lo, v.x);
+        pair_add_square(hi, lo, v.y);
+        pair_add_square(hi, lo, v.z);
+        pair_add_square(hi, lo, v.w);
+    }
+    const float rms = rms_of(block_sum_pairs(hi, lo, red), cols, eps);
+    float amax = 0.0f, unused = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = xr[i];
+        const float4 g = __ldg(g4 + i);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(norm1(v.x, rms, g.x)), fabsf(norm1(v.y, rms, g.y))),
+                                 fmaxf(fabsf(norm1(v.z, rms, g.z)), fabsf(norm1(v.w, rms, g.w)))));
+    }
+    block_max2<false>(amax, unused, red2);
+    const float sc = sym_scale(amax);
+    if (threadIdx.x == 0) s[row] = sc;
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = __ldcs(xr + i);
+        const float4 g = __ldg(g4 + i);
+        qr[i] = pack4(sym_code(norm1(v.x, rms, g.x), sc), sym_code(norm1(v.y, rms, g.y), sc),
+                      sym_code(norm1(v.z, rms, g.z), sc), sym_code(norm1(v.w, rms, g.w), sc));
+    }
+}
+
+template <int VPT>
+cudaError_t launch_rms_rows(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps, int threads,
+                            int8_t* q, float* s, cudaStream_t st) {
+    rmsnorm_quantize_rows_kernel<VPT><<<(unsigned)rows, threads, 0, st>>>(x, gamma, cols, eps, q, s);
+    note_launch();
+    return cudaGetLastError();
+}
+
 int num_sms() {
     static int sms = 0;
     if (sms == 0) {
@@ -321,6 +474,24 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per
     }
     return z ? dispatch_tensor<true>(x, rows * cols, q, s, z, stream)
              : dispatch_tensor<false>(x, rows * cols, q, s, z, stream);
+}
+
+cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps,
+                                   int8_t* q, float* s, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const int64_t n4 = cols / 4;
+    auto threads_for = [&](int vpt) {
+        int64_t t = (n4 + vpt - 1) / vpt;
+        t = ((t + kWarp - 1) / kWarp) * kWarp;
+        return (int)(t < kWarp ? kWarp : t);
+    };
+    if (n4 <= 1024 * 1) return launch_rms_rows<1>(x, gamma, rows, cols, eps, threads_for(1), q, s, stream);
+    if (n4 <= 1024 * 2) return launch_rms_rows<2>(x, gamma, rows, cols, eps, threads_for(2), q, s, stream);
+    if (n4 <= 1024 * 4) return launch_rms_rows<4>(x, gamma, rows, cols, eps, threads_for(4), q, s, stream);
+    if (n4 <= 1024 * 8) return launch_rms_rows<8>(x, gamma, rows, cols, eps, threads_for(8), q, s, stream);
+    rmsnorm_quantize_long_rows_kernel<<<(unsigned)rows, 1024, 0, stream>>>(x, gamma, cols, eps, q, s);
+    note_launch();
+    return cudaGetLastError();
 }
 
 cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream) {

@@ -73,6 +73,21 @@ def test_gemm_rejects_bad_arguments(lib):
     assert lib.q8_launch_count() == before
 
 
+def test_rmsnorm_quantize_rejects_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    f = lambda a, g, M, K, eps, qa, sa: lib.q8_rmsnorm_quantize_act(a, g, M, K, ctypes.c_float(eps), qa, sa, None)
+    assert f(FAKE, FAKE, 0, 32, 1e-6, FAKE, FAKE) == q8.Q8_OK                       # empty: nothing enqueued
+    assert f(FAKE, FAKE, 4, 32, 0.0, FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG           # eps must be > 0
+    assert f(FAKE, FAKE, 4, 32, float("inf"), FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 32, float("nan"), FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, -1, 32, 1e-6, FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 0, 1e-6, FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG           # mean over no elements
+    assert f(FAKE, None, 4, 32, 1e-6, FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG          # gamma required
+    assert f(FAKE, MISALIGNED, 4, 32, 1e-6, FAKE, FAKE) == q8.Q8_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 24, 1e-6, FAKE, FAKE) == q8.Q8_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, 4, (1 << 24) + 16, 1e-6, FAKE, FAKE) == q8.Q8_ERR_UNSUPPORTED
+
+
 def test_k_limits_are_the_int32_bounds():
     # 128*128*K < 2^31 for raw codes; 255*128*K < 2^31 with a zero point.
     assert 128 * 128 * 131056 < 2 ** 31 <= 128 * 128 * (131056 + 16)

@@ -1,0 +1,127 @@
+"""GPU parity of the fused RMSNorm + per-token quantization (q8_rmsnorm_quantize_act)
+against the oracle ("Activation Quantization Architecture", Fusion pseudocode).
+
+Reading shared by both sides: the sum of squares of a row is the exact sum rounded
+once to fp32; everything after it is fp32 IEEE arithmetic in the order written. The
+oracle forms the sum in long double, the kernel with error-free pair arithmetic, so
+both round to the same fp32 value unless the exact sum lies on (within 2^-36 of) a
+midpoint between two fp32 values, where either neighbour is a correct rounding. Rows
+away from a midpoint must match bit for bit (codes and scales); a flagged row may
+differ by one code step and a few ulp of scale.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gates
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module")
+def q8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import int8_quantized_gemm_gb300 as q8mod
+    from int8_quantized_gemm_gb300 import build
+    build.build()
+    q8mod.load()
+    return q8mod
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def compare(qa, s_a, ref):
+    flag = gates.near_f32_midpoint(ref["sumsq"])
+    ok = ~flag
+    np.testing.assert_array_equal(s_a[ok], ref["sa"][ok])
+    np.testing.assert_array_equal(qa[ok], ref["qa"][ok])
+    if flag.any():
+        assert int(gates.ulp_distance(s_a[flag], ref["sa"][flag]).max()) <= 4
+        assert int(np.abs(qa[flag].astype(np.int32) - ref["qa"][flag]).max()) <= 1
+    return int(flag.sum())
+
+
+CASES = [
+    # (M, K, workload the activations are shaped like): K spans every kernel tier
+    (16, 256, "tiny"),
+    (512, 2048, "prefill2k"),
+    (33, 4112, "prefill2k"),      # 1028 float4 per row: two per thread
+    (16, 8192, "decode"),
+    (40, 8208, "relu4k"),         # four per thread
+    (64, 16384, "prefill16k"),    # four per thread, 1024 threads
+    (9, 20000, "prefill2k"),      # eight per thread
+    (5, 40000, "prefill2k"),      # longer than the register budget: three sweeps
+    (1, 16, "tiny"),
+]
+
+
+@pytest.mark.parametrize("M,K,name", CASES)
+def test_rmsnorm_quantize_matches_oracle(q8, M, K, name):
+    a = workloads.make_activations(workloads.WORKLOADS[name], M=M, K=K)
+    if M > 2:
+        a[M // 2] = 0.0                                  # a padding token: rms = sqrt(eps)
+        a[1] *= np.float32(1e-3)                         # a row where eps is not negligible
+    gamma = workloads.make_norm_weights(K, seed=M + K)
+    qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
+    torch.cuda.synchronize()
+    compare(host(qa), host(s_a), oracle.rmsnorm_quantize(a, gamma, EPS))
+
+
+def test_rmsnorm_quantize_full_size_sampled_rows(q8):
+    wl = workloads.WORKLOADS["prefill16k"]
+    a = workloads.make_activations(wl)
+    gamma = workloads.make_norm_weights(wl.K, seed=4)
+    qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(0).choice(wl.M, size=256, replace=False)
+    rows.sort()
+    ref = oracle.rmsnorm_quantize(a[rows], gamma, EPS)
+    compare(host(qa)[rows], host(s_a)[rows], ref)
+
+
+def test_rmsnorm_constant_rows_exact(q8):
+    # closed form: a row of c gives y = sign(c) gamma exactly when eps is negligible
+    K = 512
+    gamma = workloads.make_norm_weights(K, seed=9)
+    a = np.stack([np.full(K, c, np.float32) for c in (3.0, -0.75, 12.0, 1.0)])
+    qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), 1e-30)
+    ref_q, ref_s = oracle.quantize_sym(np.sign(a) * gamma[None, :], per_row=True)
+    np.testing.assert_array_equal(host(qa), ref_q)
+    np.testing.assert_array_equal(host(s_a), ref_s)
+
+
+def test_fused_then_gemm_matches_oracle_layer(q8):
+    wl = workloads.WORKLOADS["prefill2k"]
+    M, N, K = 300, 264, 2048
+    a = workloads.make_activations(wl, M=M, K=K)
+    w = workloads.make_weights(wl, N=N, K=K)
+    gamma = workloads.make_norm_weights(K, seed=1)
+    qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
+    qw, s_w = q8.q8_quantize_weight(dev(w), per_row=True)
+    y = q8.q8_gemm_dequant(qa, s_a, None, qw, s_w)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_quantize(a, gamma, EPS)
+    assert not gates.near_f32_midpoint(ref["sumsq"]).any()
+    rqw, rsw = oracle.quantize_sym(w, per_row=True)
+    ry, st = oracle.linear_codes(ref["qa"], ref["sa"], None, rqw, rsw, a_per_row=True, w_per_row=True)
+    assert st == oracle.OK
+    yi = host(y).view(np.int32).astype(np.int64)
+    ri = ry.view(np.int32).astype(np.int64)
+    assert np.max(np.abs(yi - ri)) <= 2
+
+
+def test_rmsnorm_empty(q8):
+    a = torch.empty((0, 64), dtype=torch.float32, device="cuda")
+    g = torch.ones(64, dtype=torch.float32, device="cuda")
+    qa, s_a = q8.q8_rmsnorm_quantize_act(a, g, EPS)
+    assert qa.shape == (0, 64) and s_a.shape == (0,)

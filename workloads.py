@@ -129,3 +129,8 @@ def gaussian(shape, seed: int, std: float = 1.0) -> np.ndarray:
 
 def uniform01(shape, seed: int) -> np.ndarray:
     return _rng(seed, 11).random(shape, dtype=np.float32)
+
+
+def make_norm_weights(K: int, seed: int = 0) -> np.ndarray:
+    """fp32 gamma[K] of an RMSNorm in front of the layer: 1 + 0.1 N(0, 1) per channel."""
+    return (np.float32(1.0) + np.float32(0.1) * _rng(seed, 12).standard_normal(K, dtype=np.float32)).astype(np.float32)
