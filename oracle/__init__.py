@@ -17,6 +17,9 @@ Every function follows a passage of the pages (cited in q8_oracle.c):
   linear_codes / linear_codes_at Day 98 (epilogue listing)
   rmsnorm / rmsnorm_quantize     "Activation Quantization Architecture" (Fusion:
                                  the fused norm-and-quantize pseudocode)
+  linear_codes_bias, to_bf16,    "Activation Quantization Architecture" (Fusion:
+  quantize_static                the epilogue adds the bias, writes bf16, or
+                                 quantizes the output for the next GEMM)
 All of them are pinned by tests/test_oracle_pins.py and tests/test_oracle_rmsnorm.py.
 """
 from __future__ import annotations
@@ -79,6 +82,12 @@ def _load():
         lib.q8o_sym_scale.argtypes = [ctypes.c_float]
         lib.q8o_sym_scale.restype = ctypes.c_float
         lib.q8o_rmsnorm.argtypes = [p, p, i64, i64, ctypes.c_float, p, p]
+        lib.q8o_linear_codes_bias.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32]
+        lib.q8o_linear_codes_bias.restype = i32
+        lib.q8o_to_bf16.argtypes = [p, i64, p]
+        lib.q8o_to_bf16.restype = None
+        lib.q8o_quantize_static.argtypes = [p, i64, ctypes.c_float, p]
+        lib.q8o_quantize_static.restype = None
         lib.q8o_rmsnorm.restype = i32
         lib.q8o_openmp_max_threads.argtypes = []
         lib.q8o_openmp_max_threads.restype = i32
@@ -189,6 +198,38 @@ def linear_codes(qa, sa, za, qw, sw, a_per_row: bool, w_per_row: bool, threads: 
     st = _load().q8o_linear_codes(_ptr(qa), _ptr(sa), _ptr(za), int(a_per_row),
                                   _ptr(qw), _ptr(sw), int(w_per_row), M, N, K, _ptr(y), threads)
     return y, st
+
+
+def linear_codes_bias(qa, sa, za, qw, sw, bias, a_per_row: bool, w_per_row: bool, threads: int = 1):
+    """fp32 y[M, N] from codes and scales plus bias[N] (None: no bias); returns (y, status)."""
+    qa = _c(qa, np.int8)
+    qw = _c(qw, np.int8)
+    sa = _c(sa, np.float32)
+    sw = _c(sw, np.float32)
+    za = None if za is None else _c(za, np.int32)
+    bias = None if bias is None else _c(bias, np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    y = np.empty((M, N), np.float32)
+    st = _load().q8o_linear_codes_bias(_ptr(qa), _ptr(sa), _ptr(za), int(a_per_row), _ptr(qw), _ptr(sw),
+                                       int(w_per_row), _ptr(bias), M, N, K, _ptr(y), threads)
+    return y, st
+
+
+def to_bf16(y: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp32 values, round-to-nearest-even."""
+    y = _c(y, np.float32)
+    out = np.empty(y.shape, np.uint16)
+    _load().q8o_to_bf16(_ptr(y), y.size, _ptr(out))
+    return out
+
+
+def quantize_static(y: np.ndarray, s_out: float) -> np.ndarray:
+    """int8 codes clamp(rint(y / s_out), -127, 127) with a fixed output scale."""
+    y = _c(y, np.float32)
+    q = np.empty(y.shape, np.int8)
+    _load().q8o_quantize_static(_ptr(y), y.size, ctypes.c_float(s_out), _ptr(q))
+    return q
 
 
 def linear_codes_at(qa, sa, za, qw, sw, ms, ns, a_per_row: bool, w_per_row: bool):

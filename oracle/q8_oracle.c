@@ -34,6 +34,12 @@
  *    after the kernel listing).
  *  - epilogue corr = acc - z * colsum, y = (float)corr * (s_a * s_w), the
  *    multiply order of the Day 98 epilogue listing.
+ *  - epilogue variants ("Activation Quantization Architecture", Fusion: the
+ *    epilogue multiplies by the per-token and per-channel scales, adds the bias
+ *    and writes bf16; some kernels quantize the output for the next GEMM):
+ *      y = fl(corr * scale) + bias[n] (one fp32 add), then either fp32, bf16
+ *    rounded to nearest-even, or int8 codes clamp(rint(y / s_out), -127, 127)
+ *    with a static per-tensor output scale s_out.
  *  - fused RMSNorm + per-token quantization ("Activation Quantization
  *    Architecture", Fusion: the fused norm-and-quantize pseudocode):
  *      rms = sqrt(mean(x * x) + eps), y = x / rms * gamma, then the symmetric
@@ -44,6 +50,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <string.h>
 
 #define Q8O_ZERO_GUARD 1e-8f
 
@@ -226,6 +233,41 @@ int q8o_linear_codes(const int8_t* qa, const float* sa, const int32_t* za, int a
 }
 
 /* y at a list of (m, n) pairs; same arguments as q8o_linear_codes. */
+/*
+ * The linear layer from codes with the epilogue variants of "Activation
+ * Quantization Architecture" (Fusion): y = fl((float)corr * (s_a * s_w)) as in
+ * q8o_linear_codes, then y + bias[n] in fp32 when bias is given.
+ */
+int q8o_linear_codes_bias(const int8_t* qa, const float* sa, const int32_t* za, int a_per_row,
+                          const int8_t* qw, const float* sw, int w_per_row, const float* bias,
+                          int64_t M, int64_t N, int64_t K, float* y, int threads) {
+    int status = q8o_linear_codes(qa, sa, za, a_per_row, qw, sw, w_per_row, M, N, K, y, threads);
+    if (bias) {
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) y[m * N + n] = y[m * N + n] + bias[n];
+    }
+    return status;
+}
+
+/*
+ * fp32 -> bf16 with round-to-nearest-even on the bit pattern: keep the high 16
+ * bits after adding 0x7FFF plus the lowest kept bit (finite inputs; the pages
+ * name bf16 as the epilogue's output type).
+ */
+void q8o_to_bf16(const float* y, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        memcpy(&u, &y[i], sizeof u);
+        u += 0x7FFFu + ((u >> 16) & 1u);
+        out[i] = (uint16_t)(u >> 16);
+    }
+}
+
+/* Static output quantization for the next GEMM: clamp(rint(y / s_out), -127, 127). */
+void q8o_quantize_static(const float* y, int64_t n, float s_out, int8_t* q) {
+    for (int64_t i = 0; i < n; ++i) q[i] = (int8_t)q8o_sym_code(y[i], s_out);
+}
+
 int q8o_linear_codes_at(const int8_t* qa, const float* sa, const int32_t* za, int a_per_row,
                         const int8_t* qw, const float* sw, int w_per_row, int64_t K,
                         const int64_t* ms, const int64_t* ns, int64_t count,
