@@ -179,6 +179,35 @@ q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* 
                              q8_granularity gw, const int32_t* colsum, int64_t M, int64_t N,
                              int64_t K, float* y, q8_gemm_kernel kernel, q8_stream_t stream);
 
+/* Output type of q8_gemm_epilogue_ex. */
+typedef enum q8_out_type {
+    Q8_OUT_F32 = 0,   /* fp32 y */
+    Q8_OUT_BF16 = 1,  /* bf16 y (uint16 bit patterns), round to nearest even */
+    Q8_OUT_I8 = 2     /* int8 codes clamp(rint(y / out_scale), -127, 127) for the next GEMM */
+} q8_out_type;
+
+/*
+ * q8_gemm_dequant_ex with the epilogue variants of "Activation Quantization
+ * Architecture" (Fusion: after the int32 accumulation the epilogue multiplies
+ * by the per-token and per-channel scales, adds the bias and writes bf16; some
+ * kernels quantize the output for the next GEMM directly):
+ *   y[m][n] = fl((float)corr * (s_a * s_w)) + bias[n]   (one fp32 add; no bias: + 0 skipped)
+ * then written as out_type. The output quantization uses a static per-tensor
+ * scale (out_scale, e.g. from calibration): a per-token output scale would need
+ * each row's maximum over all N before any code could be written.
+ *
+ * bias      : fp32 [N] or NULL, 4-byte aligned.
+ * out       : fp32 / bf16 / int8 [M, N] by out_type, written, 16-byte aligned.
+ * out_scale : Q8_OUT_I8 only: > 0 and finite.
+ * Other arguments, limits and errors as q8_gemm_dequant_ex. With K == 0 the
+ * output is bias (or zeros) in the requested type.
+ */
+q8_status q8_gemm_epilogue_ex(const int8_t* qa, const float* s_a, const int32_t* z_a,
+                              q8_granularity ga, const int8_t* qw, const float* s_w,
+                              q8_granularity gw, const int32_t* colsum, const float* bias,
+                              int64_t M, int64_t N, int64_t K, q8_out_type out_type, void* out,
+                              float out_scale, q8_gemm_kernel kernel, q8_stream_t stream);
+
 /*
  * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),
  * computed by the same main loop as q8_gemm_dequant_ex with the same kernel

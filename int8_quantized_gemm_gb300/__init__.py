@@ -9,6 +9,7 @@ CPU fallback; if the library is missing or a call fails, an exception says so.
   q8_quantize_weight(w, per_row=True)                 -> qw, s_w
   q8_colsum(qw)                                       -> colsum
   q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum)      -> y
+  q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum, bias, out_dtype, out_scale) -> y (+bias; fp32/bf16/int8)
   q8_gemm_s32(qa, qw)                                 -> acc (raw INT32 accumulators)
   q8_linear(a, qw, s_w, colsum)                       -> y   (quantize A, then GEMM)
 """
@@ -23,7 +24,7 @@ from . import build as _build
 
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
-    "q8_gemm_s32", "q8_linear", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -58,6 +59,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_colsum.argtypes = [p, i64, i64, p, p]
     lib.q8_gemm_dequant.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, p]
     lib.q8_gemm_dequant_ex.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32, p]
+    lib.q8_gemm_epilogue_ex.argtypes = [p, p, p, i32, p, p, i32, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_gemm_pick.argtypes = [i64, i64, i64]
     lib.q8_status_string.argtypes = [i32]
@@ -66,7 +68,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_launch_count.argtypes = []
     lib.q8_launch_count.restype = ctypes.c_uint64
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
-                 "q8_gemm_dequant_ex", "q8_gemm_s32_ex", "q8_gemm_pick", "q8_device_error"):
+                 "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_gemm_pick", "q8_device_error"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -185,6 +187,47 @@ def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "a
                                      _ptr(colsum if z_a is not None else None), M, N, K, _ptr(y),
                                      KERNELS[kernel], _stream(stream)), "q8_gemm_dequant")
     return y
+
+
+OUT_TYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int8: 2}
+
+
+def q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
+                     out=None, kernel: str = "auto", stream=None):
+    """Quantized linear layer with the epilogue variants: y = (acc - z_a*colsum) * (s_a*s_w) + bias,
+    written as fp32, bf16, or int8 codes with the static output scale out_scale."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw, torch.int8, "qw", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qa and qw disagree on K")
+    if out_dtype not in OUT_TYPES:
+        raise TypeError("out_dtype must be torch.float32, torch.bfloat16 or torch.int8")
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    if s_a.numel() not in (1, M) or s_w.numel() not in (1, N):
+        raise ValueError("s_a must have 1 or M entries and s_w 1 or N entries")
+    ga = Q8_PER_ROW if (s_a.numel() == M and M != 1) else Q8_PER_TENSOR
+    gw = Q8_PER_ROW if (s_w.numel() == N and N != 1) else Q8_PER_TENSOR
+    if z_a is not None:
+        _need(z_a, torch.int32, "z_a", 1)
+        if colsum is None:
+            raise ValueError("an asymmetric A needs the weight column sums")
+        _need(colsum, torch.int32, "colsum", 1)
+    if bias is not None:
+        _need(bias, torch.float32, "bias", 1)
+        if bias.numel() != N:
+            raise ValueError("bias must have N entries")
+    if out_dtype == torch.int8 and out_scale is None:
+        raise ValueError("int8 output needs out_scale")
+    out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    _need(out, out_dtype, "out", 2)
+    _check(load().q8_gemm_epilogue_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
+                                      _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
+                                      OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),
+                                      KERNELS[kernel], _stream(stream)), "q8_gemm_epilogue")
+    return out
 
 
 def q8_gemm_s32(qa, qw, out=None, kernel: str = "auto", stream=None):

@@ -50,10 +50,18 @@ q8_status check_quant_args(const float* x, int64_t rows, int64_t cols, q8_granul
     return Q8_OK;
 }
 
+// Epilogue variants of q8_gemm_epilogue_ex (bias, output type); nullptr for the plain fp32 entries.
+struct Variant {
+    const float* bias;
+    q8_out_type out_type;
+    void* out;
+    float out_scale;
+};
+
 q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
-                      q8_stream_t stream) {
+                      q8_stream_t stream, const Variant* var = nullptr) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -66,9 +74,18 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         if (kst != Q8_OK) return kst;
     }
     if (M == 0 || N == 0) return Q8_OK;   // empty output: nothing is read or written
+    if (var) {
+        if (var->out_type != Q8_OUT_F32 && var->out_type != Q8_OUT_BF16 && var->out_type != Q8_OUT_I8)
+            return Q8_ERR_INVALID_ARG;
+        if (var->out_type == Q8_OUT_I8 && !(var->out_scale > 0.0f && var->out_scale < INFINITY))
+            return Q8_ERR_INVALID_ARG;
+        if (var->bias && !aligned(var->bias, 4)) return Q8_ERR_INVALID_ARG;
+        if (!var->out || !aligned(var->out, 16)) return Q8_ERR_INVALID_ARG;
+        y = var->out_type == Q8_OUT_F32 ? static_cast<float*>(var->out) : nullptr;
+    }
     if (epilogue) {
-        if (!s_a || !s_w || !y) return Q8_ERR_INVALID_ARG;
-        if (!aligned(s_a, 4) || !aligned(s_w, 4) || !aligned(y, 16)) return Q8_ERR_INVALID_ARG;
+        if (!s_a || !s_w || (!y && !var)) return Q8_ERR_INVALID_ARG;
+        if (!aligned(s_a, 4) || !aligned(s_w, 4) || (y && !aligned(y, 16))) return Q8_ERR_INVALID_ARG;
         if (z_a && (!colsum || !aligned(z_a, 4) || !aligned(colsum, 4))) return Q8_ERR_INVALID_ARG;
     } else if (!aligned(out_i32, 16)) {
         return Q8_ERR_INVALID_ARG;
@@ -79,12 +96,20 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
     if (M > INT32_MAX || N > INT32_MAX) return Q8_ERR_UNSUPPORTED;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    q8::Epilogue ep{s_a, z_a, s_w, colsum, ga == Q8_PER_ROW, gw == Q8_PER_ROW, y, out_i32};
+    if (var) {
+        ep.bias = var->bias;
+        ep.out_kind = var->out_type == Q8_OUT_BF16 ? q8::kOutBF16 : var->out_type == Q8_OUT_I8 ? q8::kOutI8 : q8::kOutF32;
+        ep.out_bf16 = var->out_type == Q8_OUT_BF16 ? static_cast<uint16_t*>(var->out) : nullptr;
+        ep.out_i8 = var->out_type == Q8_OUT_I8 ? static_cast<int8_t*>(var->out) : nullptr;
+        ep.out_scale = var->out_scale;
+    }
     if (K == 0) {
-        // Empty dot products: acc = 0, colsum = 0, so y = 0 * scale = +0.0f.
+        // Empty dot products: acc = 0, colsum = 0, so y = 0 * scale = +0.0f (+ bias).
+        if (var && (var->bias || var->out_type != Q8_OUT_F32)) return from_cuda(q8::launch_epilogue_fill(ep, M, N, s));
         const size_t bytes = (size_t)M * (size_t)N * 4;
         return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
     }
-    q8::Epilogue ep{s_a, z_a, s_w, colsum, ga == Q8_PER_ROW, gw == Q8_PER_ROW, y, out_i32};
     if (kernel == Q8_GEMM_AUTO) kernel = q8_gemm_pick(M, N, K);
     switch (kernel) {
         case Q8_GEMM_TCGEN05:
@@ -165,6 +190,14 @@ q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* 
                              int64_t M, int64_t N, int64_t K, float* y, q8_gemm_kernel kernel,
                              q8_stream_t stream) {
     return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, kernel, stream);
+}
+
+q8_status q8_gemm_epilogue_ex(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                              const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                              const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type, void* out,
+                              float out_scale, q8_gemm_kernel kernel, q8_stream_t stream) {
+    const Variant var{bias, out_type, out, out_scale};
+    return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, nullptr, nullptr, kernel, stream, &var);
 }
 
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(Cfg<BM, BN, WM, WN, STAGES>::kThreads)
                     } else {
                         const int corr = ep.z_a ? a - za_m * ep.colsum[nn] : a;
                         const float scale = __fmul_rn(sa_m, ep.s_w[ep.w_per_row ? nn : 0]);
-                        ep.y[(int64_t)m * N + nn] = __fmul_rn(__int2float_rn(corr), scale);
+                        epi_store(ep, (int64_t)m * N + nn, epi_bias(ep, __fmul_rn(__int2float_rn(corr), scale), nn));
                     }
                 }
             }

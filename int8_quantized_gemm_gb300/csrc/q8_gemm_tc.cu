@@ -311,8 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int q = 0; q < 4; ++q) {
                             const int corr = acc[e4 * 4 + q] - za * cs4[q];
                             o[q] = __fmul_rn(__int2float_rn(corr), __fmul_rn(sa, sw4[q]));
+                            if (ep.bias) o[q] = __fadd_rn(o[q], __ldg(ep.bias + (n + q < N ? n + q : 0)));
                         }
-                        if (vec && n + 3 < N) {
+                        if (ep.out_kind != kOutF32) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (n + q < N) epi_store(ep, (int64_t)m * N + n + q, o[q]);
+                        } else if (vec && n + 3 < N) {
                             *reinterpret_cast<float4*>(row + n) = make_float4(o[0], o[1], o[2], o[3]);
                         } else {
 #pragma unroll
@@ -392,16 +397,24 @@ bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, in
     return make_map_impl(map, base, rows, K, box_rows, 64, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-bool make_tma_map_out32(CUtensorMap* map, void* base, bool is_float, int64_t rows, int64_t cols) {
+bool make_tma_map_out(CUtensorMap* map, void* base, int kind, int64_t rows, int64_t cols) {
     auto enc = get_encode();
-    if (!enc || (cols % 4) != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    CUtensorMapDataType dt;
+    int esz;
+    switch (kind) {
+        case kMapF32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; esz = 4; break;
+        case kMapI32: dt = CU_TENSOR_MAP_DATA_TYPE_INT32; esz = 4; break;
+        case kMapBF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; esz = 2; break;
+        case kMapI8: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; esz = 1; break;
+        default: return false;
+    }
+    if (!enc || ((cols * esz) % 16) != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -27,12 +27,28 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "q8_internal.h"
 #include "q8_tc_ptx.cuh"
 
 namespace q8 {
 
 static __device__ unsigned int g_tc2_error;
+
+// Two fp32 values (bit patterns) as a bf16x2 word, low half first, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Four fp32 values (bit patterns) as int8 codes clamp(rint(v / s), -127, 127), packed.
+__device__ __forceinline__ uint32_t pack_codes4(uint4 v, float s) {
+    auto code = [&](uint32_t b) {
+        return (uint32_t)(min(max(__float2int_rn(__fdiv_rn(__uint_as_float(b), s)), -127), 127) & 0xFF);
+    };
+    return code(v.x) | (code(v.y) << 8) | (code(v.z) << 16) | (code(v.w) << 24);
+}
 
 namespace {
 
@@ -316,29 +332,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 uint32_t o[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    o[q] = __float_as_uint(__fmul_rn(__int2float_rn(acc[e + q] - za * cs4[q]), __fmul_rn(sa, sw4[q])));
+                for (int q = 0; q < 4; ++q) {
+                    float v = __fmul_rn(__int2float_rn(acc[e + q] - za * cs4[q]), __fmul_rn(sa, sw4[q]));
+                    if (ep.bias) v = __fadd_rn(v, __ldg(ep.bias + (n + q < N ? n + q : 0)));
+                    o[q] = __float_as_uint(v);
+                }
                 return make_uint4(o[0], o[1], o[2], o[3]);
             };
             if (tma_out) {
-                // Each 32 x 32 block goes through this warp's shared buffer (128-byte swizzle: row
-                // `lane`, 16-byte chunk c at chunk c ^ (lane & 7)) and one TMA store, which writes
-                // whole lines and clips rows >= M and columns >= N.
+                // Each block of 32 rows x 128 bytes (32 fp32, 64 bf16 or 128 int8 columns) goes
+                // through this warp's shared buffer (128-byte swizzle: row `lane`, 16-byte chunk c
+                // at chunk c ^ (lane & 7)) and one TMA store, which writes whole lines and clips
+                // rows >= M and columns >= N. ESZ (bytes per output) is a compile-time constant
+                // so that acc[] stays in registers.
                 const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - 8) * kEpiBytes);
+                auto blocks = [&](auto esz_tag) {
+                    constexpr int ESZ = decltype(esz_tag)::value;
+                    constexpr int BCOLS = 128 / ESZ;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
-                    __syncwarp();
+                    for (int j = 0; j < ESZ; ++j) {
+                        if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
+                        __syncwarp();
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        sts128(ebuf + (uint32_t)(lane * 128 + ((c4 ^ (lane & 7)) << 4)),
-                               out4(j * 32 + c4 * 4, nb + j * 32 + c4 * 4));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmap_out, ebuf, nb + j * 32, mrow0);
-                        bulk_commit();
+                        for (int c = 0; c < 8; ++c) {
+                            const int e0 = j * BCOLS + c * (16 / ESZ);
+                            uint4 w;
+                            if constexpr (ESZ == 4) {
+                                w = out4(e0, nb + e0);
+                            } else if constexpr (ESZ == 2) {
+                                const uint4 a = out4(e0, nb + e0), b = out4(e0 + 4, nb + e0 + 4);
+                                w = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                                               pack_bf16x2(b.z, b.w));
+                            } else {
+                                uint32_t q[4];
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    const uint4 a = out4(e0 + 4 * t, nb + e0 + 4 * t);
+                                    q[t] = pack_codes4(a, ep.out_scale);
+                                }
+                                w = make_uint4(q[0], q[1], q[2], q[3]);
+                            }
+                            sts128(ebuf + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4)), w);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_out, ebuf, nb + j * BCOLS, mrow0);
+                            bulk_commit();
+                        }
                     }
+                };
+                if (ep.out_i32 || ep.out_kind == kOutF32)
+                    blocks(std::integral_constant<int, 4>{});
+                else if (ep.out_kind == kOutBF16)
+                    blocks(std::integral_constant<int, 2>{});
+                else
+                    blocks(std::integral_constant<int, 1>{});
+            } else if (m < M && !ep.out_i32 && ep.out_kind != kOutF32) {
+#pragma unroll
+                for (int e4 = 0; e4 < 32; ++e4) {
+                    const int n = nb + e4 * 4;
+                    const uint4 o = out4(e4 * 4, n);
+                    if (n < N) epi_store(ep, (int64_t)m * N + n, __uint_as_float(o.x));
+                    if (n + 1 < N) epi_store(ep, (int64_t)m * N + n + 1, __uint_as_float(o.y));
+                    if (n + 2 < N) epi_store(ep, (int64_t)m * N + n + 2, __uint_as_float(o.z));
+                    if (n + 3 < N) epi_store(ep, (int64_t)m * N + n + 3, __uint_as_float(o.w));
                 }
             } else if (m < M) {
                 uint32_t* row = ep.out_i32 ? reinterpret_cast<uint32_t*>(ep.out_i32) + (int64_t)m * N
@@ -414,8 +472,10 @@ cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64
     const int64_t pairs = resident_pairs();
     const int clusters = (int)(tiles < pairs ? tiles : pairs);
     CUtensorMap mo;
-    const bool tma_out = ep.out_i32 ? make_tma_map_out32(&mo, ep.out_i32, false, M, N)
-                                    : make_tma_map_out32(&mo, ep.y, true, M, N);
+    const bool tma_out = ep.out_i32                  ? make_tma_map_out(&mo, ep.out_i32, kMapI32, M, N)
+                         : ep.out_kind == kOutF32  ? make_tma_map_out(&mo, ep.y, kMapF32, M, N)
+                         : ep.out_kind == kOutBF16 ? make_tma_map_out(&mo, ep.out_bf16, kMapBF16, M, N)
+                                                   : make_tma_map_out(&mo, ep.out_i8, kMapI8, M, N);
     if (!tma_out) memset(&mo, 0, sizeof(mo));
     gemm_tc2_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N, (int)K,
                                                                 ep);

@@ -232,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (em + 8 < M) ep.out_i32[(int64_t)(em + 8) * N + n] = v1;
                     } else {
                         if (em < M)
-                            ep.y[(int64_t)em * N + n] =
-                                __fmul_rn(__int2float_rn(v0 - eza0 * ecs), __fmul_rn(esa0, esw));
+                            epi_store(ep, (int64_t)em * N + n,
+                                      epi_bias(ep, __fmul_rn(__int2float_rn(v0 - eza0 * ecs), __fmul_rn(esa0, esw)), n));
                         if (em + 8 < M)
-                            ep.y[(int64_t)(em + 8) * N + n] =
-                                __fmul_rn(__int2float_rn(v1 - eza1 * ecs), __fmul_rn(esa1, esw));
+                            epi_store(ep, (int64_t)(em + 8) * N + n,
+                                      epi_bias(ep, __fmul_rn(__int2float_rn(v1 - eza1 * ecs), __fmul_rn(esa1, esw)), n));
                     }
                 }
             }

@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j < M) {
                             const int r = ep.a_per_row ? j : 0;
                             const int corr = ep.z_a ? acc[j] - __ldg(ep.z_a + r) * cs : acc[j];
-                            ep.y[(int64_t)j * N + n] =
-                                __fmul_rn(__int2float_rn(corr), __fmul_rn(__ldg(ep.s_a + r), sw));
+                            epi_store(ep, (int64_t)j * N + n,
+                                      epi_bias(ep, __fmul_rn(__int2float_rn(corr), __fmul_rn(__ldg(ep.s_a + r), sw)), n));
                         }
                     }
                 }

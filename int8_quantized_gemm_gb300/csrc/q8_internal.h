@@ -3,6 +3,9 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#endif
 
 #include "../../include/q8.h"
 
@@ -30,6 +33,8 @@ cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsu
 
 // Epilogue operands shared by every GEMM kernel. When out_i32 != nullptr the
 // kernel writes the raw accumulators there instead of y.
+enum OutKind : int { kOutF32 = 0, kOutBF16 = 1, kOutI8 = 2 };
+
 struct Epilogue {
     const float* s_a;
     const int32_t* z_a;      // nullptr: symmetric A
@@ -37,9 +42,35 @@ struct Epilogue {
     const int32_t* colsum;   // used iff z_a != nullptr
     bool a_per_row;
     bool w_per_row;
-    float* y;
-    int32_t* out_i32;
+    float* y;                // kOutF32 output
+    int32_t* out_i32;        // raw accumulators instead of the epilogue (diagnostic export)
+    // Epilogue variants: y + bias[n], written as fp32 (y), bf16 (out_bf16, round to nearest
+    // even) or int8 codes clamp(rint(y / out_scale), -127, 127) (out_i8).
+    const float* bias = nullptr;
+    int out_kind = kOutF32;
+    uint16_t* out_bf16 = nullptr;
+    int8_t* out_i8 = nullptr;
+    float out_scale = 1.0f;
 };
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float epi_bias(const Epilogue& ep, float v, int64_t n) {
+    return ep.bias ? __fadd_rn(v, __ldg(ep.bias + n)) : v;
+}
+
+__device__ __forceinline__ void epi_store(const Epilogue& ep, int64_t idx, float v) {
+    if (ep.out_kind == kOutBF16) {
+        ep.out_bf16[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    } else if (ep.out_kind == kOutI8) {
+        ep.out_i8[idx] = (int8_t)min(max(__float2int_rn(__fdiv_rn(v, ep.out_scale)), -127), 127);
+    } else {
+        ep.y[idx] = v;
+    }
+}
+#endif
+
+// Output of a layer with K == 0 in the epilogue's output type (bias only).
+cudaError_t launch_epilogue_fill(const Epilogue& ep, int64_t M, int64_t N, cudaStream_t stream);
 
 cudaError_t launch_gemm_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
                             const Epilogue& ep, bool skinny, cudaStream_t stream);

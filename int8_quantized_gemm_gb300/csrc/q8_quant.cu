@@ -494,6 +494,25 @@ cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t 
     return cudaGetLastError();
 }
 
+// The layer output when K == 0 (every dot product empty, corr = 0): y = fl(0 * scale) + bias[n]
+// written in the requested output type.
+__global__ void epilogue_fill_kernel(Epilogue ep, int64_t M, int64_t N) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+        epi_store(ep, i, epi_bias(ep, 0.0f, i % N));
+}
+
+cudaError_t launch_epilogue_fill(const Epilogue& ep, int64_t M, int64_t N, cudaStream_t stream) {
+    const int64_t total = M * N;
+    if (total == 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    epilogue_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ep, M, N);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
     const int warps_per_block = 8;

@@ -343,10 +343,11 @@ bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t
 // Same with box [box_rows, 64] and the 64-byte swizzle: the 16-byte chunk c of row r
 // lands at chunk c ^ ((r >> 1) & 3) of its 64-byte row (shared-memory base 512-byte aligned).
 bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows);
-// Output map for TMA stores: 4-byte elements (fp32 or int32) of a row-major [rows, cols]
-// matrix, box [32 rows, 32 cols] with the 128-byte swizzle. False unless cols % 4 == 0 and
-// the base is 16-byte aligned (the row pitch must be a multiple of 16 bytes).
-bool make_tma_map_out32(CUtensorMap* map, void* base, bool is_float, int64_t rows, int64_t cols);
+// Output map for TMA stores of a row-major [rows, cols] matrix of fp32, int32, bf16 or int8:
+// box [32 rows, 128 bytes of columns] with the 128-byte swizzle. False unless the row pitch
+// is a multiple of 16 bytes and the base is 16-byte aligned.
+enum { kMapF32 = 0, kMapI32 = 1, kMapBF16 = 2, kMapI8 = 3 };
+bool make_tma_map_out(CUtensorMap* map, void* base, int kind, int64_t rows, int64_t cols);
 int device_sm_count();
 
 }  // namespace q8

@@ -88,6 +88,21 @@ def test_rmsnorm_quantize_rejects_bad_arguments(lib):
     assert f(FAKE, FAKE, 4, (1 << 24) + 16, 1e-6, FAKE, FAKE) == q8.Q8_ERR_UNSUPPORTED
 
 
+def test_epilogue_variant_rejects_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+
+    def f(out_type=0, out=FAKE, scale=0.0, bias=None, K=16):
+        return lib.q8_gemm_epilogue_ex(FAKE, FAKE, None, 1, FAKE, FAKE, 1, None, bias, 8, 8, K, out_type, out,
+                                       ctypes.c_float(scale), 0, None)
+    assert f(out_type=3) == q8.Q8_ERR_INVALID_ARG                  # unknown output type
+    assert f(out_type=2, scale=0.0) == q8.Q8_ERR_INVALID_ARG       # int8 output needs a scale > 0
+    assert f(out_type=2, scale=float("inf")) == q8.Q8_ERR_INVALID_ARG
+    assert f(out=None) == q8.Q8_ERR_INVALID_ARG
+    assert f(out=MISALIGNED) == q8.Q8_ERR_INVALID_ARG
+    assert f(bias=P(0x10002)) == q8.Q8_ERR_INVALID_ARG            # bias must be 4-byte aligned
+    assert f(K=24) == q8.Q8_ERR_UNSUPPORTED
+
+
 def test_k_limits_are_the_int32_bounds():
     # 128*128*K < 2^31 for raw codes; 255*128*K < 2^31 with a zero point.
     assert 128 * 128 * 131056 < 2 ** 31 <= 128 * 128 * (131056 + 16)
