@@ -17,6 +17,8 @@ Every function follows a passage of the pages (cited in q8_oracle.c):
   linear_codes / linear_codes_at Day 98 (epilogue listing)
   rmsnorm / rmsnorm_quantize     "Activation Quantization Architecture" (Fusion:
                                  the fused norm-and-quantize pseudocode)
+  quantize_int4, pack_int4,      TileLang tutorial ch. 27 (2.4 int8 / int4; the int4
+  unpack_int4                    GEMM example's packing and sign extension)
   linear_codes_bias, to_bf16,    "Activation Quantization Architecture" (Fusion:
   quantize_static                the epilogue adds the bias, writes bf16, or
                                  quantizes the output for the next GEMM)
@@ -82,6 +84,12 @@ def _load():
         lib.q8o_sym_scale.argtypes = [ctypes.c_float]
         lib.q8o_sym_scale.restype = ctypes.c_float
         lib.q8o_rmsnorm.argtypes = [p, p, i64, i64, ctypes.c_float, p, p]
+        lib.q8o_quantize_int4.argtypes = [p, i64, i64, p, p]
+        lib.q8o_quantize_int4.restype = i32
+        lib.q8o_pack_int4.argtypes = [p, i64, i64, p]
+        lib.q8o_pack_int4.restype = i32
+        lib.q8o_unpack_int4.argtypes = [p, i64, i64, p]
+        lib.q8o_unpack_int4.restype = i32
         lib.q8o_linear_codes_bias.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32]
         lib.q8o_linear_codes_bias.restype = i32
         lib.q8o_to_bf16.argtypes = [p, i64, p]
@@ -214,6 +222,34 @@ def linear_codes_bias(qa, sa, za, qw, sw, bias, a_per_row: bool, w_per_row: bool
     st = _load().q8o_linear_codes_bias(_ptr(qa), _ptr(sa), _ptr(za), int(a_per_row), _ptr(qw), _ptr(sw),
                                        int(w_per_row), _ptr(bias), M, N, K, _ptr(y), threads)
     return y, st
+
+
+def quantize_int4(w: np.ndarray):
+    """Per-row symmetric int4 codes (one per int8 element, in [-8, 7]) and scales s = absmax / 7."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), np.int8)
+    s = np.empty(rows, np.float32)
+    assert _load().q8o_quantize_int4(_ptr(w), rows, cols, _ptr(q), _ptr(s)) == OK
+    return q, s
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """Two int4 codes per byte along each row, low nibble first: uint8 [rows, cols / 2]."""
+    q = _c(q, np.int8)
+    rows, cols = q.shape
+    out = np.empty((rows, cols // 2), np.uint8)
+    assert _load().q8o_pack_int4(_ptr(q), rows, cols, _ptr(out)) == OK
+    return out
+
+
+def unpack_int4(packed: np.ndarray, cols: int) -> np.ndarray:
+    """Inverse of pack_int4, sign-extending each nibble."""
+    packed = _c(packed, np.uint8)
+    rows = packed.shape[0]
+    out = np.empty((rows, cols), np.int8)
+    assert _load().q8o_unpack_int4(_ptr(packed), rows, cols, _ptr(out)) == OK
+    return out
 
 
 def to_bf16(y: np.ndarray) -> np.ndarray:

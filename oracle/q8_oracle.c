@@ -40,6 +40,11 @@
  *      y = fl(corr * scale) + bias[n] (one fp32 add), then either fp32, bf16
  *    rounded to nearest-even, or int8 codes clamp(rint(y / s_out), -127, 127)
  *    with a static per-tensor output scale s_out.
+ *  - int4 weights for W4A8 (TileLang tutorial ch. 27, low-precision quantization:
+ *    2.4 int8 / int4, qmax = 7, s = absmax / qmax, q = clip(round(x / s), -qmax-1,
+ *    qmax); its int4 GEMM and dequantize-GEMM examples: two codes per byte,
+ *    (a & 0x0F) | ((b & 0x0F) << 4), decoded by shifting left 4 and then right 4
+ *    arithmetically to sign-extend).
  *  - fused RMSNorm + per-token quantization ("Activation Quantization
  *    Architecture", Fusion: the fused norm-and-quantize pseudocode):
  *      rms = sqrt(mean(x * x) + eps), y = x / rms * gamma, then the symmetric
@@ -286,6 +291,50 @@ int q8o_linear_codes_at(const int8_t* qa, const float* sa, const int32_t* za, in
         if (st > status) status = st;
     }
     return status;
+}
+
+/*
+ * Symmetric int4 quantization of each row of w[rows][cols] (per output channel):
+ * s = max(absmax, 1e-8) / 7, q = clamp(rint(w / s), -8, 7) (-8 is reachable only
+ * through rounding, as |w / s| <= 7 up to one ulp). Codes are returned one per
+ * int8 element; q8o_pack_int4 packs them.
+ */
+int q8o_quantize_int4(const float* w, int64_t rows, int64_t cols, int8_t* q, float* s) {
+    if (rows < 0 || cols < 0) return Q8O_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* wr = w + r * cols;
+        const float amax = q8o_amax(wr, cols);
+        const float sc = (amax > Q8O_ZERO_GUARD ? amax : Q8O_ZERO_GUARD) / 7.0f;
+        s[r] = sc;
+        for (int64_t k = 0; k < cols; ++k) q[r * cols + k] = (int8_t)q8o_clampi((long)rintf(wr[k] / sc), -8, 7);
+    }
+    return Q8O_OK;
+}
+
+/* Two int4 codes per byte along each row: byte i = (q[2i] & 0x0F) | ((q[2i+1] & 0x0F) << 4). */
+int q8o_pack_int4(const int8_t* q, int64_t rows, int64_t cols, uint8_t* packed) {
+    if (rows < 0 || cols < 0 || (cols & 1)) return Q8O_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < cols / 2; ++i) {
+            const uint8_t lo = (uint8_t)(q[r * cols + 2 * i] & 0x0F);
+            const uint8_t hi = (uint8_t)(q[r * cols + 2 * i + 1] & 0x0F);
+            packed[r * (cols / 2) + i] = (uint8_t)(lo | (hi << 4));
+        }
+    return Q8O_OK;
+}
+
+/* Inverse of q8o_pack_int4: each nibble sign-extended (shift left 4, arithmetic right 4). */
+int q8o_unpack_int4(const uint8_t* packed, int64_t rows, int64_t cols, int8_t* q) {
+    if (rows < 0 || cols < 0 || (cols & 1)) return Q8O_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < cols / 2; ++i) {
+            const int b = packed[r * (cols / 2) + i];
+            const int lo = ((int)(int8_t)(uint8_t)(b << 4)) >> 4;
+            const int hi = ((int)(int8_t)(uint8_t)b) >> 4;
+            q[r * cols + 2 * i] = (int8_t)lo;
+            q[r * cols + 2 * i + 1] = (int8_t)hi;
+        }
+    return Q8O_OK;
 }
 
 /*
