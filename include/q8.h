@@ -125,6 +125,28 @@ q8_status q8_rmsnorm_quantize_act(const float* a, const float* gamma, int64_t M,
                                   int8_t* qa, float* s_a, q8_stream_t stream);
 
 /*
+ * Offline int4 weight quantization for W4A8, per output channel: TileLang tutorial
+ * ch. 27 (low-precision quantization), 2.4 int8 / int4 with qmax = 7:
+ *   s_w[n] = max(absmax_n, 1e-8) / 7,  q = clamp(rint(w / s_w[n]), -8, 7),
+ * packed two codes per byte along K, low nibble first: byte i of row n holds
+ * (q[n][2i] & 0xF) | (q[n][2i+1] & 0xF) << 4 (the int4 GEMM example's packing;
+ * decoders sign-extend each nibble).
+ *
+ * w    : fp32 W[N, K], read only, 16-byte aligned.
+ * qw4  : uint8 [N, K / 2], written, 16-byte aligned.
+ * s_w  : fp32 [N], written.
+ * Errors: Q8_ERR_INVALID_ARG for null or misaligned pointers (N, K > 0) or N, K < 0;
+ * Q8_ERR_UNSUPPORTED for K % 32 != 0 (whole 16-byte packed rows).
+ */
+q8_status q8_quantize_weight_int4(const float* w, int64_t N, int64_t K, uint8_t* qw4, float* s_w,
+                                  q8_stream_t stream);
+
+/* Column sums of int4 weights, colsum[n] = sum_k q[n][k] (for asymmetric
+ * activations in W4A8): qw4 uint8 [N, K / 2] as written by q8_quantize_weight_int4. */
+q8_status q8_colsum_int4(const uint8_t* qw4, int64_t N, int64_t K, int32_t* colsum,
+                         q8_stream_t stream);
+
+/*
  * Offline symmetric weight quantization, per output channel or per tensor,
  * with the symmetric rule above ("Activation Quantization Architecture", the
  * numpy reference quantize_per_channel; Day 98, one scale per column of B).
@@ -207,6 +229,31 @@ q8_status q8_gemm_epilogue_ex(const int8_t* qa, const float* s_a, const int32_t*
                               q8_granularity gw, const int32_t* colsum, const float* bias,
                               int64_t M, int64_t N, int64_t K, q8_out_type out_type, void* out,
                               float out_scale, q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
+ * W4A8: the quantized linear layer with int4 weights (TileLang tutorial ch. 27,
+ * low-precision quantization: 2.4 int8 / int4 and the int4 / dequantize GEMM
+ * examples): acc[m][n] = sum_k qa[m][k] * q4[n][k] (exact int32; |acc| <= K *
+ * 128 * 8), then the epilogue of q8_gemm_epilogue_ex with per-channel s_w.
+ *
+ * qw4    : uint8 [N, K / 2], two sign-extended int4 codes per byte, low nibble
+ *          first (as written by q8_quantize_weight_int4), 16-byte aligned.
+ * s_w    : fp32 [N] (per output channel).
+ * colsum : int32 [N] from q8_colsum_int4, required iff z_a is given.
+ * kernel : Q8_GEMM_AUTO (decode kernel for M <= 16, else the CTA-pair kernel),
+ *          Q8_GEMM_DECODE or Q8_GEMM_TCGEN05_PAIR; other kernels return
+ *          Q8_ERR_UNSUPPORTED.
+ * Other arguments and errors as q8_gemm_epilogue_ex; K % 32 != 0 returns
+ * Q8_ERR_UNSUPPORTED.
+ */
+q8_status q8_gemm_w4a8_ex(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                          const uint8_t* qw4, const float* s_w, const int32_t* colsum,
+                          const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type,
+                          void* out, float out_scale, q8_gemm_kernel kernel, q8_stream_t stream);
+
+/* Raw INT32 accumulators of the W4A8 product (diagnostic export, for bit-exact checks). */
+q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, int64_t N, int64_t K,
+                              int32_t* acc, q8_gemm_kernel kernel, q8_stream_t stream);
 
 /*
  * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),

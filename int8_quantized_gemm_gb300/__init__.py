@@ -11,6 +11,7 @@ CPU fallback; if the library is missing or a call fails, an exception says so.
   q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum)      -> y
   q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum, bias, out_dtype, out_scale) -> y (+bias; fp32/bf16/int8)
   q8_gemm_s32(qa, qw)                                 -> acc (raw INT32 accumulators)
+  q8_quantize_weight_int4(w) -> qw4, s_w;  q8_colsum_int4(qw4, K);  q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, ...)
   q8_linear(a, qw, s_w, colsum)                       -> y   (quantize A, then GEMM)
 """
 from __future__ import annotations
@@ -24,7 +25,8 @@ from . import build as _build
 
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
-    "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
+    "q8_gemm_w4a8_s32", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -61,6 +63,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_dequant_ex.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32, p]
     lib.q8_gemm_epilogue_ex.argtypes = [p, p, p, i32, p, p, i32, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
+    lib.q8_quantize_weight_int4.argtypes = [p, i64, i64, p, p, p]
+    lib.q8_colsum_int4.argtypes = [p, i64, i64, p, p]
+    lib.q8_gemm_w4a8_ex.argtypes = [p, p, p, i32, p, p, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
+    lib.q8_gemm_w4a8_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_gemm_pick.argtypes = [i64, i64, i64]
     lib.q8_status_string.argtypes = [i32]
     lib.q8_status_string.restype = ctypes.c_char_p
@@ -68,7 +74,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_launch_count.argtypes = []
     lib.q8_launch_count.restype = ctypes.c_uint64
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
-                 "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_gemm_pick", "q8_device_error"):
+                 "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
+                 "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_gemm_pick", "q8_device_error"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -227,6 +234,74 @@ def q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=to
                                       _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
                                       OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),
                                       KERNELS[kernel], _stream(stream)), "q8_gemm_epilogue")
+    return out
+
+
+def q8_quantize_weight_int4(w: torch.Tensor, qw4=None, s_w=None, stream=None):
+    """Per-channel symmetric int4 codes of fp32 W[N, K], packed two per byte: (qw4 uint8 [N, K/2], s_w [N])."""
+    _need(w, torch.float32, "w", 2)
+    N, K = w.shape
+    qw4 = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device) if qw4 is None else qw4
+    s_w = torch.empty(N, dtype=torch.float32, device=w.device) if s_w is None else s_w
+    _check(load().q8_quantize_weight_int4(_ptr(w), N, K, _ptr(qw4), _ptr(s_w), _stream(stream)),
+           "q8_quantize_weight_int4")
+    return qw4, s_w
+
+
+def q8_colsum_int4(qw4: torch.Tensor, K: int, out=None, stream=None):
+    _need(qw4, torch.uint8, "qw4", 2)
+    N = qw4.shape[0]
+    if qw4.shape[1] * 2 != K:
+        raise ValueError("qw4 must be [N, K / 2]")
+    out = torch.empty(N, dtype=torch.int32, device=qw4.device) if out is None else out
+    _check(load().q8_colsum_int4(_ptr(qw4), N, K, _ptr(out), _stream(stream)), "q8_colsum_int4")
+    return out
+
+
+def q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
+                 out=None, kernel: str = "auto", stream=None):
+    """W4A8 linear layer: int8 activations x packed int4 weights, epilogue as q8_gemm_epilogue."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw4, torch.uint8, "qw4", 2)
+    M, K = qa.shape
+    N = qw4.shape[0]
+    if qw4.shape[1] * 2 != K:
+        raise ValueError("qw4 must be [N, K / 2]")
+    if out_dtype not in OUT_TYPES:
+        raise TypeError("out_dtype must be torch.float32, torch.bfloat16 or torch.int8")
+    _need(s_a, torch.float32, "s_a", 1)
+    _need(s_w, torch.float32, "s_w", 1)
+    if s_a.numel() not in (1, M) or s_w.numel() != N:
+        raise ValueError("s_a must have 1 or M entries and s_w N entries")
+    ga = Q8_PER_ROW if (s_a.numel() == M and M != 1) else Q8_PER_TENSOR
+    if z_a is not None:
+        _need(z_a, torch.int32, "z_a", 1)
+        if colsum is None:
+            raise ValueError("an asymmetric A needs the weight column sums")
+        _need(colsum, torch.int32, "colsum", 1)
+    if bias is not None:
+        _need(bias, torch.float32, "bias", 1)
+    if out_dtype == torch.int8 and out_scale is None:
+        raise ValueError("int8 output needs out_scale")
+    out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    _need(out, out_dtype, "out", 2)
+    _check(load().q8_gemm_w4a8_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw4), _ptr(s_w),
+                                  _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
+                                  OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),
+                                  KERNELS[kernel], _stream(stream)), "q8_gemm_w4a8")
+    return out
+
+
+def q8_gemm_w4a8_s32(qa, qw4, out=None, kernel: str = "auto", stream=None):
+    """Raw INT32 accumulators of int8 qa x packed int4 qw4 (diagnostic export)."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw4, torch.uint8, "qw4", 2)
+    M, K = qa.shape
+    N = qw4.shape[0]
+    out = torch.empty((M, N), dtype=torch.int32, device=qa.device) if out is None else out
+    _need(out, torch.int32, "out", 2)
+    _check(load().q8_gemm_w4a8_s32_ex(_ptr(qa), _ptr(qw4), M, N, K, _ptr(out), KERNELS[kernel], _stream(stream)),
+           "q8_gemm_w4a8_s32")
     return out
 
 

@@ -61,7 +61,7 @@ struct Variant {
 q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
-                      q8_stream_t stream, const Variant* var = nullptr) {
+                      q8_stream_t stream, const Variant* var = nullptr, bool w4 = false) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -72,6 +72,7 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
     {
         q8_status kst = check_k(K, epilogue && z_a != nullptr);
         if (kst != Q8_OK) return kst;
+        if (w4 && K % 32 != 0) return Q8_ERR_UNSUPPORTED;   // packed int4 rows: whole 16-byte multiples
     }
     if (M == 0 || N == 0) return Q8_OK;   // empty output: nothing is read or written
     if (var) {
@@ -109,6 +110,15 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         if (var && (var->bias || var->out_type != Q8_OUT_F32)) return from_cuda(q8::launch_epilogue_fill(ep, M, N, s));
         const size_t bytes = (size_t)M * (size_t)N * 4;
         return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
+    }
+    if (w4) {
+        // int4 weights run on the decode kernel (M <= 16) and the CTA-pair kernel
+        if (kernel == Q8_GEMM_AUTO) kernel = q8::gemv_mma_supports(M, N, K, true) ? Q8_GEMM_DECODE : Q8_GEMM_TCGEN05_PAIR;
+        if (kernel == Q8_GEMM_DECODE) {
+            if (!q8::gemv_mma_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
+            return from_cuda(q8::launch_gemv_mma(qa, qw, M, N, K, ep, s, true));
+        }
+        return Q8_ERR_UNSUPPORTED;
     }
     if (kernel == Q8_GEMM_AUTO) kernel = q8_gemm_pick(M, N, K);
     switch (kernel) {
@@ -161,6 +171,25 @@ q8_status q8_rmsnorm_quantize_act(const float* a, const float* gamma, int64_t M,
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+q8_status q8_quantize_weight_int4(const float* w, int64_t N, int64_t K, uint8_t* qw4, float* s_w,
+                                  q8_stream_t stream) {
+    if (N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return Q8_ERR_UNSUPPORTED;
+    if (N == 0) return Q8_OK;
+    if (!s_w || !aligned(s_w, 4)) return Q8_ERR_INVALID_ARG;
+    if (K > 0 && (!w || !qw4 || !aligned(w, 16) || !aligned(qw4, 16))) return Q8_ERR_INVALID_ARG;
+    return from_cuda(q8::launch_quantize_int4(w, N, K, qw4, s_w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_colsum_int4(const uint8_t* qw4, int64_t N, int64_t K, int32_t* colsum, q8_stream_t stream) {
+    if (N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return Q8_ERR_UNSUPPORTED;
+    if (N == 0) return Q8_OK;
+    if (!colsum || !aligned(colsum, 4)) return Q8_ERR_INVALID_ARG;
+    if (K > 0 && (!qw4 || !aligned(qw4, 16))) return Q8_ERR_INVALID_ARG;
+    return from_cuda(q8::launch_colsum_int4(qw4, N, K, colsum, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 q8_status q8_quantize_weight(const float* w, int64_t N, int64_t K, q8_granularity g, int8_t* qw, float* s_w,
                              q8_stream_t stream) {
     q8_status st = check_quant_args(w, N, K, g, qw, s_w, N > 0 && K > 0);
@@ -198,6 +227,21 @@ q8_status q8_gemm_epilogue_ex(const int8_t* qa, const float* s_a, const int32_t*
                               float out_scale, q8_gemm_kernel kernel, q8_stream_t stream) {
     const Variant var{bias, out_type, out, out_scale};
     return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, nullptr, nullptr, kernel, stream, &var);
+}
+
+q8_status q8_gemm_w4a8_ex(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga, const uint8_t* qw4,
+                          const float* s_w, const int32_t* colsum, const float* bias, int64_t M, int64_t N, int64_t K,
+                          q8_out_type out_type, void* out, float out_scale, q8_gemm_kernel kernel,
+                          q8_stream_t stream) {
+    const Variant var{bias, out_type, out, out_scale};
+    return gemm_common(qa, s_a, z_a, ga, reinterpret_cast<const int8_t*>(qw4), s_w, Q8_PER_ROW, colsum, M, N, K,
+                       nullptr, nullptr, kernel, stream, &var, true);
+}
+
+q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, int64_t N, int64_t K, int32_t* acc,
+                              q8_gemm_kernel kernel, q8_stream_t stream) {
+    return gemm_common(qa, nullptr, nullptr, Q8_PER_ROW, reinterpret_cast<const int8_t*>(qw4), nullptr, Q8_PER_ROW,
+                       nullptr, M, N, K, nullptr, acc, kernel, stream, nullptr, true);
 }
 
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,

@@ -46,22 +46,41 @@ using namespace tc;
 
 constexpr int RW = 64;             // weight rows per tile
 constexpr int NT = 16;             // token rows (MMA M)
-constexpr int BK = 256;            // K per stage: two 128-byte swizzled boxes per operand
+constexpr int BK = 256;            // K per stage: 128-byte swizzled boxes
 constexpr int BKH = 128;
-constexpr int S8 = 10;             // stages in the ring
-constexpr int kW8 = RW * BK;       // 16 KB of weights per stage: [half 0 | half 1]
 constexpr int kA8 = NT * BK;       // 4 KB of activations per stage
-constexpr int kStage = kW8 + kA8;
 constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
 constexpr int kThreads = 32 * (1 + kComputeWarps);
-constexpr int kStagesPerChunk = 64;   // 64 stages x 16 K per warp = 1024 products per fp32 sum
 // int32 tile sums [2 (tile parity)][16 tokens][64 rows], token rows padded to 72 words so
 // that the eight tokens of one atomic instruction fall in different banks (2-way, not 8-way)
 constexpr int RWP = RW + 8;
-constexpr int kOffRed = S8 * kStage;
 constexpr int kRedBytes = 2 * NT * RWP * 4;
-constexpr int kOffBar = kOffRed + kRedBytes;
-constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
+
+// Weight format: int8 codes (two 128-byte boxes of 64 rows per stage, 16 KB) or int4 codes
+// packed two per byte (one box, 8 KB). An fp32 partial sum may hold 2^24 / max|product|
+// products exactly: 1024 for int8 x int8 (|p| <= 2^14), 16384 for int8 x int4 (|p| <= 2^10);
+// each warp adds 16 per stage.
+template <bool W4>
+struct GemvCfg {
+    static constexpr int kW8 = RW * (W4 ? BK / 2 : BK);
+    static constexpr int kStage = kW8 + kA8;
+    static constexpr int S8 = W4 ? 16 : 10;   // stages in the ring
+    static constexpr int kStagesPerChunk = W4 ? 1024 : 64;
+    static constexpr int kOffRed = S8 * kStage;
+    static constexpr int kOffBar = kOffRed + kRedBytes;
+    static constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
+};
+
+// Two packed bytes (K 4t, 4t+1 | 4t+2, 4t+3 as low/high nibbles) -> fp16x2 of the low nibbles
+// (K 4t, 4t+2) and of the high nibbles (K 4t+1, 4t+3): the pairs cvt_word gives an int8 word, so
+// activations and int4 weights share the K order. n ^ 8 = n + 8 for a two's-complement nibble;
+// 0x6400 | (n + 8) is the fp16 value 1024 + n + 8, exactly n after subtracting 1032.
+__device__ __forceinline__ void cvt_int4x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    const uint32_t l = (v & 0x000Fu) | ((v & 0x0F00u) << 8);
+    const uint32_t h = ((v >> 4) & 0x000Fu) | ((v & 0xF000u) << 4);
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"((l ^ 0x00080008u) | 0x64006400u), "r"(0x64086408u));
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"((h ^ 0x00080008u) | 0x64006400u), "r"(0x64086408u));
+}
 
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -77,13 +96,23 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
 
+template <bool W4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     int M, int N, int K, Epilogue ep) {
+    using C = GemvCfg<W4>;
+    constexpr int S8 = C::S8, kW8 = C::kW8, kStage = C::kStage, kStagesPerChunk = C::kStagesPerChunk;
+    constexpr int kOffRed = C::kOffRed, kOffBar = C::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -126,8 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
                 const uint32_t dst = sbase + s * kStage;
                 mbar_expect_tx(bar_full + 8 * s, kStage);
-                tma_load_2d(dst, &tmap_w, kx, n0, bar_full + 8 * s);
-                tma_load_2d(dst + RW * BKH, &tmap_w, kx + BKH, n0, bar_full + 8 * s);
+                if constexpr (W4) {
+                    tma_load_2d(dst, &tmap_w, kx / 2, n0, bar_full + 8 * s);   // 256 K = 128 packed bytes
+                } else {
+                    tma_load_2d(dst, &tmap_w, kx, n0, bar_full + 8 * s);
+                    tma_load_2d(dst + RW * BKH, &tmap_w, kx + BKH, n0, bar_full + 8 * s);
+                }
                 tma_load_2d(dst + kW8, &tmap_a, kx, 0, bar_full + 8 * s);
                 tma_load_2d(dst + kW8 + NT * BKH, &tmap_a, kx + BKH, 0, bar_full + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
@@ -140,9 +173,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g8 = lane >> 2, t = lane & 3;
         const int half = ks >> 3, kc = ks & 7;   // which 128-byte box, 16-byte chunk in its rows
         // weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t
+        // int4: the step's 16 K are 8 packed bytes, half of chunk ks / 2 of the single box;
+        // lane quad t takes bytes 2t, 2t + 1 of them (K 4t .. 4t + 3)
         uint32_t w_off[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w_off[j] = half * (RW * BKH) + sw128(8 * j + g8, kc) + 4 * t;
+        for (int j = 0; j < 8; ++j)
+            w_off[j] = W4 ? sw128(8 * j + g8, ks >> 1) + 8 * (ks & 1) + 2 * t
+                          : half * (RW * BKH) + sw128(8 * j + g8, kc) + 4 * t;
         const uint32_t a_off0 = kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
         const uint32_t a_off1 = kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
         for (int i = ct; i < 2 * NT * RWP; i += 32 * kComputeWarps) red[i] = 0;
@@ -179,13 +216,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = sbase + s * kStage;
             uint32_t wq[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_off[j]);
+            for (int j = 0; j < 8; ++j) wq[j] = W4 ? lds16(st + w_off[j]) : lds32(st + w_off[j]);
             const uint32_t aq0 = lds32(st + a_off0), aq1 = lds32(st + a_off1);
             uint32_t a[4], b[8][2];
             cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
             cvt_word(aq1, a[1], a[3]);     // token row g+8
 #pragma unroll
-            for (int j = 0; j < 8; ++j) cvt_word(wq[j], b[j][0], b[j][1]);   // weight row 8j + g
+            for (int j = 0; j < 8; ++j) {   // weight row 8j + g
+                if constexpr (W4)
+                    cvt_int4x4(wq[j], b[j][0], b[j][1]);
+                else
+                    cvt_word(wq[j], b[j][0], b[j][1]);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
 #pragma unroll
@@ -258,27 +300,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool gemv_mma_supports(int64_t M, int64_t N, int64_t K) {
-    if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % 16) == 0)) return false;
+bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4) {
+    if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % (w4 ? 32 : 16)) == 0)) return false;
     const int64_t tiles = (N + RW - 1) / RW;
     const int64_t kb = (K + BK - 1) / BK;
     return tiles * kb < (1LL << 31);
 }
 
-cudaError_t launch_gemv_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
-                            const Epilogue& ep, cudaStream_t stream) {
-    if (!gemv_mma_supports(M, N, K)) return cudaErrorNotSupported;
+template <bool W4>
+static cudaError_t launch_gemv_mma_t(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
+                                     const Epilogue& ep, cudaStream_t stream) {
+    using C = GemvCfg<W4>;
     CUtensorMap mw, ma;
-    if (!make_tma_map_i8(&mw, qw, N, K, RW, BKH, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BKH, true))
+    // int4: the packed weights are an int8 byte matrix [N, K / 2]; one box covers 256 K
+    if (!make_tma_map_i8(&mw, static_cast<const int8_t*>(qw), N, W4 ? K / 2 : K, RW, BKH, true) ||
+        !make_tma_map_i8(&ma, qa, M, K, NT, BKH, true))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<W4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (N + RW - 1) / RW;
     const int sms = device_sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
-    gemv_mma_kernel<<<grid, kThreads, kSmem, stream>>>(mw, ma, (int)M, (int)N, (int)K, ep);
+    gemv_mma_kernel<W4><<<grid, kThreads, C::kSmem, stream>>>(mw, ma, (int)M, (int)N, (int)K, ep);
     note_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_mma(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+                            cudaStream_t stream, bool w4) {
+    if (!gemv_mma_supports(M, N, K, w4)) return cudaErrorNotSupported;
+    return w4 ? launch_gemv_mma_t<true>(qa, qw, M, N, K, ep, stream)
+              : launch_gemv_mma_t<false>(qa, qw, M, N, K, ep, stream);
 }
 
 cudaError_t read_and_clear_gemv_mma_error(uint32_t* code) {

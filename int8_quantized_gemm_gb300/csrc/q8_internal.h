@@ -25,6 +25,12 @@ constexpr float kZeroGuard = 1e-8f;
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row,
                             int8_t* q, float* s, int32_t* z, cudaStream_t stream);
 
+// int4 weights (W4A8): per-row symmetric codes packed two per byte (K % 32 == 0), and their
+// column sums.
+cudaError_t launch_quantize_int4(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* s,
+                                 cudaStream_t stream);
+cudaError_t launch_colsum_int4(const uint8_t* q, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream);
+
 // Fused RMSNorm + per-token symmetric quantization of x[rows, cols] (cols % 4 == 0).
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps,
                                    int8_t* q, float* s, cudaStream_t stream);
@@ -90,10 +96,10 @@ cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream);
 bool gemv_tc_supports(int64_t M, int64_t N, int64_t K);
 
-// Warp-level fp16 MMA kernel for M <= 16 (decode), weights streamed by TMA.
-cudaError_t launch_gemv_mma(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
-                            const Epilogue& ep, cudaStream_t stream);
-bool gemv_mma_supports(int64_t M, int64_t N, int64_t K);
+// Warp-level fp16 MMA kernel for M <= 16 (decode), int8 or packed int4 (w4) weights streamed by TMA.
+cudaError_t launch_gemv_mma(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+                            cudaStream_t stream, bool w4 = false);
+bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4 = false);
 
 // Device error words (bounded waits that gave up), one per kernel file and device.
 cudaError_t read_and_clear_gemm_tc_error(uint32_t* code);

@@ -405,6 +405,93 @@ cudaError_t launch_rms_rows(const float* x, const float* gamma, int64_t rows, in
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ int4 weights (W4A8)
+// Per-row symmetric int4 codes: s = max(absmax, 1e-8) / 7, q = clamp(rint(w / s), -8, 7),
+// two codes per byte along the row, low nibble first ((q0 & 0xF) | (q1 & 0xF) << 4).
+__device__ __forceinline__ uint32_t int4_code(float x, float s) {
+    return (uint32_t)clampi(__float2int_rn(__fdiv_rn(x, s)), -8, 7) & 0xFu;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1))
+    quantize_int4_rows_kernel(const float* __restrict__ w, int64_t cols, uint8_t* __restrict__ q,
+                              float* __restrict__ s) {
+    __shared__ float red[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* wr = reinterpret_cast<const float4*>(w + row * cols);
+    float4 v[VPT];
+    float hi = 0.0f, unused = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4) {
+            v[j] = wr[i];
+            hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+        }
+    }
+    block_max2<false>(hi, unused, red);
+    const float sc = __fdiv_rn(fmaxf(hi, kZeroGuard), 7.0f);
+    if (threadIdx.x == 0) s[row] = sc;
+    uint16_t* qr = reinterpret_cast<uint16_t*>(q + row * (cols / 2));
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        if (i < n4)
+            qr[i] = (uint16_t)(int4_code(v[j].x, sc) | (int4_code(v[j].y, sc) << 4) | (int4_code(v[j].z, sc) << 8) |
+                               (int4_code(v[j].w, sc) << 12));
+    }
+}
+
+// Rows longer than the register budget: range sweep, then code sweep.
+__global__ void __launch_bounds__(1024) quantize_int4_long_rows_kernel(const float* __restrict__ w, int64_t cols,
+                                                                     uint8_t* __restrict__ q,
+                                                                     float* __restrict__ s) {
+    __shared__ float red[64];
+    const int64_t row = blockIdx.x;
+    const int64_t n4 = cols / 4;
+    const float4* wr = reinterpret_cast<const float4*>(w + row * cols);
+    float hi = 0.0f, unused = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = wr[i];
+        hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    block_max2<false>(hi, unused, red);
+    const float sc = __fdiv_rn(fmaxf(hi, kZeroGuard), 7.0f);
+    if (threadIdx.x == 0) s[row] = sc;
+    uint16_t* qr = reinterpret_cast<uint16_t*>(q + row * (cols / 2));
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = wr[i];
+        qr[i] = (uint16_t)(int4_code(v.x, sc) | (int4_code(v.y, sc) << 4) | (int4_code(v.z, sc) << 8) |
+                           (int4_code(v.w, sc) << 12));
+    }
+}
+
+// colsum[n] = sum_k q[n][k] over sign-extended nibbles: for the low (or high) nibbles of a
+// word, u = nibble value 0..15 in each byte, and (u ^ 8) - 8 is the signed code, so a dp4a of
+// (u ^ 8) against ones minus 32 sums the four codes.
+__global__ void __launch_bounds__(256) colsum_int4_kernel(const uint8_t* __restrict__ q, int64_t N, int64_t K,
+                                                          int32_t* __restrict__ colsum) {
+    const int64_t n = blockIdx.x * (int64_t)(blockDim.x / kWarp) + threadIdx.x / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    if (n >= N) return;
+    const uint4* r = reinterpret_cast<const uint4*>(q + n * (K / 2));
+    const int64_t n16 = K / 32;
+    int acc = 0;
+    for (int64_t i = lane; i < n16; i += kWarp) {
+        const uint4 v = r[i];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            acc = __dp4a((int)((w4[t] & 0x0F0F0F0Fu) ^ 0x08080808u), 0x01010101, acc) - 32;
+            acc = __dp4a((int)(((w4[t] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u), 0x01010101, acc) - 32;
+        }
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) colsum[n] = acc;
+}
+
 int num_sms() {
     static int sms = 0;
     if (sms == 0) {
@@ -509,6 +596,39 @@ cudaError_t launch_epilogue_fill(const Epilogue& ep, int64_t M, int64_t N, cudaS
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     epilogue_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ep, M, N);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_int4(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* s,
+                                 cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const int64_t n4 = cols / 4;
+    auto threads_for = [&](int vpt) {
+        int64_t t = (n4 + vpt - 1) / vpt;
+        t = ((t + kWarp - 1) / kWarp) * kWarp;
+        return (int)(t < kWarp ? kWarp : t);
+    };
+    if (n4 <= 1024 * 1) {
+        quantize_int4_rows_kernel<1><<<(unsigned)rows, threads_for(1), 0, stream>>>(w, cols, q, s);
+    } else if (n4 <= 1024 * 2) {
+        quantize_int4_rows_kernel<2><<<(unsigned)rows, threads_for(2), 0, stream>>>(w, cols, q, s);
+    } else if (n4 <= 1024 * 4) {
+        quantize_int4_rows_kernel<4><<<(unsigned)rows, threads_for(4), 0, stream>>>(w, cols, q, s);
+    } else if (n4 <= 1024 * 8) {
+        quantize_int4_rows_kernel<8><<<(unsigned)rows, threads_for(8), 0, stream>>>(w, cols, q, s);
+    } else {
+        quantize_int4_long_rows_kernel<<<(unsigned)rows, 1024, 0, stream>>>(w, cols, q, s);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_int4(const uint8_t* q, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
+    colsum_int4_kernel<<<(unsigned)blocks, warps_per_block * kWarp, 0, stream>>>(q, N, K, colsum);
     note_launch();
     return cudaGetLastError();
 }
