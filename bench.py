@@ -271,6 +271,9 @@ def run_ours(args, world, rank, local):
     # ---- decode-shaped workload (HBM-bound): same step, reported beside the headline
     decode = None if args.no_decode else measure_decode(q8, device, args, hbm_peak, flush)
 
+    # ---- W4A8: the same layers with int4 weights
+    w4 = None if args.no_decode else measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops)
+
     # ---- the same GEMM with the bias + bf16 epilogue (the pages' output side)
     epi = measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops)
 
@@ -303,6 +306,7 @@ def run_ours(args, world, rank, local):
             "decode": decode,
             "rmsnorm_quantize": rmsq,
             "gemm_bias_bf16": epi,
+            "w4a8": w4,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "weight_prep_ms": round(weight_prep_ms, 3),
@@ -409,6 +413,67 @@ def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode
             "gemm_GB/s": round(gemm_bytes / (gq * 1e-3) / 1e9, 1),
             "gemm_frac_hbm": round(gemm_bytes / (gq * 1e-3) / 1e9 / hbm_peak, 4),
             "algorithmic_bytes": gemm_bytes, "per_kernel": per_kernel}
+
+
+def measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops):
+    """W4A8 (packed int4 weights): the decode GEMM (graph-timed back-to-back launches; the int4
+    weights, N K / 2 bytes, still exceed L2) and the prefill GEMM (L2 flushed per launch)."""
+    import torch
+
+    def graph_ms(fn, n):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            for _ in range(n):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    wl, a_d, w_d = layer_inputs(DECODE, device)
+    Md, Nd, Kd = wl.M, wl.N, wl.K
+    qw4, s4 = q8.q8_quantize_weight_int4(w_d)
+    del w_d
+    qad, sad, _ = q8.q8_quantize_act(a_d)
+    yd = torch.empty((Md, Nd), dtype=torch.float32, device=device)
+    dec = lambda: q8.q8_gemm_w4a8(qad, sad, None, qw4, s4, out=yd)
+    for _ in range(3):
+        dec()
+    dms = graph_ms(dec, max(20, args.steps))
+    dbytes = Nd * Kd // 2 + Md * Kd + 4 * Nd + 4 * Md + 4 * Md * Nd
+    del qw4, yd
+
+    M, K = qa.shape
+    wlh = workloads.WORKLOADS[HEADLINE]
+    wp = torch.from_numpy(workloads.make_weights(wlh)).to(device)
+    qw4p, s4p = q8.q8_quantize_weight_int4(wp)
+    del wp
+    y = torch.empty((M, qw4p.shape[0]), dtype=torch.float32, device=device)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(max(5, args.steps)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    pms = statistics.mean(ms)
+    return {"decode": {"workload": f"{DECODE}: A [{Md},{Kd}] x W int4 [{Nd},{Kd}]", "gemm_ms": round(dms, 4),
+                       "GB/s": round(dbytes / (dms * 1e-3) / 1e9, 1),
+                       "frac_hbm": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": dbytes},
+            "prefill": {"workload": f"{HEADLINE}: A [{M},{K}] x W int4 [{qw4p.shape[0]},{K}]", "gemm_ms": round(pms, 4),
+                        "TFLOP/s": round(ops / (pms * 1e-3) / 1e12, 1)}}
 
 
 def measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops):
@@ -548,6 +613,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped workload")
+    ap.add_argument("--w4-only", action="store_true",
+                    help="only the W4A8 (int4 weight) measurements (one JSON object, for profiling)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode-shaped workload (one JSON object, for profiling)")
     args = ap.parse_args()
@@ -557,6 +624,21 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup()
+    if args.w4_only:
+        import torch
+        import int8_quantized_gemm_gb300 as q8
+        from int8_quantized_gemm_gb300 import build
+        build.build()
+        q8.load()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        wl = workloads.WORKLOADS[HEADLINE]
+        a = torch.from_numpy(workloads.make_activations(wl)).to(device)
+        qa, s_a, _ = q8.q8_quantize_act(a)
+        del a
+        print(json.dumps(measure_w4a8(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K)))
+        return
     if args.decode_only:
         import torch
         import int8_quantized_gemm_gb300 as q8

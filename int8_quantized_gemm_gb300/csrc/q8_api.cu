@@ -118,6 +118,10 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
             if (!q8::gemv_mma_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
             return from_cuda(q8::launch_gemv_mma(qa, qw, M, N, K, ep, s, true));
         }
+        if (kernel == Q8_GEMM_TCGEN05_PAIR) {
+            if (!q8::gemm_tc2_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
+            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, true));
+        }
         return Q8_ERR_UNSUPPORTED;
     }
     if (kernel == Q8_GEMM_AUTO) kernel = q8_gemm_pick(M, N, K);

@@ -59,28 +59,35 @@ constexpr int BMH = 128;
 constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per CTA)
 constexpr int BNH = 128;
 constexpr int BK = 64;
-constexpr int S8 = 4;               // int8 staging stages (16 KB)
 constexpr int S16 = 4;              // fp16 operand stages (32 KB)
-constexpr int KB_PER_CHUNK = 16;    // 1024 K per exact fp32 chunk
 constexpr int kConv = 192;          // converter threads, warps 2..7 of each CTA
 constexpr int kDrainWarps = 8;      // warps 8..15 of each CTA
 constexpr int kThreads = 512;
 constexpr int kRegsLow = 72, kRegsHigh = 184;
 constexpr int kTmemCols = 512;      // two 128 x 256 fp32 accumulator buffers per CTA
 
-constexpr int kA8 = BMH * BK, kB8 = BNH * BK, kStage8 = kA8 + kB8;                // 16 KB
+constexpr int kA8 = BMH * BK;                                                     // 8 KB int8 A staging
 constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16;   // 32 KB
-constexpr int kChunks8 = kStage8 / 16;                                            // 1024
 constexpr int kOffStage8 = S16 * kStage16;
-constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 32 block of 4-byte outputs (TMA store source)
-constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
-constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
-constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
-constexpr int kSmem = kOffBar + kBarBytes + 1024;
+constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 128-byte output block (TMA store source)
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 constexpr uint16_t kPairMask = 0x3;
 
-static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages must keep 1024-byte alignment");
+// Weight format: int8 codes (staged as 128 rows x 64 bytes per CTA) or int4 codes packed
+// two per byte (128 rows x 32 bytes). An fp32 TMEM chunk holds 2^24 / max|product| products
+// exactly: 1024 K for int8 x int8 (|p| <= 2^14), 16384 K for int8 x int4 (|p| <= 2^10).
+template <bool W4>
+struct PairCfg {
+    static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
+    static constexpr int kStage8 = kA8 + kB8;                 // 16 KB (int8) or 12 KB (int4)
+    static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
+    static constexpr int KB_PER_CHUNK = W4 ? 256 : 16;
+    static constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
+    static constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
+    static constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;
+    static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages must keep 1024-byte alignment");
+};
 
 struct PairGeom {
     int num_m, num_n, tiles;
@@ -96,9 +103,13 @@ __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, 
     n0 = (within / rows) * BN;
 }
 
+template <bool W4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, Epilogue ep) {
+    using C = PairCfg<W4>;
+    constexpr int S8 = C::S8, kB8 = C::kB8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
+    constexpr int kOffEpi = C::kOffEpi, kOffBar = C::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -167,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
                 mbar_expect_tx(bar_full8 + 8 * s, kStage8);
                 tma_load_2d(dst, &tmap_a, kb * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
-                tma_load_2d(dst + kA8, &tmap_w, kb * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                tma_load_2d(dst + kA8, &tmap_w, W4 ? kb * (BK / 2) : kb * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
@@ -223,44 +234,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 64-byte staging row); thread ct takes idx = ct + 192 j (j < 6, idx < 1024): row
         // ct / 4 + 48 j, chunk ct % 4. (row & 7) does not change with j, so the swizzled
         // fp16 address is a per-thread base plus 6144 j bytes.
-        const int ct = threadIdx.x - 64;
-        const int r0 = ct >> 2, c0 = ct & 3;
-        const uint32_t src0 = (uint32_t)(ct * 16);
-        const uint32_t dst0 = sw128(r0, 2 * c0);
-        const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
-        for (int g = 0; g < total_g; ++g) {
-            const int s8 = g % S8, s16 = g % S16;
-            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
-                break;
-            const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
-            uint4 in[6];
-#pragma unroll
-            for (int j = 0; j < 6; ++j)
-                in[j] = (ct + kConv * j < kChunks8) ? lds128(st8 + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
-            if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
-                           &g_tc2_error))
-                break;
-            const uint32_t st16 = sbase + s16 * kStage16;
-#pragma unroll
-            for (int j = 0; j < 6; ++j) {
-                if (ct + kConv * j < kChunks8) {
-                    uint4 o0, o1;
-                    cvt_word(in[j].x, o0.x, o0.y);
-                    cvt_word(in[j].y, o0.z, o0.w);
-                    cvt_word(in[j].z, o1.x, o1.y);
-                    cvt_word(in[j].w, o1.z, o1.w);
-                    sts128(st16 + dst0 + 6144 * j, o0);
-                    sts128(st16 + dst1 + 6144 * j, o1);
+        if constexpr (!W4) {
+            const int ct = threadIdx.x - 64;
+            const int r0 = ct >> 2, c0 = ct & 3;
+            const uint32_t src0 = (uint32_t)(ct * 16);
+            const uint32_t dst0 = sw128(r0, 2 * c0);
+            const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
+            for (int g = 0; g < total_g; ++g) {
+                const int s8 = g % S8, s16 = g % S16;
+                if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
+                    break;
+                const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
+                uint4 in[6];
+    #pragma unroll
+                for (int j = 0; j < 6; ++j)
+                    in[j] = (ct + kConv * j < 1024) ? lds128(st8 + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
+                               &g_tc2_error))
+                    break;
+                const uint32_t st16 = sbase + s16 * kStage16;
+    #pragma unroll
+                for (int j = 0; j < 6; ++j) {
+                    if (ct + kConv * j < 1024) {
+                        uint4 o0, o1;
+                        cvt_word(in[j].x, o0.x, o0.y);
+                        cvt_word(in[j].y, o0.z, o0.w);
+                        cvt_word(in[j].z, o1.x, o1.y);
+                        cvt_word(in[j].w, o1.z, o1.w);
+                        sts128(st16 + dst0 + 6144 * j, o0);
+                        sts128(st16 + dst1 + 6144 * j, o1);
+                    }
+                }
+                // Every lane makes its fp16 stores visible to the tensor core, then one lane per
+                // warp arrives: on the MMA barrier in the even CTA, on the relay's barrier in
+                // the odd one.
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive((leader ? bar_full16 : bar_conv16) + 8 * s16);
+                    mbar_arrive(bar_empty8 + 8 * s8);   // after the loaded registers were consumed
                 }
             }
-            // Every lane makes its fp16 stores visible to the tensor core, then one lane per
-            // warp arrives: on the MMA barrier in the even CTA, on the relay's barrier in
-            // the odd one.
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive((leader ? bar_full16 : bar_conv16) + 8 * s16);
-                mbar_arrive(bar_empty8 + 8 * s8);   // after the loaded registers were consumed
+        } else {
+            // int4 weights: A as above over its 512 chunks (j < 3, idx < 512); W's 256 packed chunks
+            // (128 rows x 2 chunks of 32 K) take idx = ct + 192 j (j < 2, idx < 256): row ct / 2 + 96 j,
+            // chunk ct % 2; each becomes four fp16 chunks 4 (ct % 2) + q of its row, word q of the
+            // packed chunk (8 K) giving fp16 chunk q through two nibble pairs, in the K order of cvt_word.
+            const int ct = threadIdx.x - 64;
+            const int ra = ct >> 2, ca = ct & 3;
+            const uint32_t srcA = (uint32_t)(ct * 16);
+            const uint32_t dA0 = sw128(ra, 2 * ca), dA1 = sw128(ra, 2 * ca + 1);
+            const int rw = ct >> 1, cw = ct & 1;
+            const uint32_t srcW = (uint32_t)(kA8 + ct * 16);
+            uint32_t dW[4];
+    #pragma unroll
+            for (int q = 0; q < 4; ++q) dW[q] = (uint32_t)kA16 + sw128(rw, 4 * cw + q);
+            for (int g = 0; g < total_g; ++g) {
+                const int s8 = g % S8, s16 = g % S16;
+                if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
+                    break;
+                const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8;
+                uint4 ia[3], iw[2];
+    #pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    ia[j] = (ct + kConv * j < 512) ? lds128(st8 + srcA + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+    #pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    iw[j] = (ct + kConv * j < 256) ? lds128(st8 + srcW + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
+                               &g_tc2_error))
+                    break;
+                const uint32_t st16 = sbase + s16 * kStage16;
+    #pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    if (ct + kConv * j < 512) {
+                        uint4 o0, o1;
+                        cvt_word(ia[j].x, o0.x, o0.y);
+                        cvt_word(ia[j].y, o0.z, o0.w);
+                        cvt_word(ia[j].z, o1.x, o1.y);
+                        cvt_word(ia[j].w, o1.z, o1.w);
+                        sts128(st16 + dA0 + 6144 * j, o0);
+                        sts128(st16 + dA1 + 6144 * j, o1);
+                    }
+                }
+    #pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (ct + kConv * j < 256) {
+                        const uint32_t wv[4] = {iw[j].x, iw[j].y, iw[j].z, iw[j].w};
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 o;
+                            cvt_int4x4<0x4140u>(wv[q], o.x, o.y);
+                            cvt_int4x4<0x4342u>(wv[q], o.z, o.w);
+                            sts128(st16 + dW[q] + 12288 * j, o);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive((leader ? bar_full16 : bar_conv16) + 8 * s16);
+                    mbar_arrive(bar_empty8 + 8 * s8);   // after the loaded registers were consumed
+                }
             }
         }
       }
@@ -433,8 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K) {
-    if (!(M >= 1 && N >= 1 && K >= 16 && (K % 16) == 0 && M < (1LL << 31) && N < (1LL << 31))) return false;
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, bool w4) {
+    if (!(M >= 1 && N >= 1 && K >= 16 && (K % (w4 ? 32 : 16)) == 0 && M < (1LL << 31) && N < (1LL << 31)))
+        return false;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t kb = (K + BK - 1) / BK;
     return tiles < (1LL << 30) && tiles * kb < (1LL << 31);
@@ -442,7 +518,8 @@ bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K) {
 
 // Clusters of two that fit on the device at once (a GPC with an odd number of
 // free SMs leaves one idle), so that the persistent grid runs in one wave.
-// Cached per device; SMs / 2 if the occupancy query fails.
+// Cached per device and weight format; SMs / 2 if the occupancy query fails.
+template <bool W4>
 static int resident_pairs() {
     static int cached[64] = {0};
     int dev = 0;
@@ -452,24 +529,27 @@ static int resident_pairs() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = PairCfg<W4>::kSmem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) == cudaSuccess && n > 0 && n < pairs) pairs = n;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<W4>, &cfg) == cudaSuccess && n > 0 && n < pairs) pairs = n;
     (void)cudaGetLastError();
     cached[dev] = pairs;
     return pairs;
 }
 
-cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
-                            const Epilogue& ep, cudaStream_t stream) {
-    if (!gemm_tc2_supports(M, N, K)) return cudaErrorNotSupported;
+template <bool W4>
+static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
+                                     const Epilogue& ep, cudaStream_t stream) {
+    using C = PairCfg<W4>;
     CUtensorMap ma, mw;
-    if (!make_tma_map_i8(&ma, qa, M, K, BMH, BK) || !make_tma_map_i8(&mw, qw, N, K, BNH, BK))
+    // int4: the packed weights are a byte matrix [N, K / 2], staged 32 bytes (64 K) per k-block
+    if (!make_tma_map_i8(&ma, qa, M, K, BMH, BK) ||
+        !make_tma_map_i8(&mw, static_cast<const int8_t*>(qw), N, W4 ? K / 2 : K, BNH, W4 ? BK / 2 : BK))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<W4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int64_t pairs = resident_pairs();
+    const int64_t pairs = resident_pairs<W4>();
     const int clusters = (int)(tiles < pairs ? tiles : pairs);
     CUtensorMap mo;
     const bool tma_out = ep.out_i32                  ? make_tma_map_out(&mo, ep.out_i32, kMapI32, M, N)
@@ -477,10 +557,17 @@ cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64
                          : ep.out_kind == kOutBF16 ? make_tma_map_out(&mo, ep.out_bf16, kMapBF16, M, N)
                                                    : make_tma_map_out(&mo, ep.out_i8, kMapI8, M, N);
     if (!tma_out) memset(&mo, 0, sizeof(mo));
-    gemm_tc2_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N, (int)K,
-                                                                ep);
+    gemm_tc2_kernel<W4><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N,
+                                                                      (int)K, ep);
     note_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+                            cudaStream_t stream, bool w4) {
+    if (!gemm_tc2_supports(M, N, K, w4)) return cudaErrorNotSupported;
+    return w4 ? launch_gemm_tc2_t<true>(qa, qw, M, N, K, ep, stream)
+              : launch_gemm_tc2_t<false>(qa, qw, M, N, K, ep, stream);
 }
 
 cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code) {

@@ -71,17 +71,6 @@ struct GemvCfg {
     static constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
 };
 
-// Two packed bytes (K 4t, 4t+1 | 4t+2, 4t+3 as low/high nibbles) -> fp16x2 of the low nibbles
-// (K 4t, 4t+2) and of the high nibbles (K 4t+1, 4t+3): the pairs cvt_word gives an int8 word, so
-// activations and int4 weights share the K order. n ^ 8 = n + 8 for a two's-complement nibble;
-// 0x6400 | (n + 8) is the fp16 value 1024 + n + 8, exactly n after subtracting 1032.
-__device__ __forceinline__ void cvt_int4x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
-    const uint32_t l = (v & 0x000Fu) | ((v & 0x0F00u) << 8);
-    const uint32_t h = ((v >> 4) & 0x000Fu) | ((v & 0xF000u) << 4);
-    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"((l ^ 0x00080008u) | 0x64006400u), "r"(0x64086408u));
-    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"((h ^ 0x00080008u) | 0x64006400u), "r"(0x64086408u));
-}
-
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -224,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {   // weight row 8j + g
                 if constexpr (W4)
-                    cvt_int4x4(wq[j], b[j][0], b[j][1]);
+                    cvt_int4x4<0x4140u>(wq[j], b[j][0], b[j][1]);
                 else
                     cvt_word(wq[j], b[j][0], b[j][1]);
             }

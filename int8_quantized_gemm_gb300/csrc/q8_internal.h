@@ -87,9 +87,9 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
 
 // tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles).
-cudaError_t launch_gemm_tc2(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
-                            const Epilogue& ep, cudaStream_t stream);
-bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+                            cudaStream_t stream, bool w4 = false);
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, bool w4 = false);
 
 // tcgen05 kernel for M <= 16 (decode): weight rows on the MMA's M side.
 cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,

@@ -152,6 +152,24 @@ __device__ __forceinline__ void cvt_word(uint32_t w, uint32_t& lo, uint32_t& hi)
     hi = hsub_1152(((w >> 8) & 0x00FF00FFu) ^ 0x64806480u);
 }
 
+// Two packed int4 bytes (K 4t, 4t+1 | 4t+2, 4t+3 as low/high nibbles) -> fp16x2 of the low
+// nibbles (K 4t, 4t+2) and of the high nibbles (K 4t+1, 4t+3): the pairs cvt_word gives for an
+// int8 word, so activations and int4 weights share the K order. SEL picks the two bytes of w
+// (0x4140: bytes 0, 1; 0x4342: bytes 2, 3) and spreads them to the low byte of each half.
+// A nibble n (two's complement) XOR 8 is n + 8. Low nibbles: (x & 0x000F000F) ^ 0x64086408 sets
+// the fp16 exponent of 1024 and flips bit 3 in one lop3, giving 1024 + n + 8; minus 1032 is n.
+// High nibbles sit four bits up: (x & 0x00F000F0) ^ 0x64806480 is 1024 + 16 (n + 8), and
+// (that / 16) - 72 = n, one fp16 FMA with exact operands and an exact result.
+template <uint32_t SEL>
+__device__ __forceinline__ void cvt_int4x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t x, l, h;
+    asm("prmt.b32 %0, %1, 0, %2;\n" : "=r"(x) : "r"(w), "n"(SEL));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(l) : "r"(x), "r"(0x000F000Fu), "r"(0x64086408u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(h) : "r"(x), "r"(0x00F000F0u), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(l), "r"(0x64086408u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(h), "r"(0x2C002C00u), "r"(0xD480D480u));
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
