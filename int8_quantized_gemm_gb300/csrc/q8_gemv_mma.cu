@@ -46,26 +46,29 @@ using namespace tc;
 
 constexpr int RW = 64;             // weight rows per tile
 constexpr int NT = 16;             // token rows (MMA M)
-constexpr int BK = 256;            // K per stage: 128-byte swizzled boxes
-constexpr int BKH = 128;
-constexpr int kA8 = NT * BK;       // 4 KB of activations per stage
-constexpr int kComputeWarps = BK / 16;   // one MMA K-step of the stage each
+constexpr int BK = 256;            // K of one step of all compute warps (one 16-wide K-step each)
+constexpr int BKH = 128;           // bytes of one swizzled TMA box row
+constexpr int kComputeWarps = BK / 16;
 constexpr int kThreads = 32 * (1 + kComputeWarps);
 // int32 tile sums [2 (tile parity)][16 tokens][64 rows], token rows padded to 72 words so
 // that the eight tokens of one atomic instruction fall in different banks (2-way, not 8-way)
 constexpr int RWP = RW + 8;
 constexpr int kRedBytes = 2 * NT * RWP * 4;
 
-// Weight format: int8 codes (two 128-byte boxes of 64 rows per stage, 16 KB) or int4 codes
-// packed two per byte (one box, 8 KB). An fp32 partial sum may hold 2^24 / max|product|
-// products exactly: 1024 for int8 x int8 (|p| <= 2^14), 16384 for int8 x int4 (|p| <= 2^10);
-// each warp adds 16 per stage.
+// Weight format: int8 codes or int4 codes packed two per byte; a stage holds two W boxes of
+// 64 rows x 128 bytes (16 KB). An fp32 partial sum may hold 2^24 / max|product| products
+// exactly: 1024 for int8 x int8 (|p| <= 2^14), 16384 for int8 x int4 (|p| <= 2^10); each warp
+// adds 16 per step. int4 stages hold two steps (512 K: two W boxes of 256 K each, four A boxes), so that the
+// per-stage costs (waits, arrives, bookkeeping) are spread over twice the MMAs.
 template <bool W4>
 struct GemvCfg {
-    static constexpr int kW8 = RW * (W4 ? BK / 2 : BK);
+    static constexpr int SPW = W4 ? 2 : 1;           // K-steps per warp per stage
+    static constexpr int kBK = BK * SPW;             // K per stage
+    static constexpr int kW8 = RW * (W4 ? kBK / 2 : kBK);
+    static constexpr int kA8 = NT * kBK;
     static constexpr int kStage = kW8 + kA8;
-    static constexpr int S8 = W4 ? 16 : 10;   // stages in the ring
-    static constexpr int kStagesPerChunk = W4 ? 1024 : 64;
+    static constexpr int S8 = W4 ? 8 : 10;   // stages in the ring
+    static constexpr int kStagesPerChunk = (W4 ? 16384 : 1024) / (16 * SPW);
     static constexpr int kOffRed = S8 * kStage;
     static constexpr int kOffBar = kOffRed + kRedBytes;
     static constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int M, int N, int K, Epilogue ep) {
     using C = GemvCfg<W4>;
     constexpr int S8 = C::S8, kW8 = C::kW8, kStage = C::kStage, kStagesPerChunk = C::kStagesPerChunk;
+    constexpr int SPW = C::SPW, kBK = C::kBK;
     constexpr int kOffRed = C::kOffRed, kOffBar = C::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     const int tiles = (N + RW - 1) / RW;
-    const int KB = (K + BK - 1) / BK;
+    const int KB = (K + kBK - 1) / kBK;
     const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total_g = my_tiles * KB;
     // each CTA starts its K sweep at its own block, spreading activation reads over L2
@@ -141,17 +145,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
                                &g_gemv_mma_error))
                     break;
-                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
+                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kBK;
                 const uint32_t dst = sbase + s * kStage;
                 mbar_expect_tx(bar_full + 8 * s, kStage);
-                if constexpr (W4) {
-                    tma_load_2d(dst, &tmap_w, kx / 2, n0, bar_full + 8 * s);   // 256 K = 128 packed bytes
-                } else {
-                    tma_load_2d(dst, &tmap_w, kx, n0, bar_full + 8 * s);
-                    tma_load_2d(dst + RW * BKH, &tmap_w, kx + BKH, n0, bar_full + 8 * s);
-                }
-                tma_load_2d(dst + kW8, &tmap_a, kx, 0, bar_full + 8 * s);
-                tma_load_2d(dst + kW8 + NT * BKH, &tmap_a, kx + BKH, 0, bar_full + 8 * s);
+                // W: two boxes of 64 rows x 128 bytes (int8: 256 K; int4: 512 K packed)
+                const int wx = W4 ? kx / 2 : kx;
+                tma_load_2d(dst, &tmap_w, wx, n0, bar_full + 8 * s);
+                tma_load_2d(dst + RW * BKH, &tmap_w, wx + BKH, n0, bar_full + 8 * s);
+#pragma unroll
+                for (int b = 0; b < kBK / BKH; ++b)   // A: 16 tokens x 128 K per box
+                    tma_load_2d(dst + kW8 + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
@@ -161,14 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ct = threadIdx.x - 32;  // 0 .. 511
         const int g8 = lane >> 2, t = lane & 3;
         const int half = ks >> 3, kc = ks & 7;   // which 128-byte box, 16-byte chunk in its rows
-        // weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t
-        // int4: the step's 16 K are 8 packed bytes, half of chunk ks / 2 of the single box;
-        // lane quad t takes bytes 2t, 2t + 1 of them (K 4t .. 4t + 3)
-        uint32_t w_off[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            w_off[j] = W4 ? sw128(8 * j + g8, ks >> 1) + 8 * (ks & 1) + 2 * t
-                          : half * (RW * BKH) + sw128(8 * j + g8, kc) + 4 * t;
+        // weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t.
+        // int4: the step's 16 K are 8 packed bytes, half of chunk ks / 2 of the first W box; lane
+        // quad t takes bytes 2t, 2t + 1 of them (K 4t .. 4t + 3). The warp's second step (K-step
+        // ks + 16 of the 512-K stage) sits one W box (64 x 128 bytes) and two A boxes further.
+        // Row 8j + g lies 1024 j bytes past row g: the swizzle depends on (row & 7) = g only.
+        const uint32_t w_base = W4 ? sw128(g8, ks >> 1) + 8 * (ks & 1) + 2 * t : half * (RW * BKH) + sw128(g8, kc) + 4 * t;
         const uint32_t a_off0 = kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
         const uint32_t a_off1 = kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
         for (int i = ct; i < 2 * NT * RWP; i += 32 * kComputeWarps) red[i] = 0;
@@ -203,26 +204,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    kErrConvFull, &g_gemv_mma_error)))
                 break;
             const uint32_t st = sbase + s * kStage;
-            uint32_t wq[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) wq[j] = W4 ? lds16(st + w_off[j]) : lds32(st + w_off[j]);
-            const uint32_t aq0 = lds32(st + a_off0), aq1 = lds32(st + a_off1);
-            uint32_t a[4], b[8][2];
-            cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
-            cvt_word(aq1, a[1], a[3]);     // token row g+8
+            for (int u = 0; u < SPW; ++u) {   // steps in turn: 17 warps leave at most 96 registers a thread
+                uint32_t wq[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {   // weight row 8j + g
-                if constexpr (W4)
-                    cvt_int4x4<0x4140u>(wq[j], b[j][0], b[j][1]);
-                else
-                    cvt_word(wq[j], b[j][0], b[j][1]);
+                for (int j = 0; j < 8; ++j)
+                    wq[j] = W4 ? lds16(st + w_base + 1024 * j + u * (RW * BKH)) : lds32(st + w_base + 1024 * j);
+                const uint32_t aq0 = lds32(st + a_off0 + u * (2 * NT * BKH));
+                const uint32_t aq1 = lds32(st + a_off1 + u * (2 * NT * BKH));
+                uint32_t a[4], b[8][2];
+                cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
+                cvt_word(aq1, a[1], a[3]);     // token row g+8
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {   // weight row 8j + g
+                    if constexpr (W4)
+                        cvt_int4x4<0x4140u>(wq[j], b[j][0], b[j][1]);
+                    else
+                        cvt_word(wq[j], b[j][0], b[j][1]);
+                }
+                if (u == SPW - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             const bool tile_end = (kb == KB - 1);
-            if (++in_chunk == kStagesPerChunk || tile_end) {
+            // int4: one exact fp32 chunk covers any tile (K <= kStagesPerChunk * kBK, checked by
+            // gemv_mma_supports), so the partials go to the tile sums directly at the tile's end
+            if (!W4 && (++in_chunk == kStagesPerChunk || tile_end)) {
                 in_chunk = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -242,8 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
                         const int r = 8 * j + 2 * t + (e & 1);
-                        atomicAdd(rb + m * RWP + r, tot[j][e]);
-                        tot[j][e] = 0;
+                        if constexpr (W4) {
+                            atomicAdd(rb + m * RWP + r, __float2int_rn(part[j][e]));
+                            part[j][e] = 0.0f;
+                        } else {
+                            atomicAdd(rb + m * RWP + r, tot[j][e]);
+                            tot[j][e] = 0;
+                        }
                     }
                 named_barrier(1, 32 * kComputeWarps);
                 // Read and re-zero this thread's two sums. The buffer is next written at tile
@@ -291,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4) {
     if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % (w4 ? 32 : 16)) == 0)) return false;
+    if (w4 && K > (int64_t)GemvCfg<true>::kStagesPerChunk * GemvCfg<true>::kBK) return false;   // one chunk per tile
     const int64_t tiles = (N + RW - 1) / RW;
     const int64_t kb = (K + BK - 1) / BK;
     return tiles * kb < (1LL << 31);
