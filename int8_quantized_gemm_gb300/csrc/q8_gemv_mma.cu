@@ -1,22 +1,22 @@
 // Decode-shaped integer GEMM (M <= 16 tokens) + dequantization epilogue on the
 // warp-level fp16 tensor-core instruction mma.sync.m16n8k16 (fp32 accumulate).
 //
-// With a handful of tokens the layer is a stream of the int8 weights from HBM
+// With a handful of tokens the layer is a stream of the weight codes from HBM
 // with little arithmetic per byte. The weights go HBM -> shared memory by TMA
-// (an 8-stage ring per SM; a stage is 64 rows x 256 bytes of K, fetched as two
-// 128-byte boxes, which streams DRAM better than 128-byte row pieces) and shared
-// memory -> registers by ordinary loads;
-// each warp converts its int8 fragments to fp16 in registers and feeds them
+// (a ring of stages per SM; an int8 stage is 64 rows x 256 bytes of K, fetched as
+// two 128-byte boxes, which streams DRAM better than 128-byte row pieces) and
+// shared memory -> registers by ordinary loads;
+// each warp converts its code fragments to fp16 in registers and feeds them
 // straight to the MMA, so converted data never goes back through shared memory.
 // (The int8 MMA of this GPU runs at a fraction of the fp16 rate, too low for
 // this stream.)
 //
-// Exactness: int8 codes and their products are exact in fp16 / fp32; each
-// fp32 accumulator holds the sum of at most 1024 products (|sum| <= 2^24, an
-// exactly representable integer) before it is converted to int32 and added to
-// an INT32 total, so the result is the exact integer dot product.
+// Exactness: the codes, offset weight codes and their products are exact in fp16 /
+// fp32, and each fp32 accumulator is drained to int32 before its integer sum can
+// pass 2^24 (the weight format note below), so the result is the exact integer
+// dot product.
 //
-// K order inside a stage: compute warp s (of 16) owns the 16 K values
+// int8 K order inside a stage: compute warp s (of 16) owns the 16 K values
 // [16s, 16s+16) of every stage, one MMA K-step; lane quad t holds the 4 bytes
 // [16s + 4t, +4) of its rows, bytes (0, 2) as the k pair (2t, 2t+1) and (1, 3)
 // as (8+2t, 9+2t).
@@ -55,23 +55,37 @@ constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int RWP = RW + 8;
 constexpr int kRedBytes = 2 * NT * RWP * 4;
 
-// Weight format: int8 codes or int4 codes packed two per byte; a stage holds two W boxes of
-// 64 rows x 128 bytes (16 KB). An fp32 partial sum may hold 2^24 / max|product| products
-// exactly: 1024 for int8 x int8 (|p| <= 2^14), 16384 for int8 x int4 (|p| <= 2^10); each warp
-// adds 16 per step. int4 stages hold two steps (512 K: two W boxes of 256 K each, four A boxes), so that the
-// per-stage costs (waits, arrives, bookkeeping) are spread over twice the MMAs.
+// Weight format: int8 codes or int4 codes packed two per byte. A weight code enters the MMA
+// offset to a non-negative integer and scaled to an fp16 subnormal, made by one lop3 (mask the
+// code, flip its sign bit), with no fp16 arithmetic:
+//   int8: (w + 128) 2^-24, exact in the 10-bit subnormal significand;
+//   int4: (n + 8) 2^-24; a high nibble, four bits up, is (n + 8) 2^-20 and meets the token code
+//         a / 16 (exact in fp16) instead of a.
+// Every product is then an integer times 2^-24 (|a (w + 128)| <= 32640, |a (n + 8)| <= 1920),
+// so an fp32 partial is exact while it holds at most 2^24 / that many products: 512 (int8; the
+// warp drains its partials to int32 every 32 K-steps) or, for int4, a whole tile (K / 16
+// products for K <= 139810). A drained partial is scaled by 2^24 (exact), and at the end
+// c sum_k a_k (c = 128 or 8), the token's code sum taken with dp4a while a CTA runs its first
+// tile, is subtracted. The int32 sums may wrap; the result, |sum_k a_k w_k| < 2^31, is exact.
+// int8: a stage is 256 K (two W boxes of 64 rows x 128 bytes, two A boxes), one K-step per warp.
+// int4: a stage is kW4Segs segments of 512 K; a segment is two W boxes (64 rows x 128 packed
+// bytes = 256 K each) and four A boxes, and warp ks owns the 32 K [32 ks, 32 ks + 32) of each
+// segment: one 4-byte load per weight row (8 codes) feeds two K-steps. Longer stages spread the
+// per-stage costs (waits, arrives, bookkeeping) over more MMAs.
+constexpr int kW4Segs = 2;
 template <bool W4>
 struct GemvCfg {
-    static constexpr int SPW = W4 ? 2 : 1;           // K-steps per warp per stage
+    static constexpr int SPW = W4 ? 2 * kW4Segs : 1;   // K-steps per warp per stage
     static constexpr int kBK = BK * SPW;             // K per stage
     static constexpr int kW8 = RW * (W4 ? kBK / 2 : kBK);
     static constexpr int kA8 = NT * kBK;
     static constexpr int kStage = kW8 + kA8;
-    static constexpr int S8 = W4 ? 8 : 10;   // stages in the ring
-    static constexpr int kStagesPerChunk = (W4 ? 16384 : 1024) / (16 * SPW);
+    static constexpr int S8 = W4 ? 8 / kW4Segs : 10;   // stages in the ring
+    static constexpr int kStagesPerChunk = 512 / 16;   // int8
     static constexpr int kOffRed = S8 * kStage;
     static constexpr int kOffBar = kOffRed + kRedBytes;
-    static constexpr int kSmem = kOffBar + 16 * S8 + 16 + 1024;
+    static constexpr int kOffSum = kOffBar + 16 * S8 + 16;    // token code sums [16]
+    static constexpr int kSmem = kOffSum + 4 * NT + 1024;
 };
 
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -88,10 +102,39 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
     return v;
+}
+
+// int8 weights: lo = {byte 0, byte 2} and hi = {byte 1, byte 3} of w as the fp16 subnormals
+// (w + 128) 2^-24: (x & 0x00FF00FF) ^ 0x00800080.
+__device__ __forceinline__ void cvt_int8_subnormal(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(lo) : "r"(w), "r"(0x00FF00FFu), "r"(0x00800080u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(hi) : "r"(w >> 8), "r"(0x00FF00FFu), "r"(0x00800080u));
+}
+
+// int4 weights (step of one 32-bit word w: bytes 0 and 2, i.e. the caller shifts w right by 8
+// for bytes 1 and 3): lo = {low nibble of byte 0, of byte 2} and hi = {high nibbles}, as fp16
+// subnormals: (x & 0x000F000F) ^ 0x00080008 is (n + 8) 2^-24, and the high nibbles four bits up
+// are (n + 8) 2^-20. One lop3 each.
+__device__ __forceinline__ void cvt_int4_subnormal(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(lo) : "r"(w), "r"(0x000F000Fu), "r"(0x00080008u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(hi) : "r"(w), "r"(0x00F000F0u), "r"(0x00800080u));
+}
+
+// The token codes that meet step U of cvt_int4_subnormal: q.x holds K 8t .. 8t + 3, q.y K 8t + 4
+// .. 8t + 7. lo = {x.byte 2U, y.byte 2U} as fp16 a (meeting the low nibbles), hi = {x.byte 2U+1,
+// y.byte 2U+1} as fp16 a / 16 (meeting the high nibbles, which carry a factor 16). With
+// 0x6480 | (byte ^ 0x80) = 1024 + 128 + a: minus 1152 gives a; / 16 - 72 gives a / 16, exactly.
+__device__ __forceinline__ void cvt_tokens_w4(int U, uint2 q, uint32_t& lo, uint32_t& hi) {
+    uint32_t p, l, h;
+    asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(p) : "r"(q.x), "r"(q.y), "r"(U ? 0x7632u : 0x5410u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(l) : "r"(p), "r"(0x00FF00FFu), "r"(0x64806480u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(h) : "r"(p >> 8), "r"(0x00FF00FFu), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(h), "r"(0x2C002C00u), "r"(0xD480D480u));
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
@@ -104,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int M, int N, int K, Epilogue ep) {
     using C = GemvCfg<W4>;
     constexpr int S8 = C::S8, kW8 = C::kW8, kStage = C::kStage, kStagesPerChunk = C::kStagesPerChunk;
-    constexpr int SPW = C::SPW, kBK = C::kBK;
+    constexpr int kBK = C::kBK;
     constexpr int kOffRed = C::kOffRed, kOffBar = C::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
@@ -114,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_empty = bar_full + 8 * S8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 16 * S8);
     int32_t* red = reinterpret_cast<int32_t*>(smem + kOffRed);
+    int32_t* tok_sum = reinterpret_cast<int32_t*>(smem + C::kOffSum);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -148,10 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kBK;
                 const uint32_t dst = sbase + s * kStage;
                 mbar_expect_tx(bar_full + 8 * s, kStage);
-                // W: two boxes of 64 rows x 128 bytes (int8: 256 K; int4: 512 K packed)
+                // W: boxes of 64 rows x 128 bytes (int8: 128 K; int4: 256 K packed)
                 const int wx = W4 ? kx / 2 : kx;
-                tma_load_2d(dst, &tmap_w, wx, n0, bar_full + 8 * s);
-                tma_load_2d(dst + RW * BKH, &tmap_w, wx + BKH, n0, bar_full + 8 * s);
+#pragma unroll
+                for (int b = 0; b < kW8 / (RW * BKH); ++b)
+                    tma_load_2d(dst + b * (RW * BKH), &tmap_w, wx + b * BKH, n0, bar_full + 8 * s);
 #pragma unroll
                 for (int b = 0; b < kBK / BKH; ++b)   // A: 16 tokens x 128 K per box
                     tma_load_2d(dst + kW8 + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
@@ -164,15 +209,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ct = threadIdx.x - 32;  // 0 .. 511
         const int g8 = lane >> 2, t = lane & 3;
         const int half = ks >> 3, kc = ks & 7;   // which 128-byte box, 16-byte chunk in its rows
-        // weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t.
-        // int4: the step's 16 K are 8 packed bytes, half of chunk ks / 2 of the first W box; lane
-        // quad t takes bytes 2t, 2t + 1 of them (K 4t .. 4t + 3). The warp's second step (K-step
-        // ks + 16 of the 512-K stage) sits one W box (64 x 128 bytes) and two A boxes further.
+        // int8: weight row 8j + g and token rows g, g+8 at chunk kc of box `half` (swizzled), word t.
+        // int4 (per 512-K segment): the warp's 32 K are chunk ks & 7 of W box ks >> 3 (16 packed
+        // bytes a row); lane quad t takes word t, K 8t .. 8t + 7: bytes 0, 1 (K 8t .. 8t + 3) for
+        // the first K-step, bytes 2, 3 for the second. The same K of the tokens are 8 bytes at 8t
+        // of the warp's 32 bytes in A box ks >> 2: chunk 2 (ks & 3) + t / 2, offset 8 (t & 1).
         // Row 8j + g lies 1024 j bytes past row g: the swizzle depends on (row & 7) = g only.
-        const uint32_t w_base = W4 ? sw128(g8, ks >> 1) + 8 * (ks & 1) + 2 * t : half * (RW * BKH) + sw128(g8, kc) + 4 * t;
-        const uint32_t a_off0 = kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
-        const uint32_t a_off1 = kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
+        const uint32_t w_base = W4 ? (ks >> 3) * (RW * BKH) + sw128(g8, ks & 7) + 4 * t
+                                   : half * (RW * BKH) + sw128(g8, kc) + 4 * t;
+        const uint32_t a_off0 = W4 ? kW8 + (ks >> 2) * (NT * BKH) + sw128(g8, 2 * (ks & 3) + (t >> 1)) + 8 * (t & 1)
+                                   : kW8 + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
+        const uint32_t a_off1 = W4 ? kW8 + (ks >> 2) * (NT * BKH) + sw128(g8 + 8, 2 * (ks & 3) + (t >> 1)) + 8 * (t & 1)
+                                   : kW8 + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
         for (int i = ct; i < 2 * NT * RWP; i += 32 * kComputeWarps) red[i] = 0;
+        if (ct < NT) tok_sum[ct] = 0;
         named_barrier(1, 32 * kComputeWarps);
         // Epilogue outputs of this thread: tokens em and em + 8, row er of each tile. The token
         // scales are loaded once here; the channel scales at the tile's end (loading them at the
@@ -197,6 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) tot[j][e] = 0, part[j][e] = 0.0f;
         int kb = 0, ti = 0, in_chunk = 0, g = 0;
+        int sum0 = 0, sum1 = 0;        // first tile: code sums of tokens g, g + 8 over this lane's K
+        int esum0 = 0, esum1 = 0;      // code sums of the epilogue tokens em, em + 8
         for (; g < total_g; ++g) {
             const int s = g % S8;
             // warp-uniform: the whole warp leaves together when a wait gives up (abort)
@@ -204,41 +256,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    kErrConvFull, &g_gemv_mma_error)))
                 break;
             const uint32_t st = sbase + s * kStage;
+            if constexpr (W4) {
 #pragma unroll
-            for (int u = 0; u < SPW; ++u) {   // steps in turn: 17 warps leave at most 96 registers a thread
+                for (int sg = 0; sg < kW4Segs; ++sg) {   // segments in turn: 17 warps leave at most 96 registers a thread
+                    uint32_t wq[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_base + 1024 * j + sg * (2 * RW * BKH));
+                    const uint2 aq0 = lds64(st + a_off0 + sg * (4 * NT * BKH));
+                    const uint2 aq1 = lds64(st + a_off1 + sg * (4 * NT * BKH));
+                    if (ti == 0) {
+                        sum0 = __dp4a((int)aq0.x, 0x01010101, __dp4a((int)aq0.y, 0x01010101, sum0));
+                        sum1 = __dp4a((int)aq1.x, 0x01010101, __dp4a((int)aq1.y, 0x01010101, sum1));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        // step u: weight bytes u, u + 2 of each word (K 8t + 2u, + 1 | 8t + 4 + 2u, + 1)
+                        uint32_t a[4], b[8][2];
+                        cvt_tokens_w4(u, aq0, a[0], a[2]);   // token row g
+                        cvt_tokens_w4(u, aq1, a[1], a[3]);   // token row g+8
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)    // weight row 8j + g
+                            cvt_int4_subnormal(u ? wq[j] >> 8 : wq[j], b[j][0], b[j][1]);
+                        if (sg == kW4Segs - 1 && u == 0) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
+                    }
+                }
+            } else {
                 uint32_t wq[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    wq[j] = W4 ? lds16(st + w_base + 1024 * j + u * (RW * BKH)) : lds32(st + w_base + 1024 * j);
-                const uint32_t aq0 = lds32(st + a_off0 + u * (2 * NT * BKH));
-                const uint32_t aq1 = lds32(st + a_off1 + u * (2 * NT * BKH));
+                for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_base + 1024 * j);
+                const uint32_t aq0 = lds32(st + a_off0);
+                const uint32_t aq1 = lds32(st + a_off1);
+                if (ti == 0) {
+                    sum0 = __dp4a((int)aq0, 0x01010101, sum0);
+                    sum1 = __dp4a((int)aq1, 0x01010101, sum1);
+                }
                 uint32_t a[4], b[8][2];
                 cvt_word(aq0, a[0], a[2]);     // token row g:   k pair (2t,2t+1) and (8+2t,9+2t)
                 cvt_word(aq1, a[1], a[3]);     // token row g+8
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {   // weight row 8j + g
-                    if constexpr (W4)
-                        cvt_int4x4<0x4140u>(wq[j], b[j][0], b[j][1]);
-                    else
-                        cvt_word(wq[j], b[j][0], b[j][1]);
-                }
-                if (u == SPW - 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
-                }
+                for (int j = 0; j < 8; ++j) cvt_int8_subnormal(wq[j], b[j][0], b[j][1]);   // weight row 8j + g
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             }
             const bool tile_end = (kb == KB - 1);
-            // int4: one exact fp32 chunk covers any tile (K <= kStagesPerChunk * kBK, checked by
-            // gemv_mma_supports), so the partials go to the tile sums directly at the tile's end
+            // int4: the fp32 partials are exact over the whole tile (K bounded in
+            // gemv_mma_supports), so they go to the tile sums directly at the tile's end
             if (!W4 && (++in_chunk == kStagesPerChunk || tile_end)) {
                 in_chunk = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        tot[j][e] += __float2int_rn(part[j][e]);
+                        tot[j][e] += __float2int_rn(part[j][e] * 16777216.0f);
                         part[j][e] = 0.0f;
                     }
             }
@@ -253,18 +329,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int m = g8 + (e >> 1) * 8;            // c0,c1: token g; c2,c3: token g+8
                         const int r = 8 * j + 2 * t + (e & 1);
                         if constexpr (W4) {
-                            atomicAdd(rb + m * RWP + r, __float2int_rn(part[j][e]));
+                            atomicAdd(rb + m * RWP + r, __float2int_rn(part[j][e] * 16777216.0f));
                             part[j][e] = 0.0f;
                         } else {
                             atomicAdd(rb + m * RWP + r, tot[j][e]);
                             tot[j][e] = 0;
                         }
                     }
+                if (ti == 0) {   // token code sums: over the lane quad, then over the warps
+                    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
+                    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
+                    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 1);
+                    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 2);
+                    if (t == 0) {
+                        atomicAdd(tok_sum + g8, sum0);
+                        atomicAdd(tok_sum + g8 + 8, sum1);
+                    }
+                }
                 named_barrier(1, 32 * kComputeWarps);
+                if (ti == 0) {
+                    esum0 = tok_sum[em];
+                    esum1 = tok_sum[em + 8];
+                }
                 // Read and re-zero this thread's two sums. The buffer is next written at tile
                 // ti + 2, after every thread has passed the tile barrier of tile ti + 1.
                 const int i0 = em * RWP + er, i1 = i0 + 8 * RWP;
-                const int v0 = rb[i0], v1 = rb[i1];
+                constexpr uint32_t kOffset = W4 ? 8u : 128u;
+                const int v0 = (int)((uint32_t)rb[i0] - kOffset * (uint32_t)esum0);
+                const int v1 = (int)((uint32_t)rb[i1] - kOffset * (uint32_t)esum1);
                 rb[i0] = 0;
                 rb[i1] = 0;
                 const int n = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + er;
@@ -306,7 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4) {
     if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % (w4 ? 32 : 16)) == 0)) return false;
-    if (w4 && K > (int64_t)GemvCfg<true>::kStagesPerChunk * GemvCfg<true>::kBK) return false;   // one chunk per tile
+    if (w4) {   // int4: each warp's fp32 partial must stay exact over a tile: products 1920 at most
+        const int64_t stages = (K + GemvCfg<true>::kBK - 1) / GemvCfg<true>::kBK;
+        if (stages * 16 * GemvCfg<true>::SPW * 1920 >= (1LL << 24)) return false;
+    }
     const int64_t tiles = (N + RW - 1) / RW;
     const int64_t kb = (K + BK - 1) / BK;
     return tiles * kb < (1LL << 31);

@@ -166,6 +166,22 @@ def test_gemm_s32_extreme_codes(q8, kernel):
     np.testing.assert_array_equal(acc, np.broadcast_to(expect, (M, N)))
 
 
+def test_decode_largest_k_extreme_codes(q8):
+    """The decode kernel offsets weight codes by 128: at the largest K its int32 tile sums of
+    a (w + 128) pass 2^31 and wrap, and the result must still be exact."""
+    M, N, K = 16, 72, 131056
+    rng = np.random.default_rng(K)
+    qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-128, 128, (N, K), dtype=np.int8)
+    qa[0], qa[1] = -128, 127
+    qw[0], qw[1], qw[2] = 127, -128, 127
+    acc = host(q8.q8_gemm_s32(dev(qa), dev(qw), kernel="decode")).astype(np.int64)
+    assert_no_device_error(q8)
+    want = oracle.gemm_acc(qa, qw, threads=8)
+    assert want[0, 0] == -128 * 127 * K and want[0, 1] == 16384 * K and want[1, 2] == 127 * 127 * K
+    np.testing.assert_array_equal(acc, want)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_gemm_s32_small_terms_next_to_large_partial_sums(q8, kernel):
     """Each 1024-deep chunk first climbs to ~2^24 with -128*-128 products, then adds +-1

@@ -62,6 +62,24 @@ def test_decode_w4a8_accumulators_bit_exact(q8, M, N, K):
     np.testing.assert_array_equal(host(acc).astype(np.int64), oracle.gemm_acc(qa, q4, threads=8))
 
 
+@pytest.mark.parametrize("kernel", ["decode", "tcgen05_pair"])
+def test_w4a8_largest_products_at_the_largest_k(q8, kernel):
+    # |a (n + 8)| and |a n| at their maxima on every k, at the largest K the API takes: the
+    # decode kernel's fp32 partials reach their bound here
+    M, N, K = (16, 72, 131040) if kernel == "decode" else (256, 256, 65536)
+    rng = np.random.default_rng(K)
+    qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+    q4 = rng.integers(-8, 8, (N, K), dtype=np.int8)
+    qa[0, :], qa[1, :], qa[2, :] = -128, 127, -128
+    q4[0, :], q4[1, :], q4[2, :] = 7, -8, -8
+    acc = q8.q8_gemm_w4a8_s32(dev(qa), dev(oracle.pack_int4(q4)), kernel=kernel)
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    want = oracle.gemm_acc(qa, q4, threads=8)
+    assert want[0, 0] == -128 * 7 * K and want[2, 2] == 1024 * K
+    np.testing.assert_array_equal(host(acc).astype(np.int64), want)
+
+
 @pytest.mark.parametrize("sym", [True, False])
 def test_decode_w4a8_layer_matches_oracle(q8, sym):
     wl = workloads.WORKLOADS["decode"]
