@@ -22,6 +22,8 @@ Every function follows a passage of the pages (cited in q8_oracle.c):
   linear_codes_bias, to_bf16,    "Activation Quantization Architecture" (Fusion:
   quantize_static                the epilogue adds the bias, writes bf16, or
                                  quantizes the output for the next GEMM)
+  quantize_weight_mx, gemm_mx,   TileLang tutorial ch. 27 (2.3 MX / block-scaled:
+  linear_mx, e8m0_ceil           block granularity + E8M0, the scale-word packing)
 All of them are pinned by tests/test_oracle_pins.py and tests/test_oracle_rmsnorm.py.
 """
 from __future__ import annotations
@@ -97,6 +99,14 @@ def _load():
         lib.q8o_quantize_static.argtypes = [p, i64, ctypes.c_float, p]
         lib.q8o_quantize_static.restype = None
         lib.q8o_rmsnorm.restype = i32
+        lib.q8o_e8m0_ceil.argtypes = [ctypes.c_float]
+        lib.q8o_e8m0_ceil.restype = i32
+        lib.q8o_quantize_weight_mx.argtypes = [p, i64, i64, i32, p, p]
+        lib.q8o_quantize_weight_mx.restype = i32
+        lib.q8o_gemm_mx.argtypes = [p, p, p, i64, i64, i64, i32, p, p, i32]
+        lib.q8o_gemm_mx.restype = i32
+        lib.q8o_linear_mx.argtypes = [p, p, i32, p, p, p, i64, i64, i64, i32, p, i32]
+        lib.q8o_linear_mx.restype = i32
         lib.q8o_openmp_max_threads.argtypes = []
         lib.q8o_openmp_max_threads.restype = i32
         _lib = lib
@@ -250,6 +260,51 @@ def unpack_int4(packed: np.ndarray, cols: int) -> np.ndarray:
     out = np.empty((rows, cols), np.int8)
     assert _load().q8o_unpack_int4(_ptr(packed), rows, cols, _ptr(out)) == OK
     return out
+
+
+def e8m0_ceil(x: float) -> int:
+    """E8M0 byte of x rounded up to a power of two (clamped to 103 .. 136)."""
+    return int(_load().q8o_e8m0_ceil(ctypes.c_float(x)))
+
+
+def mx_words(K: int, G: int) -> int:
+    """32-bit scale words per weight row: four E8M0 bytes per word."""
+    return (K // G + 3) // 4
+
+
+def quantize_weight_mx(w: np.ndarray, G: int):
+    """Block-scaled int8 weights: codes int8 [N, K] and E8M0 scale words uint32
+    [ceil(K / G / 4), N] (byte b of word w is group 4w + b; group-major)."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), np.int8)
+    sf = np.empty((mx_words(K, G), N), np.uint32)
+    assert _load().q8o_quantize_weight_mx(_ptr(w), N, K, G, _ptr(q), _ptr(sf)) == OK
+    return q, sf
+
+
+def gemm_mx(qa: np.ndarray, q: np.ndarray, sf: np.ndarray, G: int, threads: int = 1):
+    """T = sum_k qa * q * s exactly, rounded once to fp32 [M, N]; and sum_k |qa * q * s| (fp64)."""
+    qa, q, sf = _c(qa, np.int8), _c(q, np.int8), _c(sf, np.uint32)
+    M, K = qa.shape
+    N = q.shape[0]
+    t = np.empty((M, N), np.float32)
+    absum = np.empty((M, N), np.float64)
+    assert _load().q8o_gemm_mx(_ptr(qa), _ptr(q), _ptr(sf), M, N, K, G, _ptr(t), _ptr(absum), threads) == OK
+    return t, absum
+
+
+def linear_mx(qa, sa, q, sf, G: int, bias=None, a_per_row: bool = True, threads: int = 1) -> np.ndarray:
+    """Block-scaled layer: y = fl(T * s_a[m]) (+ bias[n])."""
+    qa, q, sf = _c(qa, np.int8), _c(q, np.int8), _c(sf, np.uint32)
+    sa = _c(np.atleast_1d(sa), np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    M, K = qa.shape
+    N = q.shape[0]
+    y = np.empty((M, N), np.float32)
+    assert _load().q8o_linear_mx(_ptr(qa), _ptr(sa), 1 if a_per_row else 0, _ptr(q), _ptr(sf), _ptr(b),
+                                 M, N, K, G, _ptr(y), threads) == OK
+    return y
 
 
 def to_bf16(y: np.ndarray) -> np.ndarray:

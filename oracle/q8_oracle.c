@@ -45,6 +45,13 @@
  *    qmax); its int4 GEMM and dequantize-GEMM examples: two codes per byte,
  *    (a & 0x0F) | ((b & 0x0F) << 4), decoded by shifting left 4 and then right 4
  *    arithmetically to sign-extend).
+ *  - MX-style block-scaled int8 weights (TileLang tutorial ch. 27, low-precision
+ *    quantization, 2.3 MX / block-scaled: block granularity + E8M0): every G
+ *    consecutive K elements of a weight row share one scale 2^(e - 127) stored
+ *    as its biased exponent byte e, amax / qmax rounded up to a power of two;
+ *    four scale bytes per 32-bit word, words laid out group-major (see
+ *    q8o_quantize_weight_mx). The product is accumulated exactly and rounded
+ *    once (q8o_gemm_mx).
  *  - fused RMSNorm + per-token quantization ("Activation Quantization
  *    Architecture", Fusion: the fused norm-and-quantize pseudocode):
  *      rms = sqrt(mean(x * x) + eps), y = x / rms * gamma, then the symmetric
@@ -367,6 +374,121 @@ int q8o_rmsnorm(const float* x, const float* gamma, int64_t rows, int64_t cols, 
         float* yr = y + r * cols;
         for (int64_t k = 0; k < cols; ++k) yr[k] = (xr[k] / rms) * gamma[k];
     }
+    return Q8O_OK;
+}
+
+/*
+ * MX-style block-scaled int8 weights (TileLang tutorial ch. 27, low-precision
+ * quantization, 2.3 MX / block-scaled: block granularity + E8M0).
+ *
+ * Each row n of w[N][K] is cut into groups of G consecutive K elements. A group's
+ * scale is a bare power of two s = 2^(e - 127), stored as the E8M0 byte e: the
+ * pages form it from x = amax / qmax by taking the biased exponent field of x and
+ * adding one when x's 23 mantissa bits are not all zero (x rounded up to a power of
+ * two, so every |w / s| <= qmax). Here qmax = 127 (the int8 rule of 2.4) and the
+ * codes are clamp(rint(w / s), -127, 127); dividing by a power of two is exact.
+ * Reading: e is clamped to [103, 136] (s from 2^-24 to 2^9) where the pages clamp
+ * to [1, 254]; in that range every q * s is an exact fp16 value. A zero group gets
+ * e = 103 and codes 0.
+ * Layout (2.3 (c)): four scale bytes are packed into one 32-bit word, byte b
+ * (bits 8b .. 8b + 7) holding group 4w + b of word w, and the words are stored
+ * group-major: word w of row n at sf[w * N + n]. Bytes past the last group are 0.
+ */
+#define Q8O_MX_EMIN 103
+#define Q8O_MX_EMAX 136
+
+int q8o_e8m0_ceil(float x) {
+    uint32_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    bits &= 0x7FFFFFFFu;
+    const int e = (int)(bits >> 23) + ((bits & 0x7FFFFFu) != 0 ? 1 : 0);
+    return q8o_clampi(e, Q8O_MX_EMIN, Q8O_MX_EMAX);
+}
+
+int q8o_quantize_weight_mx(const float* w, int64_t N, int64_t K, int G, int8_t* q, uint32_t* sf) {
+    if (N < 0 || K < 0 || G <= 0 || K % G != 0) return Q8O_BAD_ARG;
+    const int64_t groups = K / G, words = (groups + 3) / 4;
+    for (int64_t i = 0; i < words * N; ++i) sf[i] = 0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < groups; ++g) {
+            const float* wg = w + n * K + g * G;
+            const float x = q8o_amax(wg, G) / 127.0f;
+            const int e = q8o_e8m0_ceil(x);
+            const float s = ldexpf(1.0f, e - 127);
+            sf[(g / 4) * N + n] |= (uint32_t)e << (8 * (g % 4));
+            for (int64_t k = 0; k < G; ++k)
+                q[n * K + g * G + k] = (int8_t)q8o_clampi((long)rintf(wg[k] / s), -127, 127);
+        }
+    return Q8O_OK;
+}
+
+/* Nearest fp32 to v * 2^-24 (ties to even), for an exact 128-bit integer v. */
+static float q8o_round_i128_unit24(__int128 v) {
+    const int neg = v < 0;
+    unsigned __int128 u = neg ? (unsigned __int128)0 - (unsigned __int128)v : (unsigned __int128)v;
+    int top = 0;
+    while (top < 127 && (u >> (top + 1)) != 0) ++top;
+    int shift = top - 23;
+    if (shift > 0) {
+        const unsigned __int128 rem = u & (((unsigned __int128)1 << shift) - 1);
+        const unsigned __int128 half = (unsigned __int128)1 << (shift - 1);
+        u >>= shift;
+        if (rem > half || (rem == half && (u & 1))) ++u;
+    } else {
+        shift = 0;
+    }
+    const float r = ldexpf((float)(uint32_t)u, shift - 24);   /* u < 2^25: exact */
+    return neg ? -r : r;
+}
+
+/*
+ * T[m][n] = sum_k qa[m][k] * q[n][k] * s[n][k / G] with the scales of
+ * q8o_quantize_weight_mx, formed exactly and rounded once to fp32. Each group's
+ * integer dot product is exact in int64; a group term is that integer times
+ * 2^(e - 103) in units of 2^-24 (e >= 103), summed exactly in a 128-bit integer.
+ * absum[m][n] (optional) receives sum_k |qa * q * s| in double (for error bounds).
+ */
+int q8o_gemm_mx(const int8_t* qa, const int8_t* q, const uint32_t* sf, int64_t M, int64_t N, int64_t K, int G,
+                float* t, double* absum, int threads) {
+    if (M < 0 || N < 0 || K < 0 || G <= 0 || K % G != 0) return Q8O_BAD_ARG;
+    const int64_t groups = K / G;
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            __int128 sum = 0;
+            double abs_acc = 0.0;
+            for (int64_t g = 0; g < groups; ++g) {
+                const int e = (int)((sf[(g / 4) * N + n] >> (8 * (g % 4))) & 0xFFu);
+                if (e < Q8O_MX_EMIN || e > Q8O_MX_EMAX) continue;   /* not produced by the quantizer */
+                int64_t dot = 0, adot = 0;
+                for (int64_t k = g * G; k < (g + 1) * G; ++k) {
+                    const int64_t p = (int64_t)qa[m * K + k] * (int64_t)q[n * K + k];
+                    dot += p;
+                    adot += p < 0 ? -p : p;
+                }
+                sum += (__int128)dot << (e - Q8O_MX_EMIN);
+                abs_acc += ldexp((double)adot, e - 127);
+            }
+            t[m * N + n] = q8o_round_i128_unit24(sum);
+            if (absum) absum[m * N + n] = abs_acc;
+        }
+    return Q8O_OK;
+}
+
+/* y[m][n] = fl(T[m][n] * s_a[m]) (+ bias[n], one fp32 add): the block-scaled layer. */
+int q8o_linear_mx(const int8_t* qa, const float* sa, int a_per_row, const int8_t* q, const uint32_t* sf,
+                  const float* bias, int64_t M, int64_t N, int64_t K, int G, float* y, int threads) {
+    const int st = q8o_gemm_mx(qa, q, sf, M, N, K, G, y, NULL, threads);
+    if (st != Q8O_OK) return st;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            float v = y[m * N + n] * sa[a_per_row ? m : 0];
+            if (bias) v = v + bias[n];
+            y[m * N + n] = v;
+        }
     return Q8O_OK;
 }
 
