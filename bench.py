@@ -274,6 +274,9 @@ def run_ours(args, world, rank, local):
     # ---- W4A8: the same layers with int4 weights
     w4 = None if args.no_decode else measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops)
 
+    # ---- block-scaled (E8M0 per K-group) weights on the same layers
+    mx = None if args.no_decode else measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops)
+
     # ---- the same GEMM with the bias + bf16 epilogue (the pages' output side)
     epi = measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops)
 
@@ -307,6 +310,7 @@ def run_ours(args, world, rank, local):
             "rmsnorm_quantize": rmsq,
             "gemm_bias_bf16": epi,
             "w4a8": w4,
+            "block_scaled": mx,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "weight_prep_ms": round(weight_prep_ms, 3),
@@ -483,6 +487,66 @@ def measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops):
                         "TFLOP/s": round(ops / (pms * 1e-3) / 1e12, 1)}}
 
 
+def measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops):
+    """Block-scaled int8 weights (one E8M0 scale per 32 or 128 K): the prefill GEMM (L2 flushed
+    per launch) for both granularities, and the decode layer (CUDA graph of back-to-back
+    launches; the int8 weights, 235 MB, exceed L2)."""
+    import torch
+    M, K = qa.shape
+    wlh = workloads.WORKLOADS[HEADLINE]
+    wp = torch.from_numpy(workloads.make_weights(wlh)).to(device)
+    out = {}
+    for G in (32, 128):
+        qw, sf = q8.q8_quantize_weight_mx(wp, G)
+        y = torch.empty((M, qw.shape[0]), dtype=torch.float32, device=device)
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y)
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(max(5, args.steps)):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y)
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        mean = statistics.mean(ms)
+        out[f"prefill_g{G}"] = {"workload": f"{HEADLINE}: A [{M},{K}] x W int8 [{qw.shape[0]},{K}], E8M0 per {G} K",
+                                "gemm_ms": round(mean, 4), "TFLOP/s": round(ops / (mean * 1e-3) / 1e12, 1)}
+        del qw, sf, y
+    del wp
+    wl, a_d, w_d = layer_inputs(DECODE, device)
+    Md, Nd, Kd = wl.M, wl.N, wl.K
+    qw, sf = q8.q8_quantize_weight_mx(w_d, 32)
+    del w_d
+    qad, sad, _ = q8.q8_quantize_act(a_d)
+    yd = torch.empty((Md, Nd), dtype=torch.float32, device=device)
+    for _ in range(3):
+        q8.q8_gemm_mx(qad, sad, qw, sf, 32, out=yd)
+    n = max(20, args.steps)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        for _ in range(n):
+            q8.q8_gemm_mx(qad, sad, qw, sf, 32, out=yd)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    dms = e0.elapsed_time(e1) / n
+    dbytes = Nd * Kd + Nd * Kd // 8 + Md * Kd + 4 * Md + 4 * Md * Nd
+    out["decode_g32"] = {"workload": f"{DECODE}: A [{Md},{Kd}] x W int8 [{Nd},{Kd}], E8M0 per 32 K (CTA-pair kernel)",
+                         "gemm_ms": round(dms, 4), "GB/s": round(dbytes / (dms * 1e-3) / 1e9, 1),
+                         "frac_hbm": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 4)}
+    return out
+
+
 def measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops):
     """The headline GEMM with a bias and bf16 output (q8_gemm_epilogue), L2 flushed before each
     launch: the output write halves (2 bytes per element)."""
@@ -622,6 +686,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped workload")
     ap.add_argument("--w4-only", action="store_true",
                     help="only the W4A8 (int4 weight) measurements (one JSON object, for profiling)")
+    ap.add_argument("--mx-only", action="store_true",
+                    help="only the block-scaled weight measurements (one JSON object, for profiling)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode-shaped workload (one JSON object, for profiling)")
     args = ap.parse_args()
@@ -645,6 +711,21 @@ def main():
         qa, s_a, _ = q8.q8_quantize_act(a)
         del a
         print(json.dumps(measure_w4a8(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K)))
+        return
+    if args.mx_only:
+        import torch
+        import int8_quantized_gemm_gb300 as q8
+        from int8_quantized_gemm_gb300 import build
+        build.build()
+        q8.load()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        wl = workloads.WORKLOADS[HEADLINE]
+        a = torch.from_numpy(workloads.make_activations(wl)).to(device)
+        qa, s_a, _ = q8.q8_quantize_act(a)
+        del a
+        print(json.dumps(measure_mx(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K)))
         return
     if args.decode_only:
         import torch

@@ -256,6 +256,51 @@ q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, i
                               int32_t* acc, q8_gemm_kernel kernel, q8_stream_t stream);
 
 /*
+ * Block-scaled (MX-style) int8 weights (TileLang tutorial ch. 27, low-precision
+ * quantization, 2.3 MX / block-scaled: block granularity + E8M0).
+ *
+ * Every `group` consecutive K elements of a weight row share one scale
+ * s = 2^(e - 127), stored as the E8M0 byte e: x = amax / 127 (fp32 division)
+ * rounded up to a power of two (the exponent field of x, plus one when its
+ * mantissa is not zero), e clamped to [103, 136] (s = 2^-24 .. 2^9: every
+ * dequantized q * s is then an exact fp16 value; weights with |w| > 127 * 2^9
+ * saturate at +-127). Codes q = clamp(rint(w / s), -127, 127).
+ *
+ * w     : fp32 [N, K] row-major, 16-byte aligned, finite.
+ * group : 32 (the native MX block) or 128; K % group != 0 -> Q8_ERR_UNSUPPORTED.
+ * qw    : int8 [N, K], written, 16-byte aligned.
+ * sf    : uint32 [ceil(K / group / 4), N], written, 4-byte aligned: four scale
+ *         bytes per word, byte b (bits 8b .. 8b + 7) of word w holding group
+ *         4w + b, words group-major (word w of row n at sf[w * N + n]); bytes
+ *         past the last group are 0.
+ * Errors: Q8_ERR_INVALID_ARG (negative sizes, group not 32 / 128, null or
+ * misaligned pointers), Q8_ERR_CUDA.
+ */
+q8_status q8_quantize_weight_mx(const float* w, int64_t N, int64_t K, int group, int8_t* qw,
+                                uint32_t* sf, q8_stream_t stream);
+
+/*
+ * The layer with block-scaled weights and symmetric int8 activations:
+ *   T[m][n] = sum_k qa[m][k] * (qw[n][k] * s[n][k / group]),
+ *   y[m][n] = fl(T[m][n] * s_a[m]) (+ bias[n]), then the output type.
+ * The weights are dequantized to fp16 before the product (exact), T is summed
+ * by the tensor core in fp32 over the whole K: not bit-reproducible against an
+ * exactly rounded sum, its error bounded by the fp32 accumulation (the products
+ * are exact). Runs on the CTA-pair kernel for every M.
+ *
+ * qa, s_a, ga : as q8_gemm_dequant_ex (symmetric activations only).
+ * qw, sf      : from q8_quantize_weight_mx with the same group.
+ * bias, out_type, out, out_scale : as q8_gemm_epilogue_ex.
+ * kernel      : Q8_GEMM_AUTO or Q8_GEMM_TCGEN05_PAIR; others -> Q8_ERR_UNSUPPORTED.
+ * Errors: as q8_gemm_epilogue_ex; group not 32 / 128 -> Q8_ERR_INVALID_ARG;
+ * K % group != 0 -> Q8_ERR_UNSUPPORTED.
+ */
+q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, const int8_t* qw,
+                        const uint32_t* sf, int group, const float* bias, int64_t M, int64_t N,
+                        int64_t K, q8_out_type out_type, void* out, float out_scale,
+                        q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
  * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),
  * computed by the same main loop as q8_gemm_dequant_ex with the same kernel
  * choice. Used to check the integer GEMM bit for bit.

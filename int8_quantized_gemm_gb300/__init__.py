@@ -12,6 +12,7 @@ CPU fallback; if the library is missing or a call fails, an exception says so.
   q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum, bias, out_dtype, out_scale) -> y (+bias; fp32/bf16/int8)
   q8_gemm_s32(qa, qw)                                 -> acc (raw INT32 accumulators)
   q8_quantize_weight_int4(w) -> qw4, s_w;  q8_colsum_int4(qw4, K);  q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, ...)
+  q8_quantize_weight_mx(w, group) -> qw, sf;  q8_gemm_mx(qa, s_a, qw, sf, group, ...)   (block-scaled weights)
   q8_linear(a, qw, s_w, colsum)                       -> y   (quantize A, then GEMM)
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -67,6 +68,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_colsum_int4.argtypes = [p, i64, i64, p, p]
     lib.q8_gemm_w4a8_ex.argtypes = [p, p, p, i32, p, p, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_w4a8_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
+    lib.q8_quantize_weight_mx.argtypes = [p, i64, i64, i32, p, p, p]
+    lib.q8_gemm_mx_ex.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_pick.argtypes = [i64, i64, i64]
     lib.q8_status_string.argtypes = [i32]
     lib.q8_status_string.restype = ctypes.c_char_p
@@ -75,7 +78,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_launch_count.restype = ctypes.c_uint64
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
-                 "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_gemm_pick", "q8_device_error"):
+                 "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
+                 "q8_gemm_pick", "q8_device_error"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -340,3 +344,44 @@ def q8_device_error() -> int:
     if st not in (Q8_OK, Q8_ERR_TIMEOUT):
         _check(st, "q8_device_error")
     return int(code.value)
+
+
+def q8_quantize_weight_mx(w: torch.Tensor, group: int = 32, qw=None, sf=None, stream=None):
+    """Block-scaled int8 codes of fp32 W[N, K]: (qw int8 [N, K], sf [ceil(K / group / 4), N] E8M0 scale
+    words, held as int32 bit patterns: byte b of word w is group 4w + b)."""
+    _need(w, torch.float32, "w", 2)
+    N, K = w.shape
+    words = (K // group + 3) // 4
+    qw = torch.empty((N, K), dtype=torch.int8, device=w.device) if qw is None else qw
+    sf = torch.empty((words, N), dtype=torch.int32, device=w.device) if sf is None else sf
+    _check(load().q8_quantize_weight_mx(_ptr(w), N, K, group, _ptr(qw), _ptr(sf), _stream(stream)),
+           "q8_quantize_weight_mx")
+    return qw, sf
+
+
+def q8_gemm_mx(qa, s_a, qw, sf, group: int = 32, bias=None, out_dtype=torch.float32, out_scale=None, out=None,
+               kernel: str = "auto", stream=None):
+    """Linear layer with block-scaled int8 weights: y = fl(T * s_a) (+ bias), T = sum_k qa * q * s."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw, torch.int8, "qw", 2)
+    _need(sf, torch.int32, "sf", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K or sf.shape[1] != N:
+        raise ValueError("qw must be [N, K] and sf [words, N]")
+    if out_dtype not in OUT_TYPES:
+        raise TypeError("out_dtype must be torch.float32, torch.bfloat16 or torch.int8")
+    _need(s_a, torch.float32, "s_a", 1)
+    if s_a.numel() not in (1, M):
+        raise ValueError("s_a must have 1 or M entries")
+    ga = Q8_PER_ROW if (s_a.numel() == M and M != 1) else Q8_PER_TENSOR
+    if bias is not None:
+        _need(bias, torch.float32, "bias", 1)
+    if out_dtype == torch.int8 and out_scale is None:
+        raise ValueError("int8 output needs out_scale")
+    out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    _need(out, out_dtype, "out", 2)
+    _check(load().q8_gemm_mx_ex(_ptr(qa), _ptr(s_a), ga, _ptr(qw), _ptr(sf), group, _ptr(bias), M, N, K,
+                                OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0), KERNELS[kernel],
+                                _stream(stream)), "q8_gemm_mx")
+    return out

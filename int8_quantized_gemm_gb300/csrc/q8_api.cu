@@ -58,10 +58,17 @@ struct Variant {
     float out_scale;
 };
 
+// Block-scaled weights of q8_gemm_mx_ex: E8M0 scale words and the group size.
+struct MxWeights {
+    const uint32_t* sf;
+    int group;
+};
+
 q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
-                      q8_stream_t stream, const Variant* var = nullptr, bool w4 = false) {
+                      q8_stream_t stream, const Variant* var = nullptr, bool w4 = false,
+                      const MxWeights* mx = nullptr) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -74,6 +81,12 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         if (kst != Q8_OK) return kst;
         if (w4 && K % 32 != 0) return Q8_ERR_UNSUPPORTED;   // packed int4 rows: whole 16-byte multiples
     }
+    if (mx) {
+        if (mx->group != 32 && mx->group != 128) return Q8_ERR_INVALID_ARG;
+        if (z_a || !epilogue) return Q8_ERR_UNSUPPORTED;     // symmetric activations, dequantized output
+        if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05_PAIR) return Q8_ERR_UNSUPPORTED;
+        if (K % mx->group != 0) return Q8_ERR_UNSUPPORTED;
+    }
     if (M == 0 || N == 0) return Q8_OK;   // empty output: nothing is read or written
     if (var) {
         if (var->out_type != Q8_OUT_F32 && var->out_type != Q8_OUT_BF16 && var->out_type != Q8_OUT_I8)
@@ -85,14 +98,15 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         y = var->out_type == Q8_OUT_F32 ? static_cast<float*>(var->out) : nullptr;
     }
     if (epilogue) {
-        if (!s_a || !s_w || (!y && !var)) return Q8_ERR_INVALID_ARG;
-        if (!aligned(s_a, 4) || !aligned(s_w, 4) || (y && !aligned(y, 16))) return Q8_ERR_INVALID_ARG;
+        if (!s_a || (!s_w && !mx) || (!y && !var)) return Q8_ERR_INVALID_ARG;
+        if (!aligned(s_a, 4) || (s_w && !aligned(s_w, 4)) || (y && !aligned(y, 16))) return Q8_ERR_INVALID_ARG;
         if (z_a && (!colsum || !aligned(z_a, 4) || !aligned(colsum, 4))) return Q8_ERR_INVALID_ARG;
     } else if (!aligned(out_i32, 16)) {
         return Q8_ERR_INVALID_ARG;
     }
     if (M > 0 && N > 0 && K > 0) {
         if (!qa || !qw || !aligned(qa, 16) || !aligned(qw, 16)) return Q8_ERR_INVALID_ARG;
+        if (mx && (!mx->sf || !aligned(mx->sf, 4))) return Q8_ERR_INVALID_ARG;
     }
     if (M > INT32_MAX || N > INT32_MAX) return Q8_ERR_UNSUPPORTED;
 
@@ -111,6 +125,14 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         const size_t bytes = (size_t)M * (size_t)N * 4;
         return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
     }
+    if (mx) {
+        // block-scaled weights run on the CTA-pair kernel at every M
+        if (!q8::gemm_tc2_supports(M, N, K, q8::kWMx)) return Q8_ERR_UNSUPPORTED;
+        ep.s_w = nullptr;
+        ep.mx_sf = mx->sf;
+        ep.mx_group = mx->group;
+        return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWMx));
+    }
     if (w4) {
         // int4 weights run on the decode kernel (M <= 16) and the CTA-pair kernel
         if (kernel == Q8_GEMM_AUTO) kernel = q8::gemv_mma_supports(M, N, K, true) ? Q8_GEMM_DECODE : Q8_GEMM_TCGEN05_PAIR;
@@ -120,7 +142,7 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         }
         if (kernel == Q8_GEMM_TCGEN05_PAIR) {
             if (!q8::gemm_tc2_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, true));
+            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWInt4));
         }
         return Q8_ERR_UNSUPPORTED;
     }
@@ -246,6 +268,24 @@ q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, i
                               q8_gemm_kernel kernel, q8_stream_t stream) {
     return gemm_common(qa, nullptr, nullptr, Q8_PER_ROW, reinterpret_cast<const int8_t*>(qw4), nullptr, Q8_PER_ROW,
                        nullptr, M, N, K, nullptr, acc, kernel, stream, nullptr, true);
+}
+
+q8_status q8_quantize_weight_mx(const float* w, int64_t N, int64_t K, int group, int8_t* qw, uint32_t* sf,
+                                q8_stream_t stream) {
+    if (N < 0 || K < 0 || (group != 32 && group != 128)) return Q8_ERR_INVALID_ARG;
+    if (K % group != 0) return Q8_ERR_UNSUPPORTED;
+    if (N == 0 || K == 0) return Q8_OK;
+    if (!w || !qw || !sf || !aligned(w, 16) || !aligned(qw, 16) || !aligned(sf, 4)) return Q8_ERR_INVALID_ARG;
+    return from_cuda(q8::launch_quantize_weight_mx(w, N, K, group, qw, sf, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, const int8_t* qw, const uint32_t* sf,
+                        int group, const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type,
+                        void* out, float out_scale, q8_gemm_kernel kernel, q8_stream_t stream) {
+    const Variant var{bias, out_type, out, out_scale};
+    const MxWeights mx{sf, group};
+    return gemm_common(qa, s_a, nullptr, ga, qw, nullptr, Q8_PER_ROW, nullptr, M, N, K, nullptr, nullptr, kernel,
+                       stream, &var, false, &mx);
 }
 
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,

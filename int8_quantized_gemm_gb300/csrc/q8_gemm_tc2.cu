@@ -27,6 +27,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cuda_fp16.h>
+
 #include <type_traits>
 
 #include "q8_internal.h"
@@ -48,6 +50,27 @@ __device__ __forceinline__ uint32_t pack_codes4(uint4 v, float s) {
         return (uint32_t)(min(max(__float2int_rn(__fdiv_rn(__uint_as_float(b), s)), -127), 127) & 0xFF);
     };
     return code(v.x) | (code(v.y) << 8) | (code(v.z) << 16) | (code(v.w) << 24);
+}
+
+// The E8M0 scale byte e as the fp16 power of two 2^(e - 127) in both halves (exact for
+// e = 103 .. 142; e = 0 gives 0).
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(e << 23), __uint_as_float(e << 23));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// cvt_word with each code times the power of two s (h = s in both halves, c = -1152 s):
+// 0x6480 | (byte ^ 0x80) is the fp16 1152 + q, and fma(1152 + q, s, -1152 s) = q s.
+__device__ __forceinline__ void cvt_word_scaled(uint32_t w, uint32_t h, uint32_t c, uint32_t& lo, uint32_t& hi) {
+    const uint32_t l = (w & 0x00FF00FFu) ^ 0x64806480u, u = ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(lo) : "r"(l), "r"(h), "r"(c));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(u), "r"(h), "r"(c));
 }
 
 namespace {
@@ -73,15 +96,19 @@ constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 128-byte output
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 constexpr uint16_t kPairMask = 0x3;
 
-// Weight format: int8 codes (staged as 128 rows x 64 bytes per CTA) or int4 codes packed
-// two per byte (128 rows x 32 bytes). An fp32 TMEM chunk holds 2^24 / max|product| products
-// exactly: 1024 K for int8 x int8 (|p| <= 2^14), 16384 K for int8 x int4 (|p| <= 2^10).
-template <bool W4>
+// Weight formats (WF): int8 codes (staged as 128 rows x 64 bytes per CTA), int4 codes packed
+// two per byte (128 rows x 32 bytes), or block-scaled int8 codes (kWMx: as int8, plus one E8M0
+// scale per row and group of G K elements). An exact fp32 TMEM chunk holds 2^24 / max|product|
+// products: 1024 K for int8 x int8 (|p| <= 2^14), 16384 K for int8 x int4 (|p| <= 2^10).
+// Block-scaled weights enter the MMA as the fp16 values q * s (exact: s = 2^-24 .. 2^9), so the
+// products are no longer integers and TMEM accumulates the whole K in fp32 (one chunk).
+template <int WF>
 struct PairCfg {
+    static constexpr bool W4 = WF == kWInt4;
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
     static constexpr int kStage8 = kA8 + kB8;                 // 16 KB (int8) or 12 KB (int4)
     static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
-    static constexpr int KB_PER_CHUNK = W4 ? 256 : 16;
+    static constexpr int KB_PER_CHUNK = W4 ? 256 : WF == kWMx ? (1 << 30) : 16;
     static constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
     static constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
     static constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
@@ -103,11 +130,12 @@ __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, 
     n0 = (within / rows) * BN;
 }
 
-template <bool W4>
+template <int WF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, Epilogue ep) {
-    using C = PairCfg<W4>;
+    using C = PairCfg<WF>;
+    constexpr bool W4 = WF == kWInt4, MX = WF == kWMx;
     constexpr int S8 = C::S8, kB8 = C::kB8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
     constexpr int kOffEpi = C::kOffEpi, kOffBar = C::kOffBar;
     extern __shared__ uint8_t smem_raw[];
@@ -240,7 +268,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t src0 = (uint32_t)(ct * 16);
             const uint32_t dst0 = sw128(r0, 2 * c0);
             const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
+            // Block-scaled weights: the thread's weight chunks are j = 2..5 with 512 <= idx < 1024
+            // (weight row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage): j = 3, 4 and
+            // one of j = 2 (ct >= 128) or j = 5 (ct < 64), kept in slot (j - 2) % 3. Their scale
+            // words are read from global memory (L2) one stage ahead of use.
+            uint32_t sfw_cur[3] = {0u, 0u, 0u}, sfw_nxt[3] = {0u, 0u, 0u};
+            int sh_cur = 0, sh_nxt = 0, pf_i = 0, pf_kb = 0;
+            int sf_n[3] = {0, 0, 0};             // weight rows of the slots in the prefetched stage's tile
+            bool sf_ok[3] = {false, false, false};
+            const int gshift = ep.mx_group == 32 ? 5 : 7;
+            auto sf_fetch = [&]() {
+                if constexpr (MX) {
+                    if (pf_kb == 0) {   // a new tile: its weight rows
+                        int pm0, pn0;
+                        pair_coords(tg, cluster + pf_i * nclusters, pm0, pn0);
+#pragma unroll
+                        for (int jw = 0; jw < 3; ++jw) {
+                            const int j = (jw == 0 && ct < 64) ? 5 : jw + 2;
+                            const int idx = ct + kConv * j;
+                            sf_n[jw] = pn0 + (int)rank * BNH + ((idx - 512) >> 2);
+                            sf_ok[jw] = idx >= 512 && idx < 1024 && sf_n[jw] < N;
+                        }
+                    }
+                    const int grp = (pf_kb * BK + 16 * c0) >> gshift;
+                    const uint32_t* base = ep.mx_sf + (int64_t)(grp >> 2) * N;
+                    sh_nxt = 8 * (grp & 3);
+#pragma unroll
+                    for (int jw = 0; jw < 3; ++jw) sfw_nxt[jw] = sf_ok[jw] ? __ldg(base + sf_n[jw]) : 0u;
+                    if (++pf_kb == KB) { pf_kb = 0; ++pf_i; }
+                }
+            };
+            if (MX && total_g > 0) sf_fetch();
             for (int g = 0; g < total_g; ++g) {
+                if constexpr (MX) {
+#pragma unroll
+                    for (int jw = 0; jw < 3; ++jw) sfw_cur[jw] = sfw_nxt[jw];
+                    sh_cur = sh_nxt;
+                    if (g + 1 < total_g) sf_fetch();
+                }
                 const int s8 = g % S8, s16 = g % S16;
                 if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
                     break;
@@ -257,10 +322,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 6; ++j) {
                     if (ct + kConv * j < 1024) {
                         uint4 o0, o1;
-                        cvt_word(in[j].x, o0.x, o0.y);
-                        cvt_word(in[j].y, o0.z, o0.w);
-                        cvt_word(in[j].z, o1.x, o1.y);
-                        cvt_word(in[j].w, o1.z, o1.w);
+                        bool scaled = false;
+                        if constexpr (MX) {
+                            if (j >= 2 && ct + kConv * j >= 512) {   // a weight chunk: q * s
+                                const uint32_t e = (sfw_cur[(j - 2) % 3] >> sh_cur) & 0xFFu;
+                                const uint32_t h = scale_f16x2(e);
+                                if (e <= 132u) {
+                                    // (1152 + q) * s - 1152 * s in one fp16 FMA: exact, as q * s and
+                                    // -1152 * s (s <= 32) are fp16 values and the FMA rounds once
+                                    const uint32_t c = hmul2(h, 0xE480E480u);
+                                    cvt_word_scaled(in[j].x, h, c, o0.x, o0.y);
+                                    cvt_word_scaled(in[j].y, h, c, o0.z, o0.w);
+                                    cvt_word_scaled(in[j].z, h, c, o1.x, o1.y);
+                                    cvt_word_scaled(in[j].w, h, c, o1.z, o1.w);
+                                } else {
+                                    cvt_word(in[j].x, o0.x, o0.y);
+                                    cvt_word(in[j].y, o0.z, o0.w);
+                                    cvt_word(in[j].z, o1.x, o1.y);
+                                    cvt_word(in[j].w, o1.z, o1.w);
+                                    o0 = make_uint4(hmul2(o0.x, h), hmul2(o0.y, h), hmul2(o0.z, h), hmul2(o0.w, h));
+                                    o1 = make_uint4(hmul2(o1.x, h), hmul2(o1.y, h), hmul2(o1.z, h), hmul2(o1.w, h));
+                                }
+                                scaled = true;
+                            }
+                        }
+                        if (!scaled) {
+                            cvt_word(in[j].x, o0.x, o0.y);
+                            cvt_word(in[j].y, o0.z, o0.w);
+                            cvt_word(in[j].z, o1.x, o1.y);
+                            cvt_word(in[j].w, o1.z, o1.w);
+                        }
                         sts128(st16 + dst0 + 6144 * j, o0);
                         sts128(st16 + dst1 + 6144 * j, o1);
                     }
@@ -362,8 +453,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t v[32];
                 tmem_ld32(taddr + j * 32, v);
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    acc[j * 32 + e] = acc[j * 32 + e] * keep + __float2int_rn(__uint_as_float(v[e]));
+                for (int e = 0; e < 32; ++e) {
+                    if constexpr (MX)
+                        acc[j * 32 + e] = (int)v[e];   // fp32 sums (bit patterns), one chunk per tile
+                    else
+                        acc[j * 32 + e] = acc[j * 32 + e] * keep + __float2int_rn(__uint_as_float(v[e]));
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -386,6 +481,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // outputs (m, n .. n + 3) of accumulator columns e .. e + 3, as 4-byte words
             auto out4 = [&](int e, int n) -> uint4 {
                 if (ep.out_i32) return make_uint4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                if constexpr (MX) {   // y = fl(T * s_a) (+ bias)
+                    uint32_t o[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float v = __fmul_rn(__uint_as_float((uint32_t)acc[e + q]), sa);
+                        if (ep.bias) v = __fadd_rn(v, __ldg(ep.bias + (n + q < N ? n + q : 0)));
+                        o[q] = __float_as_uint(v);
+                    }
+                    return make_uint4(o[0], o[1], o[2], o[3]);
+                }
                 const bool full = n + 3 < N;
                 float sw4[4];
                 int cs4[4] = {0, 0, 0, 0};
@@ -508,8 +613,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, bool w4) {
-    if (!(M >= 1 && N >= 1 && K >= 16 && (K % (w4 ? 32 : 16)) == 0 && M < (1LL << 31) && N < (1LL << 31)))
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, int wfmt) {
+    if (!(M >= 1 && N >= 1 && K >= 16 && (K % (wfmt == kWInt4 ? 32 : 16)) == 0 && M < (1LL << 31) && N < (1LL << 31)))
         return false;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t kb = (K + BK - 1) / BK;
@@ -519,7 +624,7 @@ bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, bool w4) {
 // Clusters of two that fit on the device at once (a GPC with an odd number of
 // free SMs leaves one idle), so that the persistent grid runs in one wave.
 // Cached per device and weight format; SMs / 2 if the occupancy query fails.
-template <bool W4>
+template <int WF>
 static int resident_pairs() {
     static int cached[64] = {0};
     int dev = 0;
@@ -529,27 +634,28 @@ static int resident_pairs() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg<W4>::kSmem;
+    cfg.dynamicSmemBytes = PairCfg<WF>::kSmem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<W4>, &cfg) == cudaSuccess && n > 0 && n < pairs) pairs = n;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<WF>, &cfg) == cudaSuccess && n > 0 && n < pairs) pairs = n;
     (void)cudaGetLastError();
     cached[dev] = pairs;
     return pairs;
 }
 
-template <bool W4>
+template <int WF>
 static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
                                      const Epilogue& ep, cudaStream_t stream) {
-    using C = PairCfg<W4>;
+    using C = PairCfg<WF>;
+    constexpr bool W4 = C::W4;
     CUtensorMap ma, mw;
     // int4: the packed weights are a byte matrix [N, K / 2], staged 32 bytes (64 K) per k-block
     if (!make_tma_map_i8(&ma, qa, M, K, BMH, BK) ||
         !make_tma_map_i8(&mw, static_cast<const int8_t*>(qw), N, W4 ? K / 2 : K, BNH, W4 ? BK / 2 : BK))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<W4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int64_t pairs = resident_pairs<W4>();
+    const int64_t pairs = resident_pairs<WF>();
     const int clusters = (int)(tiles < pairs ? tiles : pairs);
     CUtensorMap mo;
     const bool tma_out = ep.out_i32                  ? make_tma_map_out(&mo, ep.out_i32, kMapI32, M, N)
@@ -557,17 +663,22 @@ static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M
                          : ep.out_kind == kOutBF16 ? make_tma_map_out(&mo, ep.out_bf16, kMapBF16, M, N)
                                                    : make_tma_map_out(&mo, ep.out_i8, kMapI8, M, N);
     if (!tma_out) memset(&mo, 0, sizeof(mo));
-    gemm_tc2_kernel<W4><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N,
+    gemm_tc2_kernel<WF><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N,
                                                                       (int)K, ep);
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
-                            cudaStream_t stream, bool w4) {
-    if (!gemm_tc2_supports(M, N, K, w4)) return cudaErrorNotSupported;
-    return w4 ? launch_gemm_tc2_t<true>(qa, qw, M, N, K, ep, stream)
-              : launch_gemm_tc2_t<false>(qa, qw, M, N, K, ep, stream);
+                            cudaStream_t stream, int wfmt) {
+    if (!gemm_tc2_supports(M, N, K, wfmt)) return cudaErrorNotSupported;
+    if (wfmt == kWMx) {
+        if (!ep.mx_sf || (ep.mx_group != 32 && ep.mx_group != 128) || K % ep.mx_group != 0 || ep.out_i32 || ep.z_a)
+            return cudaErrorInvalidValue;
+        return launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream);
+    }
+    return wfmt == kWInt4 ? launch_gemm_tc2_t<kWInt4>(qa, qw, M, N, K, ep, stream)
+                          : launch_gemm_tc2_t<kWInt8>(qa, qw, M, N, K, ep, stream);
 }
 
 cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code) {

@@ -31,6 +31,14 @@ cudaError_t launch_quantize_int4(const float* w, int64_t rows, int64_t cols, uin
                                  cudaStream_t stream);
 cudaError_t launch_colsum_int4(const uint8_t* q, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream);
 
+// Block-scaled int8 weights: one E8M0 scale per (row, group of G K elements), amax / 127
+// rounded up to a power of two with the exponent clamped to [103, 136]; codes
+// clamp(rint(w / s), -127, 127); scale bytes packed four per 32-bit word (byte g % 4 of word
+// g / 4), words group-major (word w of row n at sf[w * N + n]). K % G == 0.
+constexpr int kMxEmin = 103, kMxEmax = 136;
+cudaError_t launch_quantize_weight_mx(const float* w, int64_t N, int64_t K, int G, int8_t* q, uint32_t* sf,
+                                      cudaStream_t stream);
+
 // Fused RMSNorm + per-token symmetric quantization of x[rows, cols] (cols % 4 == 0).
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps,
                                    int8_t* q, float* s, cudaStream_t stream);
@@ -57,6 +65,10 @@ struct Epilogue {
     uint16_t* out_bf16 = nullptr;
     int8_t* out_i8 = nullptr;
     float out_scale = 1.0f;
+    // Block-scaled weights (CTA-pair kernel): E8M0 scale words and group size; the kernel then
+    // accumulates sum_k qa * (q * s) in fp32 and the epilogue is y = fl(T * s_a) (+ bias).
+    const uint32_t* mx_sf = nullptr;
+    int mx_group = 0;
 };
 
 #ifdef __CUDACC__
@@ -86,10 +98,13 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream);
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
 
+// Weight formats of the CTA-pair kernel: int8 codes, packed int4 codes, block-scaled int8.
+enum WeightFormat : int { kWInt8 = 0, kWInt4 = 1, kWMx = 2 };
+
 // tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles).
 cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
-                            cudaStream_t stream, bool w4 = false);
-bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, bool w4 = false);
+                            cudaStream_t stream, int wfmt = kWInt8);
+bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, int wfmt = kWInt8);
 
 // tcgen05 kernel for M <= 16 (decode): weight rows on the MMA's M side.
 cudaError_t launch_gemv_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,

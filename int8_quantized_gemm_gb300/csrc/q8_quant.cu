@@ -492,6 +492,38 @@ __global__ void __launch_bounds__(256) colsum_int4_kernel(const uint8_t* __restr
     if (lane == 0) colsum[n] = acc;
 }
 
+// Block-scaled int8 weights, one warp per (row, group of G K elements). The scale is
+// x = amax / 127 rounded up to a power of two as an E8M0 byte: the exponent field of x, plus
+// one when its mantissa is not zero, clamped to [kMxEmin, kMxEmax] (2^-24 .. 2^9, where every
+// q * s is exact in fp16); s = 2^(e - 127); codes clamp(rint(w / s), -127, 127) with an IEEE
+// division (exact for a power of two). Lane 0 writes the scale byte: byte g % 4 of word g / 4
+// of the row, words group-major (word w of row n at index w * N + n); the last group of a row
+// also zeroes the bytes after it in its word.
+__global__ void __launch_bounds__(256) quantize_weight_mx_kernel(const float* __restrict__ w, int64_t N, int64_t K,
+                                                                 int G, int8_t* __restrict__ q,
+                                                                 uint8_t* __restrict__ sf_bytes) {
+    const int64_t groups = K / G;
+    const int64_t item = blockIdx.x * (int64_t)(blockDim.x / kWarp) + threadIdx.x / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    if (item >= N * groups) return;
+    const int64_t n = item / groups, g = item - n * groups;
+    const float* wg = w + n * K + g * G;
+    uint32_t amax_bits = 0;
+    for (int k = lane; k < G; k += kWarp) amax_bits = max(amax_bits, __float_as_uint(fabsf(wg[k])));
+    amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
+    const uint32_t xb = __float_as_uint(__fdiv_rn(__uint_as_float(amax_bits), 127.0f));
+    const int e = min(max((int)(xb >> 23) + ((xb & 0x7FFFFFu) != 0 ? 1 : 0), kMxEmin), kMxEmax);
+    const float s = __uint_as_float((uint32_t)e << 23);
+    int8_t* qg = q + n * K + g * G;
+    for (int k = lane; k < G; k += kWarp) qg[k] = (int8_t)min(max(__float2int_rn(__fdiv_rn(wg[k], s)), -127), 127);
+    if (lane == 0) {
+        uint8_t* word = sf_bytes + ((g / 4) * N + n) * 4;
+        word[g % 4] = (uint8_t)e;
+        if (g == groups - 1)
+            for (int b = (int)(g % 4) + 1; b < 4; ++b) word[b] = 0;
+    }
+}
+
 int num_sms() {
     static int sms = 0;
     if (sms == 0) {
@@ -629,6 +661,19 @@ cudaError_t launch_colsum_int4(const uint8_t* q, int64_t N, int64_t K, int32_t* 
     const int warps_per_block = 8;
     const int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
     colsum_int4_kernel<<<(unsigned)blocks, warps_per_block * kWarp, 0, stream>>>(q, N, K, colsum);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weight_mx(const float* w, int64_t N, int64_t K, int G, int8_t* q, uint32_t* sf,
+                                      cudaStream_t stream) {
+    if (N == 0 || K == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const int64_t items = N * (K / G);
+    const int64_t blocks = (items + warps_per_block - 1) / warps_per_block;
+    if (blocks >= (1LL << 31)) return cudaErrorNotSupported;
+    quantize_weight_mx_kernel<<<(unsigned)blocks, warps_per_block * kWarp, 0, stream>>>(
+        w, N, K, G, q, reinterpret_cast<uint8_t*>(sf));
     note_launch();
     return cudaGetLastError();
 }

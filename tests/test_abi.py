@@ -103,6 +103,34 @@ def test_epilogue_variant_rejects_bad_arguments(lib):
     assert f(K=24) == q8.Q8_ERR_UNSUPPORTED
 
 
+def test_block_scaled_entries_reject_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+
+    def g(group=32, K=64, kernel=0, sf=FAKE, sa=FAKE, out=FAKE, M=8, N=8):
+        return lib.q8_gemm_mx_ex(FAKE, sa, 1, FAKE, sf, group, None, M, N, K, 0, out, ctypes.c_float(0.0),
+                                 kernel, None)
+    assert g(group=64) == q8.Q8_ERR_INVALID_ARG                   # the granularity is 32 or 128
+    assert g(group=0) == q8.Q8_ERR_INVALID_ARG
+    assert g(K=48) == q8.Q8_ERR_UNSUPPORTED                       # K % group
+    assert g(group=128, K=192) == q8.Q8_ERR_UNSUPPORTED
+    assert g(kernel=q8.KERNELS["decode"]) == q8.Q8_ERR_UNSUPPORTED
+    assert g(sf=None) == q8.Q8_ERR_INVALID_ARG
+    assert g(sf=P(0x10002)) == q8.Q8_ERR_INVALID_ARG
+    assert g(sa=None) == q8.Q8_ERR_INVALID_ARG
+    assert g(out=None) == q8.Q8_ERR_INVALID_ARG
+    before = lib.q8_launch_count()
+    assert g(M=0) == q8.Q8_OK and g(N=0) == q8.Q8_OK
+    assert lib.q8_launch_count() == before
+    w = lambda N, K, group, qw=FAKE, sf=FAKE: lib.q8_quantize_weight_mx(FAKE, N, K, group, qw, sf, None)
+    assert w(4, 64, 16) == q8.Q8_ERR_INVALID_ARG
+    assert w(4, 96, 64) == q8.Q8_ERR_INVALID_ARG
+    assert w(4, 160, 128) == q8.Q8_ERR_UNSUPPORTED
+    assert w(4, 64, 32, sf=None) == q8.Q8_ERR_INVALID_ARG
+    assert w(4, 64, 32, qw=MISALIGNED) == q8.Q8_ERR_INVALID_ARG
+    assert w(-1, 64, 32) == q8.Q8_ERR_INVALID_ARG
+    assert w(0, 64, 32) == q8.Q8_OK
+
+
 def test_k_limits_are_the_int32_bounds():
     # 128*128*K < 2^31 for raw codes; 255*128*K < 2^31 with a zero point.
     assert 128 * 128 * 131056 < 2 ** 31 <= 128 * 128 * (131056 + 16)
