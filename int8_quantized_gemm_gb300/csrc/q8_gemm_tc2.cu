@@ -83,10 +83,8 @@ constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per
 constexpr int BNH = 128;
 constexpr int BK = 64;
 constexpr int S16 = 4;              // fp16 operand stages (32 KB)
-constexpr int kConv = 192;          // converter threads, warps 2..7 of each CTA
-constexpr int kDrainWarps = 8;      // warps 8..15 of each CTA
+constexpr int kConv = 192;          // converter threads of the int8 / int4 formats: warps 2..7
 constexpr int kThreads = 512;
-constexpr int kRegsLow = 72, kRegsHigh = 184;
 constexpr int kTmemCols = 512;      // two 128 x 256 fp32 accumulator buffers per CTA
 
 constexpr int kA8 = BMH * BK;                                                     // 8 KB int8 A staging
@@ -102,9 +100,23 @@ constexpr uint16_t kPairMask = 0x3;
 // products: 1024 K for int8 x int8 (|p| <= 2^14), 16384 K for int8 x int4 (|p| <= 2^10).
 // Block-scaled weights enter the MMA as the fp16 values q * s (exact: s = 2^-24 .. 2^9), so the
 // products are no longer integers and TMEM accumulates the whole K in fp32 (one chunk).
+// Warp roles: warp 0 TMA, warp 1 MMA (even CTA) or relay (odd CTA), then kConvWarps converter
+// warps, then kDrainWarps drain warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..).
+// The int8 and int4 formats drain every exact chunk and take 6 converters and 8 drains; the
+// block-scaled format drains once per tile and takes 10 converters and 4 drains (each drain warp
+// then reads its 256 accumulator columns in two halves). Registers: the producer-side warps
+// shrink to kRegsLow, the drain warps grow to kRegsHigh; (2 + kConvWarps) * 32 * kRegsLow +
+// kDrainWarps * 32 * kRegsHigh <= 512 * 128, the registers the block is launched with.
 template <int WF>
 struct PairCfg {
     static constexpr bool W4 = WF == kWInt4;
+    static constexpr int kConvWarps = WF == kWMx ? 10 : 6;
+    static constexpr int kDrainWarps = 16 - 2 - kConvWarps;
+    static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
+    static constexpr int kRegsLow = WF == kWMx ? 88 : 72, kRegsHigh = 184;
+    static_assert((2 + kConvWarps) * 32 * kRegsLow + kDrainWarps * 32 * kRegsHigh <= kThreads * 128,
+                  "register split above the launch's registers");
+    static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
     static constexpr int kStage8 = kA8 + kB8;                 // 16 KB (int8) or 12 KB (int4)
     static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
@@ -136,8 +148,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, Epilogue ep) {
     using C = PairCfg<WF>;
     constexpr bool W4 = WF == kWInt4, MX = WF == kWMx;
-    constexpr int S8 = C::S8, kB8 = C::kB8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
+    constexpr int S8 = C::S8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
     constexpr int kOffEpi = C::kOffEpi, kOffBar = C::kOffBar;
+    constexpr int kConvWarps = C::kConvWarps, kDrainWarps = C::kDrainWarps;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -159,12 +172,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S8; ++s) {
             mbar_init(bar_full8 + 8 * s, 1);
-            mbar_init(bar_empty8 + 8 * s, kConv / 32);
+            mbar_init(bar_empty8 + 8 * s, kConvWarps);
         }
         for (int s = 0; s < S16; ++s) {
-            mbar_init(bar_full16 + 8 * s, kConv / 32 + 1);
+            mbar_init(bar_full16 + 8 * s, (kConvWarps) + 1);
             mbar_init(bar_empty16 + 8 * s, 1);
-            mbar_init(bar_conv16 + 8 * s, kConv / 32);
+            mbar_init(bar_conv16 + 8 * s, kConvWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
@@ -191,8 +204,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int my_tiles = cluster < tg.tiles ? (tg.tiles - 1 - cluster) / nclusters + 1 : 0;
     const int total_g = my_tiles * KB;
 
-    if (warp < 8) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
+    if (warp < 2 + kConvWarps) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::kRegsLow));
       if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -259,23 +272,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         // ---------------------------------------------------------------- converters
         // 1024 16-byte int8 chunks per stage ([A 128 rows | W 128 rows] x 4 chunks of each
-        // 64-byte staging row); thread ct takes idx = ct + 192 j (j < 6, idx < 1024): row
-        // ct / 4 + 48 j, chunk ct % 4. (row & 7) does not change with j, so the swizzled
-        // fp16 address is a per-thread base plus 6144 j bytes.
+        // 64-byte staging row); thread ct takes idx = ct + T j (T = kConvT converter threads,
+        // j < kIters, idx < 1024): row ct / 4 + (T / 4) j, chunk ct % 4. (row & 7) does not
+        // change with j, so the swizzled fp16 address is a per-thread base plus 32 T j bytes.
         if constexpr (!W4) {
+            constexpr int T = C::kConvT, NJ = (1024 + T - 1) / T;   // NJ: chunks per thread and stage
+            static_assert(!MX || T == 320, "the block-scaled slot map assumes 10 converter warps");
             const int ct = threadIdx.x - 64;
             const int r0 = ct >> 2, c0 = ct & 3;
             const uint32_t src0 = (uint32_t)(ct * 16);
             const uint32_t dst0 = sw128(r0, 2 * c0);
             const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
-            // Block-scaled weights: the thread's weight chunks are j = 2..5 with 512 <= idx < 1024
-            // (weight row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage): j = 3, 4 and
-            // one of j = 2 (ct >= 128) or j = 5 (ct < 64), kept in slot (j - 2) % 3. Their scale
-            // words are read from global memory (L2) one stage ahead of use.
-            uint32_t sfw_cur[3] = {0u, 0u, 0u}, sfw_nxt[3] = {0u, 0u, 0u};
+            // Block-scaled weights (T = 320): the thread's weight chunks (512 <= idx < 1024; weight
+            // row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage) are j = 2 (slot 1) and
+            // one of j = 1 (ct >= 192) or j = 3 (ct < 64) (slot 0). Their scale words are read from
+            // global memory (L2) one stage ahead of use.
+            uint32_t sfw_cur[2] = {0u, 0u}, sfw_nxt[2] = {0u, 0u};
             int sh_cur = 0, sh_nxt = 0, pf_i = 0, pf_kb = 0;
-            int sf_n[3] = {0, 0, 0};             // weight rows of the slots in the prefetched stage's tile
-            bool sf_ok[3] = {false, false, false};
+            int sf_n[2] = {0, 0};                // weight rows of the slots in the prefetched stage's tile
+            bool sf_ok[2] = {false, false};
             const int gshift = ep.mx_group == 32 ? 5 : 7;
             auto sf_fetch = [&]() {
                 if constexpr (MX) {
@@ -283,9 +298,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         int pm0, pn0;
                         pair_coords(tg, cluster + pf_i * nclusters, pm0, pn0);
 #pragma unroll
-                        for (int jw = 0; jw < 3; ++jw) {
-                            const int j = (jw == 0 && ct < 64) ? 5 : jw + 2;
-                            const int idx = ct + kConv * j;
+                        for (int jw = 0; jw < 2; ++jw) {
+                            const int j = jw == 1 ? 2 : (ct < 64 ? 3 : 1);
+                            const int idx = ct + T * j;
                             sf_n[jw] = pn0 + (int)rank * BNH + ((idx - 512) >> 2);
                             sf_ok[jw] = idx >= 512 && idx < 1024 && sf_n[jw] < N;
                         }
@@ -294,7 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t* base = ep.mx_sf + (int64_t)(grp >> 2) * N;
                     sh_nxt = 8 * (grp & 3);
 #pragma unroll
-                    for (int jw = 0; jw < 3; ++jw) sfw_nxt[jw] = sf_ok[jw] ? __ldg(base + sf_n[jw]) : 0u;
+                    for (int jw = 0; jw < 2; ++jw) sfw_nxt[jw] = sf_ok[jw] ? __ldg(base + sf_n[jw]) : 0u;
                     if (++pf_kb == KB) { pf_kb = 0; ++pf_i; }
                 }
             };
@@ -302,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int g = 0; g < total_g; ++g) {
                 if constexpr (MX) {
 #pragma unroll
-                    for (int jw = 0; jw < 3; ++jw) sfw_cur[jw] = sfw_nxt[jw];
+                    for (int jw = 0; jw < 2; ++jw) sfw_cur[jw] = sfw_nxt[jw];
                     sh_cur = sh_nxt;
                     if (g + 1 < total_g) sf_fetch();
                 }
@@ -310,50 +325,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
                     break;
                 const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
-                uint4 in[6];
+                uint4 in[NJ];
     #pragma unroll
-                for (int j = 0; j < 6; ++j)
-                    in[j] = (ct + kConv * j < 1024) ? lds128(st8 + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < NJ; ++j)
+                    in[j] = (ct + T * j < 1024) ? lds128(st8 + T * 16 * j) : make_uint4(0, 0, 0, 0);
                 if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
                                &g_tc2_error))
                     break;
                 const uint32_t st16 = sbase + s16 * kStage16;
-    #pragma unroll
-                for (int j = 0; j < 6; ++j) {
-                    if (ct + kConv * j < 1024) {
-                        uint4 o0, o1;
-                        bool scaled = false;
-                        if constexpr (MX) {
-                            if (j >= 2 && ct + kConv * j >= 512) {   // a weight chunk: q * s
-                                const uint32_t e = (sfw_cur[(j - 2) % 3] >> sh_cur) & 0xFFu;
-                                const uint32_t h = scale_f16x2(e);
-                                if (e <= 132u) {
-                                    // (1152 + q) * s - 1152 * s in one fp16 FMA: exact, as q * s and
-                                    // -1152 * s (s <= 32) are fp16 values and the FMA rounds once
-                                    const uint32_t c = hmul2(h, 0xE480E480u);
-                                    cvt_word_scaled(in[j].x, h, c, o0.x, o0.y);
-                                    cvt_word_scaled(in[j].y, h, c, o0.z, o0.w);
-                                    cvt_word_scaled(in[j].z, h, c, o1.x, o1.y);
-                                    cvt_word_scaled(in[j].w, h, c, o1.z, o1.w);
-                                } else {
-                                    cvt_word(in[j].x, o0.x, o0.y);
-                                    cvt_word(in[j].y, o0.z, o0.w);
-                                    cvt_word(in[j].z, o1.x, o1.y);
-                                    cvt_word(in[j].w, o1.z, o1.w);
-                                    o0 = make_uint4(hmul2(o0.x, h), hmul2(o0.y, h), hmul2(o0.z, h), hmul2(o0.w, h));
-                                    o1 = make_uint4(hmul2(o1.x, h), hmul2(o1.y, h), hmul2(o1.z, h), hmul2(o1.w, h));
-                                }
-                                scaled = true;
+                if constexpr (MX) {
+                    // A weight chunk becomes q * s through one fp16 FMA per code pair,
+                    // fma(1152 + q, s, -1152 s): exact while 1152 s is an fp16 value (s <= 32,
+                    // e <= 132), as q * s and -1152 s are fp16 values and the FMA rounds once. An
+                    // activation chunk takes s = 1 (fma(1152 + q, 1, -1152) = q). A warp in which
+                    // some lane holds a larger scale converts with s / 16 and multiplies by 16
+                    // (both exact); the choice is per warp, so the common path has no branch.
+                    uint32_t h[2], c[2], post[2];
+                    bool big = false;
+#pragma unroll
+                    for (int jw = 0; jw < 2; ++jw) {
+                        const uint32_t e = min((sfw_cur[jw] >> sh_cur) & 0xFFu, 136u);
+                        const bool hi = e > 132u;
+                        big |= hi;
+                        h[jw] = scale_f16x2(hi ? e - 4u : e);
+                        c[jw] = hmul2(h[jw], 0xE480E480u);
+                        post[jw] = hi ? 0x4C004C00u : 0x3C003C00u;   // 16 or 1
+                    }
+                    const bool slow = __any_sync(0xffffffffu, big);
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        if (ct + T * j < 1024) {
+                            const bool wchunk = ct + T * j >= 512;
+                            const int sl = j == 2 ? 1 : 0;
+                            const uint32_t hj = wchunk ? h[sl] : 0x3C003C00u;
+                            const uint32_t cj = wchunk ? c[sl] : 0xE480E480u;
+                            uint4 o0, o1;
+                            cvt_word_scaled(in[j].x, hj, cj, o0.x, o0.y);
+                            cvt_word_scaled(in[j].y, hj, cj, o0.z, o0.w);
+                            cvt_word_scaled(in[j].z, hj, cj, o1.x, o1.y);
+                            cvt_word_scaled(in[j].w, hj, cj, o1.z, o1.w);
+                            if (slow) {
+                                const uint32_t pj = wchunk ? post[sl] : 0x3C003C00u;
+                                o0 = make_uint4(hmul2(o0.x, pj), hmul2(o0.y, pj), hmul2(o0.z, pj), hmul2(o0.w, pj));
+                                o1 = make_uint4(hmul2(o1.x, pj), hmul2(o1.y, pj), hmul2(o1.z, pj), hmul2(o1.w, pj));
                             }
+                            sts128(st16 + dst0 + 32 * T * j, o0);
+                            sts128(st16 + dst1 + 32 * T * j, o1);
                         }
-                        if (!scaled) {
+                    }
+                } else {
+    #pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        if (ct + T * j < 1024) {
+                            uint4 o0, o1;
                             cvt_word(in[j].x, o0.x, o0.y);
                             cvt_word(in[j].y, o0.z, o0.w);
                             cvt_word(in[j].z, o1.x, o1.y);
                             cvt_word(in[j].w, o1.z, o1.w);
+                            sts128(st16 + dst0 + 32 * T * j, o0);
+                            sts128(st16 + dst1 + 32 * T * j, o1);
                         }
-                        sts128(st16 + dst0 + 6144 * j, o0);
-                        sts128(st16 + dst1 + 6144 * j, o1);
                     }
                 }
                 // Every lane makes its fp16 stores visible to the tensor core, then one lane per
@@ -432,9 +463,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     } else {
         // ---------------------------------------------------------------- drain + epilogue
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsHigh));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::kRegsHigh));
         const int quarter = warp & 3;
-        const int col_half = (warp - 8) >> 2;
+        // 8 drain warps: warp pair (w, w + 4) takes accumulator columns [0, 128) and [128, 256);
+        // 4 drain warps: each takes both halves, one after the other
+        constexpr int kHalves = 8 / kDrainWarps;
+        const int col_half = kHalves == 1 ? (warp - 2 - kConvWarps) >> 2 : 0;
         int acc[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) acc[c] = 0;
@@ -445,153 +479,158 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar_accfull + 8 * buf, (uint32_t)((c >> 1) & 1), abort_flag, kErrDrain, &g_tc2_error))
                 break;
             tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + col_half * 128);
-            const int keep = cc != 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t v[32];
-                tmem_ld32(taddr + j * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if constexpr (MX)
-                        acc[j * 32 + e] = (int)v[e];   // fp32 sums (bit patterns), one chunk per tile
-                    else
-                        acc[j * 32 + e] = acc[j * 32 + e] * keep + __float2int_rn(__uint_as_float(v[e]));
+            for (int hh = 0; hh < kHalves; ++hh) {
+                const int chalf = kHalves == 1 ? col_half : hh;
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + chalf * 128);
+                const int keep = cc != 0;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + j * 32, v);
+    #pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if constexpr (MX)
+                            acc[j * 32 + e] = (int)v[e];   // fp32 sums (bit patterns), one chunk per tile
+                        else
+                            acc[j * 32 + e] = acc[j * 32 + e] * keep + __float2int_rn(__uint_as_float(v[e]));
+                    }
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_accempty + 8 * buf, 0));
-            if (cc != CPT - 1) continue;
-            int m0, n0;
-            pair_coords(tg, cluster + ti * nclusters, m0, n0);
-            const int mrow0 = m0 + (int)rank * BMH + quarter * 32;
-            const int m = mrow0 + lane;
-            const int nb = n0 + col_half * 128;
-            float sa = 0.0f;
-            int za = 0;
-            if (!ep.out_i32 && m < M) {
-                sa = ep.s_a[ep.a_per_row ? m : 0];
-                za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
-            }
-            const bool vec = ((N & 3) == 0);
-            const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
-            const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
-            // outputs (m, n .. n + 3) of accumulator columns e .. e + 3, as 4-byte words
-            auto out4 = [&](int e, int n) -> uint4 {
-                if (ep.out_i32) return make_uint4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-                if constexpr (MX) {   // y = fl(T * s_a) (+ bias)
+                if (hh == kHalves - 1) {   // the whole buffer has been read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_accempty + 8 * buf, 0));
+                }
+                if (cc != CPT - 1) continue;
+                int m0, n0;
+                pair_coords(tg, cluster + ti * nclusters, m0, n0);
+                const int mrow0 = m0 + (int)rank * BMH + quarter * 32;
+                const int m = mrow0 + lane;
+                const int nb = n0 + chalf * 128;
+                float sa = 0.0f;
+                int za = 0;
+                if (!ep.out_i32 && m < M) {
+                    sa = ep.s_a[ep.a_per_row ? m : 0];
+                    za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
+                }
+                const bool vec = ((N & 3) == 0);
+                const bool vsw = ep.w_per_row && vec && ((reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0);
+                const bool vcs = ep.z_a && vec && ((reinterpret_cast<uintptr_t>(ep.colsum) & 15) == 0);
+                // outputs (m, n .. n + 3) of accumulator columns e .. e + 3, as 4-byte words
+                auto out4 = [&](int e, int n) -> uint4 {
+                    if (ep.out_i32) return make_uint4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                    if constexpr (MX) {   // y = fl(T * s_a) (+ bias)
+                        uint32_t o[4];
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float v = __fmul_rn(__uint_as_float((uint32_t)acc[e + q]), sa);
+                            if (ep.bias) v = __fadd_rn(v, __ldg(ep.bias + (n + q < N ? n + q : 0)));
+                            o[q] = __float_as_uint(v);
+                        }
+                        return make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    const bool full = n + 3 < N;
+                    float sw4[4];
+                    int cs4[4] = {0, 0, 0, 0};
+                    if (vsw && full) {
+                        const float4 t4 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
+                        sw4[0] = t4.x; sw4[1] = t4.y; sw4[2] = t4.z; sw4[3] = t4.w;
+                    } else {
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
+                    }
+                    if (ep.z_a) {
+                        if (vcs && full) {
+                            const int4 t4 = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
+                            cs4[0] = t4.x; cs4[1] = t4.y; cs4[2] = t4.z; cs4[3] = t4.w;
+                        } else {
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
+                        }
+                    }
                     uint32_t o[4];
-#pragma unroll
+    #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        float v = __fmul_rn(__uint_as_float((uint32_t)acc[e + q]), sa);
+                        float v = __fmul_rn(__int2float_rn(acc[e + q] - za * cs4[q]), __fmul_rn(sa, sw4[q]));
                         if (ep.bias) v = __fadd_rn(v, __ldg(ep.bias + (n + q < N ? n + q : 0)));
                         o[q] = __float_as_uint(v);
                     }
                     return make_uint4(o[0], o[1], o[2], o[3]);
-                }
-                const bool full = n + 3 < N;
-                float sw4[4];
-                int cs4[4] = {0, 0, 0, 0};
-                if (vsw && full) {
-                    const float4 t4 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n));
-                    sw4[0] = t4.x; sw4[1] = t4.y; sw4[2] = t4.z; sw4[3] = t4.w;
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) sw4[q] = __ldg(ep.s_w + (ep.w_per_row ? (n + q < N ? n + q : 0) : 0));
-                }
-                if (ep.z_a) {
-                    if (vcs && full) {
-                        const int4 t4 = __ldg(reinterpret_cast<const int4*>(ep.colsum + n));
-                        cs4[0] = t4.x; cs4[1] = t4.y; cs4[2] = t4.z; cs4[3] = t4.w;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) cs4[q] = __ldg(ep.colsum + (n + q < N ? n + q : 0));
-                    }
-                }
-                uint32_t o[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float v = __fmul_rn(__int2float_rn(acc[e + q] - za * cs4[q]), __fmul_rn(sa, sw4[q]));
-                    if (ep.bias) v = __fadd_rn(v, __ldg(ep.bias + (n + q < N ? n + q : 0)));
-                    o[q] = __float_as_uint(v);
-                }
-                return make_uint4(o[0], o[1], o[2], o[3]);
-            };
-            if (tma_out) {
-                // Each block of 32 rows x 128 bytes (32 fp32, 64 bf16 or 128 int8 columns) goes
-                // through this warp's shared buffer (128-byte swizzle: row `lane`, 16-byte chunk c
-                // at chunk c ^ (lane & 7)) and one TMA store, which writes whole lines and clips
-                // rows >= M and columns >= N. ESZ (bytes per output) is a compile-time constant
-                // so that acc[] stays in registers.
-                const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - 8) * kEpiBytes);
-                auto blocks = [&](auto esz_tag) {
-                    constexpr int ESZ = decltype(esz_tag)::value;
-                    constexpr int BCOLS = 128 / ESZ;
-#pragma unroll
-                    for (int j = 0; j < ESZ; ++j) {
-                        if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int e0 = j * BCOLS + c * (16 / ESZ);
-                            uint4 w;
-                            if constexpr (ESZ == 4) {
-                                w = out4(e0, nb + e0);
-                            } else if constexpr (ESZ == 2) {
-                                const uint4 a = out4(e0, nb + e0), b = out4(e0 + 4, nb + e0 + 4);
-                                w = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                                               pack_bf16x2(b.z, b.w));
-                            } else {
-                                uint32_t q[4];
-#pragma unroll
-                                for (int t = 0; t < 4; ++t) {
-                                    const uint4 a = out4(e0 + 4 * t, nb + e0 + 4 * t);
-                                    q[t] = pack_codes4(a, ep.out_scale);
-                                }
-                                w = make_uint4(q[0], q[1], q[2], q[3]);
-                            }
-                            sts128(ebuf + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4)), w);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmap_out, ebuf, nb + j * BCOLS, mrow0);
-                            bulk_commit();
-                        }
-                    }
                 };
-                if (ep.out_i32 || ep.out_kind == kOutF32)
-                    blocks(std::integral_constant<int, 4>{});
-                else if (ep.out_kind == kOutBF16)
-                    blocks(std::integral_constant<int, 2>{});
-                else
-                    blocks(std::integral_constant<int, 1>{});
-            } else if (m < M && !ep.out_i32 && ep.out_kind != kOutF32) {
-#pragma unroll
-                for (int e4 = 0; e4 < 32; ++e4) {
-                    const int n = nb + e4 * 4;
-                    const uint4 o = out4(e4 * 4, n);
-                    if (n < N) epi_store(ep, (int64_t)m * N + n, __uint_as_float(o.x));
-                    if (n + 1 < N) epi_store(ep, (int64_t)m * N + n + 1, __uint_as_float(o.y));
-                    if (n + 2 < N) epi_store(ep, (int64_t)m * N + n + 2, __uint_as_float(o.z));
-                    if (n + 3 < N) epi_store(ep, (int64_t)m * N + n + 3, __uint_as_float(o.w));
-                }
-            } else if (m < M) {
-                uint32_t* row = ep.out_i32 ? reinterpret_cast<uint32_t*>(ep.out_i32) + (int64_t)m * N
-                                           : reinterpret_cast<uint32_t*>(ep.y) + (int64_t)m * N;
-#pragma unroll
-                for (int e4 = 0; e4 < 32; ++e4) {
-                    const int n = nb + e4 * 4;
-                    const uint4 o = out4(e4 * 4, n);
-                    if (vec && n + 3 < N) {
-                        *reinterpret_cast<uint4*>(row + n) = o;
-                    } else {
-                        if (n < N) row[n] = o.x;
-                        if (n + 1 < N) row[n + 1] = o.y;
-                        if (n + 2 < N) row[n + 2] = o.z;
-                        if (n + 3 < N) row[n + 3] = o.w;
+                if (tma_out) {
+                    // Each block of 32 rows x 128 bytes (32 fp32, 64 bf16 or 128 int8 columns) goes
+                    // through this warp's shared buffer (128-byte swizzle: row `lane`, 16-byte chunk c
+                    // at chunk c ^ (lane & 7)) and one TMA store, which writes whole lines and clips
+                    // rows >= M and columns >= N. ESZ (bytes per output) is a compile-time constant
+                    // so that acc[] stays in registers.
+                    const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - 2 - kConvWarps) * kEpiBytes);
+                    auto blocks = [&](auto esz_tag) {
+                        constexpr int ESZ = decltype(esz_tag)::value;
+                        constexpr int BCOLS = 128 / ESZ;
+    #pragma unroll
+                        for (int j = 0; j < ESZ; ++j) {
+                            if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
+                            __syncwarp();
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const int e0 = j * BCOLS + c * (16 / ESZ);
+                                uint4 w;
+                                if constexpr (ESZ == 4) {
+                                    w = out4(e0, nb + e0);
+                                } else if constexpr (ESZ == 2) {
+                                    const uint4 a = out4(e0, nb + e0), b = out4(e0 + 4, nb + e0 + 4);
+                                    w = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                                                   pack_bf16x2(b.z, b.w));
+                                } else {
+                                    uint32_t q[4];
+    #pragma unroll
+                                    for (int t = 0; t < 4; ++t) {
+                                        const uint4 a = out4(e0 + 4 * t, nb + e0 + 4 * t);
+                                        q[t] = pack_codes4(a, ep.out_scale);
+                                    }
+                                    w = make_uint4(q[0], q[1], q[2], q[3]);
+                                }
+                                sts128(ebuf + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4)), w);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmap_out, ebuf, nb + j * BCOLS, mrow0);
+                                bulk_commit();
+                            }
+                        }
+                    };
+                    if (ep.out_i32 || ep.out_kind == kOutF32)
+                        blocks(std::integral_constant<int, 4>{});
+                    else if (ep.out_kind == kOutBF16)
+                        blocks(std::integral_constant<int, 2>{});
+                    else
+                        blocks(std::integral_constant<int, 1>{});
+                } else if (m < M && !ep.out_i32 && ep.out_kind != kOutF32) {
+    #pragma unroll
+                    for (int e4 = 0; e4 < 32; ++e4) {
+                        const int n = nb + e4 * 4;
+                        const uint4 o = out4(e4 * 4, n);
+                        if (n < N) epi_store(ep, (int64_t)m * N + n, __uint_as_float(o.x));
+                        if (n + 1 < N) epi_store(ep, (int64_t)m * N + n + 1, __uint_as_float(o.y));
+                        if (n + 2 < N) epi_store(ep, (int64_t)m * N + n + 2, __uint_as_float(o.z));
+                        if (n + 3 < N) epi_store(ep, (int64_t)m * N + n + 3, __uint_as_float(o.w));
+                    }
+                } else if (m < M) {
+                    uint32_t* row = ep.out_i32 ? reinterpret_cast<uint32_t*>(ep.out_i32) + (int64_t)m * N
+                                               : reinterpret_cast<uint32_t*>(ep.y) + (int64_t)m * N;
+    #pragma unroll
+                    for (int e4 = 0; e4 < 32; ++e4) {
+                        const int n = nb + e4 * 4;
+                        const uint4 o = out4(e4 * 4, n);
+                        if (vec && n + 3 < N) {
+                            *reinterpret_cast<uint4*>(row + n) = o;
+                        } else {
+                            if (n < N) row[n] = o.x;
+                            if (n + 1 < N) row[n + 1] = o.y;
+                            if (n + 2 < N) row[n + 2] = o.z;
+                            if (n + 3 < N) row[n + 3] = o.w;
+                        }
                     }
                 }
             }
