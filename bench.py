@@ -540,8 +540,8 @@ def measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops):
     e1.record()
     torch.cuda.synchronize()
     dms = e0.elapsed_time(e1) / n
-    dbytes = Nd * Kd + Nd * Kd // 8 + Md * Kd + 4 * Md + 4 * Md * Nd
-    out["decode_g32"] = {"workload": f"{DECODE}: A [{Md},{Kd}] x W int8 [{Nd},{Kd}], E8M0 per 32 K (CTA-pair kernel)",
+    dbytes = Nd * Kd + Nd * Kd // 32 + Md * Kd + 4 * Md + 4 * Md * Nd   # codes, E8M0 bytes, tokens, s_a, y
+    out["decode_g32"] = {"workload": f"{DECODE}: A [{Md},{Kd}] x W int8 [{Nd},{Kd}], E8M0 per 32 K (decode kernel)",
                          "gemm_ms": round(dms, 4), "GB/s": round(dbytes / (dms * 1e-3) / 1e9, 1),
                          "frac_hbm": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 4)}
     return out

@@ -286,12 +286,14 @@ q8_status q8_quantize_weight_mx(const float* w, int64_t N, int64_t K, int group,
  * The weights are dequantized to fp16 before the product (exact), T is summed
  * by the tensor core in fp32 over the whole K: not bit-reproducible against an
  * exactly rounded sum, its error bounded by the fp32 accumulation (the products
- * are exact). Runs on the CTA-pair kernel for every M.
+ * are exact); the same inputs give the same bits on every run.
  *
  * qa, s_a, ga : as q8_gemm_dequant_ex (symmetric activations only).
  * qw, sf      : from q8_quantize_weight_mx with the same group.
  * bias, out_type, out, out_scale : as q8_gemm_epilogue_ex.
- * kernel      : Q8_GEMM_AUTO or Q8_GEMM_TCGEN05_PAIR; others -> Q8_ERR_UNSUPPORTED.
+ * kernel      : Q8_GEMM_AUTO (the decode kernel where it applies, else the pair
+ *               kernel), Q8_GEMM_DECODE (M <= 16, N % 4 == 0, sf 16-byte aligned),
+ *               Q8_GEMM_TCGEN05_PAIR (any M); others -> Q8_ERR_UNSUPPORTED.
  * Errors: as q8_gemm_epilogue_ex; group not 32 / 128 -> Q8_ERR_INVALID_ARG;
  * K % group != 0 -> Q8_ERR_UNSUPPORTED.
  */

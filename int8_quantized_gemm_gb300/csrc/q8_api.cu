@@ -84,7 +84,8 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
     if (mx) {
         if (mx->group != 32 && mx->group != 128) return Q8_ERR_INVALID_ARG;
         if (z_a || !epilogue) return Q8_ERR_UNSUPPORTED;     // symmetric activations, dequantized output
-        if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05_PAIR) return Q8_ERR_UNSUPPORTED;
+        if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05_PAIR && kernel != Q8_GEMM_DECODE)
+            return Q8_ERR_UNSUPPORTED;
         if (K % mx->group != 0) return Q8_ERR_UNSUPPORTED;
     }
     if (M == 0 || N == 0) return Q8_OK;   // empty output: nothing is read or written
@@ -126,11 +127,18 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
     }
     if (mx) {
-        // block-scaled weights run on the CTA-pair kernel at every M
-        if (!q8::gemm_tc2_supports(M, N, K, q8::kWMx)) return Q8_ERR_UNSUPPORTED;
+        // block-scaled weights: the decode kernel for M <= 16 (N % 4 == 0, 16-byte aligned scale
+        // words), the CTA-pair kernel otherwise
         ep.s_w = nullptr;
         ep.mx_sf = mx->sf;
         ep.mx_group = mx->group;
+        if (kernel == Q8_GEMM_AUTO)
+            kernel = q8::gemv_mx_supports(M, N, K, mx->group, mx->sf) ? Q8_GEMM_DECODE : Q8_GEMM_TCGEN05_PAIR;
+        if (kernel == Q8_GEMM_DECODE) {
+            if (!q8::gemv_mx_supports(M, N, K, mx->group, mx->sf)) return Q8_ERR_UNSUPPORTED;
+            return from_cuda(q8::launch_gemv_mx(qa, qw, mx->sf, mx->group, M, N, K, ep, s));
+        }
+        if (!q8::gemm_tc2_supports(M, N, K, q8::kWMx)) return Q8_ERR_UNSUPPORTED;
         return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWMx));
     }
     if (w4) {

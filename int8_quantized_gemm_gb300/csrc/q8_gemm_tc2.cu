@@ -27,8 +27,6 @@
 #include <stdint.h>
 #include <string.h>
 
-#include <cuda_fp16.h>
-
 #include <type_traits>
 
 #include "q8_internal.h"
@@ -50,27 +48,6 @@ __device__ __forceinline__ uint32_t pack_codes4(uint4 v, float s) {
         return (uint32_t)(min(max(__float2int_rn(__fdiv_rn(__uint_as_float(b), s)), -127), 127) & 0xFF);
     };
     return code(v.x) | (code(v.y) << 8) | (code(v.z) << 16) | (code(v.w) << 24);
-}
-
-// The E8M0 scale byte e as the fp16 power of two 2^(e - 127) in both halves (exact for
-// e = 103 .. 142; e = 0 gives 0).
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e) {
-    const __half2 h = __floats2half2_rn(__uint_as_float(e << 23), __uint_as_float(e << 23));
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// cvt_word with each code times the power of two s (h = s in both halves, c = -1152 s):
-// 0x6480 | (byte ^ 0x80) is the fp16 1152 + q, and fma(1152 + q, s, -1152 s) = q s.
-__device__ __forceinline__ void cvt_word_scaled(uint32_t w, uint32_t h, uint32_t c, uint32_t& lo, uint32_t& hi) {
-    const uint32_t l = (w & 0x00FF00FFu) ^ 0x64806480u, u = ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(lo) : "r"(l), "r"(h), "r"(c));
-    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(u), "r"(h), "r"(c));
 }
 
 namespace {

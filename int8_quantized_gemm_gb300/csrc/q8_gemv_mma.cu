@@ -394,6 +394,203 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ------------------------------------------------------------------------------------------
+// Block-scaled int8 weights (one E8M0 scale per row and group of G = 32 or 128 K), M <= 16.
+// The same stream as the int8 kernel (64-row tiles, 256-K stages, sixteen compute warps each
+// owning one 16-wide K-step of every stage) plus, per stage, the tile's two scale words of the
+// stage's K (64 rows x 8 bytes by TMA, the 4-byte words viewed as a byte matrix [words, 4 N]).
+// A weight fragment enters the MMA as the fp16 values q * s (exact: the codes are exact in
+// fp16 and s = 2^(e - 127) scales them without rounding for e = 103 .. 136); the four codes of
+// a fragment lie in one 16-K step, hence in one group. The MMA sums the exact products in fp32
+// over the tile, so the result is not bit-reproducible against an exactly rounded sum. At the
+// tile's end the sixteen per-warp partials are added in a fixed order (warp w + 8 onto warp w
+// in shared memory, then the eight sums in warp order), so every run gives the same bits.
+constexpr int kMxS8 = 8;                          // stages in the ring
+constexpr int kMxSf = RW * 2 * 4;                 // scale bytes per stage: 64 rows x 2 words
+constexpr int kMxStage = RW * BK + NT * BK;       // 16 KB of weights + 4 KB of tokens
+constexpr int kMxOffSf = kMxS8 * kMxStage;
+constexpr int kMxOffRed = kMxOffSf + kMxS8 * kMxSf;
+constexpr int kMxRedBytes = 8 * NT * RWP * 4;     // fp32 [8 warps][16 tokens][72 (64 rows)]
+constexpr int kMxOffBar = kMxOffRed + kMxRedBytes;
+constexpr int kMxSmem = kMxOffBar + 16 * kMxS8 + 16 + 1024;
+
+__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_mx_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_sf, int M, int N, int K, int G, Epilogue ep) {
+    constexpr int S8 = kMxS8;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sraw = smem_u32(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - sraw);
+    const uint32_t bar_full = sbase + kMxOffBar;
+    const uint32_t bar_empty = bar_full + 8 * S8;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMxOffBar + 16 * S8);
+    float* red = reinterpret_cast<float*>(smem + kMxOffRed);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kComputeWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_sf)) : "memory");
+    }
+    __syncthreads();
+
+    const int tiles = (N + RW - 1) / RW;
+    const int KB = (K + BK - 1) / BK;
+    const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total_g = my_tiles * KB;
+    const int k_rot = (int)(((long long)blockIdx.x * KB) / gridDim.x);
+    const int wshift = G == 32 ? 7 : 9;   // K per scale word: 4 G
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int i = 0, kb = 0;
+            for (int g = 0; g < total_g; ++g) {
+                const int n0 = ((int)blockIdx.x + i * (int)gridDim.x) * RW;
+                const int s = g % S8;
+                if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
+                               &g_gemv_mma_error))
+                    break;
+                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
+                const uint32_t dst = sbase + s * kMxStage;
+                mbar_expect_tx(bar_full + 8 * s, kMxStage + kMxSf);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)   // W: 64 rows x 128 K per box
+                    tma_load_2d(dst + b * (RW * BKH), &tmap_w, kx + b * BKH, n0, bar_full + 8 * s);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)   // A: 16 tokens x 128 K per box
+                    tma_load_2d(dst + RW * BK + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
+                // scales: words kx / 4G and the next one, bytes [4 n0, 4 n0 + 256) of each
+                tma_load_2d(sbase + kMxOffSf + s * kMxSf, &tmap_sf, 4 * n0, kx >> wshift, bar_full + 8 * s);
+                if (++kb == KB) { kb = 0; ++i; }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int ks = warp - 1;          // K-step of each stage: K [16 ks, 16 ks + 16)
+        const int ct = threadIdx.x - 32;  // 0 .. 511
+        const int g8 = lane >> 2, t = lane & 3;
+        const int half = ks >> 3, kc = ks & 7;
+        // weight row 8j + g8 and token rows g8, g8 + 8 at chunk kc of box `half` (swizzled), word t
+        const uint32_t w_base = half * (RW * BKH) + sw128(g8, kc) + 4 * t;
+        const uint32_t a_off0 = RW * BK + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
+        const uint32_t a_off1 = RW * BK + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
+        // scale byte of weight row r for this K-step: word (16 ks) / 4G of the stage's two, byte
+        // ((kx + 16 ks) / G) % 4; G = 32: word ks / 8, byte (ks / 2) % 4 (kx is a multiple of 256)
+        const uint32_t sf_row0 = (uint32_t)((G == 32 ? half : 0) * (RW * 4) + g8 * 4);
+        const int em = ct / RW, er = ct % RW;   // epilogue outputs: tokens em, em + 8 of row er
+        float esa0 = 0.0f, esa1 = 0.0f;
+        if (em < M) esa0 = __ldg(ep.s_a + (ep.a_per_row ? em : 0));
+        if (em + 8 < M) esa1 = __ldg(ep.s_a + (ep.a_per_row ? em + 8 : 0));
+        float part[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) part[j][e] = 0.0f;
+        int kb = 0, ti = 0, g = 0;
+        for (; g < total_g; ++g) {
+            const int s = g % S8;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag,
+                                                   kErrConvFull, &g_gemv_mma_error)))
+                break;
+            const uint32_t st = sbase + s * kMxStage;
+            const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
+            const uint32_t byte = G == 32 ? (uint32_t)((ks >> 1) & 3) : (uint32_t)(((kx >> 7) + half) & 3);
+            const uint32_t sfa = sbase + kMxOffSf + s * kMxSf + sf_row0 + byte;
+            uint32_t wq[8], ev[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_base + 1024 * j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ev[j] = lds8(sfa + 32 * j);   // row 8j + g8
+            const uint32_t aq0 = lds32(st + a_off0);
+            const uint32_t aq1 = lds32(st + a_off1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
+            uint32_t a[4], b[8][2];
+            cvt_word(aq0, a[0], a[2]);     // token row g8:   k pair (2t,2t+1) and (8+2t,9+2t)
+            cvt_word(aq1, a[1], a[3]);     // token row g8+8
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // weight row 8j + g8: q exactly, then q * s (exact)
+                const uint32_t h = scale_f16x2(min(ev[j], 136u));
+                cvt_word(wq[j], b[j][0], b[j][1]);
+                b[j][0] = hmul2(b[j][0], h);
+                b[j][1] = hmul2(b[j][1], h);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
+            if (kb == KB - 1) {
+                // Tile end: warps 0-7 write their partials, warps 8-15 add theirs onto warp
+                // ks - 8's, then every thread sums the eight slots of its two outputs in order.
+                float* slot = red + (ks & 7) * (NT * RWP);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = g8 + (e >> 1) * 8, r = 8 * j + 2 * t + (e & 1);
+                        if (ks < 8) slot[m * RWP + r] = part[j][e];
+                    }
+                named_barrier(1, 32 * kComputeWarps);
+                if (ks >= 8) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int m = g8 + (e >> 1) * 8, r = 8 * j + 2 * t + (e & 1);
+                            slot[m * RWP + r] = __fadd_rn(slot[m * RWP + r], part[j][e]);
+                        }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) part[j][e] = 0.0f;
+                named_barrier(1, 32 * kComputeWarps);
+                float T0 = 0.0f, T1 = 0.0f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    T0 = __fadd_rn(T0, red[w * (NT * RWP) + em * RWP + er]);
+                    T1 = __fadd_rn(T1, red[w * (NT * RWP) + (em + 8) * RWP + er]);
+                }
+                const int n = ((int)blockIdx.x + ti * (int)gridDim.x) * RW + er;
+                if (n < N) {
+                    if (em < M) epi_store(ep, (int64_t)em * N + n, epi_bias(ep, __fmul_rn(T0, esa0), n));
+                    if (em + 8 < M) epi_store(ep, (int64_t)(em + 8) * N + n, epi_bias(ep, __fmul_rn(T1, esa1), n));
+                }
+                named_barrier(1, 32 * kComputeWarps);   // the slots are free for the next tile
+            }
+            if (++kb == KB) { kb = 0; ++ti; }
+        }
+        // After an abort: pass the tile-end barriers still ahead, so that no compute warp
+        // waits at one forever.
+        for (; g < total_g; ++g) {
+            if (kb == KB - 1) {
+                named_barrier(1, 32 * kComputeWarps);
+                named_barrier(1, 32 * kComputeWarps);
+                named_barrier(1, 32 * kComputeWarps);
+            }
+            if (++kb == KB) kb = 0;
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1LL << 22)) __nanosleep(1000);
+    }
+}
+
 }  // namespace
 
 bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4) {
@@ -431,6 +628,34 @@ cudaError_t launch_gemv_mma(const int8_t* qa, const void* qw, int64_t M, int64_t
     if (!gemv_mma_supports(M, N, K, w4)) return cudaErrorNotSupported;
     return w4 ? launch_gemv_mma_t<true>(qa, qw, M, N, K, ep, stream)
               : launch_gemv_mma_t<false>(qa, qw, M, N, K, ep, stream);
+}
+
+bool gemv_mx_supports(int64_t M, int64_t N, int64_t K, int G, const void* sf) {
+    // the scale words are fetched by TMA as a byte matrix [words, 4 N]: 16-byte row pitch and base
+    if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 29) && K >= 16 && K % 16 == 0 && (G == 32 || G == 128) &&
+          K % G == 0 && N % 4 == 0 && (reinterpret_cast<uintptr_t>(sf) & 15) == 0))
+        return false;
+    const int64_t tiles = (N + RW - 1) / RW;
+    const int64_t kb = (K + BK - 1) / BK;
+    return tiles * kb < (1LL << 31);
+}
+
+cudaError_t launch_gemv_mx(const int8_t* qa, const int8_t* qw, const uint32_t* sf, int G, int64_t M, int64_t N,
+                           int64_t K, const Epilogue& ep, cudaStream_t stream) {
+    if (!gemv_mx_supports(M, N, K, G, sf)) return cudaErrorNotSupported;
+    const int64_t words = (K / G + 3) / 4;
+    CUtensorMap mw, ma, ms;
+    if (!make_tma_map_i8(&mw, qw, N, K, RW, BKH, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BKH, true) ||
+        !make_tma_map_i8(&ms, reinterpret_cast<const int8_t*>(sf), words, 4 * N, 2, RW * 4))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemv_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (N + RW - 1) / RW;
+    const int sms = device_sm_count();
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    gemv_mx_kernel<<<grid, kThreads, kMxSmem, stream>>>(mw, ma, ms, (int)M, (int)N, (int)K, G, ep);
+    note_launch();
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_gemv_mma_error(uint32_t* code) {

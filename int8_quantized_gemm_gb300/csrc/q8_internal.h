@@ -115,6 +115,10 @@ bool gemv_tc_supports(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv_mma(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
                             cudaStream_t stream, bool w4 = false);
 bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4 = false);
+// Block-scaled int8 weights (E8M0 words sf, group G) for M <= 16, on the same stream design.
+cudaError_t launch_gemv_mx(const int8_t* qa, const int8_t* qw, const uint32_t* sf, int G, int64_t M, int64_t N,
+                           int64_t K, const Epilogue& ep, cudaStream_t stream);
+bool gemv_mx_supports(int64_t M, int64_t N, int64_t K, int G, const void* sf);
 
 // Device error words (bounded waits that gave up), one per kernel file and device.
 cudaError_t read_and_clear_gemm_tc_error(uint32_t* code);

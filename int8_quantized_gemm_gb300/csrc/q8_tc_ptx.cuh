@@ -152,6 +152,30 @@ __device__ __forceinline__ void cvt_word(uint32_t w, uint32_t& lo, uint32_t& hi)
     hi = hsub_1152(((w >> 8) & 0x00FF00FFu) ^ 0x64806480u);
 }
 
+// Block-scaled weights. The E8M0 scale byte e as the fp16 power of two 2^(e - 127) in both
+// halves (exact for e = 103 .. 142; e = 0 gives 0).
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t e) {
+    const float f = __uint_as_float(e << 23);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(f), "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// cvt_word with each code times the power of two s (h = s in both halves, c = -1152 s):
+// 0x6480 | (byte ^ 0x80) is the fp16 1152 + q, and fma(1152 + q, s, -1152 s) = q s, exact
+// while -1152 s is an fp16 value (s <= 32).
+__device__ __forceinline__ void cvt_word_scaled(uint32_t w, uint32_t h, uint32_t c, uint32_t& lo, uint32_t& hi) {
+    const uint32_t l = (w & 0x00FF00FFu) ^ 0x64806480u, u = ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(lo) : "r"(l), "r"(h), "r"(c));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(u), "r"(h), "r"(c));
+}
+
 // Two packed int4 bytes (K 4t, 4t+1 | 4t+2, 4t+3 as low/high nibbles) -> fp16x2 of the low
 // nibbles (K 4t, 4t+2) and of the high nibbles (K 4t+1, 4t+3): the pairs cvt_word gives for an
 // int8 word, so activations and int4 weights share the K order. SEL picks the two bytes of w

@@ -113,7 +113,7 @@ def test_block_scaled_entries_reject_bad_arguments(lib):
     assert g(group=0) == q8.Q8_ERR_INVALID_ARG
     assert g(K=48) == q8.Q8_ERR_UNSUPPORTED                       # K % group
     assert g(group=128, K=192) == q8.Q8_ERR_UNSUPPORTED
-    assert g(kernel=q8.KERNELS["decode"]) == q8.Q8_ERR_UNSUPPORTED
+    assert g(kernel=q8.KERNELS["mma_s8"]) == q8.Q8_ERR_UNSUPPORTED      # pair or decode kernels only
     assert g(sf=None) == q8.Q8_ERR_INVALID_ARG
     assert g(sf=P(0x10002)) == q8.Q8_ERR_INVALID_ARG
     assert g(sa=None) == q8.Q8_ERR_INVALID_ARG

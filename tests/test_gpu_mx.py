@@ -193,3 +193,104 @@ def test_full_size_sampled_outputs(q8):
     t_s = host(t)[np.ix_(ms, ns)]
     accumulation_gate(t_s, t_ref, absum, K)
     np.testing.assert_array_equal(host(y)[np.ix_(ms, ns)], (t_s * sa_s[:, None]).astype(np.float32))
+
+
+DECODE_EXACT = [(16, 264, 1024, 128), (1, 72, 512, 128), (7, 200, 2080, 32), (16, 4096, 8192, 32), (3, 68, 32, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,G", DECODE_EXACT)
+@pytest.mark.parametrize("kernel", ["decode", "tcgen05_pair"])
+def test_decode_shapes_exact_where_fp32_sums_are_exact(q8, M, N, K, G, kernel):
+    # both kernels that take M <= 16, on the designed exact cases (ragged N, K tails of 16 and
+    # of 32 past a 256-K stage, every token count's padding)
+    rng = np.random.default_rng(M * 7 + N + K)
+    qa = rng.integers(-3, 4, (M, K), dtype=np.int8)
+    q = rng.integers(-3, 4, (N, K), dtype=np.int8)
+    base = rng.integers(103, 133, (N, 1))
+    e = base + rng.integers(0, 4, (N, K // G))
+    sf = sf_from_exponents(e)
+    t_ref, _ = oracle.gemm_mx(qa, q, sf, G, threads=8)
+    t = host(q8.q8_gemm_mx(dev(qa), unit_scales(M), dev(q), dev(words(sf)), G, kernel=kernel))
+    assert q8.q8_device_error() == 0
+    np.testing.assert_array_equal(t.view(np.int32), t_ref.view(np.int32))
+
+
+@pytest.mark.parametrize("M,N,K,G", [(16, 1000, 8192, 32), (5, 520, 4096, 128), (16, 2048, 16384, 32)])
+def test_decode_kernel_within_the_accumulation_bound(q8, M, N, K, G):
+    wl = workloads.WORKLOADS["decode"]
+    a = workloads.make_activations(wl, M=M, K=K)
+    w = block_weights(N, K, G, seed=K + 1)
+    w[1, :G] *= np.float32(3e6)                              # one group with s > 32 (e = 133 .. 136)
+    qa, sa = oracle.quantize_sym(a, per_row=True)
+    q, sf = oracle.quantize_weight_mx(w, G)
+    assert ((sf[0, 1] & 0xFF) > 132)
+    t_ref, absum = oracle.gemm_mx(qa, q, sf, G, threads=8)
+    t = host(q8.q8_gemm_mx(dev(qa), unit_scales(M), dev(q), dev(words(sf)), G, kernel="decode"))
+    assert q8.q8_device_error() == 0
+    accumulation_gate(t, t_ref, absum, K)
+    y = host(q8.q8_gemm_mx(dev(qa), dev(sa), dev(q), dev(words(sf)), G, kernel="decode"))
+    np.testing.assert_array_equal(y, (t * sa[:, None]).astype(np.float32))
+    y2 = host(q8.q8_gemm_mx(dev(qa), dev(sa), dev(q), dev(words(sf)), G))   # auto picks the decode kernel
+    np.testing.assert_array_equal(y.view(np.int32), y2.view(np.int32))
+
+
+def test_decode_kernel_epilogue_variants(q8):
+    M, N, K, G = 11, 264, 2048, 32
+    wl = workloads.WORKLOADS["decode"]
+    a = workloads.make_activations(wl, M=M, K=K)
+    w = block_weights(N, K, G, seed=9)
+    qa, sa = oracle.quantize_sym(a, per_row=True)
+    q, sf = oracle.quantize_weight_mx(w, G)
+    bias = workloads.gaussian((N,), 21) * np.float32(0.1)
+    d = dict(qa=dev(qa), s_a=dev(sa), qw=dev(q), sf=dev(words(sf)), group=G, kernel="decode")
+    y0 = host(q8.q8_gemm_mx(**d))
+    yb = host(q8.q8_gemm_mx(bias=dev(bias), **d))
+    np.testing.assert_array_equal(yb, (y0 + bias[None, :]).astype(np.float32))
+    y16 = host(q8.q8_gemm_mx(bias=dev(bias), out_dtype=torch.bfloat16, **d).view(torch.int16)).view(np.uint16)
+    np.testing.assert_array_equal(y16, oracle.to_bf16(yb))
+    s_out = float(np.float32(np.abs(yb).max() / np.float32(100.0)))
+    y8 = host(q8.q8_gemm_mx(bias=dev(bias), out_dtype=torch.int8, out_scale=s_out, **d))
+    np.testing.assert_array_equal(y8, oracle.quantize_static(yb, s_out))
+    yt = host(q8.q8_gemm_mx(d["qa"], dev(sa[:1].copy()), d["qw"], d["sf"], G, kernel="decode"))   # per-tensor s_a
+    t = host(q8.q8_gemm_mx(d["qa"], unit_scales(M), d["qw"], d["sf"], G, kernel="decode"))
+    np.testing.assert_array_equal(yt, (t * sa[0]).astype(np.float32))
+
+
+def test_decode_kernel_rejects_what_it_cannot_take(q8):
+    qa = torch.zeros((17, 64), dtype=torch.int8, device="cuda")   # M > 16
+    qw = torch.zeros((8, 64), dtype=torch.int8, device="cuda")
+    sf = torch.zeros((1, 8), dtype=torch.int32, device="cuda")
+    with pytest.raises(q8.Q8Error):
+        q8.q8_gemm_mx(qa, torch.ones(17, device="cuda"), qw, sf, 32, kernel="decode")
+    qw6 = torch.zeros((6, 64), dtype=torch.int8, device="cuda")   # N % 4 != 0: the pair kernel takes it
+    sf6 = torch.zeros((1, 6), dtype=torch.int32, device="cuda")
+    with pytest.raises(q8.Q8Error):
+        q8.q8_gemm_mx(qa[:4], torch.ones(4, device="cuda"), qw6, sf6, 32, kernel="decode")
+    y = q8.q8_gemm_mx(qa[:4], torch.ones(4, device="cuda"), qw6, sf6, 32)
+    torch.cuda.synchronize()
+    assert float(y.abs().sum()) == 0.0
+
+
+def test_decode_full_size_sampled_outputs(q8):
+    # the decode workload (16 x 8192 tokens x 28672 rows) with block-scaled weights, G = 32
+    wl = workloads.WORKLOADS["decode"]
+    M, N, K, G = wl.M, wl.N, wl.K, 32
+    a_np = workloads.make_activations(wl)
+    w_np = block_weights(N, K, G, seed=4)
+    qa, sa, _ = q8.q8_quantize_act(dev(a_np))
+    qw, sf = q8.q8_quantize_weight_mx(dev(w_np), G)
+    t = q8.q8_gemm_mx(qa, torch.ones(M, device="cuda"), qw, sf, G)
+    y = q8.q8_gemm_mx(qa, sa, qw, sf, G)
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    rng = np.random.default_rng(1)
+    ns = np.unique(np.concatenate([rng.integers(0, N, 300), [0, N - 1]]))
+    qa_s, sa_s = oracle.quantize_sym(a_np, per_row=True)
+    qw_s, sf_s = oracle.quantize_weight_mx(w_np[ns], G)
+    np.testing.assert_array_equal(host(qa), qa_s)
+    np.testing.assert_array_equal(host(qw)[ns], qw_s)
+    np.testing.assert_array_equal(host(sf)[:, ns], words(sf_s))
+    t_ref, absum = oracle.gemm_mx(qa_s, qw_s, sf_s, G, threads=8)
+    t_s = host(t)[:, ns]
+    accumulation_gate(t_s, t_ref, absum, K)
+    np.testing.assert_array_equal(host(y)[:, ns], (t_s * sa_s[:, None]).astype(np.float32))
