@@ -90,7 +90,7 @@ struct PairCfg {
     static constexpr int kConvWarps = WF == kWMx ? 10 : 6;
     static constexpr int kDrainWarps = 16 - 2 - kConvWarps;
     static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
-    static constexpr int kRegsLow = WF == kWMx ? 88 : 72, kRegsHigh = 184;
+    static constexpr int kRegsLow = WF == kWMx ? 104 : 72, kRegsHigh = 184;
     static_assert((2 + kConvWarps) * 32 * kRegsLow + kDrainWarps * 32 * kRegsHigh <= kThreads * 128,
                   "register split above the launch's registers");
     static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
@@ -311,40 +311,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 const uint32_t st16 = sbase + s16 * kStage16;
                 if constexpr (MX) {
-                    // A weight chunk becomes q * s through one fp16 FMA per code pair,
-                    // fma(1152 + q, s, -1152 s): exact while 1152 s is an fp16 value (s <= 32,
-                    // e <= 132), as q * s and -1152 s are fp16 values and the FMA rounds once. An
-                    // activation chunk takes s = 1 (fma(1152 + q, 1, -1152) = q). A warp in which
-                    // some lane holds a larger scale converts with s / 16 and multiplies by 16
-                    // (both exact); the choice is per warp, so the common path has no branch.
-                    uint32_t h[2], c[2], post[2];
+                    // A weight chunk becomes q * s in two steps per code pair (a lop3, an fp16 add). The
+                    // fp16 with exponent field E = e - 102 (s = 2^(e - 127) = 2^(E - 25)) and the
+                    // code in the low mantissa bits, M | (byte ^ 0x80) with M = E << 10 | 0x80, is
+                    // (1152 + q) s exactly; subtracting 1152 s (the same bits with the sign set) is
+                    // exact. E must be a normal exponent, e <= 132: a warp in which some lane has a
+                    // larger scale builds (1152 + q) s / 16 and multiplies the difference by 16
+                    // (exact). Activation chunks are converted as in the int8 format.
+                    uint32_t ev[2], mg[2];
                     bool big = false;
 #pragma unroll
                     for (int jw = 0; jw < 2; ++jw) {
-                        const uint32_t e = min((sfw_cur[jw] >> sh_cur) & 0xFFu, 136u);
-                        const bool hi = e > 132u;
-                        big |= hi;
-                        h[jw] = scale_f16x2(hi ? e - 4u : e);
-                        c[jw] = hmul2(h[jw], 0xE480E480u);
-                        post[jw] = hi ? 0x4C004C00u : 0x3C003C00u;   // 16 or 1
+                        ev[jw] = min(max((sfw_cur[jw] >> sh_cur) & 0xFFu, 103u), 136u);
+                        big |= ev[jw] > 132u;
                     }
                     const bool slow = __any_sync(0xffffffffu, big);
 #pragma unroll
+                    for (int jw = 0; jw < 2; ++jw) {
+                        const bool hi = ev[jw] > 132u;
+                        mg[jw] = (((ev[jw] - (hi ? 106u : 102u)) << 10) | 0x80u) * 0x10001u;
+                    }
+#pragma unroll
                     for (int j = 0; j < NJ; ++j) {
                         if (ct + T * j < 1024) {
-                            const bool wchunk = ct + T * j >= 512;
-                            const int sl = j == 2 ? 1 : 0;
-                            const uint32_t hj = wchunk ? h[sl] : 0x3C003C00u;
-                            const uint32_t cj = wchunk ? c[sl] : 0xE480E480u;
                             uint4 o0, o1;
-                            cvt_word_scaled(in[j].x, hj, cj, o0.x, o0.y);
-                            cvt_word_scaled(in[j].y, hj, cj, o0.z, o0.w);
-                            cvt_word_scaled(in[j].z, hj, cj, o1.x, o1.y);
-                            cvt_word_scaled(in[j].w, hj, cj, o1.z, o1.w);
-                            if (slow) {
-                                const uint32_t pj = wchunk ? post[sl] : 0x3C003C00u;
-                                o0 = make_uint4(hmul2(o0.x, pj), hmul2(o0.y, pj), hmul2(o0.z, pj), hmul2(o0.w, pj));
-                                o1 = make_uint4(hmul2(o1.x, pj), hmul2(o1.y, pj), hmul2(o1.z, pj), hmul2(o1.w, pj));
+                            if (ct + T * j >= 512) {   // a weight chunk (warp-uniform)
+                                const uint32_t m = mg[j == 2 ? 1 : 0], c = m | 0x80008000u;
+                                cvt_word_magic(in[j].x, m, c, o0.x, o0.y);
+                                cvt_word_magic(in[j].y, m, c, o0.z, o0.w);
+                                cvt_word_magic(in[j].z, m, c, o1.x, o1.y);
+                                cvt_word_magic(in[j].w, m, c, o1.z, o1.w);
+                                if (slow) {   // rows with e > 132 were built at s / 16
+                                    const uint32_t pj = ev[j == 2 ? 1 : 0] > 132u ? 0x4C004C00u : 0x3C003C00u;   // 16 or 1
+                                    o0 = make_uint4(hmul2(o0.x, pj), hmul2(o0.y, pj), hmul2(o0.z, pj), hmul2(o0.w, pj));
+                                    o1 = make_uint4(hmul2(o1.x, pj), hmul2(o1.y, pj), hmul2(o1.z, pj), hmul2(o1.w, pj));
+                                }
+                            } else {
+                                cvt_word(in[j].x, o0.x, o0.y);
+                                cvt_word(in[j].y, o0.z, o0.w);
+                                cvt_word(in[j].z, o1.x, o1.y);
+                                cvt_word(in[j].w, o1.z, o1.w);
                             }
                             sts128(st16 + dst0 + 32 * T * j, o0);
                             sts128(st16 + dst1 + 32 * T * j, o1);

@@ -176,6 +176,18 @@ __device__ __forceinline__ void cvt_word_scaled(uint32_t w, uint32_t h, uint32_t
     asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(hi) : "r"(u), "r"(h), "r"(c));
 }
 
+// cvt_word with a per-row magic m = (E << 10 | 0x80) in both halves and c = m with both sign
+// bits set: (x & 0x00FF00FF) ^ m puts (byte ^ 0x80) = q + 128 in the low mantissa bits of the
+// fp16 2^(E - 15) (1 + 128 / 1024), i.e. (1152 + q) 2^(E - 25), and adding c = -1152 2^(E - 25)
+// leaves q 2^(E - 25), exactly (1 <= E <= 30).
+__device__ __forceinline__ void cvt_word_magic(uint32_t w, uint32_t m, uint32_t c, uint32_t& lo, uint32_t& hi) {
+    uint32_t l, u;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(l) : "r"(w), "r"(0x00FF00FFu), "r"(m));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;\n" : "=r"(u) : "r"(w >> 8), "r"(0x00FF00FFu), "r"(m));
+    asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(l), "r"(c));
+    asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(u), "r"(c));
+}
+
 // Two packed int4 bytes (K 4t, 4t+1 | 4t+2, 4t+3 as low/high nibbles) -> fp16x2 of the low
 // nibbles (K 4t, 4t+2) and of the high nibbles (K 4t+1, 4t+3): the pairs cvt_word gives for an
 // int8 word, so activations and int4 weights share the K order. SEL picks the two bytes of w
