@@ -170,13 +170,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (every rank gets it): the job's time is its slowest rank's."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step_max: float, scale: float = 1e12) -> float:
+    """Whole-job throughput: the units all ranks processed in one step over the slowest rank's
+    step time (weak scaling: every rank runs the same per-rank workload)."""
+    return units_per_rank * world / (ms_per_step_max * 1e-3) / scale
 
 
 # ------------------------------------------------------------------ our arm
@@ -257,7 +265,7 @@ def run_ours(args, world, rank, local):
     ms_step = max_over_ranks(statistics.mean(step_ms), world)
 
     ops = 2.0 * M * N * K
-    value = ops * world / (ms_step * 1e-3) / 1e12
+    value = job_rate(ops, world, ms_step)
     gemm_avg = statistics.mean(gemm_ms)
     quant_avg = statistics.mean(quant_ms)
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
@@ -348,7 +356,7 @@ def measure_e2e(a, y, step, ops, world, args):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
-    return {"value": round(ops * world / (ms * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": M * K * 4,
+    return {"value": round(job_rate(ops, world, ms), 3), "unit": "TOPS", "h2d_bytes_per_step": M * K * 4,
             "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(ms, 3)}
 
 
