@@ -37,6 +37,7 @@
 #ifndef Q8_H_
 #define Q8_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -301,6 +302,36 @@ q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, c
                         const uint32_t* sf, int group, const float* bias, int64_t M, int64_t N,
                         int64_t K, q8_out_type out_type, void* out, float out_scale,
                         q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
+ * The whole layer on host buffers ("Activation Quantization Architecture", the
+ * quantizer itself and the integer GEMM; Day 98's epilogue): A fp32 [M, K] in host
+ * memory -> per-token quantization (symmetric, or asymmetric with colsum) -> the
+ * INT32 GEMM against device-resident weights -> y fp32 [M, N] in host memory. The
+ * token rows go through in slices of chunk_rows rows (0: about a quarter of M,
+ * whole 256-row tiles): the copy of one slice in, the device work on the previous
+ * one and the copy out of the one before overlap. y is the same as that of
+ * q8_quantize_act (Q8_PER_ROW) + q8_gemm_dequant over all rows.
+ *
+ * a_host, y_host : host memory; page-locked (cudaHostAlloc / pinned) for the copies
+ *                  to overlap, else they run synchronously. a_host may be NULL iff K == 0.
+ * qw, s_w, gw, colsum : device buffers as q8_gemm_dequant (colsum iff asymmetric).
+ * workspace      : device memory of at least q8_linear_host_workspace(M, N, K,
+ *                  chunk_rows) bytes, 256-byte aligned, owned by the caller; not
+ *                  touched after the call's work on `stream` completes.
+ * stream         : the device work runs on it; the call returns once everything is
+ *                  queued, and `stream` completes only after the last slice of y has
+ *                  reached the host. The first call on a device creates two copy
+ *                  streams and seven events, kept until the process exits; calls from
+ *                  several host threads are queued one after another.
+ * Errors: Q8_ERR_INVALID_ARG (sizes, pointers, alignment, a workspace too small),
+ * Q8_ERR_UNSUPPORTED (K % 16, K above the int32 bound), Q8_ERR_CUDA.
+ */
+size_t q8_linear_host_workspace(int64_t M, int64_t N, int64_t K, int64_t chunk_rows);
+q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
+                         const float* s_w, q8_granularity gw, const int32_t* colsum, int64_t N,
+                         float* y_host, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
+                         q8_stream_t stream);
 
 /*
  * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),

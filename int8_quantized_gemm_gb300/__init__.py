@@ -14,6 +14,7 @@ CPU fallback; if the library is missing or a call fails, an exception says so.
   q8_quantize_weight_int4(w) -> qw4, s_w;  q8_colsum_int4(qw4, K);  q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, ...)
   q8_quantize_weight_mx(w, group) -> qw, sf;  q8_gemm_mx(qa, s_a, qw, sf, group, ...)   (block-scaled weights)
   q8_linear(a, qw, s_w, colsum)                       -> y   (quantize A, then GEMM)
+  q8_linear_host(a_host, qw, s_w, colsum, y_host)      (host buffers; copies overlapped with the device work)
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -70,6 +71,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_w4a8_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_quantize_weight_mx.argtypes = [p, i64, i64, i32, p, p, p]
     lib.q8_gemm_mx_ex.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
+    lib.q8_linear_host_workspace.argtypes = [i64, i64, i64, i64]
+    lib.q8_linear_host_workspace.restype = ctypes.c_size_t
+    lib.q8_linear_host.argtypes = [p, i64, i64, i32, p, p, i32, p, i64, p, i64, p, ctypes.c_size_t, p]
     lib.q8_gemm_pick.argtypes = [i64, i64, i64]
     lib.q8_status_string.argtypes = [i32]
     lib.q8_status_string.restype = ctypes.c_char_p
@@ -79,7 +83,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
                  "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
-                 "q8_gemm_pick", "q8_device_error"):
+                 "q8_linear_host", "q8_gemm_pick", "q8_device_error"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -327,6 +331,39 @@ def q8_linear(a, qw, s_w, colsum=None, per_row: bool = True, symmetric: bool = T
     """Whole W8A8 layer on fp32 activations: dynamic quantization of a, then the GEMM + epilogue."""
     qa, s_a, z_a = q8_quantize_act(a, per_row=per_row, symmetric=symmetric, stream=stream)
     return q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, kernel=kernel, stream=stream)
+
+
+def q8_linear_host_workspace(M: int, N: int, K: int, chunk_rows: int = 0) -> int:
+    """Device workspace bytes that q8_linear_host needs."""
+    return int(load().q8_linear_host_workspace(M, N, K, chunk_rows))
+
+
+def q8_linear_host(a_host, qw, s_w, colsum=None, y_host=None, symmetric: bool = True, chunk_rows: int = 0,
+                   workspace=None, stream=None):
+    """Whole layer on host buffers: a_host fp32 [M, K] (CPU, pinned for overlap) -> y_host fp32 [M, N] (CPU),
+    per-token quantization on the device. The result is in y_host once `stream` (default: the current
+    stream) has completed."""
+    if a_host.device.type != "cpu" or a_host.dtype != torch.float32 or a_host.dim() != 2 or not a_host.is_contiguous():
+        raise ValueError("a_host must be a contiguous fp32 [M, K] CPU tensor")
+    _need(qw, torch.int8, "qw", 2)
+    M, K = a_host.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qw must be [N, K]")
+    _need(s_w, torch.float32, "s_w", 1)
+    gw = Q8_PER_ROW if (s_w.numel() == N and N != 1) else Q8_PER_TENSOR
+    if y_host is None:
+        y_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    if y_host.device.type != "cpu" or y_host.dtype != torch.float32 or tuple(y_host.shape) != (M, N) \
+            or not y_host.is_contiguous():
+        raise ValueError("y_host must be a contiguous fp32 [M, N] CPU tensor")
+    need = q8_linear_host_workspace(M, N, K, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=qw.device)
+    _check(load().q8_linear_host(_ptr(a_host), M, K, Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qw),
+                                 _ptr(s_w), gw, _ptr(colsum), N, _ptr(y_host), chunk_rows, _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "q8_linear_host")
+    return y_host
 
 
 def q8_gemm_pick(M: int, N: int, K: int) -> str:

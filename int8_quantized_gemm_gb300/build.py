@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libq8.so")
-SOURCES = ["q8_api.cu", "q8_quant.cu", "q8_gemm_mma.cu", "q8_gemm_tc.cu", "q8_gemv_tc.cu", "q8_gemv_mma.cu", "q8_gemm_tc2.cu"]
+SOURCES = ["q8_api.cu", "q8_quant.cu", "q8_gemm_mma.cu", "q8_gemm_tc.cu", "q8_gemv_tc.cu", "q8_gemv_mma.cu", "q8_gemm_tc2.cu",
+           "q8_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

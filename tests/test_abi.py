@@ -171,3 +171,27 @@ def test_binding_refuses_cpu_tensors():
     import int8_quantized_gemm_gb300 as q8
     with pytest.raises(ValueError):
         q8.q8_quantize_act(torch.zeros(4, 32))
+
+
+def test_host_layer_rejects_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    ws_need = lib.q8_linear_host_workspace(64, 32, 64, 0)
+    assert ws_need > 0 and lib.q8_linear_host_workspace(0, 32, 64, 0) == 0
+    assert lib.q8_linear_host_workspace(1000, 32, 64, 1) < lib.q8_linear_host_workspace(1000, 32, 64, 0)
+
+    def h(M=64, K=64, N=32, sym=0, a=FAKE, qw=FAKE, sw=FAKE, cs=None, y=FAKE, chunk=0, ws=P(0x100000), wsb=None):
+        return lib.q8_linear_host(a, M, K, sym, qw, sw, 1, cs, N, y, chunk, ws, ws_need if wsb is None else wsb,
+                                  None)
+    assert h(wsb=ws_need - 1) == q8.Q8_ERR_INVALID_ARG            # workspace too small
+    assert h(ws=P(0x100010)) == q8.Q8_ERR_INVALID_ARG             # not 256-byte aligned
+    assert h(ws=None) == q8.Q8_ERR_INVALID_ARG
+    assert h(K=24) == q8.Q8_ERR_UNSUPPORTED                        # K % 16
+    assert h(sym=1) == q8.Q8_ERR_INVALID_ARG                       # asymmetric needs column sums
+    assert h(sym=7) == q8.Q8_ERR_INVALID_ARG
+    assert h(y=None) == q8.Q8_ERR_INVALID_ARG
+    assert h(a=None) == q8.Q8_ERR_INVALID_ARG
+    assert h(qw=MISALIGNED) == q8.Q8_ERR_INVALID_ARG
+    assert h(M=-1) == q8.Q8_ERR_INVALID_ARG and h(chunk=-2) == q8.Q8_ERR_INVALID_ARG
+    before = lib.q8_launch_count()
+    assert h(M=0) == q8.Q8_OK and h(N=0) == q8.Q8_OK               # nothing to do
+    assert lib.q8_launch_count() == before
