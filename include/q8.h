@@ -334,6 +334,36 @@ q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q8_symmetry 
                          q8_stream_t stream);
 
 /*
+ * q8_linear_host without a caller-supplied workspace: the same layer, the same result,
+ * for callers that cannot allocate device memory themselves. Examples: a plugin inside an
+ * inference server or framework whose device memory all belongs to the host
+ * application's pool (allocating outside it breaks the pool's accounting and limits),
+ * and code on a latency-critical path, where cudaMalloc/cudaFree are off limits because
+ * they can synchronize the whole device. No counterpart in the source material: this is
+ * a packaging of the layer, not a step of the method.
+ *
+ * The workspace is a fixed device array of q8_linear_host_static_limit() bytes
+ * (64 MiB) inside this library. Every device that loads the library holds it until the
+ * process exits, and every call on that device uses the same array; nothing in it has to
+ * start at zero, and it keeps whatever the last call left. Calls whose device work
+ * overlaps (on different streams, or from different host threads onto different
+ * streams) race on the array; calls on one stream run one after another and do not.
+ * The call allocates no device memory (no cudaMalloc / cudaFree, no allocating library
+ * routine). The first call on a device does set-up: it looks up the array's device
+ * address (with that device current) and creates the two copy streams and seven events
+ * that q8_linear_host keeps per device; make that first call before any stream capture.
+ *
+ * Arguments as q8_linear_host. chunk_rows = 0 picks the largest slice whose two
+ * workspace slots fit the array (whole 256-row tiles when one fits). Errors: as
+ * q8_linear_host; Q8_ERR_UNSUPPORTED when q8_linear_host_workspace(M, N, K, chunk_rows)
+ * (or, for chunk_rows = 0, that of a one-row slice) exceeds the array.
+ */
+size_t q8_linear_host_static_limit(void);
+q8_status q8_linear_host_static(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
+                                const float* s_w, q8_granularity gw, const int32_t* colsum, int64_t N,
+                                float* y_host, int64_t chunk_rows, q8_stream_t stream);
+
+/*
  * Diagnostic export of the raw INT32 accumulators acc[m][n] (no epilogue),
  * computed by the same main loop as q8_gemm_dequant_ex with the same kernel
  * choice. Used to check the integer GEMM bit for bit.

@@ -178,3 +178,66 @@ extern "C" q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q
     if (st == Q8_OK && e2 != cudaSuccess) st = status_of(e2);
     return st;
 }
+
+// ------------------------------------------------------------------------------------------
+// q8_linear_host_static: q8_linear_host with its workspace in a fixed device array of this
+// library instead of caller memory, for callers that must not allocate device memory
+// themselves (see include/q8.h). The array is kStaticScratchBytes on every device that loads
+// the library, held until the process exits, and shared by all calls.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)64 << 20;   // 64 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch per device (host code only sees a stand-in for it).
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+q8_status static_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q8_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return Q8_ERR_CUDA;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return Q8_OK;
+}
+
+}  // namespace
+
+extern "C" size_t q8_linear_host_static_limit(void) { return kStaticScratchBytes; }
+
+extern "C" q8_status q8_linear_host_static(const float* a_host, int64_t M, int64_t K, q8_symmetry sym,
+                                           const int8_t* qw, const float* s_w, q8_granularity gw,
+                                           const int32_t* colsum, int64_t N, float* y_host, int64_t chunk_rows,
+                                           q8_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || chunk_rows < 0) return Q8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return Q8_OK;
+    int64_t R = chunk_rows;
+    if (R == 0) {
+        // the largest slice whose two workspace slots fit in the array (whole 256-row tiles when
+        // at least one tile fits)
+        if (q8_linear_host_workspace(M, N, K, 1) > kStaticScratchBytes) return Q8_ERR_UNSUPPORTED;
+        int64_t lo = 1, hi = M;
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo + 1) / 2;
+            if (q8_linear_host_workspace(M, N, K, mid) <= kStaticScratchBytes) lo = mid;
+            else hi = mid - 1;
+        }
+        R = lo >= 256 ? lo / 256 * 256 : lo;
+    } else if (q8_linear_host_workspace(M, N, K, R) > kStaticScratchBytes) {
+        return Q8_ERR_UNSUPPORTED;
+    }
+    void* scratch = nullptr;
+    const q8_status st = static_scratch(&scratch);
+    if (st != Q8_OK) return st;
+    return q8_linear_host(a_host, M, K, sym, qw, s_w, gw, colsum, N, y_host, R, scratch, kStaticScratchBytes,
+                          stream);
+}
