@@ -397,18 +397,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------------------------------
 // Block-scaled int8 weights (one E8M0 scale per row and group of G = 32 or 128 K), M <= 16.
-// The same stream as the int8 kernel (64-row tiles, 256-K stages, sixteen compute warps each
-// owning one 16-wide K-step of every stage) plus, per stage, the tile's two scale words of the
-// stage's K (64 rows x 8 bytes by TMA, the 4-byte words viewed as a byte matrix [words, 4 N]).
+// The int8 stream design (64-row tiles, sixteen compute warps) with 512-K stages: warp ks owns
+// the 32 K [32 ks, 32 ks + 32) of every stage, one group for G = 32 (inside one for G = 128),
+// so each row's scale is read and converted once per stage; a lane's 8-byte load of a row
+// (K 32 ks + 8 t .. + 8) feeds two MMA K-steps (bytes 0-3, then 4-7), and the tokens take the
+// same K order. Per stage the TMA also brings the tile's four scale words of the stage's K
+// (64 rows x 16 bytes, the 4-byte words viewed as a byte matrix [words, 4 N]).
 // A weight fragment enters the MMA as the fp16 values q * s (exact: the codes are exact in
-// fp16 and s = 2^(e - 127) scales them without rounding for e = 103 .. 136); the four codes of
-// a fragment lie in one 16-K step, hence in one group. The MMA sums the exact products in fp32
-// over the tile, so the result is not bit-reproducible against an exactly rounded sum. At the
-// tile's end the sixteen per-warp partials are added in a fixed order (warp w + 8 onto warp w
-// in shared memory, then the eight sums in warp order), so every run gives the same bits.
-constexpr int kMxS8 = 8;                          // stages in the ring
-constexpr int kMxSf = RW * 2 * 4;                 // scale bytes per stage: 64 rows x 2 words
-constexpr int kMxStage = RW * BK + NT * BK;       // 16 KB of weights + 4 KB of tokens
+// fp16 and s = 2^(e - 127) scales them without rounding for e = 103 .. 136). The MMA sums the
+// exact products in fp32 over the tile, so the result is not bit-reproducible against an
+// exactly rounded sum. At the tile's end the sixteen per-warp partials are added in a fixed
+// order (warp w + 8 onto warp w in shared memory, then the eight sums in warp order), so every
+// run gives the same bits.
+constexpr int kMxBK = 512;                        // K per stage
+constexpr int kMxS8 = 4;                          // stages in the ring
+constexpr int kMxSf = RW * 4 * 4;                 // scale bytes per stage: 64 rows x 4 words
+constexpr int kMxStage = RW * kMxBK + NT * kMxBK; // 32 KB of weights + 8 KB of tokens
 constexpr int kMxOffSf = kMxS8 * kMxStage;
 constexpr int kMxOffRed = kMxOffSf + kMxS8 * kMxSf;
 constexpr int kMxRedBytes = 8 * NT * RWP * 4;     // fp32 [8 warps][16 tokens][72 (64 rows)]
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     const int tiles = (N + RW - 1) / RW;
-    const int KB = (K + BK - 1) / BK;
+    const int KB = (K + kMxBK - 1) / kMxBK;
     const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total_g = my_tiles * KB;
     const int k_rot = (int)(((long long)blockIdx.x * KB) / gridDim.x);
@@ -465,33 +469,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
                                &g_gemv_mma_error))
                     break;
-                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
+                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kMxBK;
                 const uint32_t dst = sbase + s * kMxStage;
                 mbar_expect_tx(bar_full + 8 * s, kMxStage + kMxSf);
 #pragma unroll
-                for (int b = 0; b < 2; ++b)   // W: 64 rows x 128 K per box
+                for (int b = 0; b < kMxBK / BKH; ++b)   // W: 64 rows x 128 K per box
                     tma_load_2d(dst + b * (RW * BKH), &tmap_w, kx + b * BKH, n0, bar_full + 8 * s);
 #pragma unroll
-                for (int b = 0; b < 2; ++b)   // A: 16 tokens x 128 K per box
-                    tma_load_2d(dst + RW * BK + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
-                // scales: words kx / 4G and the next one, bytes [4 n0, 4 n0 + 256) of each
+                for (int b = 0; b < kMxBK / BKH; ++b)   // A: 16 tokens x 128 K per box
+                    tma_load_2d(dst + RW * kMxBK + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
+                // scales: words kx / 4G .. + 3, bytes [4 n0, 4 n0 + 256) of each
                 tma_load_2d(sbase + kMxOffSf + s * kMxSf, &tmap_sf, 4 * n0, kx >> wshift, bar_full + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
     } else {
         // ---------------------------------------------------------------- compute warps
-        const int ks = warp - 1;          // K-step of each stage: K [16 ks, 16 ks + 16)
+        const int ks = warp - 1;          // K of each stage: [32 ks, 32 ks + 32)
         const int ct = threadIdx.x - 32;  // 0 .. 511
         const int g8 = lane >> 2, t = lane & 3;
-        const int half = ks >> 3, kc = ks & 7;
-        // weight row 8j + g8 and token rows g8, g8 + 8 at chunk kc of box `half` (swizzled), word t
-        const uint32_t w_base = half * (RW * BKH) + sw128(g8, kc) + 4 * t;
-        const uint32_t a_off0 = RW * BK + half * (NT * BKH) + sw128(g8, kc) + 4 * t;
-        const uint32_t a_off1 = RW * BK + half * (NT * BKH) + sw128(g8 + 8, kc) + 4 * t;
-        // scale byte of weight row r for this K-step: word (16 ks) / 4G of the stage's two, byte
-        // ((kx + 16 ks) / G) % 4; G = 32: word ks / 8, byte (ks / 2) % 4 (kx is a multiple of 256)
-        const uint32_t sf_row0 = (uint32_t)((G == 32 ? half : 0) * (RW * 4) + g8 * 4);
+        // weight row 8j + g8 and token rows g8, g8 + 8: 8 bytes at byte 8 (t & 1) of chunk
+        // 2 (ks & 3) + t / 2 of box ks / 4 (swizzled); row 8j + g8 lies 1024 j bytes past row g8
+        const int box = ks >> 2, chunk = 2 * (ks & 3) + (t >> 1);
+        const uint32_t w_base = box * (RW * BKH) + sw128(g8, chunk) + 8 * (t & 1);
+        const uint32_t a_off0 = RW * kMxBK + box * (NT * BKH) + sw128(g8, chunk) + 8 * (t & 1);
+        const uint32_t a_off1 = RW * kMxBK + box * (NT * BKH) + sw128(g8 + 8, chunk) + 8 * (t & 1);
+        // scale byte of weight row r for this warp's 32 K: G = 32: group ks of the stage's 16, word
+        // ks / 4 of the four, byte ks % 4; G = 128: group ks / 4 of the stage's 4 (kx is a multiple
+        // of 512), word 0, byte ks / 4
+        const uint32_t sf_off = (uint32_t)((G == 32 ? (ks >> 2) * (RW * 4) + (ks & 3) : (ks >> 2)) + g8 * 4);
         const int em = ct / RW, er = ct % RW;   // epilogue outputs: tokens em, em + 8 of row er
         float esa0 = 0.0f, esa1 = 0.0f;
         if (em < M) esa0 = __ldg(ep.s_a + (ep.a_per_row ? em : 0));
@@ -508,30 +514,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    kErrConvFull, &g_gemv_mma_error)))
                 break;
             const uint32_t st = sbase + s * kMxStage;
-            const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * BK;
-            const uint32_t byte = G == 32 ? (uint32_t)((ks >> 1) & 3) : (uint32_t)(((kx >> 7) + half) & 3);
-            const uint32_t sfa = sbase + kMxOffSf + s * kMxSf + sf_row0 + byte;
-            uint32_t wq[8], ev[8];
+            const uint32_t sfa = sbase + kMxOffSf + s * kMxSf + sf_off;
+            uint2 wq[8];
+            uint32_t h[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) wq[j] = lds32(st + w_base + 1024 * j);
+            for (int j = 0; j < 8; ++j) wq[j] = lds64(st + w_base + 1024 * j);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ev[j] = lds8(sfa + 32 * j);   // row 8j + g8
-            const uint32_t aq0 = lds32(st + a_off0);
-            const uint32_t aq1 = lds32(st + a_off1);
+            for (int j = 0; j < 8; ++j) h[j] = lds8(sfa + 32 * j);   // row 8j + g8
+            const uint2 aq0 = lds64(st + a_off0);
+            const uint2 aq1 = lds64(st + a_off1);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // every loaded word has been consumed
-            uint32_t a[4], b[8][2];
-            cvt_word(aq0, a[0], a[2]);     // token row g8:   k pair (2t,2t+1) and (8+2t,9+2t)
-            cvt_word(aq1, a[1], a[3]);     // token row g8+8
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {  // weight row 8j + g8: q exactly, then q * s (exact)
-                const uint32_t h = scale_f16x2(min(ev[j], 136u));
-                cvt_word(wq[j], b[j][0], b[j][1]);
-                b[j][0] = hmul2(b[j][0], h);
-                b[j][1] = hmul2(b[j][1], h);
+            for (int j = 0; j < 8; ++j) h[j] = scale_f16x2(min(h[j], 136u));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {  // K-step u: bytes 4u .. 4u + 3 of every 8-byte load
+                uint32_t a[4], b[8][2];
+                cvt_word(u ? aq0.y : aq0.x, a[0], a[2]);     // token row g8
+                cvt_word(u ? aq1.y : aq1.x, a[1], a[3]);     // token row g8 + 8
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // weight row 8j + g8: q exactly, then q * s (exact)
+                    cvt_word(u ? wq[j].y : wq[j].x, b[j][0], b[j][1]);
+                    b[j][0] = hmul2(b[j][0], h[j]);
+                    b[j][1] = hmul2(b[j][1], h[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mma_m16n8k16(part[j], a, b[j][0], b[j][1]);
             if (kb == KB - 1) {
                 // Tile end: warps 0-7 write their partials, warps 8-15 add theirs onto warp
                 // ks - 8's, then every thread sums the eight slots of its two outputs in order.
@@ -636,7 +645,7 @@ bool gemv_mx_supports(int64_t M, int64_t N, int64_t K, int G, const void* sf) {
           K % G == 0 && N % 4 == 0 && (reinterpret_cast<uintptr_t>(sf) & 15) == 0))
         return false;
     const int64_t tiles = (N + RW - 1) / RW;
-    const int64_t kb = (K + BK - 1) / BK;
+    const int64_t kb = (K + kMxBK - 1) / kMxBK;
     return tiles * kb < (1LL << 31);
 }
 
@@ -646,7 +655,7 @@ cudaError_t launch_gemv_mx(const int8_t* qa, const int8_t* qw, const uint32_t* s
     const int64_t words = (K / G + 3) / 4;
     CUtensorMap mw, ma, ms;
     if (!make_tma_map_i8(&mw, qw, N, K, RW, BKH, true) || !make_tma_map_i8(&ma, qa, M, K, NT, BKH, true) ||
-        !make_tma_map_i8(&ms, reinterpret_cast<const int8_t*>(sf), words, 4 * N, 2, RW * 4))
+        !make_tma_map_i8(&ms, reinterpret_cast<const int8_t*>(sf), words, 4 * N, 4, RW * 4))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemv_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
     if (e != cudaSuccess) return e;
