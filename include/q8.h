@@ -19,7 +19,8 @@
  *  - All array arguments are DEVICE pointers (memory the caller allocated on
  *    the current CUDA device) unless stated otherwise. The caller owns every
  *    buffer; the library keeps no pointer after a call returns and allocates
- *    no device memory.
+ *    no device memory (the fixed array behind q8_linear_host_static is part of
+ *    the loaded library, not an allocation).
  *  - Matrices are row-major and dense. A is [M, K]; the weight is stored
  *    K-major as W[N, K] (row n holds output channel n), the (N, K) layout of
  *    "Write Int8 Quantized Kernel" (Common failure modes); y is [M, N].
