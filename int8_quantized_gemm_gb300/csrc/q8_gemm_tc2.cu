@@ -328,8 +328,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const bool slow = __any_sync(0xffffffffu, big);
 #pragma unroll
                     for (int jw = 0; jw < 2; ++jw) {
-                        const bool hi = ev[jw] > 132u;
-                        mg[jw] = (((ev[jw] - (hi ? 106u : 102u)) << 10) | 0x80u) * 0x10001u;
+                        // ((e - 102) << 10 | 0x80) in both halves is e * 0x04000400 - 0x97819780 (mod 2^32,
+                        // no carry between the halves); e > 132: (e - 106), 0x10001000 less
+                        mg[jw] = ev[jw] * 0x04000400u - (ev[jw] > 132u ? 0xA781A780u : 0x97819780u);
                     }
 #pragma unroll
                     for (int j = 0; j < NJ; ++j) {

@@ -99,3 +99,18 @@ def test_too_small_workspace_is_rejected_before_anything_runs(q8):
         q8.q8_linear_host(a, qw, s_w, None, y, workspace=small)
     torch.cuda.synchronize()
     assert float(y.min()) == 3.0
+
+
+def test_full_size_host_layer_as_the_bench_times_it(q8):
+    # the prefill16k layer (8192 x 16384 tokens, 8192 channels) with the default slicing that
+    # bench.py's e2e figure uses: bit-identical to the device path on every output
+    wl = workloads.WORKLOADS["prefill16k"]
+    a = torch.from_numpy(workloads.make_activations(wl))
+    w = torch.from_numpy(workloads.make_weights(wl)).cuda()
+    qw, s_w = q8.q8_quantize_weight(w, per_row=True)
+    del w
+    y = q8.q8_linear_host(pinned(a), qw, s_w, None)
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    ref = device_layer(q8, a, qw, s_w, None, True)
+    np.testing.assert_array_equal(y.numpy().view(np.int32), ref.numpy().view(np.int32))
