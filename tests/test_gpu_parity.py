@@ -337,3 +337,22 @@ def test_full_size_worst_case_codes(q8):
     assert_no_device_error(q8)
     assert torch.all(acc == wl.K * 16256).item()
     assert wl.K * 16256 == 266338304
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05_pair", "tcgen05", "mma_s8"])
+def test_prefill_kernels_at_the_largest_k(q8, kernel):
+    """K = 131056, the largest symmetric K the API takes: -128 * -128 on every k brings the INT32
+    accumulator to 16384 * 131056 = 2^31 - 2^18 through 128 exact fp32 chunks (tensor-core
+    kernels); other rows mix in +127 and random codes."""
+    M, N, K = 130, 260, 131056
+    rng = np.random.default_rng(11)
+    qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-128, 128, (N, K), dtype=np.int8)
+    qa[0] = -128
+    qw[0] = -128
+    qw[1] = 127
+    acc = host(q8.q8_gemm_s32(dev(qa), dev(qw), kernel=kernel)).astype(np.int64)
+    assert_no_device_error(q8)
+    want = oracle.gemm_acc(qa, qw, threads=8)
+    assert want[0, 0] == 16384 * K and want[0, 1] == -128 * 127 * K
+    np.testing.assert_array_equal(acc, want)
