@@ -1,0 +1,89 @@
+"""Seeded random ragged shapes through every GEMM kernel that takes them.
+
+Integer results (int8 and int4 weights) are compared with the oracle's int64 GEMM bit for
+bit; block-scaled results use codes in [-3, 3] and exponents within four binades of a row
+base, where every partial sum is exact in fp32, so they too must match the oracle's exactly
+rounded sum bit for bit. A kernel that does not take a shape rejects it (Q8Error) and is
+skipped for that shape; every shape runs on at least the CTA-pair kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+INT8_KERNELS = ("tcgen05_pair", "tcgen05", "mma_s8", "skinny", "decode", "decode_tc")
+
+
+@pytest.fixture(scope="module")
+def q8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import int8_quantized_gemm_gb300 as q8mod
+    from int8_quantized_gemm_gb300 import build
+    build.build()
+    q8mod.load()
+    return q8mod
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def shapes(seed, count):
+    rng = np.random.default_rng(seed)
+    for _ in range(count):
+        M = int(rng.choice([1, 2, 7, 15, 16, 17, 33, 64, 100, 255, 256, 257, 300, 513]))
+        N = int(rng.integers(1, 700))
+        K = int(rng.integers(1, 200)) * 32
+        yield rng, M, N, K
+
+
+def run_kernels(q8, fn, kernels):
+    """{kernel: result} for the kernels that take the shape."""
+    out = {}
+    for k in kernels:
+        try:
+            out[k] = fn(k)
+        except q8.Q8Error:
+            continue
+        assert q8.q8_device_error() == 0
+    assert "tcgen05_pair" in out
+    return out
+
+
+@pytest.mark.parametrize("seed", [101, 202])
+def test_random_shapes_int8_and_int4_weights(q8, seed):
+    for rng, M, N, K in shapes(seed, 20):
+        qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+        qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+        want = oracle.gemm_acc(qa, qw, threads=8)
+        got = run_kernels(q8, lambda k: q8.q8_gemm_s32(dev(qa), dev(qw), kernel=k).cpu().numpy(), INT8_KERNELS)
+        for k, acc in got.items():
+            np.testing.assert_array_equal(acc.astype(np.int64), want, err_msg=f"int8 {k} {M}x{N}x{K}")
+        q4 = rng.integers(-8, 8, (N, K), dtype=np.int8)
+        want4 = oracle.gemm_acc(qa, q4, threads=8)
+        packed = dev(oracle.pack_int4(q4))
+        got4 = run_kernels(q8, lambda k: q8.q8_gemm_w4a8_s32(dev(qa), packed, kernel=k).cpu().numpy(),
+                           ("tcgen05_pair", "decode"))
+        for k, acc in got4.items():
+            np.testing.assert_array_equal(acc.astype(np.int64), want4, err_msg=f"int4 {k} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("seed", [303])
+def test_random_shapes_block_scaled_weights(q8, seed):
+    for rng, M, N, K in shapes(seed, 20):
+        G = 32 if K % 128 else int(rng.choice([32, 128]))
+        qa = rng.integers(-3, 4, (M, K), dtype=np.int8)
+        q = rng.integers(-3, 4, (N, K), dtype=np.int8)
+        e = rng.integers(103, 133, (N, 1)) + rng.integers(0, 4, (N, K // G))
+        sf = np.zeros(((K // G + 3) // 4, N), np.uint32)
+        for g in range(K // G):
+            sf[g // 4] |= e[:, g].astype(np.uint32) << np.uint32(8 * (g % 4))
+        t_ref, _ = oracle.gemm_mx(qa, q, sf, G, threads=8)
+        ones = dev(np.ones(M, np.float32))
+        got = run_kernels(q8, lambda k: q8.q8_gemm_mx(dev(qa), ones, dev(q), dev(sf.view(np.int32)), G,
+                                                       kernel=k).cpu().numpy(), ("tcgen05_pair", "decode"))
+        for k, t in got.items():
+            np.testing.assert_array_equal(t.view(np.int32), t_ref.view(np.int32), err_msg=f"mx {k} G{G} {M}x{N}x{K}")
