@@ -122,7 +122,8 @@ __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, 
 template <int WF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, Epilogue ep) {
+                    const __grid_constant__ CUtensorMap tmap_out, int tma_out, int M, int N, int K, int ksplit,
+                    Epilogue ep) {
     using C = PairCfg<WF>;
     constexpr bool W4 = WF == kWInt4, MX = WF == kWMx;
     constexpr int S8 = C::S8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
@@ -176,9 +177,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tg.num_n = (N + BN - 1) / BN;
     tg.tiles = tg.num_m * tg.num_n;
     const int cluster = (int)(blockIdx.x >> 1), nclusters = (int)(gridDim.x >> 1);
-    const int KB = (K + BK - 1) / BK;
+    // Work units: (tile, K slice) for ksplit slices of KB k-blocks each (the host makes the K-blocks
+    // divide evenly); unit u is slice u % ksplit of tile u / ksplit. With ksplit > 1 the INT32
+    // partial sums are added into ep.out_i32 (zeroed by the host) by TMA reduce-add.
+    const int KB = (K + BK - 1) / BK / ksplit;
     const int CPT = (KB + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
-    const int my_tiles = cluster < tg.tiles ? (tg.tiles - 1 - cluster) / nclusters + 1 : 0;
+    const int units = tg.tiles * ksplit;
+    const int my_tiles = cluster < units ? (units - 1 - cluster) / nclusters + 1 : 0;
     const int total_g = my_tiles * KB;
 
     if (warp < 2 + kConvWarps) {
@@ -186,17 +191,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int i = 0, kb = 0, m0 = 0, n0 = 0;
+            int i = 0, kb = 0, m0 = 0, n0 = 0, k0 = 0;
             for (int g = 0; g < total_g; ++g) {
-                if (kb == 0) pair_coords(tg, cluster + i * nclusters, m0, n0);
+                if (kb == 0) {
+                    const int u = cluster + i * nclusters;
+                    pair_coords(tg, u / ksplit, m0, n0);
+                    k0 = (u % ksplit) * KB;   // the unit's first k-block
+                }
                 const int s = g % S8;
                 if (!mbar_wait(bar_empty8 + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
                                &g_tc2_error))
                     break;
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
                 mbar_expect_tx(bar_full8 + 8 * s, kStage8);
-                tma_load_2d(dst, &tmap_a, kb * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
-                tma_load_2d(dst + kA8, &tmap_w, W4 ? kb * (BK / 2) : kb * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                const int kx = k0 + kb;
+                tma_load_2d(dst, &tmap_a, kx * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
+                tma_load_2d(dst + kA8, &tmap_w, W4 ? kx * (BK / 2) : kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
@@ -273,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if constexpr (MX) {
                     if (pf_kb == 0) {   // a new tile: its weight rows
                         int pm0, pn0;
-                        pair_coords(tg, cluster + pf_i * nclusters, pm0, pn0);
+                        pair_coords(tg, (cluster + pf_i * nclusters) / ksplit, pm0, pn0);   // MX: ksplit 1
 #pragma unroll
                         for (int jw = 0; jw < 2; ++jw) {
                             const int j = jw == 1 ? 2 : (ct < 64 ? 3 : 1);
@@ -487,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (cc != CPT - 1) continue;
                 int m0, n0;
-                pair_coords(tg, cluster + ti * nclusters, m0, n0);
+                pair_coords(tg, (cluster + ti * nclusters) / ksplit, m0, n0);
                 const int mrow0 = m0 + (int)rank * BMH + quarter * 32;
                 const int m = mrow0 + lane;
                 const int nb = n0 + chalf * 128;
@@ -579,6 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
+                                if (ksplit > 1)
+                                tma_reduce_add_2d(&tmap_out, ebuf, nb + j * BCOLS, mrow0);
+                            else
                                 tma_store_2d(&tmap_out, ebuf, nb + j * BCOLS, mrow0);
                                 bulk_commit();
                             }
@@ -665,9 +678,31 @@ static int resident_pairs() {
     return pairs;
 }
 
+// The dequantization epilogue over INT32 sums that the K-split kernel left in y's storage,
+// in place: y = fl(fl((float)(acc - z_a colsum) * fl(s_a s_w)) + bias), the fused epilogue's
+// arithmetic. N % 4 == 0 (4 outputs per thread step).
+__global__ void __launch_bounds__(256) splitk_epilogue_kernel(Epilogue ep, int64_t M, int64_t N) {
+    const int64_t total4 = M * N / 4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total4; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t idx = 4 * i, m = idx / N, n = idx - m * N;
+        const int4 acc = *reinterpret_cast<const int4*>(ep.y + idx);
+        const float sa = ep.s_a[ep.a_per_row ? m : 0];
+        const int za = ep.z_a ? ep.z_a[ep.a_per_row ? m : 0] : 0;
+        const int a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        float o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float sw = ep.s_w[ep.w_per_row ? n + q : 0];
+            const int cs = ep.z_a ? ep.colsum[n + q] : 0;
+            o[q] = epi_bias(ep, __fmul_rn(__int2float_rn(a4[q] - za * cs), __fmul_rn(sa, sw)), n + q);
+        }
+        *reinterpret_cast<float4*>(ep.y + idx) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 template <int WF>
 static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
-                                     const Epilogue& ep, cudaStream_t stream) {
+                                     const Epilogue& ep, cudaStream_t stream, int ksplit) {
     using C = PairCfg<WF>;
     constexpr bool W4 = C::W4;
     CUtensorMap ma, mw;
@@ -677,17 +712,59 @@ static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * ksplit;
     const int64_t pairs = resident_pairs<WF>();
-    const int clusters = (int)(tiles < pairs ? tiles : pairs);
+    const int clusters = (int)(units < pairs ? units : pairs);
     CUtensorMap mo;
     const bool tma_out = ep.out_i32                  ? make_tma_map_out(&mo, ep.out_i32, kMapI32, M, N)
                          : ep.out_kind == kOutF32  ? make_tma_map_out(&mo, ep.y, kMapF32, M, N)
                          : ep.out_kind == kOutBF16 ? make_tma_map_out(&mo, ep.out_bf16, kMapBF16, M, N)
                                                    : make_tma_map_out(&mo, ep.out_i8, kMapI8, M, N);
-    if (!tma_out) memset(&mo, 0, sizeof(mo));
+    if (!tma_out) {
+        if (ksplit > 1) return cudaErrorInvalidValue;   // partial sums are added by TMA only
+        memset(&mo, 0, sizeof(mo));
+    }
     gemm_tc2_kernel<WF><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, tma_out ? 1 : 0, (int)M, (int)N,
-                                                                      (int)K, ep);
+                                                                      (int)K, ksplit, ep);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Slices of K for grids that would leave most clusters idle: the largest of 2, 4, 8 that keeps
+// the (tile, slice) units within one wave of resident clusters, divides the k-blocks evenly and
+// leaves each slice at least 8 k-blocks (512 K). Only where the INT32 sums have 4-byte room to
+// be added in: the INT32 export, or fp32 output (the sums go into y, then the epilogue runs in
+// place); rows of whole 16-byte multiples (N % 4 == 0) for the TMA reduce-add.
+template <int WF>
+static int pick_ksplit(int64_t M, int64_t N, int64_t K, const Epilogue& ep) {
+    const bool i32 = ep.out_i32 != nullptr;
+    if (!i32 && !(ep.out_kind == kOutF32 && ep.y)) return 1;
+    const void* target = i32 ? static_cast<const void*>(ep.out_i32) : static_cast<const void*>(ep.y);
+    if (N % 4 != 0 || (reinterpret_cast<uintptr_t>(target) & 15) != 0) return 1;
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t kb = (K + BK - 1) / BK;
+    const int64_t pairs = resident_pairs<WF>();
+    int best = 1;
+    for (int sl = 2; sl <= 8; sl *= 2)
+        if (tiles * sl <= pairs && kb % sl == 0 && kb / sl >= 8) best = sl;
+    return best;
+}
+
+template <int WF>
+static cudaError_t launch_gemm_tc2_split(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
+                                         const Epilogue& ep, cudaStream_t stream) {
+    const int ksplit = pick_ksplit<WF>(M, N, K, ep);
+    if (ksplit == 1) return launch_gemm_tc2_t<WF>(qa, qw, M, N, K, ep, stream, 1);
+    Epilogue ek = ep;   // the kernel adds INT32 sums into the output's storage
+    if (!ek.out_i32) ek.out_i32 = reinterpret_cast<int32_t*>(ep.y);
+    cudaError_t e = cudaMemsetAsync(ek.out_i32, 0, (size_t)M * (size_t)N * 4, stream);
+    if (e == cudaSuccess) e = launch_gemm_tc2_t<WF>(qa, qw, M, N, K, ek, stream, ksplit);
+    if (e != cudaSuccess || ep.out_i32) return e;
+    const int64_t total4 = M * N / 4;
+    int64_t blocks = (total4 + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    splitk_epilogue_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ep, M, N);
     note_launch();
     return cudaGetLastError();
 }
@@ -698,10 +775,10 @@ cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t
     if (wfmt == kWMx) {
         if (!ep.mx_sf || (ep.mx_group != 32 && ep.mx_group != 128) || K % ep.mx_group != 0 || ep.out_i32 || ep.z_a)
             return cudaErrorInvalidValue;
-        return launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream);
+        return launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream, 1);
     }
-    return wfmt == kWInt4 ? launch_gemm_tc2_t<kWInt4>(qa, qw, M, N, K, ep, stream)
-                          : launch_gemm_tc2_t<kWInt8>(qa, qw, M, N, K, ep, stream);
+    return wfmt == kWInt4 ? launch_gemm_tc2_split<kWInt4>(qa, qw, M, N, K, ep, stream)
+                          : launch_gemm_tc2_split<kWInt8>(qa, qw, M, N, K, ep, stream);
 }
 
 cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code) {

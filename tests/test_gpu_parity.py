@@ -356,3 +356,36 @@ def test_prefill_kernels_at_the_largest_k(q8, kernel):
     want = oracle.gemm_acc(qa, qw, threads=8)
     assert want[0, 0] == 16384 * K and want[0, 1] == -128 * 127 * K
     np.testing.assert_array_equal(acc, want)
+
+
+# Shapes whose pair-kernel grid would leave most clusters idle: the kernel then splits K into
+# 2, 4 or 8 slices whose INT32 partial sums are added by TMA reduce-add (into y's storage for fp32
+# output, followed by the in-place epilogue). (M, N, K, expected slices on 76 resident pairs.)
+SPLIT_CASES = [(300, 520, 4096, 8), (512, 2048, 2048, 4), (16, 1024, 8192, 8), (257, 2052, 1024, 2)]
+
+
+@pytest.mark.parametrize("M,N,K,_slices", SPLIT_CASES)
+def test_k_split_pair_kernel_is_exact(q8, M, N, K, _slices):
+    rng = np.random.default_rng(M + N + K)
+    qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    want = oracle.gemm_acc(qa, qw, threads=8)
+    acc = host(q8.q8_gemm_s32(dev(qa), dev(qw), kernel="tcgen05_pair")).astype(np.int64)
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(acc, want)
+    # the fp32 layer with asymmetric activations (zero points, column sums), and with a bias
+    sa = (rng.random(M, dtype=np.float32) + np.float32(0.5)) * np.float32(1e-2)
+    sw = (rng.random(N, dtype=np.float32) + np.float32(0.5)) * np.float32(1e-2)
+    za = rng.integers(-128, 128, M, dtype=np.int32)
+    cs = q8.q8_colsum(dev(qw))
+    y = host(q8.q8_gemm_dequant(dev(qa), dev(sa), dev(za), dev(qw), dev(sw), cs, kernel="tcgen05_pair"))
+    assert_no_device_error(q8)
+    y_ref, st = oracle.linear_codes(qa, sa, za, qw, sw, True, True, threads=8)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(y.view(np.int32), y_ref.view(np.int32))
+    bias = rng.standard_normal(N, dtype=np.float32)
+    yb = host(q8.q8_gemm_epilogue(dev(qa), dev(sa), dev(za), dev(qw), dev(sw), cs, bias=dev(bias),
+                                  kernel="tcgen05_pair"))
+    assert_no_device_error(q8)
+    yb_ref, st = oracle.linear_codes_bias(qa, sa, za, qw, sw, bias, True, True, threads=8)
+    np.testing.assert_array_equal(yb.view(np.int32), yb_ref.view(np.int32))
