@@ -314,8 +314,8 @@ q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t 
 q8_gemm_kernel q8_gemm_pick(int64_t M, int64_t N, int64_t K) {
     if (q8::gemv_mma_supports(M, N, K)) return Q8_GEMM_DECODE;
     if (M >= 1 && N >= 1) {
-        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        if ((M <= 64 && N * K <= (int64_t(1) << 25)) || (M <= 512 && pair_tiles <= 8)) return Q8_GEMM_SKINNY;
+        // measured with the pair kernel's K split: the mma.sync kernel wins only on small layers
+        if (M <= 128 && N * K <= (int64_t(1) << 22)) return Q8_GEMM_SKINNY;
     }
     if (q8::gemm_tc2_supports(M, N, K)) return Q8_GEMM_TCGEN05_PAIR;
     if (q8::gemm_tc_supports(M, N, K)) return Q8_GEMM_TCGEN05;

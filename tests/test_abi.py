@@ -162,8 +162,9 @@ def test_kernel_pick_is_a_concrete_kernel(lib):
     assert q8.q8_gemm_pick(16, 28672, 8192) == "decode"
     assert q8.q8_gemm_pick(8192, 8192, 16384) == "tcgen05_pair"
     assert q8.q8_gemm_pick(2048, 4096, 4096) == "tcgen05_pair"
-    assert q8.q8_gemm_pick(17, 4096, 4096) == "skinny"
-    assert q8.q8_gemm_pick(300, 1000, 1024) == "skinny"
+    assert q8.q8_gemm_pick(17, 4096, 4096) == "tcgen05_pair"
+    assert q8.q8_gemm_pick(300, 1000, 1024) == "tcgen05_pair"
+    assert q8.q8_gemm_pick(100, 2048, 2048) == "skinny"
 
 
 def test_binding_refuses_cpu_tensors():
