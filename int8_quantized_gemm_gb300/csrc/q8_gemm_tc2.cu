@@ -22,6 +22,14 @@
 //   both CTAs   warp 1       allocates / frees TMEM collectively with the peer
 // setmaxnreg: 72 registers for warpgroups 0-1, 184 for the drain warpgroups.
 // Waits on mbarriers are bounded (device error word + abort flag).
+//
+// Weight formats: int8 codes (above), packed int4 codes (same roles; 16384-K exact chunks)
+// and block-scaled int8 codes (each weight enters the MMA as the exact fp16 value q * s, the
+// accumulator runs in fp32 over the whole K and is drained once per tile: warps 2..11
+// convert, warps 12..15 drain, each taking its 256 columns in two halves).
+// K split: for grids that fill at most half of the resident clusters the host splits K into
+// slices; each (tile, slice) unit adds its INT32 partial sums into the output's storage by
+// TMA reduce-add, and the host runs the dequantization epilogue in place afterwards.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
