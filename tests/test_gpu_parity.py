@@ -389,3 +389,26 @@ def test_k_split_pair_kernel_is_exact(q8, M, N, K, _slices):
     assert_no_device_error(q8)
     yb_ref, st = oracle.linear_codes_bias(qa, sa, za, qw, sw, bias, True, True, threads=8)
     np.testing.assert_array_equal(yb.view(np.int32), yb_ref.view(np.int32))
+
+
+@pytest.mark.parametrize("apr,wpr", [(False, False), (True, False), (False, True)])
+def test_k_split_with_per_tensor_scales_and_int4_weights(q8, apr, wpr):
+    # 512 x 2048 x 2048 splits K in 4 on the pair kernel: per-tensor activation and weight scales
+    # through the in-place epilogue, and the same split with packed int4 weights
+    M, N, K = 512, 2048, 2048
+    rng = np.random.default_rng(17 + 2 * apr + wpr)
+    qa = rng.integers(-128, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    sa = (rng.random(M if apr else 1, dtype=np.float32) + np.float32(0.5)) * np.float32(1e-2)
+    sw = (rng.random(N if wpr else 1, dtype=np.float32) + np.float32(0.5)) * np.float32(1e-2)
+    za = rng.integers(-128, 128, M if apr else 1, dtype=np.int32)
+    y = host(q8.q8_gemm_dequant(dev(qa), dev(sa), dev(za), dev(qw), dev(sw), q8.q8_colsum(dev(qw)),
+                                kernel="tcgen05_pair"))
+    assert_no_device_error(q8)
+    y_ref, st = oracle.linear_codes(qa, sa, za, qw, sw, apr, wpr, threads=8)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(y.view(np.int32), y_ref.view(np.int32))
+    q4 = rng.integers(-8, 8, (N, K), dtype=np.int8)
+    acc4 = host(q8.q8_gemm_w4a8_s32(dev(qa), dev(oracle.pack_int4(q4)), kernel="tcgen05_pair")).astype(np.int64)
+    assert_no_device_error(q8)
+    np.testing.assert_array_equal(acc4, oracle.gemm_acc(qa, q4, threads=8))
