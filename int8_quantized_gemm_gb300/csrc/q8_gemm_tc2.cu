@@ -818,9 +818,7 @@ static void plan_split(int64_t M, int64_t N, int64_t K, const Epilogue& ep, int&
     if (N % 4 != 0 || (reinterpret_cast<uintptr_t>(target) & 15) != 0) return;
     const int64_t kb = (K + BK - 1) / BK;
     const int64_t pairs = resident_pairs<WF>();
-    // (the last-wave slicing measured 9 us slower for packed int4 weights at 8192 x 16384 x 8192,
-    // 21 us faster for int8: int4 takes the small-grid slicing only)
-    const int64_t sliced = 2 * tg.tiles <= pairs ? tg.tiles : (WF == kWInt4 ? 0 : tg.tiles % pairs);
+    const int64_t sliced = 2 * tg.tiles <= pairs ? tg.tiles : tg.tiles % pairs;
     if (sliced == 0) return;
     int best = 1;
     for (int sl = 2; sl <= 8; sl *= 2)
