@@ -96,6 +96,13 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch: the decode kernels are launched so that they may start while
+// the kernel before them on the stream (the activation quantizer) is still running. Nothing they
+// read from that kernel's outputs (token codes, token scales and zero points) is touched before
+// griddep_wait(), which returns once the preceding kernel has completed and its writes are
+// visible (at once when there is none); the weight stream starts before it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
@@ -182,24 +189,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int i = 0, kb = 0;
-            for (int g = 0; g < total_g; ++g) {
+            // The first ring's worth of stages gets its weight boxes before the wait on the
+            // quantizer, its token boxes after it (the ring is empty, so no empty-slot waits).
+            const int pre = total_g < S8 ? total_g : S8;
+            auto kx_of = [&](int kb) { return (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kBK; };
+            auto load_w = [&](int g, int kb, int i) {
                 const int n0 = ((int)blockIdx.x + i * (int)gridDim.x) * RW;
+                const int s = g % S8;
+                const int wx = W4 ? kx_of(kb) / 2 : kx_of(kb);
+                // W: boxes of 64 rows x 128 bytes (int8: 128 K; int4: 256 K packed)
+#pragma unroll
+                for (int b = 0; b < kW8 / (RW * BKH); ++b)
+                    tma_load_2d(sbase + s * kStage + b * (RW * BKH), &tmap_w, wx + b * BKH, n0, bar_full + 8 * s);
+            };
+            auto load_a = [&](int g, int kb) {
+                const int s = g % S8;
+#pragma unroll
+                for (int b = 0; b < kBK / BKH; ++b)   // A: 16 tokens x 128 K per box
+                    tma_load_2d(sbase + s * kStage + kW8 + b * (NT * BKH), &tmap_a, kx_of(kb) + b * BKH, 0,
+                                bar_full + 8 * s);
+            };
+            int i = 0, kb = 0;
+            for (int g = 0; g < pre; ++g) {
+                mbar_expect_tx(bar_full + 8 * (g % S8), kStage);
+                load_w(g, kb, i);
+                if (++kb == KB) { kb = 0; ++i; }
+            }
+            griddep_wait();
+            for (int g = 0; g < pre; ++g) load_a(g, g % KB);
+            for (int g = pre; g < total_g; ++g) {
                 const int s = g % S8;
                 if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
                                &g_gemv_mma_error))
                     break;
-                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kBK;
-                const uint32_t dst = sbase + s * kStage;
                 mbar_expect_tx(bar_full + 8 * s, kStage);
-                // W: boxes of 64 rows x 128 bytes (int8: 128 K; int4: 256 K packed)
-                const int wx = W4 ? kx / 2 : kx;
-#pragma unroll
-                for (int b = 0; b < kW8 / (RW * BKH); ++b)
-                    tma_load_2d(dst + b * (RW * BKH), &tmap_w, wx + b * BKH, n0, bar_full + 8 * s);
-#pragma unroll
-                for (int b = 0; b < kBK / BKH; ++b)   // A: 16 tokens x 128 K per box
-                    tma_load_2d(dst + kW8 + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
+                load_w(g, kb, i);
+                load_a(g, kb);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
@@ -224,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = ct; i < 2 * NT * RWP; i += 32 * kComputeWarps) red[i] = 0;
         if (ct < NT) tok_sum[ct] = 0;
         named_barrier(1, 32 * kComputeWarps);
+        griddep_wait();   // the token scales and zero points below come from the quantizer
         // Epilogue outputs of this thread: tokens em and em + 8, row er of each tile. The token
         // scales are loaded once here; the channel scales at the tile's end (loading them at the
         // tile's first stage measured slower).
@@ -462,24 +488,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int i = 0, kb = 0;
-            for (int g = 0; g < total_g; ++g) {
+            // As in the int8 kernel: the first ring's weight and scale boxes before the wait on
+            // the quantizer, its token boxes after it.
+            const int pre = total_g < S8 ? total_g : S8;
+            auto kx_of = [&](int kb) { return (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kMxBK; };
+            auto load_w = [&](int g, int kb, int i) {
                 const int n0 = ((int)blockIdx.x + i * (int)gridDim.x) * RW;
+                const int s = g % S8, kx = kx_of(kb);
+#pragma unroll
+                for (int b = 0; b < kMxBK / BKH; ++b)   // W: 64 rows x 128 K per box
+                    tma_load_2d(sbase + s * kMxStage + b * (RW * BKH), &tmap_w, kx + b * BKH, n0, bar_full + 8 * s);
+                // scales: words kx / 4G .. + 3, bytes [4 n0, 4 n0 + 256) of each
+                tma_load_2d(sbase + kMxOffSf + s * kMxSf, &tmap_sf, 4 * n0, kx >> wshift, bar_full + 8 * s);
+            };
+            auto load_a = [&](int g, int kb) {
+                const int s = g % S8, kx = kx_of(kb);
+#pragma unroll
+                for (int b = 0; b < kMxBK / BKH; ++b)   // A: 16 tokens x 128 K per box
+                    tma_load_2d(sbase + s * kMxStage + RW * kMxBK + b * (NT * BKH), &tmap_a, kx + b * BKH, 0,
+                                bar_full + 8 * s);
+            };
+            int i = 0, kb = 0;
+            for (int g = 0; g < pre; ++g) {
+                mbar_expect_tx(bar_full + 8 * (g % S8), kMxStage + kMxSf);
+                load_w(g, kb, i);
+                if (++kb == KB) { kb = 0; ++i; }
+            }
+            griddep_wait();
+            for (int g = 0; g < pre; ++g) load_a(g, g % KB);
+            for (int g = pre; g < total_g; ++g) {
                 const int s = g % S8;
                 if (!mbar_wait(bar_empty + 8 * s, (uint32_t)(((g / S8) & 1) ^ 1), abort_flag, kErrProducer,
                                &g_gemv_mma_error))
                     break;
-                const int kx = (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kMxBK;
-                const uint32_t dst = sbase + s * kMxStage;
                 mbar_expect_tx(bar_full + 8 * s, kMxStage + kMxSf);
-#pragma unroll
-                for (int b = 0; b < kMxBK / BKH; ++b)   // W: 64 rows x 128 K per box
-                    tma_load_2d(dst + b * (RW * BKH), &tmap_w, kx + b * BKH, n0, bar_full + 8 * s);
-#pragma unroll
-                for (int b = 0; b < kMxBK / BKH; ++b)   // A: 16 tokens x 128 K per box
-                    tma_load_2d(dst + RW * kMxBK + b * (NT * BKH), &tmap_a, kx + b * BKH, 0, bar_full + 8 * s);
-                // scales: words kx / 4G .. + 3, bytes [4 n0, 4 n0 + 256) of each
-                tma_load_2d(sbase + kMxOffSf + s * kMxSf, &tmap_sf, 4 * n0, kx >> wshift, bar_full + 8 * s);
+                load_w(g, kb, i);
+                load_a(g, kb);
                 if (++kb == KB) { kb = 0; ++i; }
             }
         }
@@ -500,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sf_off = (uint32_t)((G == 32 ? (ks >> 2) * (RW * 4) + (ks & 3) : (ks >> 2)) + g8 * 4);
         const int em = ct / RW, er = ct % RW;   // epilogue outputs: tokens em, em + 8 of row er
         float esa0 = 0.0f, esa1 = 0.0f;
+        griddep_wait();   // the token scales come from the quantizer
         if (em < M) esa0 = __ldg(ep.s_a + (ep.a_per_row ? em : 0));
         if (em + 8 < M) esa1 = __ldg(ep.s_a + (ep.a_per_row ? em + 8 : 0));
         float part[8][4];
@@ -602,6 +647,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// Launch with programmatic stream serialization: the kernel may start before the preceding
+// kernel on the stream has finished (it waits for it with griddepcontrol.wait where needed).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 bool gemv_mma_supports(int64_t M, int64_t N, int64_t K, bool w4) {
     if (!(M >= 1 && M <= NT && N >= 1 && N < (1LL << 31) && K >= 16 && (K % (w4 ? 32 : 16)) == 0)) return false;
     if (w4) {   // int4: each warp's fp32 partial must stay exact over a tile: products 1920 at most
@@ -627,7 +690,8 @@ static cudaError_t launch_gemv_mma_t(const int8_t* qa, const void* qw, int64_t M
     const int64_t tiles = (N + RW - 1) / RW;
     const int sms = device_sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
-    gemv_mma_kernel<W4><<<grid, kThreads, C::kSmem, stream>>>(mw, ma, (int)M, (int)N, (int)K, ep);
+    e = launch_pdl(gemv_mma_kernel<W4>, grid, kThreads, C::kSmem, stream, mw, ma, (int)M, (int)N, (int)K, ep);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -662,7 +726,8 @@ cudaError_t launch_gemv_mx(const int8_t* qa, const int8_t* qw, const uint32_t* s
     const int64_t tiles = (N + RW - 1) / RW;
     const int sms = device_sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
-    gemv_mx_kernel<<<grid, kThreads, kMxSmem, stream>>>(mw, ma, ms, (int)M, (int)N, (int)K, G, ep);
+    e = launch_pdl(gemv_mx_kernel, grid, kThreads, kMxSmem, stream, mw, ma, ms, (int)M, (int)N, (int)K, G, ep);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }

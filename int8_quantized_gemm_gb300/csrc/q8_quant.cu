@@ -76,6 +76,9 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
                                                             float* __restrict__ s,
                                                             int32_t* __restrict__ z) {
     __shared__ float red[64];
+    // A decode GEMM launched after this kernel with programmatic stream serialization may start
+    // its weight stream now; it reads the codes and scales only after waiting for this grid.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int64_t row = blockIdx.x;
     const int64_t n4 = cols / 4;
     const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
