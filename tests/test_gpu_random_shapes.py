@@ -87,3 +87,20 @@ def test_random_shapes_block_scaled_weights(q8, seed):
                                                        kernel=k).cpu().numpy(), ("tcgen05_pair", "decode"))
         for k, t in got.items():
             np.testing.assert_array_equal(t.view(np.int32), t_ref.view(np.int32), err_msg=f"mx {k} G{G} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("seed", [404])
+def test_random_shapes_fp32_layer_with_the_default_kernel(q8, seed):
+    # the fp32 epilogue (asymmetric tokens, per-channel weights) on whatever kernel the pick and the
+    # K split choose for the shape, straight after the activation quantizer on the same stream
+    for rng, M, N, K in shapes(seed, 16):
+        a = rng.standard_normal((M, K), dtype=np.float32)
+        qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+        sw = (rng.random(N, dtype=np.float32) + np.float32(0.5)) * np.float32(1e-2)
+        qa, sa, za = q8.q8_quantize_act(dev(a), per_row=True, symmetric=False)
+        y = q8.q8_gemm_dequant(qa, sa, za, dev(qw), dev(sw), q8.q8_colsum(dev(qw))).cpu().numpy()
+        assert q8.q8_device_error() == 0
+        y_ref, st = oracle.linear_codes(qa.cpu().numpy(), sa.cpu().numpy(), za.cpu().numpy(), qw, sw, True, True,
+                                        threads=8)
+        assert st == oracle.OK
+        np.testing.assert_array_equal(y.view(np.int32), y_ref.view(np.int32), err_msg=f"{M}x{N}x{K}")
