@@ -30,12 +30,24 @@ __device__ __forceinline__ void asym_params(float lo, float hi, float* s, int* z
     *z = clampi(-128 - __float2int_rn(__fdiv_rn(lo, sc)), -128, 127);
 }
 
-__device__ __forceinline__ int sym_code(float x, float s) {
-    return clampi(__float2int_rn(__fdiv_rn(x, s)), -127, 127);
+// rint(RN(x / s)), the code of the IEEE quotient rounded half to even, for |x / s| <= 256, from the
+// row's reciprocal r = RN(1 / s). t = RN(x r) carries two roundings of relative size <= 2^-24 each,
+// RN(x / s) one, so |t - RN(x / s)| <= 256 (1.5 2^-23 + 2^-48) < 2^-14. Unless t lies within 2^-14
+// of a half-integer, no half-integer separates the two and they round to the same integer; near a
+// half-integer (exact ties included) the IEEE quotient itself is rounded. t - rint(t) is exact.
+__device__ __forceinline__ int rint_quot(float x, float s, float r) {
+    const float t = __fmul_rn(x, r);
+    const float k = rintf(t);
+    if (fabsf(__fsub_rn(t, k)) >= 0.5f - 0x1p-14f) return __float2int_rn(__fdiv_rn(x, s));
+    return (int)k;
 }
 
-__device__ __forceinline__ int asym_code(float x, float s, int z) {
-    return clampi(__float2int_rn(__fdiv_rn(x, s)) + z, -128, 127);
+__device__ __forceinline__ int sym_code(float x, float s, float r) {
+    return clampi(rint_quot(x, s, r), -127, 127);
+}
+
+__device__ __forceinline__ int asym_code(float x, float s, float r, int z) {
+    return clampi(rint_quot(x, s, r) + z, -128, 127);
 }
 
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
@@ -110,6 +122,7 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
         s[row] = sc;
         if (ASYM) z[row] = zp;
     }
+    const float rc = __fdiv_rn(1.0f, sc);
     uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
@@ -117,11 +130,11 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
         if (i < n4) {
             uint32_t w;
             if (ASYM)
-                w = pack4(asym_code(v[j].x, sc, zp), asym_code(v[j].y, sc, zp),
-                          asym_code(v[j].z, sc, zp), asym_code(v[j].w, sc, zp));
+                w = pack4(asym_code(v[j].x, sc, rc, zp), asym_code(v[j].y, sc, rc, zp),
+                          asym_code(v[j].z, sc, rc, zp), asym_code(v[j].w, sc, rc, zp));
             else
-                w = pack4(sym_code(v[j].x, sc), sym_code(v[j].y, sc), sym_code(v[j].z, sc),
-                          sym_code(v[j].w, sc));
+                w = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
+                          sym_code(v[j].w, sc, rc));
             qr[i] = w;
         }
     }
@@ -160,12 +173,14 @@ __global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* _
         s[row] = sc;
         if (ASYM) z[row] = zp;
     }
+    const float rc = __fdiv_rn(1.0f, sc);
     uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         float4 v = __ldcs(xr + i);
-        qr[i] = ASYM ? pack4(asym_code(v.x, sc, zp), asym_code(v.y, sc, zp), asym_code(v.z, sc, zp),
-                             asym_code(v.w, sc, zp))
-                     : pack4(sym_code(v.x, sc), sym_code(v.y, sc), sym_code(v.z, sc), sym_code(v.w, sc));
+        qr[i] = ASYM ? pack4(asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
+                             asym_code(v.w, sc, rc, zp))
+                     : pack4(sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
+                             sym_code(v.w, sc, rc));
     }
 }
 
@@ -221,15 +236,17 @@ __global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restri
                                                            const int32_t* __restrict__ z,
                                                            int8_t* __restrict__ q) {
     const float sc = s[0];
+    const float rc = __fdiv_rn(1.0f, sc);
     const int zp = ASYM ? z[0] : 0;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 v = __ldcs(x4 + i);
-        q4[i] = ASYM ? pack4(asym_code(v.x, sc, zp), asym_code(v.y, sc, zp), asym_code(v.z, sc, zp),
-                             asym_code(v.w, sc, zp))
-                     : pack4(sym_code(v.x, sc), sym_code(v.y, sc), sym_code(v.z, sc), sym_code(v.w, sc));
+        q4[i] = ASYM ? pack4(asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
+                             asym_code(v.w, sc, rc, zp))
+                     : pack4(sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
+                             sym_code(v.w, sc, rc));
     }
 }
 
@@ -352,12 +369,14 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1))
     block_max2<false>(amax, unused, red2);
     const float sc = sym_scale(amax);
     if (threadIdx.x == 0) s[row] = sc;
+    const float rc = __fdiv_rn(1.0f, sc);
     uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
         if (i < n4)
-            qr[i] = pack4(sym_code(v[j].x, sc), sym_code(v[j].y, sc), sym_code(v[j].z, sc), sym_code(v[j].w, sc));
+            qr[i] = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
+                          sym_code(v[j].w, sc, rc));
     }
 }
 
@@ -391,12 +410,13 @@ __global__ void __launch_bounds__(1024)
     block_max2<false>(amax, unused, red2);
     const float sc = sym_scale(amax);
     if (threadIdx.x == 0) s[row] = sc;
+    const float rc = __fdiv_rn(1.0f, sc);
     uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         const float4 v = __ldcs(xr + i);
         const float4 g = __ldg(g4 + i);
-        qr[i] = pack4(sym_code(norm1(v.x, rms, g.x), sc), sym_code(norm1(v.y, rms, g.y), sc),
-                      sym_code(norm1(v.z, rms, g.z), sc), sym_code(norm1(v.w, rms, g.w), sc));
+        qr[i] = pack4(sym_code(norm1(v.x, rms, g.x), sc, rc), sym_code(norm1(v.y, rms, g.y), sc, rc),
+                      sym_code(norm1(v.z, rms, g.z), sc, rc), sym_code(norm1(v.w, rms, g.w), sc, rc));
     }
 }
 

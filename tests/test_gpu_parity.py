@@ -412,3 +412,36 @@ def test_k_split_with_per_tensor_scales_and_int4_weights(q8, apr, wpr):
     acc4 = host(q8.q8_gemm_w4a8_s32(dev(qa), dev(oracle.pack_int4(q4)), kernel="tcgen05_pair")).astype(np.int64)
     assert_no_device_error(q8)
     np.testing.assert_array_equal(acc4, oracle.gemm_acc(qa, q4, threads=8))
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+@pytest.mark.parametrize("per_row", [True, False])
+def test_codes_next_to_half_integer_quotients(q8, symmetric, per_row):
+    """Values whose quotient x / s lies on a half-integer or within a few ulp of one (and farther
+    out) under random scales: the quantizer multiplies by the row's reciprocal and falls back to the
+    IEEE quotient near half-integers, so every code must still equal the oracle's (IEEE division,
+    round half to even)."""
+    rng = np.random.default_rng(99 + 2 * symmetric + per_row)
+    rows, cols = 64, 1024
+    x = np.zeros((rows, cols), np.float32)
+    offsets = np.array([0.0, 1e-7, -1e-7, 6e-6, -6e-6, 3e-5, -3e-5, 6.2e-5, -6.2e-5, 2e-4, -2e-4, 0.25],
+                       np.float64)
+    for r in range(rows):
+        amax = np.float32(np.exp(rng.uniform(np.log(1e-3), np.log(1e3))))
+        s = np.float32(amax / np.float32(127.0)) if symmetric else np.float32(amax / np.float32(255.0))
+        k = rng.integers(-126, 126, cols - 2)
+        q = (k + 0.5 + rng.choice(offsets, cols - 2)) * np.float64(s)
+        if not symmetric:
+            q = np.abs(q)                         # one-signed row: lo = 0, codes span 0 .. 255
+        x[r, 2:] = np.clip(q, -amax, amax).astype(np.float32)
+        x[r, 0] = amax
+        x[r, 1] = -amax if symmetric else 0.0
+    if symmetric:
+        qa, sa, _ = q8.q8_quantize_act(dev(x), per_row=per_row)
+        q_ref, s_ref = oracle.quantize_sym(x, per_row)
+    else:
+        qa, sa, za = q8.q8_quantize_act(dev(x), per_row=per_row, symmetric=False)
+        q_ref, s_ref, z_ref = oracle.quantize_asym(x, per_row)
+        np.testing.assert_array_equal(host(za), z_ref)
+    np.testing.assert_array_equal(host(sa), s_ref)
+    np.testing.assert_array_equal(host(qa), q_ref)
