@@ -288,6 +288,9 @@ def run_ours(args, world, rank, local):
     # ---- the same GEMM with the bias + bf16 epilogue (the pages' output side)
     epi = measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops)
 
+    # ---- the same step with the activation codes written as fp16 values (TMA-fed A operand)
+    f16a = measure_f16a(q8, a, qw, s_w, y, flush, args, hbm_peak, tc_peak, ops) if sym else None
+
     # ---- fused RMSNorm + per-token quantization of the same activations (HBM-bound)
     rmsq = measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak)
 
@@ -317,6 +320,7 @@ def run_ours(args, world, rank, local):
             "decode": decode,
             "rmsnorm_quantize": rmsq,
             "gemm_bias_bf16": epi,
+            "f16_codes": f16a,
             "w4a8": w4,
             "block_scaled": mx,
             "e2e": e2e,
@@ -589,6 +593,50 @@ def measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops):
     mean = statistics.mean(ms)
     return {"ms": round(mean, 4), "TFLOP/s": round(ops / (mean * 1e-3) / 1e12, 1),
             "kernel": q8.q8_gemm_pick(qa.shape[0], N, qa.shape[1])}
+
+
+def measure_f16a(q8, a, qw, s_w, y, flush, args, hbm_peak, tc_peak, ops):
+    """The headline step with the activation codes stored as fp16 values: q8_quantize_act_f16
+    (read A, 4 M K bytes; write codes, 2 M K) then q8_gemm_f16a (the pair kernel loading the fp16
+    codes by TMA into its operand stages), L2 flushed before each step."""
+    import torch
+    M, K = a.shape
+    qa16 = torch.empty((M, K), dtype=torch.float16, device=a.device)
+    s_a = torch.empty(M, dtype=torch.float32, device=a.device)
+
+    def quant():
+        q8.q8_quantize_act_f16(a, per_row=True, symmetric=True, qa16=qa16, s_a=s_a)
+
+    def gemm():
+        q8.q8_gemm_f16a(qa16, s_a, None, qw, s_w, out=y)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        quant()
+        gemm()
+    torch.cuda.synchronize()
+    qms, gms = [], []
+    for _ in range(max(5, args.steps)):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        quant()
+        ev[1].record()
+        gemm()
+        ev[2].record()
+        torch.cuda.synchronize()
+        qms.append(ev[0].elapsed_time(ev[1]))
+        gms.append(ev[1].elapsed_time(ev[2]))
+    assert q8.q8_device_error() == 0
+    q, g = statistics.mean(qms), statistics.mean(gms)
+    qbytes = M * K * 6 + 4 * M
+    gtf = ops / (g * 1e-3) / 1e12
+    return {"workload": "same layer; codes as fp16 values", "step_ms": round(q + g, 4),
+            "TOPS": round(ops / ((q + g) * 1e-3) / 1e12, 1),
+            "quantizer": {"ms": round(q, 4), "GB/s": round(qbytes / (q * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(qbytes / (q * 1e-3) / 1e9 / hbm_peak, 4), "bytes": qbytes},
+            "gemm": {"ms": round(g, 4), "TFLOP/s": round(gtf, 1), "frac": round(gtf / tc_peak, 4),
+                     "kernel": "tcgen05_pair (fp16 A by TMA)"}}
 
 
 def measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak):

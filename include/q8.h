@@ -305,6 +305,41 @@ q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, c
                         q8_gemm_kernel kernel, q8_stream_t stream);
 
 /*
+ * Activation codes stored as fp16 values. The quantization is that of
+ * q8_quantize_act (the same scales, zero points and codes: rint of the IEEE
+ * quotient, clamped), but each code is written as the fp16 number of equal value
+ * (exact, |code| <= 128), two bytes per element. The pages store the codes as
+ * int8; the fp16 form is the operand type of this library's tensor-core GEMM,
+ * which otherwise converts every activation code once per 256-column output tile
+ * it enters. Written once per code here, it is converted once in all. The
+ * weights stay int8.
+ *
+ * qa16 : fp16 bit patterns [M, K], written, 16-byte aligned. Other arguments and
+ * errors as q8_quantize_act.
+ */
+q8_status q8_quantize_act_f16(const float* a, int64_t M, int64_t K, q8_granularity g,
+                              q8_symmetry sym, uint16_t* qa16, float* s_a, int32_t* z_a,
+                              q8_stream_t stream);
+
+/*
+ * q8_gemm_epilogue_ex on activation codes from q8_quantize_act_f16: the same
+ * INT8 x INT8 -> INT32 products and sums (the fp16 values are the int8 codes),
+ * the same epilogue and output types, on the CTA-pair tcgen05 kernel (TMA loads
+ * the fp16 codes straight into its operand stages). qa16 values must be integers
+ * in [-128, 127]; other values give unspecified results.
+ * Errors as q8_gemm_epilogue_ex.
+ */
+q8_status q8_gemm_f16a_ex(const uint16_t* qa16, const float* s_a, const int32_t* z_a,
+                          q8_granularity ga, const int8_t* qw, const float* s_w,
+                          q8_granularity gw, const int32_t* colsum, const float* bias, int64_t M,
+                          int64_t N, int64_t K, q8_out_type out_type, void* out, float out_scale,
+                          q8_stream_t stream);
+
+/* The raw INT32 accumulators of q8_gemm_f16a_ex (as q8_gemm_s32_ex). */
+q8_status q8_gemm_f16a_s32(const uint16_t* qa16, const int8_t* qw, int64_t M, int64_t N, int64_t K,
+                           int32_t* acc, q8_stream_t stream);
+
+/*
  * The whole layer on host buffers ("Activation Quantization Architecture", the
  * quantizer itself and the integer GEMM; Day 98's epilogue): A fp32 [M, K] in host
  * memory -> per-token quantization (symmetric, or asymmetric with colsum) -> the

@@ -28,7 +28,7 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -65,6 +65,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_dequant_ex.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32, p]
     lib.q8_gemm_epilogue_ex.argtypes = [p, p, p, i32, p, p, i32, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
+    lib.q8_quantize_act_f16.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
+    lib.q8_gemm_f16a_ex.argtypes = [p, p, p, i32, p, p, i32, p, p, i64, i64, i64, i32, p, ctypes.c_float, p]
+    lib.q8_gemm_f16a_s32.argtypes = [p, p, i64, i64, i64, p, p]
     lib.q8_quantize_weight_int4.argtypes = [p, i64, i64, p, p, p]
     lib.q8_colsum_int4.argtypes = [p, i64, i64, p, p]
     lib.q8_gemm_w4a8_ex.argtypes = [p, p, p, i32, p, p, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
@@ -207,11 +210,9 @@ def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "a
 OUT_TYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int8: 2}
 
 
-def q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
-                     out=None, kernel: str = "auto", stream=None):
-    """Quantized linear layer with the epilogue variants: y = (acc - z_a*colsum) * (s_a*s_w) + bias,
-    written as fp32, bf16, or int8 codes with the static output scale out_scale."""
-    _need(qa, torch.int8, "qa", 2)
+def _epilogue_args(qa, qa_dtype, s_a, z_a, qw, s_w, colsum, bias, out_dtype, out_scale, out):
+    """Checks of the epilogue entries; returns (M, N, K, ga, gw, out)."""
+    _need(qa, qa_dtype, "qa", 2)
     _need(qw, torch.int8, "qw", 2)
     M, K = qa.shape
     N = qw.shape[0]
@@ -238,6 +239,60 @@ def q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=to
         raise ValueError("int8 output needs out_scale")
     out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
     _need(out, out_dtype, "out", 2)
+    return M, N, K, ga, gw, out
+
+
+def q8_quantize_act_f16(a: torch.Tensor, per_row: bool = True, symmetric: bool = True, qa16=None, s_a=None,
+                        z_a=None, stream=None):
+    """q8_quantize_act with the codes written as fp16 values; returns (qa16 float16, s_a, z_a or None)."""
+    _need(a, torch.float32, "a", 2)
+    M, K = a.shape
+    n = M if per_row else 1
+    qa16 = torch.empty((M, K), dtype=torch.float16, device=a.device) if qa16 is None else qa16
+    _need(qa16, torch.float16, "qa16", 2)
+    s_a = torch.empty(n, dtype=torch.float32, device=a.device) if s_a is None else s_a
+    if not symmetric and z_a is None:
+        z_a = torch.empty(n, dtype=torch.int32, device=a.device)
+    if symmetric:
+        z_a = None
+    _check(load().q8_quantize_act_f16(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
+                                      Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa16), _ptr(s_a),
+                                      _ptr(z_a), _stream(stream)), "q8_quantize_act_f16")
+    return qa16, s_a, z_a
+
+
+def q8_gemm_f16a(qa16, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
+                 out=None, stream=None):
+    """q8_gemm_epilogue on fp16-valued activation codes (from q8_quantize_act_f16)."""
+    M, N, K, ga, gw, out = _epilogue_args(qa16, torch.float16, s_a, z_a, qw, s_w, colsum, bias, out_dtype,
+                                          out_scale, out)
+    _check(load().q8_gemm_f16a_ex(_ptr(qa16), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
+                                  _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
+                                  OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),
+                                  _stream(stream)), "q8_gemm_f16a")
+    return out
+
+
+def q8_gemm_f16a_s32(qa16, qw, out=None, stream=None):
+    """Raw INT32 accumulators of q8_gemm_f16a."""
+    _need(qa16, torch.float16, "qa16", 2)
+    _need(qw, torch.int8, "qw", 2)
+    M, K = qa16.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qa16 and qw disagree on K")
+    out = torch.empty((M, N), dtype=torch.int32, device=qa16.device) if out is None else out
+    _need(out, torch.int32, "out", 2)
+    _check(load().q8_gemm_f16a_s32(_ptr(qa16), _ptr(qw), M, N, K, _ptr(out), _stream(stream)), "q8_gemm_f16a_s32")
+    return out
+
+
+def q8_gemm_epilogue(qa, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
+                     out=None, kernel: str = "auto", stream=None):
+    """Quantized linear layer with the epilogue variants: y = (acc - z_a*colsum) * (s_a*s_w) + bias,
+    written as fp32, bf16, or int8 codes with the static output scale out_scale."""
+    M, N, K, ga, gw, out = _epilogue_args(qa, torch.int8, s_a, z_a, qw, s_w, colsum, bias, out_dtype, out_scale,
+                                          out)
     _check(load().q8_gemm_epilogue_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
                                       _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
                                       OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),

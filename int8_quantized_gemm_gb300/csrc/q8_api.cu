@@ -64,11 +64,12 @@ struct MxWeights {
     int group;
 };
 
-q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+// qa: int8 codes, or (a16) the same codes as fp16 values.
+q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
                       q8_stream_t stream, const Variant* var = nullptr, bool w4 = false,
-                      const MxWeights* mx = nullptr) {
+                      const MxWeights* mx = nullptr, bool a16 = false) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -81,6 +82,7 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         if (kst != Q8_OK) return kst;
         if (w4 && K % 32 != 0) return Q8_ERR_UNSUPPORTED;   // packed int4 rows: whole 16-byte multiples
     }
+    if (a16 && kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05_PAIR) return Q8_ERR_UNSUPPORTED;
     if (mx) {
         if (mx->group != 32 && mx->group != 128) return Q8_ERR_INVALID_ARG;
         if (z_a || !epilogue) return Q8_ERR_UNSUPPORTED;     // symmetric activations, dequantized output
@@ -126,6 +128,12 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
         const size_t bytes = (size_t)M * (size_t)N * 4;
         return from_cuda(cudaMemsetAsync(epilogue ? (void*)y : (void*)out_i32, 0, bytes, s));
     }
+    const int8_t* qa8 = static_cast<const int8_t*>(qa);
+    if (a16) {
+        // fp16 activation codes: the CTA-pair kernel with TMA loads of A into its operand ring
+        if (!q8::gemm_tc2_supports(M, N, K, q8::kWA16)) return Q8_ERR_UNSUPPORTED;
+        return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWA16));
+    }
     if (mx) {
         // block-scaled weights: the decode kernel for M <= 16 (N % 4 == 0, 16-byte aligned scale
         // words), the CTA-pair kernel otherwise
@@ -136,21 +144,21 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
             kernel = q8::gemv_mx_supports(M, N, K, mx->group, mx->sf) ? Q8_GEMM_DECODE : Q8_GEMM_TCGEN05_PAIR;
         if (kernel == Q8_GEMM_DECODE) {
             if (!q8::gemv_mx_supports(M, N, K, mx->group, mx->sf)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemv_mx(qa, qw, mx->sf, mx->group, M, N, K, ep, s));
+            return from_cuda(q8::launch_gemv_mx(qa8, qw, mx->sf, mx->group, M, N, K, ep, s));
         }
         if (!q8::gemm_tc2_supports(M, N, K, q8::kWMx)) return Q8_ERR_UNSUPPORTED;
-        return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWMx));
+        return from_cuda(q8::launch_gemm_tc2(qa8, qw, M, N, K, ep, s, q8::kWMx));
     }
     if (w4) {
         // int4 weights run on the decode kernel (M <= 16) and the CTA-pair kernel
         if (kernel == Q8_GEMM_AUTO) kernel = q8::gemv_mma_supports(M, N, K, true) ? Q8_GEMM_DECODE : Q8_GEMM_TCGEN05_PAIR;
         if (kernel == Q8_GEMM_DECODE) {
             if (!q8::gemv_mma_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemv_mma(qa, qw, M, N, K, ep, s, true));
+            return from_cuda(q8::launch_gemv_mma(qa8, qw, M, N, K, ep, s, true));
         }
         if (kernel == Q8_GEMM_TCGEN05_PAIR) {
             if (!q8::gemm_tc2_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s, q8::kWInt4));
+            return from_cuda(q8::launch_gemm_tc2(qa8, qw, M, N, K, ep, s, q8::kWInt4));
         }
         return Q8_ERR_UNSUPPORTED;
     }
@@ -158,21 +166,21 @@ q8_status gemm_common(const int8_t* qa, const float* s_a, const int32_t* z_a, q8
     switch (kernel) {
         case Q8_GEMM_TCGEN05:
             if (!q8::gemm_tc_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemm_tc(qa, qw, M, N, K, ep, s));
+            return from_cuda(q8::launch_gemm_tc(qa8, qw, M, N, K, ep, s));
         case Q8_GEMM_TCGEN05_PAIR:
             if (!q8::gemm_tc2_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemm_tc2(qa, qw, M, N, K, ep, s));
+            return from_cuda(q8::launch_gemm_tc2(qa8, qw, M, N, K, ep, s));
         case Q8_GEMM_DECODE:
             if (!q8::gemv_mma_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemv_mma(qa, qw, M, N, K, ep, s));
+            return from_cuda(q8::launch_gemv_mma(qa8, qw, M, N, K, ep, s));
         case Q8_GEMM_DECODE_TC:
             if (!q8::gemv_tc_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
-            return from_cuda(q8::launch_gemv_tc(qa, qw, M, N, K, ep, s));
+            return from_cuda(q8::launch_gemv_tc(qa8, qw, M, N, K, ep, s));
         case Q8_GEMM_SKINNY:
-            return from_cuda(q8::launch_gemm_mma(qa, qw, M, N, K, ep, true, s));
+            return from_cuda(q8::launch_gemm_mma(qa8, qw, M, N, K, ep, true, s));
         case Q8_GEMM_MMA_S8:
         default:
-            return from_cuda(q8::launch_gemm_mma(qa, qw, M, N, K, ep, false, s));
+            return from_cuda(q8::launch_gemm_mma(qa8, qw, M, N, K, ep, false, s));
     }
 }
 
@@ -190,6 +198,18 @@ q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g
     if (g == Q8_PER_ROW && M == 0) return Q8_OK;
     return from_cuda(q8::launch_quantize(a, M, K, g == Q8_PER_ROW, qa, s_a, z_a,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+q8_status q8_quantize_act_f16(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym,
+                              uint16_t* qa16, float* s_a, int32_t* z_a, q8_stream_t stream) {
+    if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
+    if ((sym == Q8_ASYMMETRIC) != (z_a != nullptr)) return Q8_ERR_INVALID_ARG;
+    if (z_a && !aligned(z_a, 4)) return Q8_ERR_INVALID_ARG;
+    q8_status st = check_quant_args(a, M, K, g, reinterpret_cast<const int8_t*>(qa16), s_a, M > 0 && K > 0);
+    if (st != Q8_OK) return st;
+    if (g == Q8_PER_ROW && M == 0) return Q8_OK;
+    return from_cuda(q8::launch_quantize_f16(a, M, K, g == Q8_PER_ROW, qa16, s_a, z_a,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 q8_status q8_rmsnorm_quantize_act(const float* a, const float* gamma, int64_t M, int64_t K, float eps, int8_t* qa,
@@ -294,6 +314,26 @@ q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, c
     const MxWeights mx{sf, group};
     return gemm_common(qa, s_a, nullptr, ga, qw, nullptr, Q8_PER_ROW, nullptr, M, N, K, nullptr, nullptr, kernel,
                        stream, &var, false, &mx);
+}
+
+q8_status q8_gemm_f16a_ex(const uint16_t* qa16, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                          const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                          const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type, void* out,
+                          float out_scale, q8_stream_t stream) {
+    const Variant var{bias, out_type, out, out_scale};
+    return gemm_common(qa16, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, nullptr, nullptr, Q8_GEMM_AUTO, stream, &var,
+                       false, nullptr, true);
+}
+
+q8_status q8_gemm_f16a_s32(const uint16_t* qa16, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,
+                           q8_stream_t stream) {
+    if (!acc && M > 0 && N > 0) return Q8_ERR_INVALID_ARG;
+    if (!acc) {  // empty output
+        if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
+        return check_k(K, false);
+    }
+    return gemm_common(qa16, nullptr, nullptr, Q8_PER_TENSOR, qw, nullptr, Q8_PER_TENSOR, nullptr, M, N, K, nullptr,
+                       acc, Q8_GEMM_AUTO, stream, nullptr, false, nullptr, true);
 }
 
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K, int32_t* acc,

@@ -393,6 +393,19 @@ bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t
                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool make_tma_map_f16(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t K, int box_rows, int box_k) {
+    auto enc = get_encode();
+    if (!enc || ((K * 2) % 16) != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows) {
     return make_map_impl(map, base, rows, K, box_rows, 64, CU_TENSOR_MAP_SWIZZLE_64B);
 }

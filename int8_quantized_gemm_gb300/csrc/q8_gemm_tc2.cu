@@ -67,14 +67,12 @@ constexpr int BMH = 128;
 constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per CTA)
 constexpr int BNH = 128;
 constexpr int BK = 64;
-constexpr int S16 = 4;              // fp16 operand stages (32 KB)
 constexpr int kConv = 192;          // converter threads of the int8 / int4 formats: warps 2..7
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;      // two 128 x 256 fp32 accumulator buffers per CTA
 
 constexpr int kA8 = BMH * BK;                                                     // 8 KB int8 A staging
 constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16;   // 32 KB
-constexpr int kOffStage8 = S16 * kStage16;
 constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 128-byte output block (TMA store source)
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 constexpr uint16_t kPairMask = 0x3;
@@ -92,9 +90,16 @@ constexpr uint16_t kPairMask = 0x3;
 // then reads its 256 accumulator columns in two halves). Registers: the producer-side warps
 // shrink to kRegsLow, the drain warps grow to kRegsHigh; (2 + kConvWarps) * 32 * kRegsLow +
 // kDrainWarps * 32 * kRegsHigh <= 512 * 128, the registers the block is launched with.
+// Activation codes as fp16 values (kWA16): TMA writes the A half of each fp16 operand stage
+// directly (the 128-byte swizzle of a [128 x 64] fp16 box is the K-major layout of the UMMA
+// descriptors), the staging ring holds the int8 weights only, and the converters convert W.
+// The freed staging bytes give the operand ring a fifth stage.
 template <int WF>
 struct PairCfg {
     static constexpr bool W4 = WF == kWInt4;
+    static constexpr bool A16 = WF == kWA16;
+    static constexpr int S16 = A16 ? 5 : 4;                   // fp16 operand stages (32 KB each)
+    static constexpr int kOffStage8 = S16 * kStage16;
     static constexpr int kConvWarps = WF == kWMx ? 10 : 6;
     static constexpr int kDrainWarps = 16 - 2 - kConvWarps;
     static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
@@ -103,7 +108,7 @@ struct PairCfg {
                   "register split above the launch's registers");
     static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
-    static constexpr int kStage8 = kA8 + kB8;                 // 16 KB (int8) or 12 KB (int4)
+    static constexpr int kStage8 = (A16 ? 0 : kA8) + kB8;     // 16 KB (int8), 12 KB (int4), 8 KB (A16)
     static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
     static constexpr int KB_PER_CHUNK = W4 ? 256 : WF == kWMx ? (1 << 30) : 16;
     static constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
@@ -111,6 +116,7 @@ struct PairCfg {
     static constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
     static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(kSmem <= 227 * 1024, "above the shared memory of one CTA");
 };
 
 struct PairGeom {
@@ -149,8 +155,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_acc,
                     int tma_out, int M, int N, int K, int n_full, int ksplit, Epilogue ep) {
     using C = PairCfg<WF>;
-    constexpr bool W4 = WF == kWInt4, MX = WF == kWMx;
-    constexpr int S8 = C::S8, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
+    constexpr bool W4 = WF == kWInt4, MX = WF == kWMx, A16 = C::A16;
+    constexpr int S8 = C::S8, S16 = C::S16, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
+    constexpr int kOffStage8 = C::kOffStage8;
     constexpr int kOffEpi = C::kOffEpi, kOffBar = C::kOffBar;
     constexpr int kConvWarps = C::kConvWarps, kDrainWarps = C::kDrainWarps;
     extern __shared__ uint8_t smem_raw[];
@@ -159,11 +166,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + (sbase - sraw);
     const uint32_t bar_full8 = sbase + kOffBar;
     const uint32_t bar_empty8 = bar_full8 + 8 * S8;
-    const uint32_t bar_full16 = bar_empty8 + 8 * S8;     // used in the even CTA: its 6 converter warps + relay
+    const uint32_t bar_full16 = bar_empty8 + 8 * S8;     // used in the even CTA: its converter warps + relay
+                                                         // (+ the A TMA's bytes for A16)
     const uint32_t bar_empty16 = bar_full16 + 8 * S16;   // both CTAs: the pair MMA's commit
     const uint32_t bar_accfull = bar_empty16 + 8 * S16;  // both CTAs: the pair MMA's commit
     const uint32_t bar_accempty = bar_accfull + 16;      // used in the even CTA: 2 x 8 drain warps
-    const uint32_t bar_conv16 = bar_accempty + 16;       // used in the odd CTA: its 6 converter warps
+    const uint32_t bar_conv16 = bar_accempty + 16;       // used in the odd CTA: its converter warps (+ A TMA)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * S8 + 3 * S16 + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -177,9 +185,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar_empty8 + 8 * s, kConvWarps);
         }
         for (int s = 0; s < S16; ++s) {
-            mbar_init(bar_full16 + 8 * s, (kConvWarps) + 1);
+            mbar_init(bar_full16 + 8 * s, kConvWarps + 1 + (A16 ? 1 : 0));
             mbar_init(bar_empty16 + 8 * s, 1);
-            mbar_init(bar_conv16 + 8 * s, kConvWarps);
+            mbar_init(bar_conv16 + 8 * s, kConvWarps + (A16 ? 1 : 0));
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_accfull + 8 * b, 1);
@@ -228,8 +236,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
                 mbar_expect_tx(bar_full8 + 8 * s, kStage8);
                 const int kx = k0 + kb;
-                tma_load_2d(dst, &tmap_a, kx * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
-                tma_load_2d(dst + kA8, &tmap_w, W4 ? kx * (BK / 2) : kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                if constexpr (A16) {
+                    tma_load_2d(dst, &tmap_w, kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                    // the fp16 A codes go straight into the operand stage once the MMA has released it;
+                    // their bytes complete on the barrier the converters arrive on
+                    const int s16 = g % S16;
+                    if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrProducer,
+                                   &g_tc2_error))
+                        break;
+                    const uint32_t fb = (leader ? bar_full16 : bar_conv16) + 8 * s16;
+                    mbar_expect_tx(fb, kA16);
+                    tma_load_2d(sbase + s16 * kStage16, &tmap_a, kx * BK, m0 + (int)rank * BMH, fb);
+                } else {
+                    tma_load_2d(dst, &tmap_a, kx * BK, m0 + (int)rank * BMH, bar_full8 + 8 * s);
+                    tma_load_2d(dst + kA8, &tmap_w, W4 ? kx * (BK / 2) : kx * BK, n0 + (int)rank * BNH,
+                                bar_full8 + 8 * s);
+                }
                 if (++kb == kbn) { kb = 0; ++i; }
             }
         }
@@ -286,6 +308,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         // ---------------------------------------------------------------- converters
+        if constexpr (A16) {
+            // W only: 512 16-byte int8 chunks per stage (128 rows x 4); thread ct takes idx = ct + T j
+            // (idx < 512): row ct / 4 + (T / 4) j, chunk ct % 4, into the W half of the operand stage.
+            constexpr int T = C::kConvT, NJ = (512 + T - 1) / T;
+            const int ct = threadIdx.x - 64;
+            const int r0 = ct >> 2, c0 = ct & 3;
+            const uint32_t src0 = (uint32_t)(ct * 16);
+            const uint32_t dst0 = (uint32_t)kA16 + sw128(r0, 2 * c0);
+            const uint32_t dst1 = (uint32_t)kA16 + sw128(r0, 2 * c0 + 1);
+            for (int g = 0; g < total_g; ++g) {
+                const int s8 = g % S8, s16 = g % S16;
+                if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
+                    break;
+                const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
+                uint4 in[NJ];
+    #pragma unroll
+                for (int j = 0; j < NJ; ++j)
+                    in[j] = (ct + T * j < 512) ? lds128(st8 + T * 16 * j) : make_uint4(0, 0, 0, 0);
+                if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
+                               &g_tc2_error))
+                    break;
+                const uint32_t st16 = sbase + s16 * kStage16;
+    #pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    if (ct + T * j < 512) {
+                        // cvt_word turns bytes (0, 1, 2, 3) into the fp16 pairs (0, 2) and (1, 3); TMA
+                        // writes A in K order, so W's bytes are first permuted to (0, 2, 1, 3)
+                        uint4 o0, o1;
+                        cvt_word(__byte_perm(in[j].x, 0u, 0x3120u), o0.x, o0.y);
+                        cvt_word(__byte_perm(in[j].y, 0u, 0x3120u), o0.z, o0.w);
+                        cvt_word(__byte_perm(in[j].z, 0u, 0x3120u), o1.x, o1.y);
+                        cvt_word(__byte_perm(in[j].w, 0u, 0x3120u), o1.z, o1.w);
+                        sts128(st16 + dst0 + 32 * T * j, o0);
+                        sts128(st16 + dst1 + 32 * T * j, o1);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive((leader ? bar_full16 : bar_conv16) + 8 * s16);
+                    mbar_arrive(bar_empty8 + 8 * s8);
+                }
+            }
+        } else
         // 1024 16-byte int8 chunks per stage ([A 128 rows | W 128 rows] x 4 chunks of each
         // 64-byte staging row); thread ct takes idx = ct + T j (T = kConvT converter threads,
         // j < kIters, idx < 1024): row ct / 4 + (T / 4) j, chunk ct % 4. (row & 7) does not
@@ -765,14 +831,17 @@ static PairGeom pair_geom(int64_t M, int64_t N) {
 }
 
 template <int WF>
-static cudaError_t launch_gemm_tc2_t(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
+static cudaError_t launch_gemm_tc2_t(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K,
                                      const Epilogue& ep, cudaStream_t stream, int n_full, int ksplit,
                                      int32_t* acc) {
     using C = PairCfg<WF>;
     constexpr bool W4 = C::W4;
     CUtensorMap ma, mw;
-    // int4: the packed weights are a byte matrix [N, K / 2], staged 32 bytes (64 K) per k-block
-    if (!make_tma_map_i8(&ma, qa, M, K, BMH, BK) ||
+    // int4: the packed weights are a byte matrix [N, K / 2], staged 32 bytes (64 K) per k-block;
+    // A16: fp16 codes in [128 rows x 64 K] boxes with the operand ring's 128-byte swizzle
+    const bool map_a = C::A16 ? make_tma_map_f16(&ma, static_cast<const uint16_t*>(qa), M, K, BMH, BK)
+                              : make_tma_map_i8(&ma, static_cast<const int8_t*>(qa), M, K, BMH, BK);
+    if (!map_a ||
         !make_tma_map_i8(&mw, static_cast<const int8_t*>(qw), N, W4 ? K / 2 : K, BNH, W4 ? BK / 2 : BK))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
@@ -830,7 +899,7 @@ static void plan_split(int64_t M, int64_t N, int64_t K, const Epilogue& ep, int&
 }
 
 template <int WF>
-static cudaError_t launch_gemm_tc2_split(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K,
+static cudaError_t launch_gemm_tc2_split(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K,
                                          const Epilogue& ep, cudaStream_t stream) {
     int n_full, ksplit;
     int32_t* acc;
@@ -848,7 +917,7 @@ static cudaError_t launch_gemm_tc2_split(const int8_t* qa, const void* qw, int64
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+cudaError_t launch_gemm_tc2(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
                             cudaStream_t stream, int wfmt) {
     if (!gemm_tc2_supports(M, N, K, wfmt)) return cudaErrorNotSupported;
     if (wfmt == kWMx) {
@@ -856,6 +925,7 @@ cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t
             return cudaErrorInvalidValue;
         return launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream, pair_geom(M, N).tiles, 1, nullptr);
     }
+    if (wfmt == kWA16) return launch_gemm_tc2_split<kWA16>(qa, qw, M, N, K, ep, stream);
     return wfmt == kWInt4 ? launch_gemm_tc2_split<kWInt4>(qa, qw, M, N, K, ep, stream)
                           : launch_gemm_tc2_split<kWInt8>(qa, qw, M, N, K, ep, stream);
 }

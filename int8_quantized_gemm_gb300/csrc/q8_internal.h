@@ -24,6 +24,9 @@ constexpr float kZeroGuard = 1e-8f;
 // or one for the whole tensor. z == nullptr selects the symmetric rule.
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row,
                             int8_t* q, float* s, int32_t* z, cudaStream_t stream);
+// The same codes written as fp16 values (exact: |code| <= 128), two bytes each.
+cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool per_row,
+                                uint16_t* q, float* s, int32_t* z, cudaStream_t stream);
 
 // int4 weights (W4A8): per-row symmetric codes packed two per byte (K % 32 == 0), and their
 // column sums.
@@ -98,11 +101,13 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
                            const Epilogue& ep, cudaStream_t stream);
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
 
-// Weight formats of the CTA-pair kernel: int8 codes, packed int4 codes, block-scaled int8.
-enum WeightFormat : int { kWInt8 = 0, kWInt4 = 1, kWMx = 2 };
+// Operand formats of the CTA-pair kernel: int8 codes, packed int4 codes, block-scaled int8
+// weights (activations as int8 codes), or int8 weights with the activation codes as fp16 values.
+enum WeightFormat : int { kWInt8 = 0, kWInt4 = 1, kWMx = 2, kWA16 = 3 };
 
-// tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles).
-cudaError_t launch_gemm_tc2(const int8_t* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+// tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles). qa: int8 codes, or fp16 code
+// values for kWA16.
+cudaError_t launch_gemm_tc2(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
                             cudaStream_t stream, int wfmt = kWInt8);
 bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, int wfmt = kWInt8);
 

@@ -6,6 +6,7 @@
 // so the row is never re-read. Arithmetic follows the rules in q8.h exactly:
 // IEEE fp32 division (__fdiv_rn), round-half-to-even (__float2int_rn), and no
 // contraction of multiplies into FMAs (the file is built with -fmad=false).
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,6 +56,21 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
            ((uint32_t)(d & 0xFF) << 24);
 }
 
+// Two codes as fp16 values (exact for |code| <= 2048), the first in the low half.
+__device__ __forceinline__ uint32_t pack_h2(int a, int b) {
+    return (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+}
+
+// Codes of elements 4i .. 4i + 3 of a row (or tensor) whose codes start at q: int8 (one 32-bit
+// word) or, for H, fp16 values (8 bytes).
+template <bool H>
+__device__ __forceinline__ void store_codes4(void* q, int64_t i, int a, int b, int c, int d) {
+    if constexpr (H)
+        reinterpret_cast<uint2*>(q)[i] = make_uint2(pack_h2(a, b), pack_h2(c, d));
+    else
+        reinterpret_cast<uint32_t*>(q)[i] = pack4(a, b, c, d);
+}
+
 // Block-wide max of two values (hi, and nlo = -lo for the asymmetric range).
 // All threads receive the results.
 template <bool ASYM>
@@ -82,9 +98,9 @@ __device__ __forceinline__ void block_max2(float& hi, float& nlo, float* red) {
 
 // One CTA per row; each thread keeps up to VPT float4 of the row in registers.
 // Requires cols % 4 == 0 and cols / 4 <= VPT * blockDim.x.
-template <int VPT, bool ASYM>
+template <int VPT, bool ASYM, bool H = false>
 __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel(const float* __restrict__ x, int64_t cols,
-                                                            int8_t* __restrict__ q,
+                                                            void* __restrict__ q,
                                                             float* __restrict__ s,
                                                             int32_t* __restrict__ z) {
     __shared__ float red[64];
@@ -123,28 +139,26 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
-    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+    void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
         if (i < n4) {
-            uint32_t w;
             if (ASYM)
-                w = pack4(asym_code(v[j].x, sc, rc, zp), asym_code(v[j].y, sc, rc, zp),
-                          asym_code(v[j].z, sc, rc, zp), asym_code(v[j].w, sc, rc, zp));
+                store_codes4<H>(qr, i, asym_code(v[j].x, sc, rc, zp), asym_code(v[j].y, sc, rc, zp),
+                                asym_code(v[j].z, sc, rc, zp), asym_code(v[j].w, sc, rc, zp));
             else
-                w = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
-                          sym_code(v[j].w, sc, rc));
-            qr[i] = w;
+                store_codes4<H>(qr, i, sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
+                                sym_code(v[j].w, sc, rc));
         }
     }
 }
 
 // Rows longer than the register budget: reduce in one sweep, code in a second
 // sweep (the second read of the row is served mostly by L2).
-template <bool ASYM>
+template <bool ASYM, bool H = false>
 __global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* __restrict__ x, int64_t cols,
-                                                                 int8_t* __restrict__ q,
+                                                                 void* __restrict__ q,
                                                                  float* __restrict__ s,
                                                                  int32_t* __restrict__ z) {
     __shared__ float red[64];
@@ -174,13 +188,15 @@ __global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* _
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
-    uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+    void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         float4 v = __ldcs(xr + i);
-        qr[i] = ASYM ? pack4(asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
-                             asym_code(v.w, sc, rc, zp))
-                     : pack4(sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
-                             sym_code(v.w, sc, rc));
+        if (ASYM)
+            store_codes4<H>(qr, i, asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
+                            asym_code(v.w, sc, rc, zp));
+        else
+            store_codes4<H>(qr, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
+                            sym_code(v.w, sc, rc));
     }
 }
 
@@ -230,23 +246,24 @@ __global__ void tensor_params_kernel(float* s, int32_t* z) {
     }
 }
 
-template <bool ASYM>
+template <bool ASYM, bool H = false>
 __global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restrict__ x, int64_t n4,
                                                            const float* __restrict__ s,
                                                            const int32_t* __restrict__ z,
-                                                           int8_t* __restrict__ q) {
+                                                           void* __restrict__ q) {
     const float sc = s[0];
     const float rc = __fdiv_rn(1.0f, sc);
     const int zp = ASYM ? z[0] : 0;
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 v = __ldcs(x4 + i);
-        q4[i] = ASYM ? pack4(asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
-                             asym_code(v.w, sc, rc, zp))
-                     : pack4(sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
-                             sym_code(v.w, sc, rc));
+        if (ASYM)
+            store_codes4<H>(q, i, asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
+                            asym_code(v.w, sc, rc, zp));
+        else
+            store_codes4<H>(q, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
+                            sym_code(v.w, sc, rc));
     }
 }
 
@@ -558,16 +575,16 @@ int num_sms() {
     return sms;
 }
 
-template <int VPT, bool ASYM>
-cudaError_t launch_rows(const float* x, int64_t rows, int64_t cols, int threads, int8_t* q, float* s,
+template <int VPT, bool ASYM, bool H>
+cudaError_t launch_rows(const float* x, int64_t rows, int64_t cols, int threads, void* q, float* s,
                         int32_t* z, cudaStream_t st) {
-    quantize_rows_kernel<VPT, ASYM><<<(unsigned)rows, threads, 0, st>>>(x, cols, q, s, z);
+    quantize_rows_kernel<VPT, ASYM, H><<<(unsigned)rows, threads, 0, st>>>(x, cols, q, s, z);
     note_launch();
     return cudaGetLastError();
 }
 
-template <bool ASYM>
-cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, int8_t* q, float* s, int32_t* z,
+template <bool ASYM, bool H>
+cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, void* q, float* s, int32_t* z,
                           cudaStream_t st) {
     const int64_t n4 = cols / 4;
     // Smallest block that covers the row with the per-thread register budget.
@@ -578,17 +595,17 @@ cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, int8_t* q,
     };
     // Up to 1024 threads per row and at most 4 float4 per thread keeps the kernel at
     // <= 32 registers, so two 1024-thread blocks (a full SM) stay resident.
-    if (n4 <= 1024 * 1) return launch_rows<1, ASYM>(x, rows, cols, threads_for(1), q, s, z, st);
-    if (n4 <= 1024 * 2) return launch_rows<2, ASYM>(x, rows, cols, threads_for(2), q, s, z, st);
-    if (n4 <= 1024 * 4) return launch_rows<4, ASYM>(x, rows, cols, threads_for(4), q, s, z, st);
-    if (n4 <= 1024 * 8) return launch_rows<8, ASYM>(x, rows, cols, threads_for(8), q, s, z, st);
-    quantize_long_rows_kernel<ASYM><<<(unsigned)rows, 1024, 0, st>>>(x, cols, q, s, z);
+    if (n4 <= 1024 * 1) return launch_rows<1, ASYM, H>(x, rows, cols, threads_for(1), q, s, z, st);
+    if (n4 <= 1024 * 2) return launch_rows<2, ASYM, H>(x, rows, cols, threads_for(2), q, s, z, st);
+    if (n4 <= 1024 * 4) return launch_rows<4, ASYM, H>(x, rows, cols, threads_for(4), q, s, z, st);
+    if (n4 <= 1024 * 8) return launch_rows<8, ASYM, H>(x, rows, cols, threads_for(8), q, s, z, st);
+    quantize_long_rows_kernel<ASYM, H><<<(unsigned)rows, 1024, 0, st>>>(x, cols, q, s, z);
     note_launch();
     return cudaGetLastError();
 }
 
-template <bool ASYM>
-cudaError_t dispatch_tensor(const float* x, int64_t n, int8_t* q, float* s, int32_t* z, cudaStream_t st) {
+template <bool ASYM, bool H>
+cudaError_t dispatch_tensor(const float* x, int64_t n, void* q, float* s, int32_t* z, cudaStream_t st) {
     const int64_t n4 = n / 4;
     cudaError_t e = cudaMemsetAsync(s, 0, sizeof(float), st);
     if (e == cudaSuccess && ASYM) e = cudaMemsetAsync(z, 0, sizeof(int32_t), st);
@@ -600,7 +617,7 @@ cudaError_t dispatch_tensor(const float* x, int64_t n, int8_t* q, float* s, int3
     tensor_range_kernel<ASYM><<<(unsigned)blocks, 512, 0, st>>>(
         x, n4, reinterpret_cast<unsigned int*>(s), reinterpret_cast<unsigned int*>(z));
     tensor_params_kernel<ASYM><<<1, 32, 0, st>>>(s, z);
-    tensor_codes_kernel<ASYM><<<(unsigned)blocks, 512, 0, st>>>(x, n4, s, z, q);
+    tensor_codes_kernel<ASYM, H><<<(unsigned)blocks, 512, 0, st>>>(x, n4, s, z, q);
     note_launch(3);
     return cudaGetLastError();
 }
@@ -611,11 +628,22 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per
                             float* s, int32_t* z, cudaStream_t stream) {
     if (per_row) {
         if (rows == 0) return cudaSuccess;
-        return z ? dispatch_rows<true>(x, rows, cols, q, s, z, stream)
-                 : dispatch_rows<false>(x, rows, cols, q, s, z, stream);
+        return z ? dispatch_rows<true, false>(x, rows, cols, q, s, z, stream)
+                 : dispatch_rows<false, false>(x, rows, cols, q, s, z, stream);
     }
-    return z ? dispatch_tensor<true>(x, rows * cols, q, s, z, stream)
-             : dispatch_tensor<false>(x, rows * cols, q, s, z, stream);
+    return z ? dispatch_tensor<true, false>(x, rows * cols, q, s, z, stream)
+             : dispatch_tensor<false, false>(x, rows * cols, q, s, z, stream);
+}
+
+cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool per_row, uint16_t* q,
+                                float* s, int32_t* z, cudaStream_t stream) {
+    if (per_row) {
+        if (rows == 0) return cudaSuccess;
+        return z ? dispatch_rows<true, true>(x, rows, cols, q, s, z, stream)
+                 : dispatch_rows<false, true>(x, rows, cols, q, s, z, stream);
+    }
+    return z ? dispatch_tensor<true, true>(x, rows * cols, q, s, z, stream)
+             : dispatch_tensor<false, true>(x, rows * cols, q, s, z, stream);
 }
 
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps,

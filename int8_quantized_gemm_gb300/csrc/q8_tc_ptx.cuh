@@ -402,6 +402,9 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 // False if the driver entry point is missing.
 bool make_tma_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows, int box_k,
                      bool swizzle128 = false);
+// fp16 [rows, K] row-major, box [box_rows, box_k] (box_k * 2 == 128 bytes), 128-byte swizzle: the
+// K-major layout of the UMMA descriptors. False unless the base and row pitch are 16-byte multiples.
+bool make_tma_map_f16(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t K, int box_rows, int box_k);
 // Same with box [box_rows, 64] and the 64-byte swizzle: the 16-byte chunk c of row r
 // lands at chunk c ^ ((r >> 1) & 3) of its 64-byte row (shared-memory base 512-byte aligned).
 bool make_tma_map_i8_sw64(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows);

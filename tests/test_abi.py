@@ -131,6 +131,36 @@ def test_block_scaled_entries_reject_bad_arguments(lib):
     assert w(0, 64, 32) == q8.Q8_OK
 
 
+def test_fp16_code_entries_reject_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    q = lib.q8_quantize_act_f16
+    assert q(FAKE, 4, 32, 1, 0, FAKE, FAKE, FAKE, None) == q8.Q8_ERR_INVALID_ARG   # z_a given for symmetric
+    assert q(FAKE, 4, 32, 1, 1, FAKE, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG   # z_a missing for asymmetric
+    assert q(FAKE, 4, 32, 1, 0, None, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG   # codes required
+    assert q(FAKE, 4, 32, 1, 0, MISALIGNED, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert q(FAKE, 4, 24, 1, 0, FAKE, FAKE, None, None) == q8.Q8_ERR_UNSUPPORTED
+    assert q(FAKE, 0, 32, 1, 0, FAKE, FAKE, None, None) == q8.Q8_OK
+
+    def g(qa=FAKE, sa=FAKE, za=None, cs=None, out=FAKE, out_type=0, K=16, M=8, N=8):
+        return lib.q8_gemm_f16a_ex(qa, sa, za, 1, FAKE, FAKE, 1, cs, None, M, N, K, out_type, out,
+                                   ctypes.c_float(0.0), None)
+    assert g(qa=None) == q8.Q8_ERR_INVALID_ARG
+    assert g(qa=MISALIGNED) == q8.Q8_ERR_INVALID_ARG
+    assert g(sa=None) == q8.Q8_ERR_INVALID_ARG
+    assert g(out=None) == q8.Q8_ERR_INVALID_ARG
+    assert g(za=FAKE) == q8.Q8_ERR_INVALID_ARG                    # asymmetric A needs colsum
+    assert g(out_type=2) == q8.Q8_ERR_INVALID_ARG                 # int8 output needs a scale
+    assert g(K=24) == q8.Q8_ERR_UNSUPPORTED
+    assert g(K=131072) == q8.Q8_ERR_UNSUPPORTED
+    before = lib.q8_launch_count()
+    assert g(M=0) == q8.Q8_OK and g(N=0) == q8.Q8_OK
+    assert lib.q8_launch_count() == before
+    s32 = lib.q8_gemm_f16a_s32
+    assert s32(FAKE, FAKE, 8, 8, 16, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert s32(FAKE, FAKE, 8, 8, 16, MISALIGNED, None) == q8.Q8_ERR_INVALID_ARG
+    assert s32(FAKE, FAKE, 8, 8, 40, FAKE, None) == q8.Q8_ERR_UNSUPPORTED
+
+
 def test_k_limits_are_the_int32_bounds():
     # 128*128*K < 2^31 for raw codes; 255*128*K < 2^31 with a zero point.
     assert 128 * 128 * 131056 < 2 ** 31 <= 128 * 128 * (131056 + 16)
