@@ -756,6 +756,8 @@ def main():
                     help="only the block-scaled weight measurements (one JSON object, for profiling)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode-shaped workload (one JSON object, for profiling)")
+    ap.add_argument("--f16a-only", action="store_true",
+                    help="only the headline step with fp16-valued activation codes (one JSON object, for profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -803,6 +805,23 @@ def main():
         torch.cuda.set_device(device)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         print(json.dumps(measure_decode(q8, device, args, peaks()[0], flush, kernels=("decode", "decode_tc"))))
+        return
+    if args.f16a_only:
+        import torch
+        import int8_quantized_gemm_gb300 as q8
+        from int8_quantized_gemm_gb300 import build
+        build.build()
+        q8.load()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        hbm_peak, tc_peak, _ = peaks()
+        wl, a, w = layer_inputs(HEADLINE, device)
+        qw, s_w = q8.q8_quantize_weight(w, per_row=wl.w_granularity == "row")
+        del w
+        y = torch.empty((wl.M, wl.N), dtype=torch.float32, device=device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        print(json.dumps(measure_f16a(q8, a, qw, s_w, y, flush, args, hbm_peak, tc_peak,
+                                      2.0 * wl.M * wl.N * wl.K)))
         return
     run_ours(args, world, rank, local)
     if world > 1:
