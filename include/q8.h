@@ -344,7 +344,7 @@ q8_status q8_gemm_f16a_s32(const uint16_t* qa16, const int8_t* qw, int64_t M, in
  * quantizer itself and the integer GEMM; Day 98's epilogue): A fp32 [M, K] in host
  * memory -> per-token quantization (symmetric, or asymmetric with colsum) -> the
  * INT32 GEMM against device-resident weights -> y fp32 [M, N] in host memory. The
- * token rows go through in slices of chunk_rows rows (0: about a quarter of M,
+ * token rows go through in slices of chunk_rows rows (0: about a sixteenth of M,
  * whole 256-row tiles): the copy of one slice in, the device work on the previous
  * one and the copy out of the one before overlap. y is the same as that of
  * q8_quantize_act (Q8_PER_ROW) + q8_gemm_dequant over all rows.

@@ -59,8 +59,10 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int64_t chunk_rows_for(int64_t M, int64_t chunk_rows) {
     if (chunk_rows > 0) return chunk_rows < M ? chunk_rows : M;
-    // default: about four slices, whole 256-row GEMM tiles
-    int64_t r = ((M + 3) / 4 + 255) / 256 * 256;
+    // default: about sixteen slices, whole 256-row GEMM tiles (the first copy in and the last
+    // copy out, which nothing overlaps, stay short; at 8192 x 16384 -> 8192, 16 slices took
+    // 3.22 ms against 3.62 ms for 4 and 3.31 ms for 32)
+    int64_t r = ((M + 15) / 16 + 255) / 256 * 256;
     return r < M ? r : M;
 }
 

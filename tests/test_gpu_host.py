@@ -41,7 +41,7 @@ def pinned(x):
     (1000, 264, 512, 1, True),        # one row per slice: 1000 slices through two slots
     (300, 520, 2064, 128, False),     # asymmetric with column sums
     (77, 130, 256, 500, True),        # one slice (chunk > M), N not a multiple of 4
-    (4096, 2048, 4096, 0, True),      # four slices of whole tiles
+    (4096, 2048, 4096, 0, True),      # default slices of whole tiles (256 rows)
 ])
 def test_host_layer_matches_the_device_path(q8, M, N, K, chunk, sym):
     wl = workloads.WORKLOADS["prefill2k" if sym else "relu4k"]
