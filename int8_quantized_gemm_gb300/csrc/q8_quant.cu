@@ -43,17 +43,25 @@ __device__ __forceinline__ int rint_quot(float x, float s, float r) {
     return (int)k;
 }
 
+// The symmetric clamp to [-127, 127] never binds: every x of the row (or tensor) has |x| <= amax
+// and s = RN(max(amax, 1e-8) / 127) >= (amax / 127)(1 - 2^-24), so |RN(x / s)| < 127.0001 and its
+// rint is at most 127 in magnitude (t above is within 2^-14 of it). The code is rint_quot itself.
 __device__ __forceinline__ int sym_code(float x, float s, float r) {
-    return clampi(rint_quot(x, s, r), -127, 127);
+    return rint_quot(x, s, r);
 }
 
 __device__ __forceinline__ int asym_code(float x, float s, float r, int z) {
     return clampi(rint_quot(x, s, r) + z, -128, 127);
 }
 
+// Four codes in [-128, 127] as int8 bytes, a in the lowest. cvt.pack.sat puts its first source in
+// bits 15..8, its second in bits 7..0 (both saturated to the int8 range, which leaves codes of that
+// range unchanged) and the low 16 bits of the third above them.
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
-           ((uint32_t)(d & 0xFF) << 24);
+    uint32_t hi, w;
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;\n" : "=r"(hi) : "r"(d), "r"(c));
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;\n" : "=r"(w) : "r"(b), "r"(a), "r"(hi));
+    return w;
 }
 
 // Two codes as fp16 values (exact for |code| <= 2048), the first in the low half.
