@@ -43,9 +43,9 @@ METRIC = "W8A8 GEMM TOPS (2MNK/s incl. act quantize)"
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# headline GEMM kernel on the headline workload, from an ncu capture (summary and
-# command in profiles/gemm_tcgen05_pair_prefill16k.md). It is reported only while the
-# kernel's source files still hash to the fingerprint the capture was taken on.
+# headline GEMM kernel on the headline workload, from the ncu capture of this kernel.
+# It is reported only while the kernel's source files still hash to the fingerprint the
+# capture was taken on.
 MEASURED_TRAFFIC = {
     "tcgen05_pair": {"bytes": 1_455_588_608 + 252_705_280,
                      "sources": ("q8_gemm_tc2.cu", "q8_tc_ptx.cuh", "q8_internal.h"),
@@ -78,6 +78,16 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def sustained_peak():
+    """The bf16 dense rate measured as a seconds-long loop under the power cap (the denominator for a
+    kernel timed inside a long run), with its source."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
 
 
 class ClockSampler:
@@ -189,12 +199,35 @@ def job_rate(units_per_rank: float, world: int, ms_per_step_max: float, scale: f
 
 # ------------------------------------------------------------------ our arm
 
+_HOST_INPUTS = {}
+
+
+def host_inputs(name):
+    """The workload's fp32 A and W as numpy arrays (drawn once per process)."""
+    if name not in _HOST_INPUTS:
+        wl = workloads.WORKLOADS[name]
+        _HOST_INPUTS[name] = (workloads.make_activations(wl), workloads.make_weights(wl))
+    return _HOST_INPUTS[name]
+
+
 def layer_inputs(name, device):
     import torch
     wl = workloads.WORKLOADS[name]
-    a = torch.from_numpy(workloads.make_activations(wl)).to(device)
-    w = torch.from_numpy(workloads.make_weights(wl)).to(device)
-    return wl, a, w
+    a_h, w_h = host_inputs(name)
+    return wl, torch.from_numpy(a_h).to(device), torch.from_numpy(w_h).to(device)
+
+
+def step_bytes(wl):
+    """Algorithmic bytes of one step: the activation quantizer (read A, write codes and scales, zero
+    points when asymmetric) and the GEMM (codes of A and W, the scales, column sums and zero points
+    when asymmetric, y)."""
+    M, N, K = wl.M, wl.N, wl.K
+    asym = not wl.act_symmetric
+    na = M if wl.act_granularity == "row" else 1
+    nw = N if wl.w_granularity == "row" else 1
+    quant = 5 * M * K + 4 * na * (2 if asym else 1)
+    gemm = M * K + N * K + 4 * nw + 4 * na * (2 if asym else 1) + (4 * N if asym else 0) + 4 * M * N
+    return quant, gemm
 
 
 def run_ours(args, world, rank, local):
@@ -273,6 +306,10 @@ def run_ours(args, world, rank, local):
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
     gemm_bytes = M * K + N * K + 4 * N + 4 * M + 4 * M * N
 
+    # ---- the same step run back to back for seconds, with the clock the power limit leaves
+    sustained = None if args.no_sustained else measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops,
+                                                                 args.sustained_s)
+
     # ---- end to end through the public API: pinned host A in, y back to pinned host
     e2e = None if args.no_e2e else measure_e2e(q8, a, y, step, qw, s_w, colsum, sym, ops, world, args)
 
@@ -294,7 +331,41 @@ def run_ours(args, world, rank, local):
     # ---- fused RMSNorm + per-token quantization of the same activations (HBM-bound)
     rmsq = measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak)
 
-    cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    # ---- every workload of the scope: the small ones measured here, decode and the headline above
+    configs = {}
+    if not args.no_configs:
+        for name in ("tiny", "prefill2k", "relu4k"):
+            configs[name] = measure_config(q8, name, device, args, hbm_peak, tc_peak, flush)
+        if decode is not None:
+            dq, dg = decode["quant_ms"], decode["gemm_ms"]
+            dwl = workloads.WORKLOADS[DECODE]
+            dqb = step_bytes(dwl)[0]
+            configs[DECODE] = {
+                "workload": decode["workload"], "M": dwl.M, "N": dwl.N, "K": dwl.K, "gemm_kernel": decode["gemm_kernel"],
+                "ms_per_step": decode["ms_per_step"], "TOPS": decode["TOPS"], "timing": decode["timing"],
+                "quantizer": {"ms": dq, "GB/s": round(dqb / (dq * 1e-3) / 1e9, 1), "bytes": dqb,
+                              "note": "16 rows: launch-latency bound"},
+                "gemm": {"ms": dg, "GB/s": decode["gemm_GB/s"]},
+                "roofline": {"bound": "hbm", "kernel": f"gemm_{decode['gemm_kernel']}", "achieved": decode["gemm_GB/s"],
+                             "peak": hbm_peak, "unit": "GB/s", "frac": decode["gemm_frac_hbm"],
+                             "algorithmic_bytes_per_launch": decode["algorithmic_bytes"], "ms_per_launch": dg}}
+        configs[HEADLINE] = {
+            "workload": f"{HEADLINE}: A fp32 [{M},{K}] per-token sym x W int8 [{N},{K}] per-channel sym",
+            "M": M, "N": N, "K": K, "gemm_kernel": kernel, "ms_per_step": round(ms_step, 4),
+            "TOPS": round(value / world, 2),
+            "quantizer": {"ms": round(quant_avg, 4), "GB/s": round(quant_gbs, 1),
+                          "frac_hbm": round(quant_gbs / hbm_peak, 4), "bytes": quant_bytes},
+            "gemm": {"ms": round(gemm_avg, 4), "TFLOP/s": round(gemm_tops, 1)},
+            "roofline": {"bound": "tensor", "kernel": f"gemm_{kernel}", "achieved": round(gemm_tops, 1),
+                         "peak": tc_peak, "unit": "TFLOP/s", "frac": round(gemm_tops / tc_peak, 4),
+                         "algorithmic_bytes_per_launch": gemm_bytes, "ms_per_launch": round(gemm_avg, 4)}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(budget_s=args.cpu_budget)
+        cores = len(os.sched_getaffinity(0))
+        for name, entry in configs.items():
+            entry["cpu_baseline"] = {"threaded": cpu} if name == HEADLINE else config_cpu(name, cores)
 
     if rank == 0:
         line = {
@@ -321,6 +392,8 @@ def run_ours(args, world, rank, local):
             "rmsnorm_quantize": rmsq,
             "gemm_bias_bf16": epi,
             "f16_codes": f16a,
+            "configs": configs,
+            "sustained": sustained,
             "w4a8": w4,
             "block_scaled": mx,
             "e2e": e2e,
@@ -346,7 +419,7 @@ def measure_e2e(q8, a, y, step, qw, s_w, colsum, sym, ops, world, args):
     y_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
     ws = torch.empty(q8.q8_linear_host_workspace(M, N, K), dtype=torch.uint8, device=a.device)
     stream = torch.cuda.current_stream()
-    steps = max(1, min(args.steps, 5))
+    steps = max(10, args.steps)
 
     def timed(fn):
         for _ in range(2):
@@ -397,6 +470,15 @@ def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode
         def gemm():
             q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, kernel=kernel)
 
+        def layer():
+            # the default kernel through the one-call layer (its weight stream may start while the
+            # quantizer runs); an explicit kernel as the two calls
+            if kernel == pick:
+                q8.q8_linear(a, qw, s_w, qa=qa, s_a=s_a, y=y)
+            else:
+                quant()
+                gemm()
+
         def loop(fn, n):
             # n launches captured in one CUDA graph, so that host launch overhead (the 16-row
             # quantizer runs for a few microseconds) does not enter the device time
@@ -421,7 +503,7 @@ def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode
         n = max(20, args.steps)
         q_ms = loop(quant, n)
         g_ms = loop(gemm, n)
-        s_ms = loop(lambda: (quant(), gemm()), n)
+        s_ms = loop(layer, n)
         return q_ms, g_ms, s_ms
 
     per_kernel = {}
@@ -667,6 +749,173 @@ def measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, hbm_peak):
             "bytes": nbytes}
 
 
+def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
+    """One workload's step exactly as the headline is timed: q8_quantize_act then q8_gemm_dequant on
+    inputs resident in HBM, the 256 MiB L2 flush before every step, CUDA events around each kernel
+    on the launching stream. The flush (68 us of device time) lets the host queue the step's two
+    launches before the device reaches them, so the events see device time, not launch gaps."""
+    import torch
+    wl, a, w = layer_inputs(name, device)
+    M, N, K = wl.M, wl.N, wl.K
+    apr, wpr, sym = wl.act_granularity == "row", wl.w_granularity == "row", wl.act_symmetric
+    qw, s_w = q8.q8_quantize_weight(w, per_row=wpr)
+    colsum = None if sym else q8.q8_colsum(qw)
+    del w
+    qa = torch.empty((M, K), dtype=torch.int8, device=device)
+    s_a = torch.empty(M if apr else 1, dtype=torch.float32, device=device)
+    z_a = None if sym else torch.empty(M if apr else 1, dtype=torch.int32, device=device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    kernel = q8.q8_gemm_pick(M, N, K)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+    torch.cuda.synchronize()
+    n = max(20, args.steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        evs[i][0].record(stream)
+        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+        evs[i][1].record(stream)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    qms = [e[0].elapsed_time(e[1]) for e in evs]
+    gms = [e[1].elapsed_time(e[2]) for e in evs]
+    sms = [q + g for q, g in zip(qms, gms)]
+    q, g, st = statistics.mean(qms), statistics.mean(gms), statistics.mean(sms)
+    ops = 2.0 * M * N * K
+    qbytes, gbytes = step_bytes(wl)
+    gtf = ops / (g * 1e-3) / 1e12
+    bound = {"tiny": "latency", "decode": "hbm"}.get(name, "tensor")
+    if bound == "tensor":
+        roof = {"bound": "tensor", "kernel": f"gemm_{kernel}", "achieved": round(gtf, 1), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(gtf / tc_peak, 4)}
+    elif bound == "hbm":
+        gbs = gbytes / (g * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": f"gemm_{kernel}", "achieved": round(gbs, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(gbs / hbm_peak, 4)}
+    else:
+        roof = {"bound": "latency", "kernel": f"gemm_{kernel}", "achieved": round(g * 1e3, 2), "unit": "us",
+                "peak": None, "frac": None, "note": "launch-latency bound: reported, no roofline fraction"}
+    roof.update({"algorithmic_bytes_per_launch": gbytes, "ms_per_launch": round(g, 4)})
+    return {
+        "workload": f"{name}: A fp32 [{M},{K}] per-{'token' if apr else 'tensor'} "
+                    f"{'sym' if sym else 'asym'} x W int8 [{N},{K}] per-{'channel' if wpr else 'tensor'} sym",
+        "M": M, "N": N, "K": K, "gemm_kernel": kernel, "steps": n,
+        "ms_per_step": round(st, 4), "step_ms": {"min": round(min(sms), 4), "median": round(statistics.median(sms), 4)},
+        "TOPS": round(ops / (st * 1e-3) / 1e12, 3),
+        "quantizer": {"ms": round(q, 4), "GB/s": round(qbytes / (q * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(qbytes / (q * 1e-3) / 1e9 / hbm_peak, 4), "bytes": qbytes},
+        "gemm": {"ms": round(g, 4), "TFLOP/s": round(gtf, 2)},
+        "roofline": roof,
+    }
+
+
+def oracle_timing(name, threads, rows=None, budget_s=None):
+    """The oracle as it stands on `threads` host cores: quantize the rows of A (the workload's
+    granularity and symmetry) and run the integer GEMM and epilogue against the offline-quantized
+    weights (C, int64 accumulation, OpenMP over output rows). All rows, or a row sample sized from a
+    short probe to take about budget_s seconds."""
+    import oracle
+    wl = workloads.WORKLOADS[name]
+    a_all, w = host_inputs(name)
+    apr, wpr, sym = wl.act_granularity == "row", wl.w_granularity == "row", wl.act_symmetric
+    qw, sw = oracle.quantize_sym(w, wpr)
+
+    def run(r0, r):
+        a = a_all[r0:r0 + r]
+        t = time.perf_counter()
+        if sym:
+            qa, sa = oracle.quantize_sym(a, apr)
+            za = None
+        else:
+            qa, sa, za = oracle.quantize_asym(a, apr)
+        _, st = oracle.linear_codes(qa, sa, za, qw, sw, apr, wpr, threads=threads)
+        assert st == oracle.OK
+        return time.perf_counter() - t
+
+    if rows is None and budget_s is not None and apr:
+        probe = max(1, threads)
+        dt = run(0, probe)
+        rows = int(max(probe, min(wl.M, probe * budget_s / max(dt, 1e-3))))
+        rows = max(probe, rows // probe * probe)
+    rows = wl.M if (rows is None or not apr) else min(rows, wl.M)
+    dt = run(0, rows)
+    if dt < 0.2:   # short runs are repeated (about 0.2 s in all) and averaged
+        reps = int(0.2 / max(dt, 1e-4)) + 1
+        dt = sum(run(0, rows) for _ in range(reps)) / reps
+    ops = 2.0 * rows * wl.N * wl.K
+    whole = "all" if rows == wl.M else f"{rows} of {wl.M}"
+    return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{whole} token rows of {name} (quantize the rows, int64 dot products against all "
+                      f"{wl.N} channels, K={wl.K}, epilogue), {dt:.3f} s", "seconds": round(dt, 3)}
+
+
+def config_cpu(name, cores):
+    """Oracle timings of one workload: threaded over all host cores (full runs where they take a few
+    seconds, a row sample of the large prefill), and single-core runs of the tiny, prefill2k and
+    decode workloads."""
+    out = {}
+    if name == HEADLINE:
+        out["threaded"] = oracle_timing(name, cores, budget_s=8.0)
+    else:
+        out["threaded"] = oracle_timing(name, cores)
+    if name in ("tiny", "prefill2k", "decode"):
+        out["single_core"] = oracle_timing(name, 1)
+    return out
+
+
+def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, seconds):
+    """The headline step back to back for about `seconds` (each step: the L2 flush, then the
+    quantizer and the GEMM between CUDA events), with the SM clock sampled through NVML: the rate a
+    layer keeps up once the power limit has pulled the clock down, against the sustained bf16 peak."""
+    import torch
+    stream = torch.cuda.current_stream()
+    probe = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        flush.zero_()
+        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        probe.append(e0.elapsed_time(e1))
+    n = int(max(50, seconds * 1e3 / statistics.median(probe)))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        w0 = time.perf_counter()
+        for i in range(n):
+            flush.zero_()
+            evs[i][0].record(stream)
+            q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+            evs[i][1].record(stream)
+            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+            evs[i][2].record(stream)
+        torch.cuda.synchronize()
+        w1 = time.perf_counter()
+    assert q8.q8_device_error() == 0
+    qms = [e[0].elapsed_time(e[1]) for e in evs]
+    gms = [e[1].elapsed_time(e[2]) for e in evs]
+    last = n // 2                                   # the second half: after the clock has settled
+    st = statistics.mean(q + g for q, g in zip(qms[last:], gms[last:]))
+    g = statistics.mean(gms[last:])
+    peak, kind = sustained_peak()
+    gtf = ops / (g * 1e-3) / 1e12
+    c = clocks.summary()
+    return {"steps": n, "seconds": round(w1 - w0, 2), "ms_per_step": round(st, 4),
+            "TOPS": round(ops / (st * 1e-3) / 1e12, 1), "gemm_ms": round(g, 4), "gemm_TFLOP/s": round(gtf, 1),
+            "frac": round(gtf / peak, 4), "peak": peak, "peak_source": f"{kind} bf16 dense sustained",
+            "first_half_ms_per_step": round(statistics.mean(q + g for q, g in zip(qms[:last], gms[:last])), 4),
+            "sm_mhz_median": c["sm_mhz"], "sm_max_mhz": c["sm_max_mhz"], "reasons": c["reasons"],
+            "clock_samples": c["samples"], "timing": "mean over the second half of the steps"}
+
+
 # ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
 
 class OracleSample:
@@ -750,6 +999,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped workload")
+    ap.add_argument("--no-configs", action="store_true", help="skip the tiny / prefill2k / relu4k workloads")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the seconds-long sustained run")
+    ap.add_argument("--sustained-s", type=float, default=2.5, help="length of the sustained run (s)")
     ap.add_argument("--w4-only", action="store_true",
                     help="only the W4A8 (int4 weight) measurements (one JSON object, for profiling)")
     ap.add_argument("--mx-only", action="store_true",

@@ -196,6 +196,27 @@ q8_status q8_gemm_dequant(const int8_t* qa, const float* s_a, const int32_t* z_a
                           q8_granularity gw, const int32_t* colsum, int64_t M, int64_t N,
                           int64_t K, float* y, q8_stream_t stream);
 
+/*
+ * The layer on device buffers in one call: q8_quantize_act(a, ga, sym) into the
+ * caller's qa / s_a / z_a, then q8_gemm_dequant (kernel by shape) into y. The
+ * results are those of the two calls made one after the other ("Activation
+ * Quantization Architecture", the quantizer itself and the integer GEMM written
+ * out; Day 98's epilogue).
+ *
+ * Both halves are validated before either is enqueued; arguments, limits and
+ * errors are those of q8_quantize_act and q8_gemm_dequant (qa, s_a, z_a are
+ * outputs of the first and inputs of the second). For M <= 16 the decode kernel
+ * streams the weights while the quantizer is still running (the two are launched
+ * back to back on `stream`); it does so only when qa, s_a and z_a share no byte
+ * with qw, s_w or colsum, and otherwise starts after the quantizer completes.
+ * A standalone q8_gemm_dequant always waits for the kernel before it on the
+ * stream before reading any operand.
+ */
+q8_status q8_linear(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_symmetry sym,
+                    int8_t* qa, float* s_a, int32_t* z_a, const int8_t* qw, const float* s_w,
+                    q8_granularity gw, const int32_t* colsum, int64_t N, float* y,
+                    q8_stream_t stream);
+
 /* q8_gemm_dequant with an explicit kernel choice. A kernel that cannot run
  * the given shape returns Q8_ERR_UNSUPPORTED (Q8_GEMM_AUTO never does). */
 q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* z_a,
@@ -385,14 +406,16 @@ q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q8_symmetry 
  * overlaps (on different streams, or from different host threads onto different
  * streams) race on the array; calls on one stream run one after another and do not.
  * The call allocates no device memory (no cudaMalloc / cudaFree, no allocating library
- * routine). The first call on a device does set-up: it looks up the array's device
- * address (with that device current) and creates the two copy streams and seven events
- * that q8_linear_host keeps per device; make that first call before any stream capture.
+ * routine). Every call looks up the array's device address with the device current (the
+ * first lookup on a device loads the library's device code there). The first call on a
+ * device also does set-up: it creates the two copy streams and seven events that
+ * q8_linear_host keeps per device; make that first call before any stream capture.
  *
  * Arguments as q8_linear_host. chunk_rows = 0 picks the largest slice whose two
  * workspace slots fit the array (whole 256-row tiles when one fits). Errors: as
- * q8_linear_host; Q8_ERR_UNSUPPORTED when q8_linear_host_workspace(M, N, K, chunk_rows)
- * (or, for chunk_rows = 0, that of a one-row slice) exceeds the array.
+ * q8_linear_host, checked first and in the same order; then Q8_ERR_UNSUPPORTED when
+ * q8_linear_host_workspace(M, N, K, chunk_rows) (or, for chunk_rows = 0, that of a
+ * one-row slice) exceeds the array.
  */
 size_t q8_linear_host_static_limit(void);
 q8_status q8_linear_host_static(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
@@ -407,6 +430,31 @@ q8_status q8_linear_host_static(const float* a_host, int64_t M, int64_t K, q8_sy
  */
 q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t N, int64_t K,
                          int32_t* acc, q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
+ * Self-test of the device-side failure path behind Q8_ERR_TIMEOUT (the bounded
+ * waits of the tensor-core and decode kernels). No counterpart in the pages:
+ * it exercises this library's own error handling.
+ *
+ * Runs `kernel` (Q8_GEMM_DECODE, M <= 16, or Q8_GEMM_TCGEN05) on the given
+ * operands with its TMA producer issuing no load and the wait of its converter
+ * (decode: compute) warps on the first loaded stage limited to wait_cycles SM
+ * clock cycles. That wait runs out with no copy and no MMA in flight; the kernel
+ * records it in the device error word, its other roles leave on the kernel's
+ * abort flag, tensor memory is released, and acc is not written. Afterwards
+ * q8_device_error returns Q8_ERR_TIMEOUT with code 2 << 16 (decode kernel: its
+ * compute warps' wait) or 2 (tcgen05 kernel: its converters' wait), and later
+ * calls run normally.
+ *
+ * qa, qw, M, N, K, acc : as q8_gemm_s32_ex (M, N, K > 0; acc is not written).
+ * wait_cycles          : 1 .. 2^31.
+ * Errors: Q8_ERR_INVALID_ARG for another kernel, wait_cycles out of range, or
+ * the argument errors of q8_gemm_s32_ex; Q8_ERR_UNSUPPORTED when the kernel
+ * cannot run the shape.
+ */
+q8_status q8_selftest_wait_timeout(q8_gemm_kernel kernel, const int8_t* qa, const int8_t* qw,
+                                   int64_t M, int64_t N, int64_t K, int32_t* acc,
+                                   int64_t wait_cycles, q8_stream_t stream);
 
 /* The kernel q8_gemm_dequant would run for this shape (never Q8_GEMM_AUTO). */
 q8_gemm_kernel q8_gemm_pick(int64_t M, int64_t N, int64_t K);

@@ -28,7 +28,8 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error", "KERNELS",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error",
+    "q8_selftest_wait_timeout", "KERNELS",
 ]
 
 LIB_PATH = _build.LIB
@@ -74,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_w4a8_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_quantize_weight_mx.argtypes = [p, i64, i64, i32, p, p, p]
     lib.q8_gemm_mx_ex.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
+    lib.q8_linear.argtypes = [p, i64, i64, i32, i32, p, p, p, p, p, i32, p, i64, p, p]
+    lib.q8_selftest_wait_timeout.argtypes = [i32, p, p, i64, i64, i64, p, i64, p]
     lib.q8_linear_host_workspace.argtypes = [i64, i64, i64, i64]
     lib.q8_linear_host_workspace.restype = ctypes.c_size_t
     lib.q8_linear_host.argtypes = [p, i64, i64, i32, p, p, i32, p, i64, p, i64, p, ctypes.c_size_t, p]
@@ -86,7 +89,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
                  "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
-                 "q8_linear_host", "q8_gemm_pick", "q8_device_error"):
+                 "q8_linear", "q8_linear_host", "q8_gemm_pick", "q8_device_error", "q8_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -382,10 +385,37 @@ def q8_gemm_s32(qa, qw, out=None, kernel: str = "auto", stream=None):
 
 
 def q8_linear(a, qw, s_w, colsum=None, per_row: bool = True, symmetric: bool = True, kernel: str = "auto",
-              stream=None):
-    """Whole W8A8 layer on fp32 activations: dynamic quantization of a, then the GEMM + epilogue."""
-    qa, s_a, z_a = q8_quantize_act(a, per_row=per_row, symmetric=symmetric, stream=stream)
-    return q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, kernel=kernel, stream=stream)
+              qa=None, s_a=None, z_a=None, y=None, stream=None):
+    """Whole W8A8 layer on fp32 activations: dynamic quantization of a, then the GEMM + epilogue
+    (one C call, q8_linear, for kernel="auto"; an explicit kernel runs the two calls). Returns y."""
+    if kernel != "auto":
+        qa, s_a, z_a = q8_quantize_act(a, per_row=per_row, symmetric=symmetric, qa=qa, s_a=s_a, z_a=z_a,
+                                       stream=stream)
+        return q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, kernel=kernel, y=y, stream=stream)
+    _need(a, torch.float32, "a", 2)
+    _need(qw, torch.int8, "qw", 2)
+    _need(s_w, torch.float32, "s_w", 1)
+    M, K = a.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qw must be [N, K] with the K of a")
+    n = M if per_row else 1
+    qa = torch.empty((M, K), dtype=torch.int8, device=a.device) if qa is None else qa
+    s_a = torch.empty(n, dtype=torch.float32, device=a.device) if s_a is None else s_a
+    if symmetric:
+        z_a = None
+    elif z_a is None:
+        z_a = torch.empty(n, dtype=torch.int32, device=a.device)
+    if not symmetric and colsum is None:
+        raise ValueError("asymmetric activations need colsum")
+    y = torch.empty((M, N), dtype=torch.float32, device=a.device) if y is None else y
+    _need(y, torch.float32, "y", 2)
+    gw = Q8_PER_ROW if (s_w.numel() == N and N != 1) else Q8_PER_TENSOR
+    _check(load().q8_linear(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
+                            Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(s_a), _ptr(z_a), _ptr(qw),
+                            _ptr(s_w), gw, _ptr(colsum if not symmetric else None), N, _ptr(y), _stream(stream)),
+           "q8_linear")
+    return y
 
 
 def q8_linear_host_workspace(M: int, N: int, K: int, chunk_rows: int = 0) -> int:
@@ -427,6 +457,19 @@ def q8_gemm_pick(M: int, N: int, K: int) -> str:
 
 def q8_launch_count() -> int:
     return int(load().q8_launch_count())
+
+
+def q8_selftest_wait_timeout(qa, qw, kernel: str = "decode", wait_cycles: int = 1 << 24, stream=None):
+    """Self-test of the bounded device waits: runs `kernel` ("decode" or "tcgen05") with its loads
+    withheld so that its first wait runs out after wait_cycles; read the result with q8_device_error()."""
+    _need(qa, torch.int8, "qa", 2)
+    _need(qw, torch.int8, "qw", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    acc = torch.zeros((M, N), dtype=torch.int32, device=qa.device)
+    _check(load().q8_selftest_wait_timeout(KERNELS[kernel], _ptr(qa), _ptr(qw), M, N, K, _ptr(acc), wait_cycles,
+                                           _stream(stream)), "q8_selftest_wait_timeout")
+    return acc
 
 
 def q8_device_error() -> int:

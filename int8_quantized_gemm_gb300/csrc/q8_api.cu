@@ -69,7 +69,8 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
                       q8_stream_t stream, const Variant* var = nullptr, bool w4 = false,
-                      const MxWeights* mx = nullptr, bool a16 = false) {
+                      const MxWeights* mx = nullptr, bool a16 = false, bool validate_only = false,
+                      bool early_weights = false, long long selftest_wait = 0) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -112,9 +113,12 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
         if (mx && (!mx->sf || !aligned(mx->sf, 4))) return Q8_ERR_INVALID_ARG;
     }
     if (M > INT32_MAX || N > INT32_MAX) return Q8_ERR_UNSUPPORTED;
+    if (validate_only) return Q8_OK;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     q8::Epilogue ep{s_a, z_a, s_w, colsum, ga == Q8_PER_ROW, gw == Q8_PER_ROW, y, out_i32};
+    ep.pdl_early_weights = early_weights;
+    ep.selftest_wait_cycles = selftest_wait;
     if (var) {
         ep.bias = var->bias;
         ep.out_kind = var->out_type == Q8_OUT_BF16 ? q8::kOutBF16 : var->out_type == Q8_OUT_I8 ? q8::kOutI8 : q8::kOutF32;
@@ -184,28 +188,63 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
     }
 }
 
+q8_status check_act_args(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym, const int8_t* qa,
+                         const float* s_a, const int32_t* z_a) {
+    if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
+    if ((sym == Q8_ASYMMETRIC) != (z_a != nullptr)) return Q8_ERR_INVALID_ARG;
+    if (z_a && !aligned(z_a, 4)) return Q8_ERR_INVALID_ARG;
+    return check_quant_args(a, M, K, g, qa, s_a, M > 0 && K > 0);
+}
+
+// [p, p + bytes) and [q, q + bytes2) share a byte.
+bool overlap(const void* p, size_t bytes, const void* q, size_t bytes2) {
+    if (!p || !q || bytes == 0 || bytes2 == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + bytes2 && b < a + bytes;
+}
+
 }  // namespace
 
 extern "C" {
 
 q8_status q8_quantize_act(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym,
                           int8_t* qa, float* s_a, int32_t* z_a, q8_stream_t stream) {
-    if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
-    if ((sym == Q8_ASYMMETRIC) != (z_a != nullptr)) return Q8_ERR_INVALID_ARG;
-    if (z_a && !aligned(z_a, 4)) return Q8_ERR_INVALID_ARG;
-    q8_status st = check_quant_args(a, M, K, g, qa, s_a, M > 0 && K > 0);
+    q8_status st = check_act_args(a, M, K, g, sym, qa, s_a, z_a);
     if (st != Q8_OK) return st;
     if (g == Q8_PER_ROW && M == 0) return Q8_OK;
     return from_cuda(q8::launch_quantize(a, M, K, g == Q8_PER_ROW, qa, s_a, z_a,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+q8_status q8_linear(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_symmetry sym, int8_t* qa, float* s_a,
+                    int32_t* z_a, const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                    int64_t N, float* y, q8_stream_t stream) {
+    // Both halves are validated before either is enqueued.
+    q8_status st = check_act_args(a, M, K, ga, sym, qa, s_a, z_a);
+    if (st != Q8_OK) return st;
+    st = gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream, nullptr, false,
+                     nullptr, false, true);
+    if (st != Q8_OK) return st;
+    if (M == 0) return Q8_OK;
+    st = q8_quantize_act(a, M, K, ga, sym, qa, s_a, z_a, stream);
+    if (st != Q8_OK) return st;
+    // The decode kernels may start their weight stream while the quantizer runs, unless the
+    // quantizer's outputs share memory with a weight operand.
+    const size_t ns = ga == Q8_PER_ROW ? (size_t)M * 4 : 4, nw = gw == Q8_PER_ROW ? (size_t)N * 4 : 4;
+    const void* outs[3] = {qa, s_a, z_a};
+    const size_t out_bytes[3] = {(size_t)M * (size_t)K, ns, z_a ? ns : 0};
+    const void* ins[3] = {qw, s_w, z_a ? colsum : nullptr};
+    const size_t in_bytes[3] = {(size_t)N * (size_t)K, nw, (size_t)N * 4};
+    bool early = true;
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j) early = early && !overlap(outs[i], out_bytes[i], ins[j], in_bytes[j]);
+    return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream, nullptr,
+                       false, nullptr, false, false, early);
+}
+
 q8_status q8_quantize_act_f16(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym,
                               uint16_t* qa16, float* s_a, int32_t* z_a, q8_stream_t stream) {
-    if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
-    if ((sym == Q8_ASYMMETRIC) != (z_a != nullptr)) return Q8_ERR_INVALID_ARG;
-    if (z_a && !aligned(z_a, 4)) return Q8_ERR_INVALID_ARG;
-    q8_status st = check_quant_args(a, M, K, g, reinterpret_cast<const int8_t*>(qa16), s_a, M > 0 && K > 0);
+    q8_status st = check_act_args(a, M, K, g, sym, reinterpret_cast<const int8_t*>(qa16), s_a, z_a);
     if (st != Q8_OK) return st;
     if (g == Q8_PER_ROW && M == 0) return Q8_OK;
     return from_cuda(q8::launch_quantize_f16(a, M, K, g == Q8_PER_ROW, qa16, s_a, z_a,
@@ -345,6 +384,15 @@ q8_status q8_gemm_s32_ex(const int8_t* qa, const int8_t* qw, int64_t M, int64_t 
     }
     return gemm_common(qa, nullptr, nullptr, Q8_PER_TENSOR, qw, nullptr, Q8_PER_TENSOR, nullptr, M, N, K,
                        nullptr, acc, kernel, stream);
+}
+
+q8_status q8_selftest_wait_timeout(q8_gemm_kernel kernel, const int8_t* qa, const int8_t* qw, int64_t M, int64_t N,
+                                   int64_t K, int32_t* acc, int64_t wait_cycles, q8_stream_t stream) {
+    if (kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_TCGEN05) return Q8_ERR_INVALID_ARG;
+    if (wait_cycles < 1 || wait_cycles > (int64_t(1) << 31)) return Q8_ERR_INVALID_ARG;
+    if (!acc || M <= 0 || N <= 0 || K <= 0) return Q8_ERR_INVALID_ARG;
+    return gemm_common(qa, nullptr, nullptr, Q8_PER_TENSOR, qw, nullptr, Q8_PER_TENSOR, nullptr, M, N, K, nullptr,
+                       acc, kernel, stream, nullptr, false, nullptr, false, false, false, (long long)wait_cycles);
 }
 
 // Measured on GB300: the CTA-pair kernel is the fastest tcgen05 kernel at every

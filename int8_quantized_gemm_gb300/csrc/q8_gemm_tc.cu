@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLow));
       if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if (lane == 0 && ep.selftest_wait_cycles == 0) {
             int i = 0, kb = 0, m0 = 0, n0 = 0;
             for (int g = 0; g < total_g; ++g) {
                 if (kb == 0) tile_coords(tg, blockIdx.x + i * gridDim.x, m0, n0);
@@ -204,9 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t src0 = (uint32_t)(ct * 16);
         const uint32_t dst0 = sw128(r0, 2 * c0);
         const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
+        const long long full_limit = ep.selftest_wait_cycles > 0 ? ep.selftest_wait_cycles : kTimeoutCycles;
         for (int g = 0; g < total_g; ++g) {
             const int s8 = g % S8, s16 = g % S16;
-            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc_error)) break;
+            if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc_error, 0,
+                           full_limit))
+                break;
             const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8 + src0;
             uint4 in[8];
 #pragma unroll

@@ -97,10 +97,15 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
 }
 
 // Programmatic dependent launch: the decode kernels are launched so that they may start while
-// the kernel before them on the stream (the activation quantizer) is still running. Nothing they
-// read from that kernel's outputs (token codes, token scales and zero points) is touched before
+// the kernel before them on the stream is still running. Nothing they read is touched before
 // griddep_wait(), which returns once the preceding kernel has completed and its writes are
-// visible (at once when there is none); the weight stream starts before it.
+// visible (at once when there is none), with one exception: when the launch follows the
+// library's own activation quantizer of the same layer (Epilogue::pdl_early_weights, set only by
+// q8_linear and the host-buffer layer, which launch the two back to back and check that the
+// quantizer's outputs do not overlap the weight operands), the first ring of weight (and scale)
+// boxes is loaded before the wait. That quantizer writes only codes, scales and zero points, and
+// it was itself launched without the attribute, so every earlier kernel has completed before it
+// started and before this kernel could start.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -188,9 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            // The first ring's worth of stages gets its weight boxes before the wait on the
-            // quantizer, its token boxes after it (the ring is empty, so no empty-slot waits).
+        if (lane == 0 && ep.selftest_wait_cycles == 0) {
+            // The first ring's worth of stages gets its weight boxes (before the wait on the
+            // quantizer where the launch allows it), its token boxes after the wait (the ring is
+            // empty, so no empty-slot waits).
             const int pre = total_g < S8 ? total_g : S8;
             auto kx_of = [&](int kb) { return (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kBK; };
             auto load_w = [&](int g, int kb, int i) {
@@ -210,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bar_full + 8 * s);
             };
             int i = 0, kb = 0;
+            if (!ep.pdl_early_weights) griddep_wait();
             for (int g = 0; g < pre; ++g) {
                 mbar_expect_tx(bar_full + 8 * (g % S8), kStage);
                 load_w(g, kb, i);
@@ -275,11 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb = 0, ti = 0, in_chunk = 0, g = 0;
         int sum0 = 0, sum1 = 0;        // first tile: code sums of tokens g, g + 8 over this lane's K
         int esum0 = 0, esum1 = 0;      // code sums of the epilogue tokens em, em + 8
+        const long long full_limit = ep.selftest_wait_cycles > 0 ? ep.selftest_wait_cycles : kTimeoutCycles;
         for (; g < total_g; ++g) {
             const int s = g % S8;
             // warp-uniform: the whole warp leaves together when a wait gives up (abort)
             if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (uint32_t)((g / S8) & 1), abort_flag,
-                                                   kErrConvFull, &g_gemv_mma_error)))
+                                                   kErrConvFull, &g_gemv_mma_error, 0, full_limit)))
                 break;
             const uint32_t st = sbase + s * kStage;
             if constexpr (W4) {
@@ -488,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            // As in the int8 kernel: the first ring's weight and scale boxes before the wait on
-            // the quantizer, its token boxes after it.
+            // As in the int8 kernel: the first ring's weight and scale boxes (before the wait on
+            // the quantizer where the launch allows it), its token boxes after the wait.
             const int pre = total_g < S8 ? total_g : S8;
             auto kx_of = [&](int kb) { return (kb + k_rot >= KB ? kb + k_rot - KB : kb + k_rot) * kMxBK; };
             auto load_w = [&](int g, int kb, int i) {
@@ -509,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bar_full + 8 * s);
             };
             int i = 0, kb = 0;
+            if (!ep.pdl_early_weights) griddep_wait();
             for (int g = 0; g < pre; ++g) {
                 mbar_expect_tx(bar_full + 8 * (g % S8), kMxStage + kMxSf);
                 load_w(g, kb, i);

@@ -105,21 +105,36 @@ extern "C" size_t q8_linear_host_workspace(int64_t M, int64_t N, int64_t K, int6
     return 2 * slot_bytes(R, N, K);
 }
 
-extern "C" q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
-                                    const float* s_w, q8_granularity gw, const int32_t* colsum, int64_t N,
-                                    float* y_host, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
-                                    q8_stream_t stream) {
+// The argument checks of the host-buffer layer (everything but the workspace). Q8_OK with
+// *empty set when there is nothing to do.
+static q8_status check_host_args(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
+                                 const float* s_w, q8_granularity gw, const int32_t* colsum, int64_t N,
+                                 const float* y_host, int64_t chunk_rows, bool* empty) {
+    *empty = false;
     if (M < 0 || N < 0 || K < 0 || chunk_rows < 0) return Q8_ERR_INVALID_ARG;
     if (sym != Q8_SYMMETRIC && sym != Q8_ASYMMETRIC) return Q8_ERR_INVALID_ARG;
     if (gw != Q8_PER_TENSOR && gw != Q8_PER_ROW) return Q8_ERR_INVALID_ARG;
     if (K % 16 != 0 || K > (sym == Q8_ASYMMETRIC ? 65792 : 131056)) return Q8_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0) return Q8_OK;
+    if (M == 0 || N == 0) {
+        *empty = true;
+        return Q8_OK;
+    }
     if (!a_host && K > 0) return Q8_ERR_INVALID_ARG;
     if (!y_host || !s_w || (K > 0 && !qw)) return Q8_ERR_INVALID_ARG;
     if (sym == Q8_ASYMMETRIC && !colsum) return Q8_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(qw) & 15) != 0 || (reinterpret_cast<uintptr_t>(s_w) & 3) != 0 ||
         (reinterpret_cast<uintptr_t>(colsum) & 3) != 0)
         return Q8_ERR_INVALID_ARG;
+    return Q8_OK;
+}
+
+extern "C" q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q8_symmetry sym, const int8_t* qw,
+                                    const float* s_w, q8_granularity gw, const int32_t* colsum, int64_t N,
+                                    float* y_host, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
+                                    q8_stream_t stream) {
+    bool empty = false;
+    const q8_status chk = check_host_args(a_host, M, K, sym, qw, s_w, gw, colsum, N, y_host, chunk_rows, &empty);
+    if (chk != Q8_OK || empty) return chk;
     const int64_t R = chunk_rows_for(M, chunk_rows);
     const size_t per_slot = slot_bytes(R, N, K);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 || workspace_bytes < 2 * per_slot)
@@ -158,10 +173,8 @@ extern "C" q8_status q8_linear_host(const float* a_host, int64_t M, int64_t K, q
             break;
         }
         int32_t* z = sym == Q8_ASYMMETRIC ? sl.z_a : nullptr;
-        if (K > 0) st = q8_quantize_act(sl.a, rows, K, Q8_PER_ROW, sym, sl.qa, sl.s_a, z, stream);
-        if (st == Q8_OK)
-            st = q8_gemm_dequant(sl.qa, sl.s_a, z, Q8_PER_ROW, qw, s_w, gw, z ? colsum : nullptr, rows, N, K, sl.y,
-                                 stream);
+        st = q8_linear(sl.a, rows, K, Q8_PER_ROW, sym, sl.qa, sl.s_a, z, qw, s_w, gw, z ? colsum : nullptr, N, sl.y,
+                       stream);
         if (st != Q8_OK) break;
         e = cudaEventRecord(p.ev_comp[b], s);
         // out: after the compute of slice i
@@ -192,23 +205,17 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)64 << 20;   // 64 MiB
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch per device (host code only sees a stand-in for it).
-void* g_scratch_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
+// Device address of g_static_scratch on the current device (host code only sees a stand-in
+// for the array). Looked up on every call, with the device current: the first lookup on a
+// device loads the module there, later ones are a table lookup, and an address can never be
+// stale after a device reset (the module, and with it the array, is then loaded anew).
 q8_status static_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q8_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
-            (void)cudaGetLastError();
-            return Q8_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+        (void)cudaGetLastError();
+        return Q8_ERR_CUDA;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return Q8_OK;
 }
 
@@ -220,8 +227,10 @@ extern "C" q8_status q8_linear_host_static(const float* a_host, int64_t M, int64
                                            const int8_t* qw, const float* s_w, q8_granularity gw,
                                            const int32_t* colsum, int64_t N, float* y_host, int64_t chunk_rows,
                                            q8_stream_t stream) {
-    if (M < 0 || N < 0 || K < 0 || chunk_rows < 0) return Q8_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return Q8_OK;
+    // the same checks, in the same order, as q8_linear_host, before the size check
+    bool empty = false;
+    const q8_status chk = check_host_args(a_host, M, K, sym, qw, s_w, gw, colsum, N, y_host, chunk_rows, &empty);
+    if (chk != Q8_OK || empty) return chk;
     int64_t R = chunk_rows;
     if (R == 0) {
         // the largest slice whose two workspace slots fit in the array (whole 256-row tiles when

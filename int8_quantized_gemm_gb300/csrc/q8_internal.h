@@ -72,6 +72,16 @@ struct Epilogue {
     // accumulates sum_k qa * (q * s) in fp32 and the epilogue is y = fl(T * s_a) (+ bias).
     const uint32_t* mx_sf = nullptr;
     int mx_group = 0;
+    // Decode kernels (programmatic dependent launch): load the first weight boxes before waiting
+    // for the preceding kernel. Only for a launch that directly follows the library's activation
+    // quantizer of the same layer on the same stream, whose outputs do not overlap the weights.
+    bool pdl_early_weights = false;
+    // Self-test of the bounded waits (q8_selftest_wait_timeout), 0 in every other launch. When
+    // > 0, the TMA producer of the single-CTA tcgen05 kernel or of the int8 decode kernel issues
+    // no load, and the consumers' wait on the first loaded stage (converter warps, compute
+    // warps) gives up after this many clock cycles, with nothing asynchronous in flight; the
+    // other roles leave on the abort flag.
+    long long selftest_wait_cycles = 0;
 };
 
 #ifdef __CUDACC__

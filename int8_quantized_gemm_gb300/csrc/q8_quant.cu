@@ -3,9 +3,11 @@
 // These kernels are HBM-bound streams: each fp32 element is read once from
 // HBM (4 bytes) and its code written once (1 byte). Per-row quantization keeps
 // the whole row in registers between the range reduction and the code pass,
-// so the row is never re-read. Arithmetic follows the rules in q8.h exactly:
-// IEEE fp32 division (__fdiv_rn), round-half-to-even (__float2int_rn), and no
-// contraction of multiplies into FMAs (the file is built with -fmad=false).
+// so the row is never re-read. Results follow the rules in q8.h exactly: the
+// codes are those of the IEEE fp32 quotient rounded half to even, and no multiply
+// is contracted into an FMA unless written as one (the file is built with
+// -fmad=false). Where a cheaper form than one division and one conversion per
+// element gives the same bits, the argument is written beside it.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -31,52 +33,61 @@ __device__ __forceinline__ void asym_params(float lo, float hi, float* s, int* z
     *z = clampi(-128 - __float2int_rn(__fdiv_rn(lo, sc)), -128, 127);
 }
 
+// 1.5 * 2^23: for |t| < 2^22, RN(t + kMagic) = kMagic + rint(t) (the addition rounds to the
+// integer grid, half to even), so the low bits of its encoding hold rint(t) in two's complement
+// (kMagicBits + rint(t)); no conversion instruction is needed.
+constexpr float kMagic = 12582912.0f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
 // rint(RN(x / s)), the code of the IEEE quotient rounded half to even, for |x / s| <= 256, from the
 // row's reciprocal r = RN(1 / s). t = RN(x r) carries two roundings of relative size <= 2^-24 each,
 // RN(x / s) one, so |t - RN(x / s)| <= 256 (1.5 2^-23 + 2^-48) < 2^-14. Unless t lies within 2^-14
 // of a half-integer, no half-integer separates the two and they round to the same integer; near a
-// half-integer (exact ties included) the IEEE quotient itself is rounded. t - rint(t) is exact.
-__device__ __forceinline__ int rint_quot(float x, float s, float r) {
+// half-integer (exact ties included) the IEEE quotient itself is rounded. t is rounded by the
+// kMagic addition, and t - rint(t) is exact. Returns a word whose value minus kMagicBits is the
+// integer (so its low byte is the int8 code).
+__device__ __forceinline__ uint32_t rint_quot_bits(float x, float s, float r) {
     const float t = __fmul_rn(x, r);
-    const float k = rintf(t);
-    if (fabsf(__fsub_rn(t, k)) >= 0.5f - 0x1p-14f) return __float2int_rn(__fdiv_rn(x, s));
-    return (int)k;
+    const float u = __fadd_rn(t, kMagic);
+    if (fabsf(__fsub_rn(t, __fsub_rn(u, kMagic))) >= 0.5f - 0x1p-14f)
+        return kMagicBits + (uint32_t)__float2int_rn(__fdiv_rn(x, s));
+    return __float_as_uint(u);
 }
 
 // The symmetric clamp to [-127, 127] never binds: every x of the row (or tensor) has |x| <= amax
 // and s = RN(max(amax, 1e-8) / 127) >= (amax / 127)(1 - 2^-24), so |RN(x / s)| < 127.0001 and its
-// rint is at most 127 in magnitude (t above is within 2^-14 of it). The code is rint_quot itself.
-__device__ __forceinline__ int sym_code(float x, float s, float r) {
-    return rint_quot(x, s, r);
+// rint is at most 127 in magnitude (t above is within 2^-14 of it). The code is rint_quot_bits
+// itself: its low byte.
+__device__ __forceinline__ uint32_t sym_code(float x, float s, float r) {
+    return rint_quot_bits(x, s, r);
 }
 
-__device__ __forceinline__ int asym_code(float x, float s, float r, int z) {
-    return clampi(rint_quot(x, s, r) + z, -128, 127);
+// Asymmetric: clamp(rint(x / s) + z, -128, 127); zoff = z - kMagicBits (mod 2^32).
+__device__ __forceinline__ uint32_t asym_code(float x, float s, float r, int zoff) {
+    return (uint32_t)clampi((int)rint_quot_bits(x, s, r) + zoff, -128, 127);
 }
 
-// Four codes in [-128, 127] as int8 bytes, a in the lowest. cvt.pack.sat puts its first source in
-// bits 15..8, its second in bits 7..0 (both saturated to the int8 range, which leaves codes of that
-// range unchanged) and the low 16 bits of the third above them.
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-    uint32_t hi, w;
-    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;\n" : "=r"(hi) : "r"(d), "r"(c));
-    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;\n" : "=r"(w) : "r"(b), "r"(a), "r"(hi));
-    return w;
+// The low bytes of four words as one word, a's in the lowest byte.
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
 
-// Two codes as fp16 values (exact for |code| <= 2048), the first in the low half.
-__device__ __forceinline__ uint32_t pack_h2(int a, int b) {
-    return (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
-}
-
-// Codes of elements 4i .. 4i + 3 of a row (or tensor) whose codes start at q: int8 (one 32-bit
-// word) or, for H, fp16 values (8 bytes).
+// Codes of elements 4i .. 4i + 3 (the low bytes of a .. d) of a row (or tensor) whose codes start
+// at q: int8 (one 32-bit word) or, for H, fp16 values (8 bytes). fp16: the half with bits
+// 0x6400 | (byte ^ 0x80) is 1024 + (code + 128) exactly, and subtracting 1152 leaves the code.
 template <bool H>
-__device__ __forceinline__ void store_codes4(void* q, int64_t i, int a, int b, int c, int d) {
-    if constexpr (H)
-        reinterpret_cast<uint2*>(q)[i] = make_uint2(pack_h2(a, b), pack_h2(c, d));
-    else
-        reinterpret_cast<uint32_t*>(q)[i] = pack4(a, b, c, d);
+__device__ __forceinline__ void store_codes4(void* q, int64_t i, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    const uint32_t w = pack4(a, b, c, d);
+    if constexpr (H) {
+        uint32_t lo, hi;
+        asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(__byte_perm(w, 0x6464u, 0x5140u) ^ 0x00800080u),
+            "r"(0x64806480u));
+        asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(__byte_perm(w, 0x6464u, 0x5342u) ^ 0x00800080u),
+            "r"(0x64806480u));
+        reinterpret_cast<uint2*>(q)[i] = make_uint2(lo, hi);
+    } else {
+        reinterpret_cast<uint32_t*>(q)[i] = w;
+    }
 }
 
 // Block-wide max of two values (hi, and nlo = -lo for the asymmetric range).
@@ -147,14 +158,15 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
+    [[maybe_unused]] const int zoff = zp - (int)kMagicBits;
     void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
         if (i < n4) {
             if (ASYM)
-                store_codes4<H>(qr, i, asym_code(v[j].x, sc, rc, zp), asym_code(v[j].y, sc, rc, zp),
-                                asym_code(v[j].z, sc, rc, zp), asym_code(v[j].w, sc, rc, zp));
+                store_codes4<H>(qr, i, asym_code(v[j].x, sc, rc, zoff), asym_code(v[j].y, sc, rc, zoff),
+                                asym_code(v[j].z, sc, rc, zoff), asym_code(v[j].w, sc, rc, zoff));
             else
                 store_codes4<H>(qr, i, sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
                                 sym_code(v[j].w, sc, rc));
@@ -196,12 +208,13 @@ __global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* _
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
+    [[maybe_unused]] const int zoff = zp - (int)kMagicBits;
     void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         float4 v = __ldcs(xr + i);
         if (ASYM)
-            store_codes4<H>(qr, i, asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
-                            asym_code(v.w, sc, rc, zp));
+            store_codes4<H>(qr, i, asym_code(v.x, sc, rc, zoff), asym_code(v.y, sc, rc, zoff), asym_code(v.z, sc, rc, zoff),
+                            asym_code(v.w, sc, rc, zoff));
         else
             store_codes4<H>(qr, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
                             sym_code(v.w, sc, rc));
@@ -261,14 +274,14 @@ __global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restri
                                                            void* __restrict__ q) {
     const float sc = s[0];
     const float rc = __fdiv_rn(1.0f, sc);
-    const int zp = ASYM ? z[0] : 0;
+    [[maybe_unused]] const int zoff = (ASYM ? z[0] : 0) - (int)kMagicBits;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 v = __ldcs(x4 + i);
         if (ASYM)
-            store_codes4<H>(q, i, asym_code(v.x, sc, rc, zp), asym_code(v.y, sc, rc, zp), asym_code(v.z, sc, rc, zp),
-                            asym_code(v.w, sc, rc, zp));
+            store_codes4<H>(q, i, asym_code(v.x, sc, rc, zoff), asym_code(v.y, sc, rc, zoff), asym_code(v.z, sc, rc, zoff),
+                            asym_code(v.w, sc, rc, zoff));
         else
             store_codes4<H>(q, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
                             sym_code(v.w, sc, rc));
@@ -318,9 +331,16 @@ __device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l
     lo = __fadd_rn(lo, __fadd_rn(l2, e));
 }
 
+// hi + lo += v * v for a running pair of non-negative parts: the square is split into its fp32
+// product and the exact remainder (one FMA), and the product is added by Fast2Sum (Dekker 1971)
+// on the larger and the smaller operand (both >= 0), whose error term is exact.
 __device__ __forceinline__ void pair_add_square(float& hi, float& lo, float v) {
     const float p = __fmul_rn(v, v);
-    pair_add(hi, lo, p, __fmaf_rn(v, v, -p));   // v * v == p + remainder exactly
+    const float e = __fmaf_rn(v, v, -p);   // v * v == p + e exactly
+    const float a = fmaxf(hi, p), b = fminf(hi, p);
+    const float s = __fadd_rn(a, b);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(b, __fsub_rn(s, a)), e));
 }
 
 // Block-wide sum of the pairs; every thread receives lane 0's fl(hi + lo), so the whole
@@ -351,7 +371,36 @@ __device__ __forceinline__ float rms_of(float sumsq, int64_t cols, float eps) {
     return __fsqrt_rn(__fadd_rn(mean, eps));
 }
 
-__device__ __forceinline__ float norm1(float x, float rms, float g) { return __fmul_rn(__fdiv_rn(x, rms), g); }
+// RN(x / d) from r = RN(1 / d) by Markstein's correction (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990): for a
+// quotient q within one ulp of x / d, the remainder x - q d is exact in one FMA, and
+// RN(q + (x - q d) r) is the correctly rounded quotient. q0 = RN(x r) is within 1.5 ulp of x / d;
+// its correction q1 is within half an ulp plus 2^-22 ulp (so within one ulp), and the correction
+// of q1 is RN(x / d). Valid while nothing under- or overflows: d in [2^-60, 2^60] and |x| >= 2^-60
+// (quotients and remainders normal); the caller checks both. x = -0 gives +0 (IEEE: -0); the
+// sign of a zero y changes neither the row maximum nor its code.
+constexpr uint32_t kDivTinyBits = 0x21800000u;   // 2^-60
+__device__ __forceinline__ float div_markstein(float x, float d, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
+    return __fmaf_rn(__fmaf_rn(-q1, d, x), r, q1);
+}
+
+// The row's normaliser: rms, its reciprocal and whether Markstein's quotient applies to the row.
+struct RowNorm {
+    float rms, rr;
+    bool fast;
+    __device__ __forceinline__ explicit RowNorm(float rms_) : rms(rms_) {
+        fast = rms_ >= 0x1p-60f && rms_ <= 0x1p60f;
+        rr = __fdiv_rn(1.0f, rms_);
+    }
+    // y = RN(RN(x / rms) * g): the quotient by Markstein's correction where it is exact, else IEEE.
+    __device__ __forceinline__ float operator()(float x, float g) const {
+        const uint32_t ax = __float_as_uint(x) & 0x7FFFFFFFu;
+        const float q = (fast && ax - 1u >= kDivTinyBits - 1u) ? div_markstein(x, rms, rr) : __fdiv_rn(x, rms);
+        return __fmul_rn(q, g);
+    }
+};
 
 // One CTA per row, the row in registers (VPT float4 per thread): one HBM read of x. Up to
 // four float4 per thread the kernel fits 32 registers, so two 1024-thread CTAs share an SM
@@ -379,15 +428,14 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1))
             pair_add_square(hi, lo, v[j].w);
         }
     }
-    const float rms = rms_of(block_sum_pairs(hi, lo, red), cols, eps);
+    const RowNorm nrm(rms_of(block_sum_pairs(hi, lo, red), cols, eps));
     float amax = 0.0f, unused = 0.0f;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
         if (i < n4) {
             const float4 g = __ldg(g4 + i);
-            v[j] = make_float4(norm1(v[j].x, rms, g.x), norm1(v[j].y, rms, g.y), norm1(v[j].z, rms, g.z),
-                               norm1(v[j].w, rms, g.w));
+            v[j] = make_float4(nrm(v[j].x, g.x), nrm(v[j].y, g.y), nrm(v[j].z, g.z), nrm(v[j].w, g.w));
             amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
         }
     }
@@ -424,13 +472,13 @@ __global__ void __launch_bounds__(1024)
         pair_add_square(hi, lo, v.z);
         pair_add_square(hi, lo, v.w);
     }
-    const float rms = rms_of(block_sum_pairs(hi, lo, red), cols, eps);
+    const RowNorm nrm(rms_of(block_sum_pairs(hi, lo, red), cols, eps));
     float amax = 0.0f, unused = 0.0f;
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         const float4 v = xr[i];
         const float4 g = __ldg(g4 + i);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(norm1(v.x, rms, g.x)), fabsf(norm1(v.y, rms, g.y))),
-                                 fmaxf(fabsf(norm1(v.z, rms, g.z)), fabsf(norm1(v.w, rms, g.w)))));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(nrm(v.x, g.x)), fabsf(nrm(v.y, g.y))),
+                                 fmaxf(fabsf(nrm(v.z, g.z)), fabsf(nrm(v.w, g.w)))));
     }
     block_max2<false>(amax, unused, red2);
     const float sc = sym_scale(amax);
@@ -440,8 +488,8 @@ __global__ void __launch_bounds__(1024)
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
         const float4 v = __ldcs(xr + i);
         const float4 g = __ldg(g4 + i);
-        qr[i] = pack4(sym_code(norm1(v.x, rms, g.x), sc, rc), sym_code(norm1(v.y, rms, g.y), sc, rc),
-                      sym_code(norm1(v.z, rms, g.z), sc, rc), sym_code(norm1(v.w, rms, g.w), sc, rc));
+        qr[i] = pack4(sym_code(nrm(v.x, g.x), sc, rc), sym_code(nrm(v.y, g.y), sc, rc),
+                      sym_code(nrm(v.z, g.z), sc, rc), sym_code(nrm(v.w, g.w), sc, rc));
     }
 }
 
@@ -572,14 +620,19 @@ __global__ void __launch_bounds__(256) quantize_weight_mx_kernel(const float* __
     }
 }
 
+// SM count of the current device, cached per device.
 int num_sms() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+    int* slot = dev < 64 ? &cached[dev] : nullptr;
+    if (slot && *slot > 0) return *slot;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        (void)cudaGetLastError();
+        return 1;
     }
+    if (slot) *slot = sms;
     return sms;
 }
 

@@ -52,11 +52,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity. Returns false if the
-// kernel is aborting (another role gave up) or this wait ran out of time.
+// kernel is aborting (another role gave up) or this wait ran out of time
+// (limit clock cycles; the failure-path self-test passes a short one).
 // sleep_ns > 0 backs off between polls, leaving issue slots to warps that
 // share the SM sub-partition (for waiters that are not latency critical).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned code, unsigned int* err_word, unsigned sleep_ns = 0) {
+                                          unsigned code, unsigned int* err_word, unsigned sleep_ns = 0,
+                                          long long limit = kTimeoutCycles) {
     if (mbar_try(bar, parity)) return true;
     long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
@@ -64,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (mbar_try(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicOr(err_word, code);
                 return false;

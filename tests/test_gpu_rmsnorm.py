@@ -41,6 +41,11 @@ def host(t):
 
 
 def compare(qa, s_a, ref):
+    # every row with a nonzero maximum has a code of magnitude exactly 127 (its maximum element,
+    # whose value the code pass must see exactly as the range pass did)
+    live = np.abs(ref["qa"]).max(axis=1) > 0 if ref["qa"].size else np.zeros(0, bool)
+    if live.any():
+        assert np.all(np.abs(qa[live].astype(np.int32)).max(axis=1) == 127)
     flag = gates.near_f32_midpoint(ref["sumsq"])
     ok = ~flag
     np.testing.assert_array_equal(s_a[ok], ref["sa"][ok])
@@ -125,3 +130,41 @@ def test_rmsnorm_empty(q8):
     g = torch.ones(64, dtype=torch.float32, device="cuda")
     qa, s_a = q8.q8_rmsnorm_quantize_act(a, g, EPS)
     assert qa.shape == (0, 64) and s_a.shape == (0,)
+
+
+def test_rmsnorm_quotient_paths(q8):
+    """Rows that take each path of the division x / rms: Markstein's corrected quotient (rms in
+    [2^-60, 2^60], |x| >= 2^-60), the IEEE quotient for elements below 2^-60 (subnormal ones
+    included) and for whole rows whose rms lies outside [2^-60, 2^60]; and signed zeros."""
+    rng = np.random.default_rng(11)
+    K = 4096
+    rows = []
+    mag = np.exp2(rng.uniform(-40.0, 40.0, K)) * rng.choice([-1.0, 1.0], K)   # quotients of every exponent
+    rows.append(mag.astype(np.float32))
+    r = rng.standard_normal(K).astype(np.float32)
+    r[::7] = (rng.standard_normal(K)[::7] * 2.0 ** -70).astype(np.float32)      # tiny elements: IEEE path
+    r[3], r[5] = np.float32(2.0 ** -60), np.nextafter(np.float32(2.0 ** -60), np.float32(0))
+    r[11:13] = np.float32(1e-40)                                                # subnormal inputs
+    rows.append(r)
+    z = rng.standard_normal(K).astype(np.float32)
+    z[::3] = np.float32(-0.0)
+    z[1::3] = np.float32(0.0)
+    rows.append(z)
+    rows.append((rng.standard_normal(K) * 1e-3).astype(np.float32))
+    a = np.stack(rows)
+    gamma = workloads.make_norm_weights(K, seed=5)
+    qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
+    torch.cuda.synchronize()
+    compare(host(qa), host(s_a), oracle.rmsnorm_quantize(a, gamma, EPS))
+    # whole rows with rms below 2^-60 and above 2^60 (values k * 2^-61 and k * 2^61 with short
+    # mantissas, so every square and sum is exact and nothing under- or overflows)
+    ks = rng.choice(np.array([1.0, 0.5, 0.75, 1.25, -1.0, -0.5, -0.75, -1.25]), size=(2, 64))
+    for scale, Kx in ((2.0 ** -61, 64), (2.0 ** 61, 16)):
+        b = np.stack([(ks[0, :Kx] * scale), rng.standard_normal(Kx)]).astype(np.float32)
+        g = workloads.make_norm_weights(Kx, seed=Kx)
+        qb, sb = q8.q8_rmsnorm_quantize_act(dev(b), dev(g), 1e-45)
+        torch.cuda.synchronize()
+        ref = oracle.rmsnorm_quantize(b, g, 1e-45)
+        rms0 = np.sqrt(np.float64(ref["sumsq"][0]) / Kx)
+        assert (rms0 < 2.0 ** -60) if scale < 1 else (rms0 > 2.0 ** 60)
+        compare(host(qb), host(sb), ref)

@@ -33,13 +33,15 @@ def q8():
     return q8mod
 
 
-def call_static(q8, a_host, qw, s_w, y_host, chunk_rows=0):
+def call_static(q8, a_host, qw, s_w, y_host, chunk_rows=0, colsum=None):
+    """Symmetric activations, or asymmetric ones (zero point per token) when colsum is given."""
     M, K = a_host.shape
     N = qw.shape[0]
     return q8.load().q8_linear_host_static(
-        ctypes.c_void_p(a_host.data_ptr()), M, K, q8.Q8_SYMMETRIC, ctypes.c_void_p(qw.data_ptr()),
-        ctypes.c_void_p(s_w.data_ptr()), q8.Q8_PER_ROW, None, N, ctypes.c_void_p(y_host.data_ptr()), chunk_rows,
-        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        ctypes.c_void_p(a_host.data_ptr()), M, K, q8.Q8_SYMMETRIC if colsum is None else q8.Q8_ASYMMETRIC,
+        ctypes.c_void_p(qw.data_ptr()), ctypes.c_void_p(s_w.data_ptr()), q8.Q8_PER_ROW,
+        None if colsum is None else ctypes.c_void_p(colsum.data_ptr()), N, ctypes.c_void_p(y_host.data_ptr()),
+        chunk_rows, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
 def test_static_workspace_matches_the_caller_workspace_on_two_calls_in_a_row(q8):
@@ -59,6 +61,45 @@ def test_static_workspace_matches_the_caller_workspace_on_two_calls_in_a_row(q8)
         torch.cuda.synchronize()
         assert q8.q8_device_error() == 0
         np.testing.assert_array_equal(y_static.numpy().view(np.int32), y_ref.numpy().view(np.int32))
+
+
+def test_static_workspace_with_asymmetric_activations(q8):
+    # zero points and column sums: the z_a slots of the array are used too
+    M, N, K = 1000, 1536, 4096
+    wl = workloads.WORKLOADS["relu4k"]
+    w = torch.from_numpy(workloads.make_weights(wl, N=N, K=K)).cuda()
+    qw, s_w = q8.q8_quantize_weight(w, per_row=True)
+    colsum = q8.q8_colsum(qw)
+    for call in range(2):
+        a = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
+        a.copy_(torch.from_numpy(workloads.make_activations(wl, M=M, K=K) + np.float32(call)))
+        y_static = torch.full((M, N), float("nan"), dtype=torch.float32, pin_memory=True)
+        assert call_static(q8, a, qw, s_w, y_static, colsum=colsum) == q8.Q8_OK
+        y_ref = q8.q8_linear_host(a, qw, s_w, colsum, symmetric=False)
+        torch.cuda.synchronize()
+        assert q8.q8_device_error() == 0
+        np.testing.assert_array_equal(y_static.numpy().view(np.int32), y_ref.numpy().view(np.int32))
+
+
+def test_argument_errors_come_before_the_size_check(q8):
+    # a shape far beyond the array with a bad argument: the argument error is reported
+    lib = q8.load()
+    N, K = 1 << 23, 16
+    a = torch.zeros((4, K), dtype=torch.float32)
+    y = torch.zeros((4, 4), dtype=torch.float32)
+    qw = torch.zeros((16, K), dtype=torch.int8, device="cuda")
+    s_w = torch.ones(16, device="cuda")
+    args = dict(a=ctypes.c_void_p(a.data_ptr()), qw=ctypes.c_void_p(qw.data_ptr()), s_w=ctypes.c_void_p(s_w.data_ptr()),
+                y=ctypes.c_void_p(y.data_ptr()))
+    bad = [
+        (args["a"], 7, args["qw"], args["s_w"], q8.Q8_PER_ROW, None, args["y"]),          # symmetry not an enum value
+        (args["a"], q8.Q8_SYMMETRIC, args["qw"], args["s_w"], 5, None, args["y"]),         # granularity
+        (args["a"], q8.Q8_ASYMMETRIC, args["qw"], args["s_w"], q8.Q8_PER_ROW, None, args["y"]),   # no colsum
+        (args["a"], q8.Q8_SYMMETRIC, None, args["s_w"], q8.Q8_PER_ROW, None, args["y"]),   # no weights
+        (args["a"], q8.Q8_SYMMETRIC, args["qw"], args["s_w"], q8.Q8_PER_ROW, None, None),  # no output
+    ]
+    for a_p, sym, qw_p, sw_p, gw, cs, y_p in bad:
+        assert lib.q8_linear_host_static(a_p, 4, K, sym, qw_p, sw_p, gw, cs, N, y_p, 0, None) == q8.Q8_ERR_INVALID_ARG
 
 
 def test_sizes_beyond_the_array_are_rejected(q8):
