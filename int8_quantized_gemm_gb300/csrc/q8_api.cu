@@ -424,13 +424,14 @@ const char* q8_status_string(q8_status status) {
 
 q8_status q8_device_error(uint32_t* code_out) {
     if (!code_out) return Q8_ERR_INVALID_ARG;
-    uint32_t a = 0, b = 0, c = 0, d = 0;
+    uint32_t a = 0, b = 0, c = 0, d = 0, qz = 0;
     cudaError_t e = q8::read_and_clear_gemm_tc_error(&a);
     if (e == cudaSuccess) e = q8::read_and_clear_gemv_tc_error(&b);
     if (e == cudaSuccess) e = q8::read_and_clear_gemv_mma_error(&c);
     if (e == cudaSuccess) e = q8::read_and_clear_gemm_tc2_error(&d);
+    if (e == cudaSuccess) e = q8::read_and_clear_quant_error(&qz);
     if (e != cudaSuccess) return Q8_ERR_CUDA;
-    *code_out = a | (b << 8) | (c << 16) | (d << 24);
+    *code_out = (a | qz) | (b << 8) | (c << 16) | (d << 24);
     return *code_out ? Q8_ERR_TIMEOUT : Q8_OK;
 }
 

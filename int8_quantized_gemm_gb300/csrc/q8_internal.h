@@ -140,5 +140,6 @@ cudaError_t read_and_clear_gemm_tc_error(uint32_t* code);
 cudaError_t read_and_clear_gemv_tc_error(uint32_t* code);
 cudaError_t read_and_clear_gemv_mma_error(uint32_t* code);
 cudaError_t read_and_clear_gemm_tc2_error(uint32_t* code);
+cudaError_t read_and_clear_quant_error(uint32_t* code);
 
 }  // namespace q8

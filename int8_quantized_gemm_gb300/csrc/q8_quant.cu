@@ -13,8 +13,14 @@
 #include <stdint.h>
 
 #include "q8_internal.h"
+#include "q8_tc_ptx.cuh"
 
 namespace q8 {
+
+// Device error word of this file: bit 0x80 (reported in the lowest byte of q8_device_error) is
+// set when the streaming RMSNorm quantizer's bounded wait for a row copy gave up.
+static __device__ unsigned int g_quant_error;
+
 namespace {
 
 constexpr int kWarp = 32;
@@ -72,6 +78,34 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
     return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
 
+// rint_quot_bits without its per-element branch: the word kMagicBits + rint(RN(x r)), and
+// dmax = max(dmax, |t - rint(t)|). When dmax stays below 0.5 - 2^-14 for every element of a
+// thread, each of its codes equals rint_quot_bits' (no t was near a half-integer); otherwise the
+// thread recomputes its codes with rint_quot_bits (rare: about 2^-13 of the quotients).
+__device__ __forceinline__ uint32_t rint_bits_tracked(float x, float r, float& dmax) {
+    const float t = __fmul_rn(x, r);
+    const float u = __fadd_rn(t, kMagic);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(t, __fsub_rn(u, kMagic))));
+    return __float_as_uint(u);
+}
+constexpr float kNearHalf = 0.5f - 0x1p-14f;
+
+// The same from the exact product x r: u = RN(x r + kMagic) holds kMagicBits + rint(x r) (one
+// rounding of the exact product to the integer grid), and d = RN(x r - rint(x r)) (one FMA) is
+// within 2^-25 of the exact distance. x r (r = RN(1 / s), |x / s| <= 256) is within
+// 256 * 2^-24 = 2^-16 of x / s, and RN(x / s) within 2^-16 of it too, so when |d| stays below
+// kNearHalf no half-integer separates x r from RN(x / s) and both have the same rint.
+__device__ __forceinline__ uint32_t rint_bits_fma_tracked(float x, float r, float& dmax) {
+    const float u = __fmaf_rn(x, r, kMagic);
+    dmax = fmaxf(dmax, fabsf(__fmaf_rn(x, r, -__fsub_rn(u, kMagic))));
+    return __float_as_uint(u);
+}
+
+__device__ __forceinline__ uint32_t sym_codes4_tracked(float4 v, float r, float& dmax) {
+    return pack4(rint_bits_fma_tracked(v.x, r, dmax), rint_bits_fma_tracked(v.y, r, dmax),
+                 rint_bits_fma_tracked(v.z, r, dmax), rint_bits_fma_tracked(v.w, r, dmax));
+}
+
 // Codes of elements 4i .. 4i + 3 (the low bytes of a .. d) of a row (or tensor) whose codes start
 // at q: int8 (one 32-bit word) or, for H, fp16 values (8 bytes). fp16: the half with bits
 // 0x6400 | (byte ^ 0x80) is 1024 + (code + 128) exactly, and subtracting 1152 leaves the code.
@@ -88,6 +122,29 @@ __device__ __forceinline__ void store_codes4(void* q, int64_t i, uint32_t a, uin
     } else {
         reinterpret_cast<uint32_t*>(q)[i] = w;
     }
+}
+
+// Codes of four elements into store_codes4 (the low byte of each word): symmetric, or asymmetric
+// clamp(rint + z, -128, 127) with zoff = z - kMagicBits; tracked as rint_bits_tracked.
+template <bool ASYM, bool H>
+__device__ __forceinline__ void store_codes4_tracked(void* q, int64_t i, float4 v, float r, int zoff, float& dmax) {
+    uint32_t c[4] = {rint_bits_tracked(v.x, r, dmax), rint_bits_tracked(v.y, r, dmax), rint_bits_tracked(v.z, r, dmax),
+                     rint_bits_tracked(v.w, r, dmax)};
+    if constexpr (ASYM) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = (uint32_t)clampi((int)c[k] + zoff, -128, 127);
+    }
+    store_codes4<H>(q, i, c[0], c[1], c[2], c[3]);
+}
+
+// The same four codes with rint_quot_bits' near-half check (the exact path).
+template <bool ASYM, bool H>
+__device__ __forceinline__ void store_codes4_exact(void* q, int64_t i, float4 v, float s, float r, int zoff) {
+    if constexpr (ASYM)
+        store_codes4<H>(q, i, asym_code(v.x, s, r, zoff), asym_code(v.y, s, r, zoff), asym_code(v.z, s, r, zoff),
+                        asym_code(v.w, s, r, zoff));
+    else
+        store_codes4<H>(q, i, sym_code(v.x, s, r), sym_code(v.y, s, r), sym_code(v.z, s, r), sym_code(v.w, s, r));
 }
 
 // Block-wide max of two values (hi, and nlo = -lo for the asymmetric range).
@@ -158,19 +215,12 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
-    [[maybe_unused]] const int zoff = zp - (int)kMagicBits;
+    const int zoff = zp - (int)kMagicBits;
     void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-        if (i < n4) {
-            if (ASYM)
-                store_codes4<H>(qr, i, asym_code(v[j].x, sc, rc, zoff), asym_code(v[j].y, sc, rc, zoff),
-                                asym_code(v[j].z, sc, rc, zoff), asym_code(v[j].w, sc, rc, zoff));
-            else
-                store_codes4<H>(qr, i, sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
-                                sym_code(v[j].w, sc, rc));
-        }
+        if (i < n4) store_codes4_exact<ASYM, H>(qr, i, v[j], sc, rc, zoff);
     }
 }
 
@@ -208,16 +258,13 @@ __global__ void __launch_bounds__(1024) quantize_long_rows_kernel(const float* _
         if (ASYM) z[row] = zp;
     }
     const float rc = __fdiv_rn(1.0f, sc);
-    [[maybe_unused]] const int zoff = zp - (int)kMagicBits;
+    const int zoff = zp - (int)kMagicBits;
     void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
     for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
-        float4 v = __ldcs(xr + i);
-        if (ASYM)
-            store_codes4<H>(qr, i, asym_code(v.x, sc, rc, zoff), asym_code(v.y, sc, rc, zoff), asym_code(v.z, sc, rc, zoff),
-                            asym_code(v.w, sc, rc, zoff));
-        else
-            store_codes4<H>(qr, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
-                            sym_code(v.w, sc, rc));
+        const float4 v = __ldcs(xr + i);
+        float dmax = 0.0f;
+        store_codes4_tracked<ASYM, H>(qr, i, v, rc, zoff, dmax);
+        if (dmax >= kNearHalf) store_codes4_exact<ASYM, H>(qr, i, v, sc, rc, zoff);
     }
 }
 
@@ -274,17 +321,14 @@ __global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restri
                                                            void* __restrict__ q) {
     const float sc = s[0];
     const float rc = __fdiv_rn(1.0f, sc);
-    [[maybe_unused]] const int zoff = (ASYM ? z[0] : 0) - (int)kMagicBits;
+    const int zoff = (ASYM ? z[0] : 0) - (int)kMagicBits;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
-        float4 v = __ldcs(x4 + i);
-        if (ASYM)
-            store_codes4<H>(q, i, asym_code(v.x, sc, rc, zoff), asym_code(v.y, sc, rc, zoff), asym_code(v.z, sc, rc, zoff),
-                            asym_code(v.w, sc, rc, zoff));
-        else
-            store_codes4<H>(q, i, sym_code(v.x, sc, rc), sym_code(v.y, sc, rc), sym_code(v.z, sc, rc),
-                            sym_code(v.w, sc, rc));
+        const float4 v = __ldcs(x4 + i);
+        float dmax = 0.0f;
+        store_codes4_tracked<ASYM, H>(q, i, v, rc, zoff, dmax);
+        if (dmax >= kNearHalf) store_codes4_exact<ASYM, H>(q, i, v, sc, rc, zoff);
     }
 }
 
@@ -372,18 +416,18 @@ __device__ __forceinline__ float rms_of(float sumsq, int64_t cols, float eps) {
 }
 
 // RN(x / d) from r = RN(1 / d) by Markstein's correction (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990): for a
-// quotient q within one ulp of x / d, the remainder x - q d is exact in one FMA, and
-// RN(q + (x - q d) r) is the correctly rounded quotient. q0 = RN(x r) is within 1.5 ulp of x / d;
-// its correction q1 is within half an ulp plus 2^-22 ulp (so within one ulp), and the correction
-// of q1 is RN(x / d). Valid while nothing under- or overflows: d in [2^-60, 2^60] and |x| >= 2^-60
-// (quotients and remainders normal); the caller checks both. x = -0 gives +0 (IEEE: -0); the
-// sign of a zero y changes neither the row maximum nor its code.
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990): with
+// q0 = RN(x r), the remainder x - q0 d is formed in one FMA and q1 = RN(q0 + (x - q0 d) r). q1 is
+// the correctly rounded quotient for every pair of significands: checked against CUDA's IEEE
+// division over all 2^23 x 2^23 pairs x, d in [1, 2). Scaling x or d by a power of two scales
+// every intermediate exactly while all of them stay normal, so the check covers every x and d
+// for which they do: d in [2^-60, 2^60] and |x| >= 2^-60 (x / d, the remainder and the
+// correction are then normal); the caller checks both. x = -0 gives +0 (IEEE: -0); the sign of
+// a zero y changes neither the row maximum nor its code.
 constexpr uint32_t kDivTinyBits = 0x21800000u;   // 2^-60
 __device__ __forceinline__ float div_markstein(float x, float d, float r) {
     const float q0 = __fmul_rn(x, r);
-    const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
-    return __fmaf_rn(__fmaf_rn(-q1, d, x), r, q1);
+    return __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
 }
 
 // The row's normaliser: rms, its reciprocal and whether Markstein's quotient applies to the row.
@@ -402,55 +446,142 @@ struct RowNorm {
     }
 };
 
+// The IEEE quotient out of line, for paths that are rarely taken (keeps the registers of an
+// inlined division sequence out of the callers' main paths).
+__device__ __noinline__ float fdiv_rare(float a, float b) { return __fdiv_rn(a, b); }
+
+// The codes of a thread's elements i = t, t + stride, ... (< n4) on the exact path, y recomputed
+// from x with the same operations as the kernel's (Markstein's quotient when fast, else IEEE).
+// Out of line: it runs only for a thread with a quotient near a half-integer, and keeps its
+// registers out of the kernel's main path.
+__device__ __noinline__ void rmsnorm_codes_exact(const float4* __restrict__ xr, const float4* __restrict__ g4,
+                                                 uint32_t* __restrict__ qr, int64_t t, int64_t stride, int64_t n4,
+                                                 float rms, float rr, bool fast, float sc, float rc) {
+    for (int64_t i = t; i < n4; i += stride) {
+        const float4 a = xr[i], g = __ldg(g4 + i);
+        float4 y;
+        if (fast)
+            y = make_float4(__fmul_rn(div_markstein(a.x, rms, rr), g.x), __fmul_rn(div_markstein(a.y, rms, rr), g.y),
+                            __fmul_rn(div_markstein(a.z, rms, rr), g.z), __fmul_rn(div_markstein(a.w, rms, rr), g.w));
+        else
+            y = make_float4(__fmul_rn(__fdiv_rn(a.x, rms), g.x), __fmul_rn(__fdiv_rn(a.y, rms), g.y),
+                            __fmul_rn(__fdiv_rn(a.z, rms), g.z), __fmul_rn(__fdiv_rn(a.w, rms), g.w));
+        qr[i] = pack4(sym_code(y.x, sc, rc), sym_code(y.y, sc, rc), sym_code(y.z, sc, rc), sym_code(y.w, sc, rc));
+    }
+}
+
 // One CTA per row, the row in registers (VPT float4 per thread): one HBM read of x. Up to
 // four float4 per thread the kernel fits 32 registers, so two 1024-thread CTAs share an SM
 // (the row phases - load, reduce, normalise, reduce, store - of one CTA overlap the other's).
+// Per element: the exact square sum (Fast2Sum pair), Markstein's quotient, the gamma product,
+// the row maximum and the code by the kMagic FMA, with no per-element branch (elements below
+// 2^-60 and quotients near a half-integer are flagged per thread, and that thread takes the
+// exact path). The block reductions are cheap for the many warps: every thread stores its pair
+// (or its maximum) to shared memory and one warp reduces them and computes the row's scalars
+// (rms and its reciprocal; the scale and its reciprocal) once, for all threads to read.
 template <int VPT>
 __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1))
     rmsnorm_quantize_rows_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int64_t cols,
                                  float eps, int8_t* __restrict__ q, float* __restrict__ s) {
-    __shared__ float red[64];
-    __shared__ float red2[64];
+    __shared__ float2 part[1024];
+    __shared__ float wmax[32];
+    __shared__ float bc[4];   // rms, 1 / rms, s, 1 / s
     const int64_t row = blockIdx.x;
     const int64_t n4 = cols / 4;
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nthreads = blockDim.x;
     const float4* xr = reinterpret_cast<const float4*>(x + row * cols);
     const float4* g4 = reinterpret_cast<const float4*>(gamma);
     float4 v[VPT];
-    float hi = 0.0f, lo = 0.0f;
+    float h0 = 0.0f, l0 = 0.0f;
+    uint32_t tmin = 0xFFFFFFFFu;   // min over the thread's elements of 2 |x|bits - 2 (zeros: huge)
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
+        const int64_t i = threadIdx.x + (int64_t)j * nthreads;
         if (i < n4) {
             v[j] = __ldcs(xr + i);
-            pair_add_square(hi, lo, v[j].x);
-            pair_add_square(hi, lo, v[j].y);
-            pair_add_square(hi, lo, v[j].z);
-            pair_add_square(hi, lo, v[j].w);
+            pair_add_square(h0, l0, v[j].x);
+            pair_add_square(h0, l0, v[j].y);
+            pair_add_square(h0, l0, v[j].z);
+            pair_add_square(h0, l0, v[j].w);
+            tmin = min(min(tmin, (__float_as_uint(v[j].x) << 1) - 2u), (__float_as_uint(v[j].y) << 1) - 2u);
+            tmin = min(min(tmin, (__float_as_uint(v[j].z) << 1) - 2u), (__float_as_uint(v[j].w) << 1) - 2u);
         }
     }
-    const RowNorm nrm(rms_of(block_sum_pairs(hi, lo, red), cols, eps));
-    float amax = 0.0f, unused = 0.0f;
+    part[threadIdx.x] = make_float2(h0, l0);
+    __syncthreads();
+    if (warp == 0) {
+        float hi = 0.0f, lo = 0.0f;
+        for (int t = lane; t < nthreads; t += kWarp) {
+            const float2 pr = part[t];
+            pair_add(hi, lo, pr.x, pr.y);
+        }
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-        if (i < n4) {
-            const float4 g = __ldg(g4 + i);
-            v[j] = make_float4(nrm(v[j].x, g.x), nrm(v[j].y, g.y), nrm(v[j].z, g.z), nrm(v[j].w, g.w));
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+        for (int o = kWarp / 2; o > 0; o >>= 1)
+            pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+        if (lane == 0) {
+            // lane 0's pair (lanes of a butterfly may differ in the last bit of lo)
+            const float rms = rms_of(__fadd_rn(hi, lo), cols, eps);
+            bc[0] = rms;
+            bc[1] = __fdiv_rn(1.0f, rms);
         }
     }
-    block_max2<false>(amax, unused, red2);
-    const float sc = sym_scale(amax);
-    if (threadIdx.x == 0) s[row] = sc;
-    const float rc = __fdiv_rn(1.0f, sc);
+    __syncthreads();
+    const float rms = bc[0], rr = bc[1];
+    // y = RN(RN(x / rms) * g): Markstein's quotient where it is exact, else the IEEE quotient
+    const bool fast = rms >= 0x1p-60f && rms <= 0x1p60f && tmin >= 2u * kDivTinyBits - 2u;
+    float amax = 0.0f;
+    if (fast) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * nthreads;
+            if (i < n4) {
+                const float4 g = __ldg(g4 + i);
+                v[j] = make_float4(__fmul_rn(div_markstein(v[j].x, rms, rr), g.x),
+                                   __fmul_rn(div_markstein(v[j].y, rms, rr), g.y),
+                                   __fmul_rn(div_markstein(v[j].z, rms, rr), g.z),
+                                   __fmul_rn(div_markstein(v[j].w, rms, rr), g.w));
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * nthreads;
+            if (i < n4) {
+                const float4 g = __ldg(g4 + i);
+                v[j] = make_float4(__fmul_rn(fdiv_rare(v[j].x, rms), g.x), __fmul_rn(fdiv_rare(v[j].y, rms), g.y),
+                                   __fmul_rn(fdiv_rare(v[j].z, rms), g.z), __fmul_rn(fdiv_rare(v[j].w, rms), g.w));
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (warp == 0) {
+        float m = lane < nthreads / kWarp ? wmax[lane] : 0.0f;
+#pragma unroll
+        for (int o = kWarp / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            const float sc = sym_scale(m);
+            s[row] = sc;
+            bc[2] = sc;
+            bc[3] = __fdiv_rn(1.0f, sc);
+        }
+    }
+    __syncthreads();
+    const float sc = bc[2], rc = bc[3];
     uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+    float dmax = 0.0f;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-        if (i < n4)
-            qr[i] = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
-                          sym_code(v[j].w, sc, rc));
+        const int64_t i = threadIdx.x + (int64_t)j * nthreads;
+        if (i < n4) qr[i] = sym_codes4_tracked(v[j], rc, dmax);
     }
+    if (dmax >= kNearHalf)   // some quotient near a half-integer (rare): this thread's codes exactly
+        rmsnorm_codes_exact(xr, g4, qr, threadIdx.x, nthreads, n4, rms, rr, fast, sc, rc);
 }
 
 // Rows longer than the register budget: three sweeps (sum of squares; y and its maximum;
@@ -491,6 +622,208 @@ __global__ void __launch_bounds__(1024)
         qr[i] = pack4(sym_code(nrm(v.x, g.x), sc, rc), sym_code(nrm(v.y, g.y), sc, rc),
                       sym_code(nrm(v.z, g.z), sc, rc), sym_code(nrm(v.w, g.w), sc, rc));
     }
+}
+
+// Streaming form for rows of up to 1024 * VPT float4 whose three copies fit in shared memory
+// (K <= 16384): a persistent grid of one 1024-thread CTA per SM takes rows blockIdx.x,
+// blockIdx.x + grid, ...; each row arrives in one of three shared-memory buffers by one bulk copy
+// (cp.async.bulk, completing on that buffer's mbarrier), issued three rows ahead, so the SM's HBM
+// stream continues through the block reductions of the row it is working on. The row is read
+// into registers (VPT float4 per thread), then: the exact square sum (Fast2Sum pair), Markstein's
+// quotient, the gamma product, the row maximum and the codes by the kMagic FMA, with no
+// per-element branch (elements below 2^-60 in magnitude and quotients near a half-integer are
+// flagged per thread and that thread takes the exact path).
+// Block reductions of the streaming kernel: every warp reduces its lanes by a butterfly and one
+// lane per warp stores the result; after a barrier warp 0 alone reduces the warps' results and
+// computes the row's scalars from them, which it stores for all threads to read after a second
+// barrier (the other warps spend no issue slots on the second level or the scalar math).
+// bc[0], bc[1]: rms and RN(1 / rms); bc[2], bc[3]: the row's scale s and RN(1 / s).
+// Returns whether `ok` holds in every thread (the vote rides on the first barrier); the row's
+// scalars are computed only when it does.
+__device__ __forceinline__ bool stream_sum_to_rms(float hi, float lo, bool ok, float2* red, float* bc, int64_t cols,
+                                                  float eps) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    if (lane == 0) red[warp] = make_float2(hi, lo);
+    if (!__syncthreads_and(ok)) return false;
+    if (warp == 0) {
+        const float2 pr = lane < (int)(blockDim.x / kWarp) ? red[lane] : make_float2(0.0f, 0.0f);
+        hi = pr.x;
+        lo = pr.y;
+#pragma unroll
+        for (int o = kWarp / 2; o > 0; o >>= 1)
+            pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+        if (lane == 0) {   // lane 0's pair (lanes of a butterfly may differ in the last bit of lo)
+            const float rms = rms_of(__fadd_rn(hi, lo), cols, eps);
+            bc[0] = rms;
+            bc[1] = __fdiv_rn(1.0f, rms);
+        }
+    }
+    __syncthreads();
+    return true;
+}
+
+__device__ __forceinline__ void stream_max_to_scale(float amax, float* red, float* bc) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    if (warp == 0) {
+        float m = lane < (int)(blockDim.x / kWarp) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = kWarp / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            const float sc = sym_scale(m);
+            bc[2] = sc;
+            bc[3] = __fdiv_rn(1.0f, sc);
+        }
+    }
+    __syncthreads();
+}
+
+constexpr int kStreamThreads = 1024;
+constexpr int kStreamBufs = 3;
+int num_sms();
+
+__device__ __forceinline__ void bulk_row_load(uint32_t dst, const float* src, uint32_t bytes, uint32_t bar) {
+    tc::mbar_expect_tx(bar, bytes);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    rmsnorm_quantize_stream_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int64_t rows,
+                                   int64_t cols, float eps, int8_t* __restrict__ q, float* __restrict__ s) {
+    extern __shared__ __align__(128) uint8_t rowbuf[];
+    __shared__ __align__(8) uint64_t bar_cells[kStreamBufs];
+    __shared__ float2 red[32];
+    __shared__ float red2[32];
+    __shared__ float bc[4];
+    __shared__ int abort_cell;
+    const uint32_t bytes = (uint32_t)(cols * 4);
+    const int64_t n4 = cols / 4;
+    const float4* g4 = reinterpret_cast<const float4*>(gamma);
+    volatile int* abort_flag = &abort_cell;
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kStreamBufs; ++b) tc::mbar_init(tc::smem_u32(&bar_cells[b]), 1);
+        abort_cell = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kStreamBufs; ++b) {
+            const int64_t r = blockIdx.x + (int64_t)b * gridDim.x;
+            if (r < rows)
+                bulk_row_load(tc::smem_u32(rowbuf) + b * bytes, x + r * cols, bytes, tc::smem_u32(&bar_cells[b]));
+        }
+    }
+    int64_t row = blockIdx.x;
+    for (uint32_t it = 0; row < rows; row += gridDim.x, ++it) {
+        const uint32_t b = it % kStreamBufs;
+        const uint32_t buf = tc::smem_u32(rowbuf) + b * bytes;
+        // every thread waits for the copy itself (bounded); the block votes on the outcome at the
+        // first reduction's barrier and leaves together if any thread's wait gave up (a thread
+        // whose wait gave up sums stale shared memory, which the vote then discards)
+        const bool arrived = tc::mbar_wait(tc::smem_u32(&bar_cells[b]), (it / kStreamBufs) & 1u, abort_flag, 0x80u,
+                                           &g_quant_error);
+        float4 v[VPT];
+        float hi = 0.0f, lo = 0.0f;
+        uint32_t tmin = 0xFFFFFFFFu;   // min over the thread's elements of 2 |x|bits - 2 (zeros: huge)
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
+            if (i < n4) {
+                const uint4 r = tc::lds128(buf + 16u * (uint32_t)i);
+                v[j] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
+                pair_add_square(hi, lo, v[j].x);
+                pair_add_square(hi, lo, v[j].y);
+                pair_add_square(hi, lo, v[j].z);
+                pair_add_square(hi, lo, v[j].w);
+                tmin = min(min(tmin, (__float_as_uint(v[j].x) << 1) - 2u), (__float_as_uint(v[j].y) << 1) - 2u);
+                tmin = min(min(tmin, (__float_as_uint(v[j].z) << 1) - 2u), (__float_as_uint(v[j].w) << 1) - 2u);
+            }
+        }
+        if (!stream_sum_to_rms(hi, lo, arrived, red, bc, cols, eps)) break;
+        // every thread has summed its values from buffer b: it takes the row kStreamBufs ahead
+        const int64_t ahead = row + (int64_t)kStreamBufs * gridDim.x;
+        if (threadIdx.x == 0 && ahead < rows) {
+            tc::fence_proxy_async_smem();
+            bulk_row_load(buf, x + ahead * cols, bytes, tc::smem_u32(&bar_cells[b]));
+        }
+        const float rms = bc[0], rr = bc[1];
+        const bool fast = rms >= 0x1p-60f && rms <= 0x1p60f && tmin >= 2u * kDivTinyBits - 2u;
+        float amax = 0.0f;
+        if (fast) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
+                if (i < n4) {
+                    const float4 g = __ldg(g4 + i);
+                    v[j] = make_float4(__fmul_rn(div_markstein(v[j].x, rms, rr), g.x),
+                                       __fmul_rn(div_markstein(v[j].y, rms, rr), g.y),
+                                       __fmul_rn(div_markstein(v[j].z, rms, rr), g.z),
+                                       __fmul_rn(div_markstein(v[j].w, rms, rr), g.w));
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
+                if (i < n4) {
+                    const float4 g = __ldg(g4 + i);
+                    v[j] = make_float4(__fmul_rn(__fdiv_rn(v[j].x, rms), g.x), __fmul_rn(__fdiv_rn(v[j].y, rms), g.y),
+                                       __fmul_rn(__fdiv_rn(v[j].z, rms), g.z), __fmul_rn(__fdiv_rn(v[j].w, rms), g.w));
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+                }
+            }
+        }
+        stream_max_to_scale(amax, red2, bc);
+        const float sc = bc[2], rc = bc[3];
+        if (threadIdx.x == 0) s[row] = sc;
+        uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
+        float dmax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
+            if (i < n4) qr[i] = sym_codes4_tracked(v[j], rc, dmax);
+        }
+        if (dmax >= kNearHalf) {   // some quotient near a half-integer (rare): this thread's codes exactly
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
+                if (i < n4)
+                    qr[i] = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
+                                  sym_code(v[j].w, sc, rc));
+            }
+        }
+        // (the reductions' shared cells: red is written again by the next row before its first
+        // barrier, after every thread has passed this row's second barrier, which follows the
+        // last read of red; red2 and bc likewise after the next row's barriers)
+    }
+    if (*abort_flag) {   // a row copy did not arrive: give copies in flight a bounded time to land
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1LL << 22)) __nanosleep(1000);
+    }
+}
+
+template <int VPT>
+cudaError_t launch_rms_stream(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps, int8_t* q,
+                              float* s, cudaStream_t st) {
+    const int smem = (int)(cols * 4) * kStreamBufs;
+    cudaError_t e = cudaFuncSetAttribute(rmsnorm_quantize_stream_kernel<VPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = num_sms();
+    const unsigned grid = (unsigned)(rows < cap ? rows : cap);
+    rmsnorm_quantize_stream_kernel<VPT><<<grid, kStreamThreads, smem, st>>>(x, gamma, rows, cols, eps, q, s);
+    note_launch();
+    return cudaGetLastError();
 }
 
 template <int VPT>
@@ -655,9 +988,10 @@ cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, void* q, f
         return (int)(t < kWarp ? kWarp : t);
     };
     // Up to 1024 threads per row and at most 4 float4 per thread keeps the kernel at
-    // <= 32 registers, so two 1024-thread blocks (a full SM) stay resident.
-    if (n4 <= 1024 * 1) return launch_rows<1, ASYM, H>(x, rows, cols, threads_for(1), q, s, z, st);
-    if (n4 <= 1024 * 2) return launch_rows<2, ASYM, H>(x, rows, cols, threads_for(2), q, s, z, st);
+    // <= 32 registers, so a full SM of threads stays resident. Rows of more than 256 float4 take
+    // four per thread (several independent loads in flight per thread, and for rows up to 1024
+    // float4 blocks of at most 256 threads, several rows per SM).
+    if (n4 <= 256) return launch_rows<1, ASYM, H>(x, rows, cols, threads_for(1), q, s, z, st);
     if (n4 <= 1024 * 4) return launch_rows<4, ASYM, H>(x, rows, cols, threads_for(4), q, s, z, st);
     if (n4 <= 1024 * 8) return launch_rows<8, ASYM, H>(x, rows, cols, threads_for(8), q, s, z, st);
     quantize_long_rows_kernel<ASYM, H><<<(unsigned)rows, 1024, 0, st>>>(x, cols, q, s, z);
@@ -716,8 +1050,11 @@ cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t 
         t = ((t + kWarp - 1) / kWarp) * kWarp;
         return (int)(t < kWarp ? kWarp : t);
     };
-    if (n4 <= 1024 * 1) return launch_rms_rows<1>(x, gamma, rows, cols, eps, threads_for(1), q, s, stream);
-    if (n4 <= 1024 * 2) return launch_rms_rows<2>(x, gamma, rows, cols, eps, threads_for(2), q, s, stream);
+    if (n4 <= 256) return launch_rms_rows<1>(x, gamma, rows, cols, eps, threads_for(1), q, s, stream);
+    // rows of 1024 .. 16384 elements with many rows: the streaming kernel (three rows in flight
+    // per SM through shared memory)
+    if (n4 > 256 && n4 <= kStreamThreads * 4 && rows >= 2 * (int64_t)num_sms())
+        return launch_rms_stream<4>(x, gamma, rows, cols, eps, q, s, stream);
     if (n4 <= 1024 * 4) return launch_rms_rows<4>(x, gamma, rows, cols, eps, threads_for(4), q, s, stream);
     if (n4 <= 1024 * 8) return launch_rms_rows<8>(x, gamma, rows, cols, eps, threads_for(8), q, s, stream);
     rmsnorm_quantize_long_rows_kernel<<<(unsigned)rows, 1024, 0, stream>>>(x, gamma, cols, eps, q, s);
@@ -788,6 +1125,18 @@ cudaError_t launch_quantize_weight_mx(const float* w, int64_t N, int64_t K, int 
         w, N, K, G, q, reinterpret_cast<uint8_t*>(sf));
     note_launch();
     return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_quant_error(uint32_t* code) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *code = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero));
+    }
+    return e;
 }
 
 cudaError_t launch_colsum(const int8_t* qw, int64_t N, int64_t K, int32_t* colsum, cudaStream_t stream) {

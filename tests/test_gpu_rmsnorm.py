@@ -168,3 +168,30 @@ def test_rmsnorm_quotient_paths(q8):
         rms0 = np.sqrt(np.float64(ref["sumsq"][0]) / Kx)
         assert (rms0 < 2.0 ** -60) if scale < 1 else (rms0 > 2.0 ** 60)
         compare(host(qb), host(sb), ref)
+
+
+def test_streaming_kernel_rows_with_every_path(q8):
+    """Enough rows (>= two per SM) and a ragged K for the streaming kernel: random rows of several
+    workloads, zero rows, rows with tiny elements (IEEE path), huge-range rows and eps-dominated
+    rows, in an order that puts each kind into every shared-memory buffer slot."""
+    rng = np.random.default_rng(21)
+    M, K = 460, 4112
+    a = workloads.make_activations(workloads.WORKLOADS["prefill2k"], M=M, K=K)
+    for r in range(0, M, 7):
+        kind = (r // 7) % 5
+        if kind == 0:
+            a[r] = 0.0
+        elif kind == 1:
+            a[r, ::5] = (rng.standard_normal(K)[::5] * 2.0 ** -72).astype(np.float32)
+        elif kind == 2:
+            a[r] = (np.exp2(rng.uniform(-30.0, 30.0, K)) * rng.choice([-1.0, 1.0], K)).astype(np.float32)
+        elif kind == 3:
+            a[r] *= np.float32(1e-4)               # eps (1e-6) dominates the mean of squares
+        else:
+            a[r, ::3] = np.float32(-0.0)
+    gamma = workloads.make_norm_weights(K, seed=3)
+    for _ in range(2):
+        qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
+        torch.cuda.synchronize()
+        assert q8.q8_device_error() == 0
+        compare(host(qa), host(s_a), oracle.rmsnorm_quantize(a, gamma, EPS))
