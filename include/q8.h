@@ -465,8 +465,15 @@ const char* q8_status_string(q8_status status);
 /*
  * Device-side error word of the current device: 0 if every bounded wait of a
  * tensor-core kernel completed, otherwise a nonzero code naming the wait that
- * gave up. Synchronises the device. Reading it resets it to 0. A nonzero
- * value means the outputs of the kernel that set it are invalid.
+ * gave up: one byte per kernel family (bits 0..7: the single-CTA tcgen05 kernel,
+ * and bit 7 the fused RMSNorm quantizer's wait for a row copy; bits 8..15: the
+ * tcgen05 decode kernel; bits 16..23: the warp-MMA decode kernels; bits 24..31:
+ * the CTA-pair kernel), within a byte one bit per role (1 TMA producer,
+ * 2 converters / compute warps waiting for loaded data, 4 converters waiting
+ * for a free stage, 8 MMA issuer waiting for converted data, 16 MMA issuer
+ * waiting for a free accumulator, 32 accumulator drain, 64 the odd CTA's relay).
+ * Synchronises the device. Reading it resets it to 0. A nonzero value means the
+ * outputs of the kernel that set it are invalid.
  */
 q8_status q8_device_error(uint32_t* code_out);
 
