@@ -263,10 +263,12 @@ def run_ours(args, world, rank, local):
     y = torch.empty((M, N), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     kernel = q8.q8_gemm_pick(M, N, K)
+    # the layer's scratch for an fp16 copy of the activation codes (allocated once, like every buffer)
+    ws = gemm_workspace(q8, M, N, K, device)
 
     def step():
         q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -285,7 +287,7 @@ def run_ours(args, world, rank, local):
             evs[i][0].record(stream)
             q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
             evs[i][1].record(stream)
-            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
             evs[i][2].record(stream)
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
@@ -306,9 +308,12 @@ def run_ours(args, world, rank, local):
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
     gemm_bytes = M * K + N * K + 4 * N + 4 * M + 4 * M * N
 
+    # ---- the same GEMM without the workspace: activation codes converted in shared memory per tile
+    direct = measure_gemm_direct(q8, qa, s_a, z_a, qw, s_w, colsum, y, flush, args, tc_peak, ops)
+
     # ---- the same step run back to back for seconds, with the clock the power limit leaves
     sustained = None if args.no_sustained else measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops,
-                                                                 args.sustained_s)
+                                                                 args.sustained_s, ws)
 
     # ---- end to end through the public API: pinned host A in, y back to pinned host
     e2e = None if args.no_e2e else measure_e2e(q8, a, y, step, qw, s_w, colsum, sym, ops, world, args)
@@ -379,7 +384,11 @@ def run_ours(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": f"{HEADLINE}: A fp32 [{M},{K}] per-token sym x W int8 [{N},{K}] per-channel"
                                    f" sym -> y fp32 [{M},{N}]",
-                       "M": M, "N": N, "K": K, "gemm_kernel": kernel, "l2": "flushed before every step (256 MiB write)",
+                       "M": M, "N": N, "K": K, "gemm_kernel": kernel,
+                       "gemm_path": ("activation codes written once as fp16 into the layer's workspace, then the "
+                                     "CTA-pair kernel with TMA loads of them (q8_gemm_dequant_ws); both kernels "
+                                     "inside the GEMM's events") if ws is not None else "q8_gemm_dequant",
+                       "l2": "flushed before every step (256 MiB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "kernel": f"gemm_{kernel}", "achieved": round(gemm_tops, 1),
                          "peak": tc_peak, "unit": "TFLOP/s", "frac": round(gemm_tops / tc_peak, 4),
@@ -392,6 +401,7 @@ def run_ours(args, world, rank, local):
             "rmsnorm_quantize": rmsq,
             "gemm_bias_bf16": epi,
             "f16_codes": f16a,
+            "gemm_int8_direct": direct,
             "configs": configs,
             "sustained": sustained,
             "w4a8": w4,
@@ -404,6 +414,38 @@ def run_ours(args, world, rank, local):
             "wall_s_timed": round(wall1 - wall0, 3),
         }
         print(json.dumps(line))
+
+
+def gemm_workspace(q8, M, N, K, device):
+    """The GEMM's optional scratch (an fp16 copy of the activation codes) for this shape, or None."""
+    import torch
+    n = q8.q8_gemm_workspace(M, N, K)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def measure_gemm_direct(q8, qa, s_a, z_a, qw, s_w, colsum, y, flush, args, tc_peak, ops):
+    """The headline GEMM without a workspace (q8_gemm_dequant): the CTA-pair kernel converts every
+    activation code to fp16 in shared memory once per 256-column tile; L2 flushed per launch."""
+    import torch
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(max(5, args.steps)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert q8.q8_device_error() == 0
+    mean = statistics.mean(ms)
+    tf = ops / (mean * 1e-3) / 1e12
+    return {"api": "q8_gemm_dequant (no workspace)", "ms": round(mean, 4), "TFLOP/s": round(tf, 1),
+            "frac": round(tf / tc_peak, 4)}
 
 
 def measure_e2e(q8, a, y, step, qw, s_w, colsum, sym, ops, world, args):
@@ -767,10 +809,11 @@ def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
     y = torch.empty((M, N), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
     kernel = q8.q8_gemm_pick(M, N, K)
+    ws = gemm_workspace(q8, M, N, K, device)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
     torch.cuda.synchronize()
     n = max(20, args.steps)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -779,7 +822,7 @@ def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
         evs[i][0].record(stream)
         q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
         evs[i][1].record(stream)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
         evs[i][2].record(stream)
     torch.cuda.synchronize()
     assert q8.q8_device_error() == 0
@@ -805,7 +848,7 @@ def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
     return {
         "workload": f"{name}: A fp32 [{M},{K}] per-{'token' if apr else 'tensor'} "
                     f"{'sym' if sym else 'asym'} x W int8 [{N},{K}] per-{'channel' if wpr else 'tensor'} sym",
-        "M": M, "N": N, "K": K, "gemm_kernel": kernel, "steps": n,
+        "M": M, "N": N, "K": K, "gemm_kernel": kernel, "workspace_bytes": 0 if ws is None else ws.numel(), "steps": n,
         "ms_per_step": round(st, 4), "step_ms": {"min": round(min(sms), 4), "median": round(statistics.median(sms), 4)},
         "TOPS": round(ops / (st * 1e-3) / 1e12, 3),
         "quantizer": {"ms": round(q, 4), "GB/s": round(qbytes / (q * 1e-3) / 1e9, 1),
@@ -869,7 +912,7 @@ def config_cpu(name, cores):
     return out
 
 
-def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, seconds):
+def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, seconds, ws=None):
     """The headline step back to back for about `seconds` (each step: the L2 flush, then the
     quantizer and the GEMM between CUDA events), with the SM clock sampled through NVML: the rate a
     layer keeps up once the power limit has pulled the clock down, against the sustained bf16 peak."""
@@ -881,7 +924,7 @@ def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, secon
         e0.record(stream)
         flush.zero_()
         q8.q8_quantize_act(a, qa=qa, s_a=s_a)
-        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, workspace=ws)
         e1.record(stream)
         torch.cuda.synchronize()
         probe.append(e0.elapsed_time(e1))
@@ -895,7 +938,7 @@ def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, secon
             evs[i][0].record(stream)
             q8.q8_quantize_act(a, qa=qa, s_a=s_a)
             evs[i][1].record(stream)
-            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y)
+            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, workspace=ws)
             evs[i][2].record(stream)
         torch.cuda.synchronize()
         w1 = time.perf_counter()

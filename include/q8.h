@@ -217,6 +217,32 @@ q8_status q8_linear(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_
                     q8_granularity gw, const int32_t* colsum, int64_t N, float* y,
                     q8_stream_t stream);
 
+/*
+ * q8_gemm_dequant with a caller-owned device workspace, same results bit for
+ * bit. For shapes that run on the CTA-pair tensor-core kernel (prefill: more than
+ * 16 tokens and a layer above the small-layer cut), the call first writes the
+ * activation codes once as the fp16 numbers of equal value into the workspace (a
+ * stream through HBM: M K bytes read, 2 M K written) and the kernel then loads
+ * them by TMA straight into its operand stages. Without the workspace the kernel
+ * converts every activation code in shared memory once per 256-column output tile
+ * it enters (N / 256 times), and that shared-memory traffic bounds it. The
+ * stored activation format stays int8; the fp16 copy is scratch.
+ *
+ * q8_gemm_workspace(M, N, K): the bytes this shape can use (2 M K, or 0 when the
+ * shape takes another kernel). workspace: NULL or smaller than that runs
+ * q8_gemm_dequant; otherwise 16-byte aligned device memory, overwritten; the caller
+ * owns it and may reuse it once the call's work on `stream` has completed; it must
+ * not overlap any operand or y.
+ * Other arguments, limits and errors as q8_gemm_dequant; a misaligned workspace
+ * returns Q8_ERR_INVALID_ARG.
+ */
+size_t q8_gemm_workspace(int64_t M, int64_t N, int64_t K);
+q8_status q8_gemm_dequant_ws(const int8_t* qa, const float* s_a, const int32_t* z_a,
+                             q8_granularity ga, const int8_t* qw, const float* s_w,
+                             q8_granularity gw, const int32_t* colsum, int64_t M, int64_t N,
+                             int64_t K, float* y, void* workspace, size_t workspace_bytes,
+                             q8_stream_t stream);
+
 /* q8_gemm_dequant with an explicit kernel choice. A kernel that cannot run
  * the given shape returns Q8_ERR_UNSUPPORTED (Q8_GEMM_AUTO never does). */
 q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* z_a,

@@ -28,7 +28,7 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error",
     "q8_selftest_wait_timeout", "KERNELS",
 ]
 
@@ -64,6 +64,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_colsum.argtypes = [p, i64, i64, p, p]
     lib.q8_gemm_dequant.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, p]
     lib.q8_gemm_dequant_ex.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, i32, p]
+    lib.q8_gemm_dequant_ws.argtypes = [p, p, p, i32, p, p, i32, p, i64, i64, i64, p, p, ctypes.c_size_t, p]
+    lib.q8_gemm_workspace.argtypes = [i64, i64, i64]
+    lib.q8_gemm_workspace.restype = ctypes.c_size_t
     lib.q8_gemm_epilogue_ex.argtypes = [p, p, p, i32, p, p, i32, p, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
     lib.q8_gemm_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_quantize_act_f16.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
@@ -87,7 +90,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_launch_count.argtypes = []
     lib.q8_launch_count.restype = ctypes.c_uint64
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
-                 "q8_gemm_dequant_ex", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
+                 "q8_gemm_dequant_ex", "q8_gemm_dequant_ws", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
                  "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
                  "q8_linear", "q8_linear_host", "q8_gemm_pick", "q8_device_error", "q8_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
@@ -180,9 +183,16 @@ def q8_colsum(qw: torch.Tensor, out=None, stream=None):
     return out
 
 
-def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "auto", stream=None):
+def q8_gemm_workspace(M: int, N: int, K: int) -> int:
+    """Device workspace bytes q8_gemm_dequant(..., workspace=) can use for this shape (0: none)."""
+    return int(load().q8_gemm_workspace(M, N, K))
+
+
+def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "auto", workspace=None,
+                    stream=None):
     """y[M, N] = (acc - z_a*colsum) * (s_a * s_w) from int8 codes; per-row scales are inferred
-    from the lengths of s_a (M entries) and s_w (N entries)."""
+    from the lengths of s_a (M entries) and s_w (N entries). workspace: an optional device tensor of
+    at least q8_gemm_workspace(M, N, K) bytes (kernel "auto" only; q8_gemm_dequant_ws)."""
     _need(qa, torch.int8, "qa", 2)
     _need(qw, torch.int8, "qw", 2)
     M, K = qa.shape
@@ -204,6 +214,16 @@ def q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum=None, y=None, kernel: str = "a
         _need(colsum, torch.int32, "colsum", 1)
     y = torch.empty((M, N), dtype=torch.float32, device=qa.device) if y is None else y
     _need(y, torch.float32, "y", 2)
+    if workspace is not None:
+        if kernel != "auto":
+            raise ValueError("a workspace goes with the automatic kernel choice")
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        _check(load().q8_gemm_dequant_ws(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
+                                         _ptr(colsum if z_a is not None else None), M, N, K, _ptr(y),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)), "q8_gemm_dequant_ws")
+        return y
     _check(load().q8_gemm_dequant_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw), _ptr(s_w), gw,
                                      _ptr(colsum if z_a is not None else None), M, N, K, _ptr(y),
                                      KERNELS[kernel], _stream(stream)), "q8_gemm_dequant")

@@ -64,13 +64,22 @@ struct MxWeights {
     int group;
 };
 
+// Workspace the automatic kernel choice can use: an fp16 copy of the activation codes (2 M K bytes)
+// for shapes on the CTA-pair kernel, else none.
+size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0) return 0;
+    if (q8_gemm_pick(M, N, K) != Q8_GEMM_TCGEN05_PAIR || !q8::gemm_tc2_supports(M, N, K, q8::kWA16)) return 0;
+    return (size_t)M * (size_t)K * 2;
+}
+
 // qa: int8 codes, or (a16) the same codes as fp16 values.
 q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                       int64_t M, int64_t N, int64_t K, float* y, int32_t* out_i32, q8_gemm_kernel kernel,
                       q8_stream_t stream, const Variant* var = nullptr, bool w4 = false,
                       const MxWeights* mx = nullptr, bool a16 = false, bool validate_only = false,
-                      bool early_weights = false, long long selftest_wait = 0) {
+                      bool early_weights = false, long long selftest_wait = 0, void* ws = nullptr,
+                      size_t ws_bytes = 0) {
     if (M < 0 || N < 0 || K < 0) return Q8_ERR_INVALID_ARG;
     if (kernel != Q8_GEMM_AUTO && kernel != Q8_GEMM_TCGEN05 && kernel != Q8_GEMM_MMA_S8 &&
         kernel != Q8_GEMM_SKINNY && kernel != Q8_GEMM_DECODE && kernel != Q8_GEMM_DECODE_TC &&
@@ -166,7 +175,19 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
         }
         return Q8_ERR_UNSUPPORTED;
     }
-    if (kernel == Q8_GEMM_AUTO) kernel = q8_gemm_pick(M, N, K);
+    if (kernel == Q8_GEMM_AUTO) {
+        kernel = q8_gemm_pick(M, N, K);
+        // With a workspace for an fp16 copy of the activation codes, the CTA-pair layer converts
+        // the codes once (a stream through HBM) and loads them by TMA straight into its operand
+        // stages, instead of converting every code once per output tile in shared memory.
+        if (kernel == Q8_GEMM_TCGEN05_PAIR && ws && ws_bytes >= gemm_ws_bytes(M, N, K) && aligned(ws, 16) &&
+            q8::gemm_tc2_supports(M, N, K, q8::kWA16)) {
+            uint16_t* qa16 = static_cast<uint16_t*>(ws);
+            cudaError_t e = q8::launch_codes_to_f16(qa8, M * K, qa16, s);
+            if (e != cudaSuccess) return from_cuda(e);
+            return from_cuda(q8::launch_gemm_tc2(qa16, qw, M, N, K, ep, s, q8::kWA16));
+        }
+    }
     switch (kernel) {
         case Q8_GEMM_TCGEN05:
             if (!q8::gemm_tc_supports(M, N, K)) return Q8_ERR_UNSUPPORTED;
@@ -305,6 +326,17 @@ q8_status q8_gemm_dequant(const int8_t* qa, const float* s_a, const int32_t* z_a
                           const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
                           int64_t M, int64_t N, int64_t K, float* y, q8_stream_t stream) {
     return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream);
+}
+
+size_t q8_gemm_workspace(int64_t M, int64_t N, int64_t K) { return gemm_ws_bytes(M, N, K); }
+
+q8_status q8_gemm_dequant_ws(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                             const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
+                             int64_t M, int64_t N, int64_t K, float* y, void* workspace, size_t workspace_bytes,
+                             q8_stream_t stream) {
+    if (workspace && !aligned(workspace, 16)) return Q8_ERR_INVALID_ARG;
+    return gemm_common(qa, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream, nullptr,
+                       false, nullptr, false, false, false, 0, workspace, workspace_bytes);
 }
 
 q8_status q8_gemm_dequant_ex(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,

@@ -28,6 +28,10 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per
 cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool per_row,
                                 uint16_t* q, float* s, int32_t* z, cudaStream_t stream);
 
+// int8 codes (n elements, n % 16 == 0, both bases 16-byte aligned) as the fp16 numbers of equal
+// value, in order.
+cudaError_t launch_codes_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t stream);
+
 // int4 weights (W4A8): per-row symmetric codes packed two per byte (K % 32 == 0), and their
 // column sums.
 cudaError_t launch_quantize_int4(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* s,

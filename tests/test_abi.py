@@ -197,6 +197,21 @@ def test_kernel_pick_is_a_concrete_kernel(lib):
     assert q8.q8_gemm_pick(100, 2048, 2048) == "skinny"
 
 
+def test_gemm_workspace_sizes(lib):
+    import int8_quantized_gemm_gb300 as q8
+    # an fp16 copy of the activation codes for shapes on the CTA-pair kernel, nothing otherwise
+    assert q8.q8_gemm_workspace(8192, 8192, 16384) == 2 * 8192 * 16384
+    assert q8.q8_gemm_workspace(2048, 4096, 4096) == 2 * 2048 * 4096
+    assert q8.q8_gemm_workspace(16, 28672, 8192) == 0          # decode kernel
+    assert q8.q8_gemm_workspace(100, 2048, 2048) == 0          # small layer: mma.sync kernel
+    assert q8.q8_gemm_workspace(300, 1000, 1000) == 0          # K % 16
+    assert q8.q8_gemm_workspace(0, 8, 64) == 0
+    # a misaligned workspace is refused before anything is enqueued
+    st = lib.q8_gemm_dequant_ws(FAKE, FAKE, None, 1, FAKE, FAKE, 1, None, 512, 512, 512, FAKE, MISALIGNED, 1 << 20,
+                                None)
+    assert st == q8.Q8_ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     import int8_quantized_gemm_gb300 as q8
