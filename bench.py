@@ -323,10 +323,10 @@ def run_ours(args, world, rank, local):
     decode = None if args.no_decode else measure_decode(q8, device, args, hbm_peak, flush)
 
     # ---- W4A8: the same layers with int4 weights
-    w4 = None if args.no_decode else measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops)
+    w4 = None if args.no_decode else measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops, ws)
 
     # ---- block-scaled (E8M0 per K-group) weights on the same layers
-    mx = None if args.no_decode else measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops)
+    mx = None if args.no_decode else measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops, ws)
 
     # ---- the same GEMM with the bias + bf16 epilogue (the pages' output side)
     epi = measure_epilogue_bf16(q8, qa, s_a, qw, s_w, flush, args, ops)
@@ -570,11 +570,32 @@ def measure_decode(q8, device, args, hbm_peak, flush, kernels=("decode", "decode
             "algorithmic_bytes": gemm_bytes, "per_kernel": per_kernel}
 
 
-def measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops):
+def flushed_ms(fn, flush, args):
+    """Mean CUDA-event time of fn() with the L2 flushed before every launch."""
+    import torch
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(max(5, args.steps)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.mean(ms)
+
+
+def measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops, ws=None):
     """W4A8 (packed int4 weights): the decode GEMM (graph-timed back-to-back launches that cycle
     through three copies of the int4 weights: one copy, N K / 2 = 117 MB, fits in the 129 MB L2,
     so each launch reads a copy last touched 235 MB of traffic earlier) and the prefill GEMM (L2
-    flushed per launch)."""
+    flushed per launch), without and with the layer's workspace (the codes copied once as fp16
+    values, loaded by TMA; the copy is inside the timed call)."""
     import torch
 
     def graph_ms(fn, n):
@@ -616,32 +637,23 @@ def measure_w4a8(q8, device, qa, s_a, flush, args, hbm_peak, ops):
     qw4p, s4p = q8.q8_quantize_weight_int4(wp)
     del wp
     y = torch.empty((M, qw4p.shape[0]), dtype=torch.float32, device=device)
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y)
-    torch.cuda.synchronize()
-    ms = []
-    for _ in range(max(5, args.steps)):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y)
-        e1.record()
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
-    pms = statistics.mean(ms)
+    pms = flushed_ms(lambda: q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y), flush, args)
+    prefill_ws = None
+    if ws is not None and ws.numel() >= 2 * M * K:
+        wms = flushed_ms(lambda: q8.q8_gemm_w4a8(qa, s_a, None, qw4p, s4p, out=y, workspace=ws), flush, args)
+        prefill_ws = {"api": "q8_gemm_w4a8_ws", "gemm_ms": round(wms, 4), "TFLOP/s": round(ops / (wms * 1e-3) / 1e12, 1)}
     return {"decode": {"workload": f"{DECODE}: A [{Md},{Kd}] x W int4 [{Nd},{Kd}]", "gemm_ms": round(dms, 4),
                        "GB/s": round(dbytes / (dms * 1e-3) / 1e9, 1),
                        "frac_hbm": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": dbytes},
             "prefill": {"workload": f"{HEADLINE}: A [{M},{K}] x W int4 [{qw4p.shape[0]},{K}]", "gemm_ms": round(pms, 4),
-                        "TFLOP/s": round(ops / (pms * 1e-3) / 1e12, 1)}}
+                        "TFLOP/s": round(ops / (pms * 1e-3) / 1e12, 1)},
+            "prefill_ws": prefill_ws}
 
 
-def measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops):
+def measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops, ws=None):
     """Block-scaled int8 weights (one E8M0 scale per 32 or 128 K): the prefill GEMM (L2 flushed
-    per launch) for both granularities, and the decode layer (CUDA graph of back-to-back
-    launches; the int8 weights, 235 MB, exceed L2)."""
+    per launch) for both granularities, without and with the layer's workspace, and the decode
+    layer (CUDA graph of back-to-back launches; the int8 weights, 235 MB, exceed L2)."""
     import torch
     M, K = qa.shape
     wlh = workloads.WORKLOADS[HEADLINE]
@@ -650,23 +662,13 @@ def measure_mx(q8, device, qa, s_a, flush, args, hbm_peak, ops):
     for G in (32, 128):
         qw, sf = q8.q8_quantize_weight_mx(wp, G)
         y = torch.empty((M, qw.shape[0]), dtype=torch.float32, device=device)
-        for _ in range(max(3, args.warmup)):
-            flush.zero_()
-            q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y)
-        torch.cuda.synchronize()
-        ms = []
-        for _ in range(max(5, args.steps)):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y)
-            e1.record()
-            torch.cuda.synchronize()
-            ms.append(e0.elapsed_time(e1))
-        mean = statistics.mean(ms)
+        mean = flushed_ms(lambda: q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y), flush, args)
         out[f"prefill_g{G}"] = {"workload": f"{HEADLINE}: A [{M},{K}] x W int8 [{qw.shape[0]},{K}], E8M0 per {G} K",
                                 "gemm_ms": round(mean, 4), "TFLOP/s": round(ops / (mean * 1e-3) / 1e12, 1)}
+        if ws is not None and ws.numel() >= 2 * M * K:
+            wms = flushed_ms(lambda: q8.q8_gemm_mx(qa, s_a, qw, sf, G, out=y, workspace=ws), flush, args)
+            out[f"prefill_g{G}"]["ws"] = {"api": "q8_gemm_mx_ws", "gemm_ms": round(wms, 4),
+                                          "TFLOP/s": round(ops / (wms * 1e-3) / 1e12, 1)}
         del qw, sf, y
     del wp
     wl, a_d, w_d = layer_inputs(DECODE, device)

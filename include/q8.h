@@ -300,6 +300,28 @@ q8_status q8_gemm_w4a8_ex(const int8_t* qa, const float* s_a, const int32_t* z_a
                           const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type,
                           void* out, float out_scale, q8_gemm_kernel kernel, q8_stream_t stream);
 
+/*
+ * q8_gemm_w4a8_ex (kernel Q8_GEMM_AUTO) with a caller workspace: where the call
+ * runs the CTA-pair kernel (M > 16, or a shape the decode kernel does not take),
+ * the activation codes are first written once into the workspace as fp16 values,
+ * each group of four K in the order 0, 2, 1, 3 in which the kernel converts the
+ * packed weight codes, and the kernel loads them by TMA straight into its operand
+ * stages; its converter warps then handle the weights only. The result is that of
+ * q8_gemm_w4a8_ex, bit for bit (the same exact INT32 sums).
+ *
+ * workspace : NULL, or 16-byte aligned device memory of workspace_bytes bytes; used
+ *             iff workspace_bytes >= 2 M K and the CTA-pair kernel runs, then
+ *             overwritten. The caller owns it, may reuse it once the call's work on
+ *             `stream` has completed, and must not let it overlap any operand or out.
+ * Other arguments and errors as q8_gemm_w4a8_ex; a misaligned workspace returns
+ * Q8_ERR_INVALID_ARG.
+ */
+q8_status q8_gemm_w4a8_ws(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
+                          const uint8_t* qw4, const float* s_w, const int32_t* colsum,
+                          const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type,
+                          void* out, float out_scale, void* workspace, size_t workspace_bytes,
+                          q8_stream_t stream);
+
 /* Raw INT32 accumulators of the W4A8 product (diagnostic export, for bit-exact checks). */
 q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, int64_t N, int64_t K,
                               int32_t* acc, q8_gemm_kernel kernel, q8_stream_t stream);
@@ -350,6 +372,21 @@ q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, c
                         const uint32_t* sf, int group, const float* bias, int64_t M, int64_t N,
                         int64_t K, q8_out_type out_type, void* out, float out_scale,
                         q8_gemm_kernel kernel, q8_stream_t stream);
+
+/*
+ * q8_gemm_mx_ex (kernel Q8_GEMM_AUTO) with a caller workspace, as q8_gemm_w4a8_ws:
+ * where the CTA-pair kernel runs, the activation codes go once into the workspace
+ * as fp16 values (each group of four K as K 0, 2, 1, 3) and are loaded by TMA; the
+ * converter warps dequantize the weights only. The tensor core then sees the same
+ * operands in the same order as without the workspace: y is bit-identical to that
+ * of q8_gemm_mx_ex.
+ * workspace, workspace_bytes : as q8_gemm_w4a8_ws (used iff >= 2 M K bytes and the
+ * CTA-pair kernel runs). Other arguments and errors as q8_gemm_mx_ex.
+ */
+q8_status q8_gemm_mx_ws(const int8_t* qa, const float* s_a, q8_granularity ga, const int8_t* qw,
+                        const uint32_t* sf, int group, const float* bias, int64_t M, int64_t N,
+                        int64_t K, q8_out_type out_type, void* out, float out_scale,
+                        void* workspace, size_t workspace_bytes, q8_stream_t stream);
 
 /*
  * Activation codes stored as fp16 values. The quantization is that of

@@ -78,6 +78,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_w4a8_s32_ex.argtypes = [p, p, i64, i64, i64, p, i32, p]
     lib.q8_quantize_weight_mx.argtypes = [p, i64, i64, i32, p, p, p]
     lib.q8_gemm_mx_ex.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, i32, p]
+    lib.q8_gemm_w4a8_ws.argtypes = [p, p, p, i32, p, p, p, p, i64, i64, i64, i32, p, ctypes.c_float, p,
+                                    ctypes.c_size_t, p]
+    lib.q8_gemm_mx_ws.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, p,
+                                  ctypes.c_size_t, p]
     lib.q8_linear.argtypes = [p, i64, i64, i32, i32, p, p, p, p, p, i32, p, i64, p, p]
     lib.q8_selftest_wait_timeout.argtypes = [i32, p, p, i64, i64, i64, p, i64, p]
     lib.q8_linear_host_workspace.argtypes = [i64, i64, i64, i64]
@@ -92,6 +96,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_dequant_ws", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
                  "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
+                 "q8_gemm_w4a8_ws", "q8_gemm_mx_ws",
                  "q8_linear", "q8_linear_host", "q8_gemm_pick", "q8_device_error", "q8_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -344,9 +349,19 @@ def q8_colsum_int4(qw4: torch.Tensor, K: int, out=None, stream=None):
     return out
 
 
+def _ws_args(workspace, kernel):
+    if kernel != "auto":
+        raise ValueError("a workspace goes with the automatic kernel choice")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 def q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
-                 out=None, kernel: str = "auto", stream=None):
-    """W4A8 linear layer: int8 activations x packed int4 weights, epilogue as q8_gemm_epilogue."""
+                 out=None, kernel: str = "auto", workspace=None, stream=None):
+    """W4A8 linear layer: int8 activations x packed int4 weights, epilogue as q8_gemm_epilogue.
+    workspace: an optional device tensor of at least 2 M K bytes for the fp16 copy of the codes
+    (kernel "auto" only; q8_gemm_w4a8_ws)."""
     _need(qa, torch.int8, "qa", 2)
     _need(qw4, torch.uint8, "qw4", 2)
     M, K = qa.shape
@@ -371,6 +386,13 @@ def q8_gemm_w4a8(qa, s_a, z_a, qw4, s_w, colsum=None, bias=None, out_dtype=torch
         raise ValueError("int8 output needs out_scale")
     out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
     _need(out, out_dtype, "out", 2)
+    if workspace is not None:
+        wp, wb = _ws_args(workspace, kernel)
+        _check(load().q8_gemm_w4a8_ws(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw4), _ptr(s_w),
+                                      _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
+                                      OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0), wp, wb,
+                                      _stream(stream)), "q8_gemm_w4a8_ws")
+        return out
     _check(load().q8_gemm_w4a8_ex(_ptr(qa), _ptr(s_a), _ptr(z_a), ga, _ptr(qw4), _ptr(s_w),
                                   _ptr(colsum if z_a is not None else None), _ptr(bias), M, N, K,
                                   OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0),
@@ -515,8 +537,9 @@ def q8_quantize_weight_mx(w: torch.Tensor, group: int = 32, qw=None, sf=None, st
 
 
 def q8_gemm_mx(qa, s_a, qw, sf, group: int = 32, bias=None, out_dtype=torch.float32, out_scale=None, out=None,
-               kernel: str = "auto", stream=None):
-    """Linear layer with block-scaled int8 weights: y = fl(T * s_a) (+ bias), T = sum_k qa * q * s."""
+               kernel: str = "auto", workspace=None, stream=None):
+    """Linear layer with block-scaled int8 weights: y = fl(T * s_a) (+ bias), T = sum_k qa * q * s.
+    workspace: as q8_gemm_w4a8 (q8_gemm_mx_ws)."""
     _need(qa, torch.int8, "qa", 2)
     _need(qw, torch.int8, "qw", 2)
     _need(sf, torch.int32, "sf", 2)
@@ -536,6 +559,12 @@ def q8_gemm_mx(qa, s_a, qw, sf, group: int = 32, bias=None, out_dtype=torch.floa
         raise ValueError("int8 output needs out_scale")
     out = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
     _need(out, out_dtype, "out", 2)
+    if workspace is not None:
+        wp, wb = _ws_args(workspace, kernel)
+        _check(load().q8_gemm_mx_ws(_ptr(qa), _ptr(s_a), ga, _ptr(qw), _ptr(sf), group, _ptr(bias), M, N, K,
+                                    OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0), wp, wb,
+                                    _stream(stream)), "q8_gemm_mx_ws")
+        return out
     _check(load().q8_gemm_mx_ex(_ptr(qa), _ptr(s_a), ga, _ptr(qw), _ptr(sf), group, _ptr(bias), M, N, K,
                                 OUT_TYPES[out_dtype], _ptr(out), ctypes.c_float(out_scale or 0.0), KERNELS[kernel],
                                 _stream(stream)), "q8_gemm_mx")

@@ -72,6 +72,12 @@ size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K) {
     return (size_t)M * (size_t)K * 2;
 }
 
+// Workspace of the int4 and block-scaled weight formats on the CTA-pair kernel: an fp16 copy of the
+// activation codes (2 M K bytes), used when the caller's buffer holds it.
+bool use_lowbit_ws(int64_t M, int64_t K, const void* ws, size_t ws_bytes) {
+    return ws && aligned(ws, 16) && ws_bytes >= (size_t)M * (size_t)K * 2;
+}
+
 // qa: int8 codes, or (a16) the same codes as fp16 values.
 q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_granularity ga,
                       const int8_t* qw, const float* s_w, q8_granularity gw, const int32_t* colsum,
@@ -160,6 +166,12 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
             return from_cuda(q8::launch_gemv_mx(qa8, qw, mx->sf, mx->group, M, N, K, ep, s));
         }
         if (!q8::gemm_tc2_supports(M, N, K, q8::kWMx)) return Q8_ERR_UNSUPPORTED;
+        if (use_lowbit_ws(M, K, ws, ws_bytes)) {   // the codes as fp16 values (pair order) by TMA
+            uint16_t* qa16 = static_cast<uint16_t*>(ws);
+            cudaError_t e = q8::launch_codes_to_f16(qa8, M * K, qa16, s, true);
+            if (e != cudaSuccess) return from_cuda(e);
+            return from_cuda(q8::launch_gemm_tc2(qa16, qw, M, N, K, ep, s, q8::kWMxA16));
+        }
         return from_cuda(q8::launch_gemm_tc2(qa8, qw, M, N, K, ep, s, q8::kWMx));
     }
     if (w4) {
@@ -170,7 +182,13 @@ q8_status gemm_common(const void* qa, const float* s_a, const int32_t* z_a, q8_g
             return from_cuda(q8::launch_gemv_mma(qa8, qw, M, N, K, ep, s, true));
         }
         if (kernel == Q8_GEMM_TCGEN05_PAIR) {
-            if (!q8::gemm_tc2_supports(M, N, K, true)) return Q8_ERR_UNSUPPORTED;
+            if (!q8::gemm_tc2_supports(M, N, K, q8::kWInt4)) return Q8_ERR_UNSUPPORTED;
+            if (use_lowbit_ws(M, K, ws, ws_bytes)) {   // the codes as fp16 values (pair order) by TMA
+                uint16_t* qa16 = static_cast<uint16_t*>(ws);
+                cudaError_t e = q8::launch_codes_to_f16(qa8, M * K, qa16, s, true);
+                if (e != cudaSuccess) return from_cuda(e);
+                return from_cuda(q8::launch_gemm_tc2(qa16, qw, M, N, K, ep, s, q8::kW4A16));
+            }
             return from_cuda(q8::launch_gemm_tc2(qa8, qw, M, N, K, ep, s, q8::kWInt4));
         }
         return Q8_ERR_UNSUPPORTED;
@@ -363,6 +381,17 @@ q8_status q8_gemm_w4a8_ex(const int8_t* qa, const float* s_a, const int32_t* z_a
                        nullptr, nullptr, kernel, stream, &var, true);
 }
 
+q8_status q8_gemm_w4a8_ws(const int8_t* qa, const float* s_a, const int32_t* z_a, q8_granularity ga, const uint8_t* qw4,
+                          const float* s_w, const int32_t* colsum, const float* bias, int64_t M, int64_t N, int64_t K,
+                          q8_out_type out_type, void* out, float out_scale, void* workspace, size_t workspace_bytes,
+                          q8_stream_t stream) {
+    if (workspace && !aligned(workspace, 16)) return Q8_ERR_INVALID_ARG;
+    const Variant var{bias, out_type, out, out_scale};
+    return gemm_common(qa, s_a, z_a, ga, reinterpret_cast<const int8_t*>(qw4), s_w, Q8_PER_ROW, colsum, M, N, K,
+                       nullptr, nullptr, Q8_GEMM_AUTO, stream, &var, true, nullptr, false, false, false, 0, workspace,
+                       workspace_bytes);
+}
+
 q8_status q8_gemm_w4a8_s32_ex(const int8_t* qa, const uint8_t* qw4, int64_t M, int64_t N, int64_t K, int32_t* acc,
                               q8_gemm_kernel kernel, q8_stream_t stream) {
     return gemm_common(qa, nullptr, nullptr, Q8_PER_ROW, reinterpret_cast<const int8_t*>(qw4), nullptr, Q8_PER_ROW,
@@ -385,6 +414,16 @@ q8_status q8_gemm_mx_ex(const int8_t* qa, const float* s_a, q8_granularity ga, c
     const MxWeights mx{sf, group};
     return gemm_common(qa, s_a, nullptr, ga, qw, nullptr, Q8_PER_ROW, nullptr, M, N, K, nullptr, nullptr, kernel,
                        stream, &var, false, &mx);
+}
+
+q8_status q8_gemm_mx_ws(const int8_t* qa, const float* s_a, q8_granularity ga, const int8_t* qw, const uint32_t* sf,
+                        int group, const float* bias, int64_t M, int64_t N, int64_t K, q8_out_type out_type,
+                        void* out, float out_scale, void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+    if (workspace && !aligned(workspace, 16)) return Q8_ERR_INVALID_ARG;
+    const Variant var{bias, out_type, out, out_scale};
+    const MxWeights mx{sf, group};
+    return gemm_common(qa, s_a, nullptr, ga, qw, nullptr, Q8_PER_ROW, nullptr, M, N, K, nullptr, nullptr,
+                       Q8_GEMM_AUTO, stream, &var, false, &mx, false, false, false, 0, workspace, workspace_bytes);
 }
 
 q8_status q8_gemm_f16a_ex(const uint16_t* qa16, const float* s_a, const int32_t* z_a, q8_granularity ga,

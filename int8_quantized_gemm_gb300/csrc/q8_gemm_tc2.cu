@@ -76,6 +76,10 @@ constexpr int kA16 = BMH * BK * 2, kB16 = BNH * BK * 2, kStage16 = kA16 + kB16; 
 constexpr int kEpiBytes = 32 * 128;    // per drain warp: a 32 x 128-byte output block (TMA store source)
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 constexpr uint16_t kPairMask = 0x3;
+// Block-scaled weights whose scale words cannot be staged by TMA (N % 4 != 0 or a scale array
+// that is not 16-byte aligned): the converters load them from global memory this many stages ahead.
+constexpr int kSfAhead = 2;
+constexpr int kSfStage = BNH * 4;   // scale words of one stage's 128 weight rows, staged by TMA
 
 // Weight formats (WF): int8 codes (staged as 128 rows x 64 bytes per CTA), int4 codes packed
 // two per byte (128 rows x 32 bytes), or block-scaled int8 codes (kWMx: as int8, plus one E8M0
@@ -90,34 +94,46 @@ constexpr uint16_t kPairMask = 0x3;
 // then reads its 256 accumulator columns in two halves). Registers: the producer-side warps
 // shrink to kRegsLow, the drain warps grow to kRegsHigh; (2 + kConvWarps) * 32 * kRegsLow +
 // kDrainWarps * 32 * kRegsHigh <= 512 * 128, the registers the block is launched with.
-// Activation codes as fp16 values (kWA16): TMA writes the A half of each fp16 operand stage
-// directly (the 128-byte swizzle of a [128 x 64] fp16 box is the K-major layout of the UMMA
-// descriptors), the staging ring holds the int8 weights only, and the converters convert W.
-// The freed staging bytes give the operand ring a fifth stage.
+// Activation codes as fp16 values (kWA16, kW4A16, kWMxA16): TMA writes the A half of each fp16
+// operand stage directly (the 128-byte swizzle of a [128 x 64] fp16 box is the K-major layout of
+// the UMMA descriptors), the staging ring holds the weights only, and the converters convert W.
+// The freed staging bytes give the operand ring a fifth stage. The converters write int8 and
+// int4 weight codes alike in pair order (each group of four K as K 0, 2, 1, 3: cvt_word's
+// pairs); with kWA16 (codes in K order, also a public input format) the int8 weight bytes are
+// permuted into K order first, with kW4A16 and kWMxA16 the fp16 codes arrive in pair order.
 template <int WF>
 struct PairCfg {
-    static constexpr bool W4 = WF == kWInt4;
-    static constexpr bool A16 = WF == kWA16;
+    static constexpr bool W4 = WF == kWInt4 || WF == kW4A16;
+    static constexpr bool MX = WF == kWMx || WF == kWMxA16;
+    static constexpr bool A16 = WF == kWA16 || WF == kW4A16 || WF == kWMxA16;
     static constexpr int S16 = A16 ? 5 : 4;                   // fp16 operand stages (32 KB each)
     static constexpr int kOffStage8 = S16 * kStage16;
-    static constexpr int kConvWarps = WF == kWMx ? 10 : 6;
+    static constexpr int kConvWarps = MX ? 10 : 6;
     static constexpr int kDrainWarps = 16 - 2 - kConvWarps;
     static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
-    static constexpr int kRegsLow = WF == kWMx ? 104 : 72, kRegsHigh = 184;
+    static constexpr int kRegsLow = MX ? 104 : 72, kRegsHigh = 184;
     static_assert((2 + kConvWarps) * 32 * kRegsLow + kDrainWarps * 32 * kRegsHigh <= kThreads * 128,
                   "register split above the launch's registers");
     static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
-    static constexpr int kStage8 = (A16 ? 0 : kA8) + kB8;     // 16 KB (int8), 12 KB (int4), 8 KB (A16)
+    static constexpr int kStage8 = (A16 ? 0 : kA8) + kB8;     // 16 KB (int8), 12 KB (int4); fp16 A: 8 KB, 4 KB
     static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
-    static constexpr int KB_PER_CHUNK = W4 ? 256 : WF == kWMx ? (1 << 30) : 16;
-    static constexpr int kOffEpi = kOffStage8 + S8 * kStage8;
+    static constexpr int KB_PER_CHUNK = W4 ? 256 : MX ? (1 << 30) : 16;
+    static constexpr int kOffSf = kOffStage8 + S8 * kStage8;   // block-scaled: S8 x 128 scale words
+    static constexpr int kOffEpi = kOffSf + (MX ? S8 * kSfStage : 0);
     static constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
     static constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
-    static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0 && kOffEpi % 1024 == 0,
+                  "stages and the swizzled output buffers must keep 1024-byte alignment");
     static_assert(kSmem <= 227 * 1024, "above the shared memory of one CTA");
 };
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 struct PairGeom {
     int num_m, num_n, tiles;
@@ -153,9 +169,10 @@ template <int WF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_acc,
-                    int tma_out, int M, int N, int K, int n_full, int ksplit, Epilogue ep) {
+                    const __grid_constant__ CUtensorMap tmap_sf, int tma_out, int sf_tma, int M, int N, int K,
+                    int n_full, int ksplit, Epilogue ep) {
     using C = PairCfg<WF>;
-    constexpr bool W4 = WF == kWInt4, MX = WF == kWMx, A16 = C::A16;
+    constexpr bool W4 = C::W4, MX = C::MX, A16 = C::A16;
     constexpr int S8 = C::S8, S16 = C::S16, kStage8 = C::kStage8, KB_PER_CHUNK = C::KB_PER_CHUNK;
     constexpr int kOffStage8 = C::kOffStage8;
     constexpr int kOffEpi = C::kOffEpi, kOffBar = C::kOffBar;
@@ -234,10 +251,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                &g_tc2_error))
                     break;
                 const uint32_t dst = sbase + kOffStage8 + s * kStage8;
-                mbar_expect_tx(bar_full8 + 8 * s, kStage8);
+                const bool sf_now = MX && sf_tma;
+                mbar_expect_tx(bar_full8 + 8 * s, kStage8 + (sf_now ? kSfStage : 0));
                 const int kx = k0 + kb;
+                if (sf_now) {
+                    // the stage's scale words of the CTA's 128 weight rows (word row kx BK / 4G of the
+                    // [words, N] array, viewed as bytes [words, 4 N]), in two 256-byte boxes
+                    const int wrow = (kx * BK) / (4 * ep.mx_group);
+                    const uint32_t sdst = sbase + C::kOffSf + s * kSfStage;
+                    const int x0 = 4 * (n0 + (int)rank * BNH);
+                    tma_load_2d(sdst, &tmap_sf, x0, wrow, bar_full8 + 8 * s);
+                    tma_load_2d(sdst + kSfStage / 2, &tmap_sf, x0 + kSfStage / 2, wrow, bar_full8 + 8 * s);
+                }
                 if constexpr (A16) {
-                    tma_load_2d(dst, &tmap_w, kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                    tma_load_2d(dst, &tmap_w, W4 ? kx * (BK / 2) : kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
                     // the fp16 A codes go straight into the operand stage once the MMA has released it;
                     // their bytes complete on the barrier the converters arrive on
                     const int s16 = g % S16;
@@ -308,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         // ---------------------------------------------------------------- converters
-        if constexpr (A16) {
+        if constexpr (A16 && !W4 && !MX) {
             // W only: 512 16-byte int8 chunks per stage (128 rows x 4); thread ct takes idx = ct + T j
             // (idx < 512): row ct / 4 + (T / 4) j, chunk ct % 4, into the W half of the operand stage.
             constexpr int T = C::kConvT, NJ = (512 + T - 1) / T;
@@ -356,51 +383,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 64-byte staging row); thread ct takes idx = ct + T j (T = kConvT converter threads,
         // j < kIters, idx < 1024): row ct / 4 + (T / 4) j, chunk ct % 4. (row & 7) does not
         // change with j, so the swizzled fp16 address is a per-thread base plus 32 T j bytes.
+        // With fp16 activations (block-scaled weights only) the staging ring holds just the 512
+        // weight chunks: the thread's chunks are idx = 512 + ct + T j (j < 2, idx < 1024), read from
+        // staging offset 16 (idx - 512), and rows 128 .. 255 of the operand stage are its W half.
         if constexpr (!W4) {
-            constexpr int T = C::kConvT, NJ = (1024 + T - 1) / T;   // NJ: chunks per thread and stage
+            constexpr int T = C::kConvT;
+            constexpr int kIdx0 = A16 ? 512 : 0;                      // chunk index of staging byte 0
+            constexpr int NJ = (1024 - kIdx0 + T - 1) / T;            // chunks per thread and stage
             static_assert(!MX || T == 320, "the block-scaled slot map assumes 10 converter warps");
             const int ct = threadIdx.x - 64;
-            const int r0 = ct >> 2, c0 = ct & 3;
+            const int r0 = (kIdx0 >> 2) + (ct >> 2), c0 = ct & 3;
             const uint32_t src0 = (uint32_t)(ct * 16);
             const uint32_t dst0 = sw128(r0, 2 * c0);
             const uint32_t dst1 = sw128(r0, 2 * c0 + 1);
             // Block-scaled weights (T = 320): the thread's weight chunks (512 <= idx < 1024; weight
-            // row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage) are j = 2 (slot 1) and
-            // one of j = 1 (ct >= 192) or j = 3 (ct < 64) (slot 0). Their scale words are read from
-            // global memory (L2) one stage ahead of use.
-            uint32_t sfw_cur[2] = {0u, 0u}, sfw_nxt[2] = {0u, 0u};
-            int sh_cur = 0, sh_nxt = 0, pf_i = 0, pf_kb = 0;
+            // row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage) are, with int8
+            // activations, j = 2 (slot 1) and one of j = 1 (ct >= 192) or j = 3 (ct < 64) (slot 0);
+            // with fp16 activations j = 0 (slot 0) and j = 1 (slot 1, ct < 192). Their scale words are
+            // read from global memory (L2) kSfAhead stages ahead of use.
+            auto slot_j = [&](int jw) { return A16 ? jw : (jw == 1 ? 2 : (ct < 64 ? 3 : 1)); };
+            auto slot_of = [](int j) { return A16 ? (j & 1) : (j == 2 ? 1 : 0); };
+            // A ring of kSfAhead prefetched stages: slot 0 is the stage being converted.
+            uint32_t sfw_cur[2] = {0u, 0u}, sfq[kSfAhead][2];
+            int sh_cur = 0, shq[kSfAhead], pf_i = 0, pf_kb = 0;
             int sf_n[2] = {0, 0};                // weight rows of the slots in the prefetched stage's tile
             bool sf_ok[2] = {false, false};
             const int gshift = ep.mx_group == 32 ? 5 : 7;
-            auto sf_fetch = [&]() {
+            auto sf_fetch = [&](uint32_t (&dst)[2], int& sh) {
                 if constexpr (MX) {
                     if (pf_kb == 0) {   // a new tile: its weight rows
                         int pm0, pn0;
                         pair_coords(tg, cluster + pf_i * nclusters, pm0, pn0);   // MX: whole tiles only
 #pragma unroll
                         for (int jw = 0; jw < 2; ++jw) {
-                            const int j = jw == 1 ? 2 : (ct < 64 ? 3 : 1);
-                            const int idx = ct + T * j;
+                            const int idx = kIdx0 + ct + T * slot_j(jw);
                             sf_n[jw] = pn0 + (int)rank * BNH + ((idx - 512) >> 2);
                             sf_ok[jw] = idx >= 512 && idx < 1024 && sf_n[jw] < N;
                         }
                     }
                     const int grp = (pf_kb * BK + 16 * c0) >> gshift;
                     const uint32_t* base = ep.mx_sf + (int64_t)(grp >> 2) * N;
-                    sh_nxt = 8 * (grp & 3);
+                    sh = 8 * (grp & 3);
 #pragma unroll
-                    for (int jw = 0; jw < 2; ++jw) sfw_nxt[jw] = sf_ok[jw] ? __ldg(base + sf_n[jw]) : 0u;
+                    for (int jw = 0; jw < 2; ++jw) dst[jw] = sf_ok[jw] ? __ldg(base + sf_n[jw]) : 0u;
                     if (++pf_kb == KB) { pf_kb = 0; ++pf_i; }   // MX: whole tiles, KB stages each
                 }
             };
-            if (MX && total_g > 0) sf_fetch();
+            // Scale words staged by TMA: the slot's weight row within the CTA's half and the stage's
+            // k-block within its tile (block-scaled launches take whole tiles, KB stages each).
+            int sf_row[2] = {0, 0}, kbc = 0;
+#pragma unroll
+            for (int jw = 0; jw < 2; ++jw) {
+                const int idx = kIdx0 + ct + T * slot_j(jw);
+                sf_row[jw] = idx >= 512 && idx < 1024 ? (idx - 512) >> 2 : -1;
+            }
+#pragma unroll
+            for (int d = 0; d < kSfAhead; ++d) {
+                sfq[d][0] = sfq[d][1] = 0u;
+                shq[d] = 0;
+                if (MX && !sf_tma && d < total_g) sf_fetch(sfq[d], shq[d]);
+            }
             for (int g = 0; g < total_g; ++g) {
                 if constexpr (MX) {
+                  if (!sf_tma) {
+                    sfw_cur[0] = sfq[0][0];
+                    sfw_cur[1] = sfq[0][1];
+                    sh_cur = shq[0];
 #pragma unroll
-                    for (int jw = 0; jw < 2; ++jw) sfw_cur[jw] = sfw_nxt[jw];
-                    sh_cur = sh_nxt;
-                    if (g + 1 < total_g) sf_fetch();
+                    for (int d = 0; d + 1 < kSfAhead; ++d) {
+                        sfq[d][0] = sfq[d + 1][0];
+                        sfq[d][1] = sfq[d + 1][1];
+                        shq[d] = shq[d + 1];
+                    }
+                    if (g + kSfAhead < total_g) sf_fetch(sfq[kSfAhead - 1], shq[kSfAhead - 1]);
+                  }
                 }
                 const int s8 = g % S8, s16 = g % S16;
                 if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
@@ -409,7 +465,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint4 in[NJ];
     #pragma unroll
                 for (int j = 0; j < NJ; ++j)
-                    in[j] = (ct + T * j < 1024) ? lds128(st8 + T * 16 * j) : make_uint4(0, 0, 0, 0);
+                    in[j] = (kIdx0 + ct + T * j < 1024) ? lds128(st8 + T * 16 * j) : make_uint4(0, 0, 0, 0);
+                if constexpr (MX) {
+                    if (sf_tma) {   // this stage's scale words arrived with its weights
+                        const uint32_t sfb = sbase + C::kOffSf + s8 * kSfStage;
+#pragma unroll
+                        for (int jw = 0; jw < 2; ++jw)
+                            sfw_cur[jw] = sf_row[jw] >= 0 ? lds32(sfb + 4 * (uint32_t)sf_row[jw]) : 0u;
+                        sh_cur = 8 * (((kbc * BK + 16 * c0) >> gshift) & 3);
+                        if (++kbc == KB) kbc = 0;
+                    }
+                }
                 if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
                                &g_tc2_error))
                     break;
@@ -438,16 +504,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < NJ; ++j) {
-                        if (ct + T * j < 1024) {
+                        if (kIdx0 + ct + T * j < 1024) {
                             uint4 o0, o1;
-                            if (ct + T * j >= 512) {   // a weight chunk (warp-uniform)
-                                const uint32_t m = mg[j == 2 ? 1 : 0], c = m | 0x80008000u;
+                            if (kIdx0 + ct + T * j >= 512) {   // a weight chunk (warp-uniform)
+                                const uint32_t m = mg[slot_of(j)], c = m | 0x80008000u;
                                 cvt_word_magic(in[j].x, m, c, o0.x, o0.y);
                                 cvt_word_magic(in[j].y, m, c, o0.z, o0.w);
                                 cvt_word_magic(in[j].z, m, c, o1.x, o1.y);
                                 cvt_word_magic(in[j].w, m, c, o1.z, o1.w);
                                 if (slow) {   // rows with e > 132 were built at s / 16
-                                    const uint32_t pj = ev[j == 2 ? 1 : 0] > 132u ? 0x4C004C00u : 0x3C003C00u;   // 16 or 1
+                                    const uint32_t pj = ev[slot_of(j)] > 132u ? 0x4C004C00u : 0x3C003C00u;   // 16 or 1
                                     o0 = make_uint4(hmul2(o0.x, pj), hmul2(o0.y, pj), hmul2(o0.z, pj), hmul2(o0.w, pj));
                                     o1 = make_uint4(hmul2(o1.x, pj), hmul2(o1.y, pj), hmul2(o1.z, pj), hmul2(o1.w, pj));
                                 }
@@ -486,16 +552,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // int4 weights: A as above over its 512 chunks (j < 3, idx < 512); W's 256 packed chunks
-            // (128 rows x 2 chunks of 32 K) take idx = ct + 192 j (j < 2, idx < 256): row ct / 2 + 96 j,
-            // chunk ct % 2; each becomes four fp16 chunks 4 (ct % 2) + q of its row, word q of the
-            // packed chunk (8 K) giving fp16 chunk q through two nibble pairs, in the K order of cvt_word.
+            // int4 weights: A as above over its 512 chunks (j < 3, idx < 512; not with fp16 activations,
+            // which TMA has put in place); W's 256 packed chunks (128 rows x 2 chunks of 32 K) take
+            // idx = ct + 192 j (j < 2, idx < 256): row ct / 2 + 96 j, chunk ct % 2; each becomes four
+            // fp16 chunks 4 (ct % 2) + q of its row, word q of the packed chunk (8 K) giving fp16 chunk
+            // q through two nibble pairs, in the pair order of cvt_word.
             const int ct = threadIdx.x - 64;
             const int ra = ct >> 2, ca = ct & 3;
             const uint32_t srcA = (uint32_t)(ct * 16);
             const uint32_t dA0 = sw128(ra, 2 * ca), dA1 = sw128(ra, 2 * ca + 1);
             const int rw = ct >> 1, cw = ct & 1;
-            const uint32_t srcW = (uint32_t)(kA8 + ct * 16);
+            const uint32_t srcW = (uint32_t)((A16 ? 0 : kA8) + ct * 16);
             uint32_t dW[4];
     #pragma unroll
             for (int q = 0; q < 4; ++q) dW[q] = (uint32_t)kA16 + sw128(rw, 4 * cw + q);
@@ -507,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint4 ia[3], iw[2];
     #pragma unroll
                 for (int j = 0; j < 3; ++j)
-                    ia[j] = (ct + kConv * j < 512) ? lds128(st8 + srcA + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                    ia[j] = (!A16 && ct + kConv * j < 512) ? lds128(st8 + srcA + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
     #pragma unroll
                 for (int j = 0; j < 2; ++j)
                     iw[j] = (ct + kConv * j < 256) ? lds128(st8 + srcW + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
@@ -517,7 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t st16 = sbase + s16 * kStage16;
     #pragma unroll
                 for (int j = 0; j < 3; ++j) {
-                    if (ct + kConv * j < 512) {
+                    if (!A16 && ct + kConv * j < 512) {
                         uint4 o0, o1;
                         cvt_word(ia[j].x, o0.x, o0.y);
                         cvt_word(ia[j].y, o0.z, o0.w);
@@ -758,7 +825,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, int wfmt) {
-    if (!(M >= 1 && N >= 1 && K >= 16 && (K % (wfmt == kWInt4 ? 32 : 16)) == 0 && M < (1LL << 31) && N < (1LL << 31)))
+    const bool w4 = wfmt == kWInt4 || wfmt == kW4A16;
+    if (!(M >= 1 && N >= 1 && K >= 16 && (K % (w4 ? 32 : 16)) == 0 && M < (1LL << 31) && N < (1LL << 31)))
         return false;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t kb = (K + BK - 1) / BK;
@@ -861,8 +929,18 @@ static cudaError_t launch_gemm_tc2_t(const void* qa, const void* qw, int64_t M, 
     } else {
         memset(&mc, 0, sizeof(mc));
     }
-    gemm_tc2_kernel<WF><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, mc, tma_out ? 1 : 0, (int)M, (int)N,
-                                                                      (int)K, n_full, ksplit, ep);
+    // block-scaled weights: the scale words [words, N] as a byte matrix [words, 4 N] for TMA, where
+    // its rows are whole 16-byte multiples and its base is 16-byte aligned
+    CUtensorMap ms;
+    bool sf_tma = false;
+    if (C::MX && N % 4 == 0 && (reinterpret_cast<uintptr_t>(ep.mx_sf) & 15) == 0) {
+        const int64_t words = (K / ep.mx_group + 3) / 4;
+        sf_tma = make_tma_map_i8(&ms, reinterpret_cast<const int8_t*>(ep.mx_sf), words, 4 * N, 1, kSfStage / 2);
+    }
+    if (!sf_tma) memset(&ms, 0, sizeof(ms));
+    gemm_tc2_kernel<WF><<<2 * clusters, kThreads, C::kSmem, stream>>>(ma, mw, mo, mc, ms, tma_out ? 1 : 0,
+                                                                      sf_tma ? 1 : 0, (int)M, (int)N, (int)K, n_full,
+                                                                      ksplit, ep);
     note_launch();
     return cudaGetLastError();
 }
@@ -920,12 +998,15 @@ static cudaError_t launch_gemm_tc2_split(const void* qa, const void* qw, int64_t
 cudaError_t launch_gemm_tc2(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
                             cudaStream_t stream, int wfmt) {
     if (!gemm_tc2_supports(M, N, K, wfmt)) return cudaErrorNotSupported;
-    if (wfmt == kWMx) {
+    if (wfmt == kWMx || wfmt == kWMxA16) {
         if (!ep.mx_sf || (ep.mx_group != 32 && ep.mx_group != 128) || K % ep.mx_group != 0 || ep.out_i32 || ep.z_a)
             return cudaErrorInvalidValue;
-        return launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream, pair_geom(M, N).tiles, 1, nullptr);
+        const int tiles = pair_geom(M, N).tiles;
+        return wfmt == kWMx ? launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream, tiles, 1, nullptr)
+                            : launch_gemm_tc2_t<kWMxA16>(qa, qw, M, N, K, ep, stream, tiles, 1, nullptr);
     }
     if (wfmt == kWA16) return launch_gemm_tc2_split<kWA16>(qa, qw, M, N, K, ep, stream);
+    if (wfmt == kW4A16) return launch_gemm_tc2_split<kW4A16>(qa, qw, M, N, K, ep, stream);
     return wfmt == kWInt4 ? launch_gemm_tc2_split<kWInt4>(qa, qw, M, N, K, ep, stream)
                           : launch_gemm_tc2_split<kWInt8>(qa, qw, M, N, K, ep, stream);
 }

@@ -29,8 +29,9 @@ cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool
                                 uint16_t* q, float* s, int32_t* z, cudaStream_t stream);
 
 // int8 codes (n elements, n % 16 == 0, both bases 16-byte aligned) as the fp16 numbers of equal
-// value, in order.
-cudaError_t launch_codes_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t stream);
+// value, in order, or (pair_order) with each group of four codes stored as codes 0, 2, 1, 3.
+cudaError_t launch_codes_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t stream,
+                                bool pair_order = false);
 
 // int4 weights (W4A8): per-row symmetric codes packed two per byte (K % 32 == 0), and their
 // column sums.
@@ -116,11 +117,13 @@ cudaError_t launch_gemm_tc(const int8_t* qa, const int8_t* qw, int64_t M, int64_
 bool gemm_tc_supports(int64_t M, int64_t N, int64_t K);
 
 // Operand formats of the CTA-pair kernel: int8 codes, packed int4 codes, block-scaled int8
-// weights (activations as int8 codes), or int8 weights with the activation codes as fp16 values.
-enum WeightFormat : int { kWInt8 = 0, kWInt4 = 1, kWMx = 2, kWA16 = 3 };
+// weights (activations as int8 codes), or int8 / packed int4 / block-scaled weights with the
+// activation codes as fp16 values (kWA16: in K order; kW4A16, kWMxA16: in pair order, each group
+// of four K stored as K 0, 2, 1, 3, the order in which the kernel converts the weight codes).
+enum WeightFormat : int { kWInt8 = 0, kWInt4 = 1, kWMx = 2, kWA16 = 3, kW4A16 = 4, kWMxA16 = 5 };
 
 // tcgen05 kernel on CTA pairs (cta_group::2, 256 x 256 tiles). qa: int8 codes, or fp16 code
-// values for kWA16.
+// values for kWA16, kW4A16 and kWMxA16.
 cudaError_t launch_gemm_tc2(const void* qa, const void* qw, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
                             cudaStream_t stream, int wfmt = kWInt8);
 bool gemm_tc2_supports(int64_t M, int64_t N, int64_t K, int wfmt = kWInt8);

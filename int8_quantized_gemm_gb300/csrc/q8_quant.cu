@@ -1127,38 +1127,42 @@ cudaError_t launch_quantize_weight_mx(const float* w, int64_t N, int64_t K, int 
     return cudaGetLastError();
 }
 
-// int8 codes -> the fp16 numbers of equal value, in order (exact: |code| <= 128). For a word of
-// codes (b0, b1, b2, b3), the bytes permuted to (b0, b2, b1, b3) give, masked to their low bytes
-// and with 0x6400 | (byte ^ 0x80) = 1024 + 128 + code as fp16, minus 1152, the pairs (b0, b1) and
-// (b2, b3). A stream: 16 codes in, 32 bytes out per thread step.
+// int8 codes -> the fp16 numbers of equal value (exact: |code| <= 128). A word of codes
+// (b0, b1, b2, b3) masked to its bytes 0 and 2, with 0x6400 | (byte ^ 0x80) = 1024 + 128 + code as
+// fp16, minus 1152, gives the pair (b0, b2), and its bytes 1 and 3 the pair (b1, b3): the codes in
+// pair order (0, 2, 1, 3). For K order the bytes are first permuted to (b0, b2, b1, b3). A stream:
+// 16 codes in, 32 bytes out per thread step.
 __device__ __forceinline__ uint32_t hsub_1152_q(uint32_t v) {
     uint32_t r;
     asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(v), "r"(0x64806480u));
     return r;
 }
+template <bool kPairOrder>
 __device__ __forceinline__ uint2 codes4_to_f16(uint32_t w) {
-    const uint32_t x = __byte_perm(w, 0u, 0x3120u);
+    const uint32_t x = kPairOrder ? w : __byte_perm(w, 0u, 0x3120u);
     return make_uint2(hsub_1152_q((x & 0x00FF00FFu) ^ 0x64806480u), hsub_1152_q(((x >> 8) & 0x00FF00FFu) ^ 0x64806480u));
 }
 
+template <bool kPairOrder>
 __global__ void __launch_bounds__(256) codes_to_f16_kernel(const uint4* __restrict__ q, int64_t n16,
                                                            uint4* __restrict__ out) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 v = __ldcs(q + i);
-        const uint2 a = codes4_to_f16(v.x), b = codes4_to_f16(v.y), c = codes4_to_f16(v.z), d = codes4_to_f16(v.w);
+        const uint2 a = codes4_to_f16<kPairOrder>(v.x), b = codes4_to_f16<kPairOrder>(v.y);
+        const uint2 c = codes4_to_f16<kPairOrder>(v.z), d = codes4_to_f16<kPairOrder>(v.w);
         out[2 * i] = make_uint4(a.x, a.y, b.x, b.y);
         out[2 * i + 1] = make_uint4(c.x, c.y, d.x, d.y);
     }
 }
 
-cudaError_t launch_codes_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t stream) {
+cudaError_t launch_codes_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t stream, bool pair_order) {
     const int64_t n16 = n / 16;
     if (n16 == 0) return cudaSuccess;
     int64_t blocks = (n16 + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    codes_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(q), n16,
-                                                               reinterpret_cast<uint4*>(out));
+    auto kern = pair_order ? codes_to_f16_kernel<true> : codes_to_f16_kernel<false>;
+    kern<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(q), n16, reinterpret_cast<uint4*>(out));
     note_launch();
     return cudaGetLastError();
 }
