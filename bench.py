@@ -264,12 +264,27 @@ def run_ours(args, world, rank, local):
     y = torch.empty((M, N), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     kernel = q8.q8_gemm_pick(M, N, K)
-    # the layer's scratch for an fp16 copy of the activation codes (allocated once, like every buffer)
+    # the layer's scratch for an fp16 copy of the activation codes (allocated once, like every buffer):
+    # the quantizer writes the int8 codes and, in the same pass, the codes as fp16 values into it;
+    # the CTA-pair kernel loads that copy by TMA (the two calls q8_linear_ws makes)
     ws = gemm_workspace(q8, M, N, K, device)
+    ws16 = ws.view(torch.float16)[:M * K].view(M, K) if ws is not None else None
+
+    def quantize():
+        if ws16 is not None:
+            q8.q8_quantize_act_dual(a, per_row=apr, symmetric=sym, qa=qa, qa16=ws16, s_a=s_a, z_a=z_a)
+        else:
+            q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+
+    def gemm():
+        if ws16 is not None:
+            q8.q8_gemm_f16a(ws16, s_a, z_a, qw, s_w, colsum, out=y)
+        else:
+            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
 
     def step():
-        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
+        quantize()
+        gemm()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -286,9 +301,9 @@ def run_ours(args, world, rank, local):
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)
-            q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+            quantize()
             evs[i][1].record(stream)
-            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
+            gemm()
             evs[i][2].record(stream)
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
@@ -305,16 +320,16 @@ def run_ours(args, world, rank, local):
     gemm_avg = statistics.mean(gemm_ms)
     quant_avg = statistics.mean(quant_ms)
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
-    quant_bytes = M * K * 5 + 4 * M
+    quant_bytes = M * K * (7 if ws16 is not None else 5) + 4 * M     # fp32 in; int8 (+ fp16) codes out
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
-    gemm_bytes = M * K + N * K + 4 * N + 4 * M + 4 * M * N
+    gemm_bytes = M * K * (2 if ws16 is not None else 1) + N * K + 4 * N + 4 * M + 4 * M * N
 
     # ---- the same GEMM without the workspace: activation codes converted in shared memory per tile
     direct = measure_gemm_direct(q8, qa, s_a, z_a, qw, s_w, colsum, y, flush, args, tc_peak, ops)
 
     # ---- the same step run back to back for seconds, with the clock the power limit leaves
-    sustained = None if args.no_sustained else measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops,
-                                                                 args.sustained_s, ws)
+    sustained = None if args.no_sustained else measure_sustained(q8, quantize, gemm, flush, args, local, ops,
+                                                                 args.sustained_s)
 
     # ---- end to end through the public API: pinned host A in, y back to pinned host
     e2e = None if args.no_e2e else measure_e2e(q8, a, y, step, qw, s_w, colsum, sym, ops, world, args)
@@ -386,9 +401,10 @@ def run_ours(args, world, rank, local):
             "config": {"workload": f"{HEADLINE}: A fp32 [{M},{K}] per-token sym x W int8 [{N},{K}] per-channel"
                                    f" sym -> y fp32 [{M},{N}]",
                        "M": M, "N": N, "K": K, "gemm_kernel": kernel,
-                       "gemm_path": ("activation codes written once as fp16 into the layer's workspace, then the "
-                                     "CTA-pair kernel with TMA loads of them (q8_gemm_dequant_ws); both kernels "
-                                     "inside the GEMM's events") if ws is not None else "q8_gemm_dequant",
+                       "gemm_path": ("the quantizer writes the int8 codes and, in the same pass, the codes as fp16 "
+                                     "values into the layer's workspace (q8_quantize_act_dual); the CTA-pair kernel "
+                                     "loads that copy by TMA (q8_gemm_f16a): the two calls of q8_linear_ws")
+                       if ws is not None else "q8_gemm_dequant",
                        "l2": "flushed before every step (256 MiB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor",
@@ -396,8 +412,8 @@ def run_ours(args, world, rank, local):
                          "achieved": round(gemm_tops, 1),
                          "peak": tc_peak, "unit": "TFLOP/s", "frac": round(gemm_tops / tc_peak, 4),
                          "peak_source": f"{peak_kind} bf16 dense burst (the GEMM runs tcgen05 kind::f16; fp16 = bf16 rate)",
-                         "timing": "CUDA events around the whole GEMM call (with a workspace: the fp16 copy of the "
-                                   "codes, the tensor-core kernel and the K-split kernels)",
+                         "timing": "CUDA events around the whole GEMM call (the tensor-core kernel and the K-split "
+                                   "kernels)",
                          "traffic": measured_traffic(kernel + ("_f16a" if ws is not None else "")),
                          "algorithmic_bytes_per_launch": gemm_bytes, "ms_per_launch": round(gemm_avg, 4)},
             "quantizer": {"ms": round(quant_avg, 4), "GB/s": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
@@ -817,19 +833,33 @@ def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
     stream = torch.cuda.current_stream()
     kernel = q8.q8_gemm_pick(M, N, K)
     ws = gemm_workspace(q8, M, N, K, device)
+    ws16 = ws.view(torch.float16)[:M * K].view(M, K) if ws is not None else None
+
+    def quantize():   # as the headline: with a workspace, the int8 codes and their fp16 copy in one pass
+        if ws16 is not None:
+            q8.q8_quantize_act_dual(a, per_row=apr, symmetric=sym, qa=qa, qa16=ws16, s_a=s_a, z_a=z_a)
+        else:
+            q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+
+    def gemm():
+        if ws16 is not None:
+            q8.q8_gemm_f16a(ws16, s_a, z_a, qw, s_w, colsum, out=y)
+        else:
+            q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y)
+
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
+        quantize()
+        gemm()
     torch.cuda.synchronize()
     n = max(20, args.steps)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     for i in range(n):
         flush.zero_()
         evs[i][0].record(stream)
-        q8.q8_quantize_act(a, per_row=apr, symmetric=sym, qa=qa, s_a=s_a, z_a=z_a)
+        quantize()
         evs[i][1].record(stream)
-        q8.q8_gemm_dequant(qa, s_a, z_a, qw, s_w, colsum, y=y, workspace=ws)
+        gemm()
         evs[i][2].record(stream)
     torch.cuda.synchronize()
     assert q8.q8_device_error() == 0
@@ -839,6 +869,9 @@ def measure_config(q8, name, device, args, hbm_peak, tc_peak, flush):
     q, g, st = statistics.mean(qms), statistics.mean(gms), statistics.mean(sms)
     ops = 2.0 * M * N * K
     qbytes, gbytes = step_bytes(wl)
+    if ws16 is not None:   # the fp16 copy: written by the quantizer, read by the GEMM instead of the int8 codes
+        qbytes += 2 * M * K
+        gbytes += M * K
     gtf = ops / (g * 1e-3) / 1e12
     bound = {"tiny": "latency", "decode": "hbm"}.get(name, "tensor")
     if bound == "tensor":
@@ -919,7 +952,7 @@ def config_cpu(name, cores):
     return out
 
 
-def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, seconds, ws=None):
+def measure_sustained(q8, quantize, gemm, flush, args, local, ops, seconds):
     """The headline step back to back for about `seconds` (each step: the L2 flush, then the
     quantizer and the GEMM between CUDA events), with the SM clock sampled through NVML: the rate a
     layer keeps up once the power limit has pulled the clock down, against the sustained bf16 peak."""
@@ -930,8 +963,8 @@ def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, secon
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         flush.zero_()
-        q8.q8_quantize_act(a, qa=qa, s_a=s_a)
-        q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, workspace=ws)
+        quantize()
+        gemm()
         e1.record(stream)
         torch.cuda.synchronize()
         probe.append(e0.elapsed_time(e1))
@@ -943,9 +976,9 @@ def measure_sustained(q8, a, qa, s_a, qw, s_w, y, flush, args, local, ops, secon
         for i in range(n):
             flush.zero_()
             evs[i][0].record(stream)
-            q8.q8_quantize_act(a, qa=qa, s_a=s_a)
+            quantize()
             evs[i][1].record(stream)
-            q8.q8_gemm_dequant(qa, s_a, None, qw, s_w, y=y, workspace=ws)
+            gemm()
             evs[i][2].record(stream)
         torch.cuda.synchronize()
         w1 = time.perf_counter()

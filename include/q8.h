@@ -406,6 +406,39 @@ q8_status q8_quantize_act_f16(const float* a, int64_t M, int64_t K, q8_granulari
                               q8_stream_t stream);
 
 /*
+ * q8_quantize_act that also writes the codes as fp16 values (in K order, the
+ * format of q8_quantize_act_f16) into qa16: the int8 codes stay the stored
+ * activation format, and qa16 is the operand q8_gemm_f16a_ex loads by TMA.
+ * Per-token rows of up to 32768 elements take one pass over a (both formats from
+ * the row held in registers); otherwise q8_quantize_act runs, then a copy kernel.
+ *
+ * qa16 : fp16 bit patterns [M, K], written, 16-byte aligned, not overlapping the
+ *        other buffers. Other arguments and errors as q8_quantize_act.
+ */
+q8_status q8_quantize_act_dual(const float* a, int64_t M, int64_t K, q8_granularity g,
+                               q8_symmetry sym, int8_t* qa, uint16_t* qa16, float* s_a,
+                               int32_t* z_a, q8_stream_t stream);
+
+/*
+ * q8_linear with a caller workspace: where q8_gemm_workspace(M, N, K) is nonzero
+ * and workspace_bytes reaches it, the quantizer writes the codes both to qa (int8)
+ * and into the workspace (fp16 values, q8_quantize_act_dual) in one pass, and the
+ * CTA-pair kernel loads the fp16 copy by TMA (q8_gemm_f16a_ex). y, qa, s_a and z_a
+ * are those of q8_linear, bit for bit. Otherwise (workspace NULL or too small, or
+ * a shape on another kernel) the call is q8_linear.
+ *
+ * workspace : NULL, or 16-byte aligned device memory, overwritten when used; the
+ *             caller owns it and may reuse it once the call's work on `stream` has
+ *             completed; it must not overlap any other buffer of the call.
+ * Other arguments and errors as q8_linear; a misaligned workspace returns
+ * Q8_ERR_INVALID_ARG.
+ */
+q8_status q8_linear_ws(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_symmetry sym,
+                       int8_t* qa, float* s_a, int32_t* z_a, const int8_t* qw, const float* s_w,
+                       q8_granularity gw, const int32_t* colsum, int64_t N, float* y,
+                       void* workspace, size_t workspace_bytes, q8_stream_t stream);
+
+/*
  * q8_gemm_epilogue_ex on activation codes from q8_quantize_act_f16: the same
  * INT8 x INT8 -> INT32 products and sums (the fp16 values are the int8 codes),
  * the same epilogue and output types, on the CTA-pair tcgen05 kernel (TMA loads

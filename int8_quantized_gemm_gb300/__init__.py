@@ -28,7 +28,7 @@ from . import build as _build
 __all__ = [
     "Q8Error", "load", "q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
     "q8_gemm_epilogue", "q8_gemm_s32", "q8_linear", "q8_quantize_weight_int4", "q8_colsum_int4", "q8_gemm_w4a8",
-    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error",
+    "q8_gemm_w4a8_s32", "q8_quantize_weight_mx", "q8_gemm_mx", "q8_quantize_act_f16", "q8_quantize_act_dual", "q8_gemm_f16a", "q8_gemm_f16a_s32", "q8_linear_host", "q8_linear_host_workspace", "q8_gemm_workspace", "q8_gemm_pick", "q8_launch_count", "q8_device_error",
     "q8_selftest_wait_timeout", "KERNELS",
 ]
 
@@ -83,6 +83,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q8_gemm_mx_ws.argtypes = [p, p, i32, p, p, i32, p, i64, i64, i64, i32, p, ctypes.c_float, p,
                                   ctypes.c_size_t, p]
     lib.q8_linear.argtypes = [p, i64, i64, i32, i32, p, p, p, p, p, i32, p, i64, p, p]
+    lib.q8_linear_ws.argtypes = [p, i64, i64, i32, i32, p, p, p, p, p, i32, p, i64, p, p, ctypes.c_size_t, p]
+    lib.q8_quantize_act_dual.argtypes = [p, i64, i64, i32, i32, p, p, p, p, p]
     lib.q8_selftest_wait_timeout.argtypes = [i32, p, p, i64, i64, i64, p, i64, p]
     lib.q8_linear_host_workspace.argtypes = [i64, i64, i64, i64]
     lib.q8_linear_host_workspace.restype = ctypes.c_size_t
@@ -96,7 +98,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("q8_quantize_act", "q8_rmsnorm_quantize_act", "q8_quantize_weight", "q8_colsum", "q8_gemm_dequant",
                  "q8_gemm_dequant_ex", "q8_gemm_dequant_ws", "q8_gemm_epilogue_ex", "q8_gemm_s32_ex", "q8_quantize_weight_int4",
                  "q8_colsum_int4", "q8_gemm_w4a8_ex", "q8_gemm_w4a8_s32_ex", "q8_quantize_weight_mx", "q8_gemm_mx_ex",
-                 "q8_gemm_w4a8_ws", "q8_gemm_mx_ws",
+                 "q8_gemm_w4a8_ws", "q8_gemm_mx_ws", "q8_linear_ws", "q8_quantize_act_dual",
                  "q8_linear", "q8_linear_host", "q8_gemm_pick", "q8_device_error", "q8_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -289,6 +291,27 @@ def q8_quantize_act_f16(a: torch.Tensor, per_row: bool = True, symmetric: bool =
     return qa16, s_a, z_a
 
 
+def q8_quantize_act_dual(a: torch.Tensor, per_row: bool = True, symmetric: bool = True, qa=None, qa16=None,
+                         s_a=None, z_a=None, stream=None):
+    """q8_quantize_act that also writes the codes as fp16 values (for q8_gemm_f16a); returns
+    (qa int8, qa16 float16, s_a, z_a or None)."""
+    _need(a, torch.float32, "a", 2)
+    M, K = a.shape
+    n = M if per_row else 1
+    qa = torch.empty((M, K), dtype=torch.int8, device=a.device) if qa is None else qa
+    qa16 = torch.empty((M, K), dtype=torch.float16, device=a.device) if qa16 is None else qa16
+    _need(qa16, torch.float16, "qa16", 2)
+    s_a = torch.empty(n, dtype=torch.float32, device=a.device) if s_a is None else s_a
+    if not symmetric and z_a is None:
+        z_a = torch.empty(n, dtype=torch.int32, device=a.device)
+    if symmetric:
+        z_a = None
+    _check(load().q8_quantize_act_dual(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
+                                       Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(qa16), _ptr(s_a),
+                                       _ptr(z_a), _stream(stream)), "q8_quantize_act_dual")
+    return qa, qa16, s_a, z_a
+
+
 def q8_gemm_f16a(qa16, s_a, z_a, qw, s_w, colsum=None, bias=None, out_dtype=torch.float32, out_scale=None,
                  out=None, stream=None):
     """q8_gemm_epilogue on fp16-valued activation codes (from q8_quantize_act_f16)."""
@@ -427,9 +450,11 @@ def q8_gemm_s32(qa, qw, out=None, kernel: str = "auto", stream=None):
 
 
 def q8_linear(a, qw, s_w, colsum=None, per_row: bool = True, symmetric: bool = True, kernel: str = "auto",
-              qa=None, s_a=None, z_a=None, y=None, stream=None):
+              qa=None, s_a=None, z_a=None, y=None, workspace=None, stream=None):
     """Whole W8A8 layer on fp32 activations: dynamic quantization of a, then the GEMM + epilogue
-    (one C call, q8_linear, for kernel="auto"; an explicit kernel runs the two calls). Returns y."""
+    (one C call, q8_linear, for kernel="auto"; an explicit kernel runs the two calls). workspace:
+    an optional device tensor of at least q8_gemm_workspace(M, N, K) bytes (q8_linear_ws: the
+    quantizer also writes the codes as fp16 values there for the CTA-pair kernel). Returns y."""
     if kernel != "auto":
         qa, s_a, z_a = q8_quantize_act(a, per_row=per_row, symmetric=symmetric, qa=qa, s_a=s_a, z_a=z_a,
                                        stream=stream)
@@ -453,6 +478,13 @@ def q8_linear(a, qw, s_w, colsum=None, per_row: bool = True, symmetric: bool = T
     y = torch.empty((M, N), dtype=torch.float32, device=a.device) if y is None else y
     _need(y, torch.float32, "y", 2)
     gw = Q8_PER_ROW if (s_w.numel() == N and N != 1) else Q8_PER_TENSOR
+    if workspace is not None:
+        wp, wb = _ws_args(workspace, kernel)
+        _check(load().q8_linear_ws(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
+                                   Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(s_a), _ptr(z_a),
+                                   _ptr(qw), _ptr(s_w), gw, _ptr(colsum if not symmetric else None), N, _ptr(y), wp,
+                                   wb, _stream(stream)), "q8_linear_ws")
+        return y
     _check(load().q8_linear(_ptr(a), M, K, Q8_PER_ROW if per_row else Q8_PER_TENSOR,
                             Q8_SYMMETRIC if symmetric else Q8_ASYMMETRIC, _ptr(qa), _ptr(s_a), _ptr(z_a), _ptr(qw),
                             _ptr(s_w), gw, _ptr(colsum if not symmetric else None), N, _ptr(y), _stream(stream)),

@@ -281,6 +281,44 @@ q8_status q8_linear(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_
                        false, nullptr, false, false, early);
 }
 
+q8_status q8_quantize_act_dual(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym, int8_t* qa,
+                               uint16_t* qa16, float* s_a, int32_t* z_a, q8_stream_t stream) {
+    q8_status st = check_act_args(a, M, K, g, sym, qa, s_a, z_a);
+    if (st != Q8_OK) return st;
+    if (M > 0 && K > 0 && (!qa16 || !aligned(qa16, 16))) return Q8_ERR_INVALID_ARG;
+    if (g == Q8_PER_ROW && M == 0) return Q8_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (g == Q8_PER_ROW && K > 0) {
+        // one pass: both code formats from the row in registers
+        cudaError_t e = q8::launch_quantize_dual(a, M, K, qa, qa16, s_a, z_a, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    cudaError_t e = q8::launch_quantize(a, M, K, g == Q8_PER_ROW, qa, s_a, z_a, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(q8::launch_codes_to_f16(qa, M * K, qa16, s));
+}
+
+q8_status q8_linear_ws(const float* a, int64_t M, int64_t K, q8_granularity ga, q8_symmetry sym, int8_t* qa,
+                       float* s_a, int32_t* z_a, const int8_t* qw, const float* s_w, q8_granularity gw,
+                       const int32_t* colsum, int64_t N, float* y, void* workspace, size_t workspace_bytes,
+                       q8_stream_t stream) {
+    if (workspace && !aligned(workspace, 16)) return Q8_ERR_INVALID_ARG;
+    const size_t need = gemm_ws_bytes(M, N, K);
+    if (!workspace || need == 0 || workspace_bytes < need)
+        return q8_linear(a, M, K, ga, sym, qa, s_a, z_a, qw, s_w, gw, colsum, N, y, stream);
+    // Both halves are validated before either is enqueued: the quantizer writes the int8 codes to qa
+    // and the same codes as fp16 values into the workspace, which the CTA-pair kernel loads by TMA.
+    q8_status st = check_act_args(a, M, K, ga, sym, qa, s_a, z_a);
+    if (st != Q8_OK) return st;
+    st = gemm_common(workspace, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream, nullptr,
+                     false, nullptr, true, true);
+    if (st != Q8_OK) return st;
+    st = q8_quantize_act_dual(a, M, K, ga, sym, qa, static_cast<uint16_t*>(workspace), s_a, z_a, stream);
+    if (st != Q8_OK) return st;
+    return gemm_common(workspace, s_a, z_a, ga, qw, s_w, gw, colsum, M, N, K, y, nullptr, Q8_GEMM_AUTO, stream,
+                       nullptr, false, nullptr, true);
+}
+
 q8_status q8_quantize_act_f16(const float* a, int64_t M, int64_t K, q8_granularity g, q8_symmetry sym,
                               uint16_t* qa16, float* s_a, int32_t* z_a, q8_stream_t stream) {
     q8_status st = check_act_args(a, M, K, g, sym, reinterpret_cast<const int8_t*>(qa16), s_a, z_a);

@@ -24,6 +24,10 @@ constexpr float kZeroGuard = 1e-8f;
 // or one for the whole tensor. z == nullptr selects the symmetric rule.
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per_row,
                             int8_t* q, float* s, int32_t* z, cudaStream_t stream);
+// Per-token quantization writing the int8 codes to q and the same codes as fp16 values to q16
+// (K order) in one pass; cudaErrorNotSupported for rows longer than 32768 elements.
+cudaError_t launch_quantize_dual(const float* x, int64_t rows, int64_t cols, int8_t* q, uint16_t* q16, float* s,
+                                 int32_t* z, cudaStream_t stream);
 // The same codes written as fp16 values (exact: |code| <= 128), two bytes each.
 cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool per_row,
                                 uint16_t* q, float* s, int32_t* z, cudaStream_t stream);

@@ -137,14 +137,20 @@ __device__ __forceinline__ void store_codes4_tracked(void* q, int64_t i, float4 
     store_codes4<H>(q, i, c[0], c[1], c[2], c[3]);
 }
 
-// The same four codes with rint_quot_bits' near-half check (the exact path).
-template <bool ASYM, bool H>
-__device__ __forceinline__ void store_codes4_exact(void* q, int64_t i, float4 v, float s, float r, int zoff) {
-    if constexpr (ASYM)
-        store_codes4<H>(q, i, asym_code(v.x, s, r, zoff), asym_code(v.y, s, r, zoff), asym_code(v.z, s, r, zoff),
-                        asym_code(v.w, s, r, zoff));
-    else
-        store_codes4<H>(q, i, sym_code(v.x, s, r), sym_code(v.y, s, r), sym_code(v.z, s, r), sym_code(v.w, s, r));
+// The same four codes with rint_quot_bits' near-half check (the exact path). DUAL: int8 codes to q
+// and the same codes as fp16 values to q16 (both in K order).
+template <bool ASYM, bool H, bool DUAL = false>
+__device__ __forceinline__ void store_codes4_exact(void* q, int64_t i, float4 v, float s, float r, int zoff,
+                                                   uint16_t* q16 = nullptr) {
+    uint32_t c[4];
+    if constexpr (ASYM) {
+        c[0] = asym_code(v.x, s, r, zoff), c[1] = asym_code(v.y, s, r, zoff);
+        c[2] = asym_code(v.z, s, r, zoff), c[3] = asym_code(v.w, s, r, zoff);
+    } else {
+        c[0] = sym_code(v.x, s, r), c[1] = sym_code(v.y, s, r), c[2] = sym_code(v.z, s, r), c[3] = sym_code(v.w, s, r);
+    }
+    store_codes4<H>(q, i, c[0], c[1], c[2], c[3]);
+    if constexpr (DUAL) store_codes4<true>(q16, i, c[0], c[1], c[2], c[3]);
 }
 
 // Block-wide max of two values (hi, and nlo = -lo for the asymmetric range).
@@ -173,12 +179,14 @@ __device__ __forceinline__ void block_max2(float& hi, float& nlo, float* red) {
 }
 
 // One CTA per row; each thread keeps up to VPT float4 of the row in registers.
-// Requires cols % 4 == 0 and cols / 4 <= VPT * blockDim.x.
-template <int VPT, bool ASYM, bool H = false>
+// Requires cols % 4 == 0 and cols / 4 <= VPT * blockDim.x. DUAL: the int8 codes and, in q16, the
+// same codes as fp16 values.
+template <int VPT, bool ASYM, bool H = false, bool DUAL = false>
 __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel(const float* __restrict__ x, int64_t cols,
                                                             void* __restrict__ q,
                                                             float* __restrict__ s,
-                                                            int32_t* __restrict__ z) {
+                                                            int32_t* __restrict__ z,
+                                                            uint16_t* __restrict__ q16) {
     __shared__ float red[64];
     // A decode GEMM launched after this kernel with programmatic stream serialization may start
     // its weight stream now; it reads the codes and scales only after waiting for this grid.
@@ -217,10 +225,11 @@ __global__ void __launch_bounds__(1024, (VPT <= 4 ? 2 : 1)) quantize_rows_kernel
     const float rc = __fdiv_rn(1.0f, sc);
     const int zoff = zp - (int)kMagicBits;
     void* qr = static_cast<uint8_t*>(q) + row * cols * (H ? 2 : 1);
+    uint16_t* q16r = DUAL ? q16 + row * cols : nullptr;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-        if (i < n4) store_codes4_exact<ASYM, H>(qr, i, v[j], sc, rc, zoff);
+        if (i < n4) store_codes4_exact<ASYM, H, DUAL>(qr, i, v[j], sc, rc, zoff, q16r);
     }
 }
 
@@ -969,12 +978,29 @@ int num_sms() {
     return sms;
 }
 
-template <int VPT, bool ASYM, bool H>
+template <int VPT, bool ASYM, bool H, bool DUAL = false>
 cudaError_t launch_rows(const float* x, int64_t rows, int64_t cols, int threads, void* q, float* s,
-                        int32_t* z, cudaStream_t st) {
-    quantize_rows_kernel<VPT, ASYM, H><<<(unsigned)rows, threads, 0, st>>>(x, cols, q, s, z);
+                        int32_t* z, cudaStream_t st, uint16_t* q16 = nullptr) {
+    quantize_rows_kernel<VPT, ASYM, H, DUAL><<<(unsigned)rows, threads, 0, st>>>(x, cols, q, s, z, q16);
     note_launch();
     return cudaGetLastError();
+}
+
+// Both code formats from one pass (rows held in registers, up to 8 float4 per thread); longer
+// rows return cudaErrorNotSupported.
+template <bool ASYM>
+cudaError_t dispatch_rows_dual(const float* x, int64_t rows, int64_t cols, int8_t* q, uint16_t* q16, float* s,
+                               int32_t* z, cudaStream_t st) {
+    const int64_t n4 = cols / 4;
+    auto threads_for = [&](int vpt) {
+        int64_t t = (n4 + vpt - 1) / vpt;
+        t = ((t + kWarp - 1) / kWarp) * kWarp;
+        return (int)(t < kWarp ? kWarp : t);
+    };
+    if (n4 <= 256) return launch_rows<1, ASYM, false, true>(x, rows, cols, threads_for(1), q, s, z, st, q16);
+    if (n4 <= 1024 * 4) return launch_rows<4, ASYM, false, true>(x, rows, cols, threads_for(4), q, s, z, st, q16);
+    if (n4 <= 1024 * 8) return launch_rows<8, ASYM, false, true>(x, rows, cols, threads_for(8), q, s, z, st, q16);
+    return cudaErrorNotSupported;
 }
 
 template <bool ASYM, bool H>
@@ -1028,6 +1054,13 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, bool per
     }
     return z ? dispatch_tensor<true, false>(x, rows * cols, q, s, z, stream)
              : dispatch_tensor<false, false>(x, rows * cols, q, s, z, stream);
+}
+
+cudaError_t launch_quantize_dual(const float* x, int64_t rows, int64_t cols, int8_t* q, uint16_t* q16, float* s,
+                                 int32_t* z, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    return z ? dispatch_rows_dual<true>(x, rows, cols, q, q16, s, z, stream)
+             : dispatch_rows_dual<false>(x, rows, cols, q, q16, s, z, stream);
 }
 
 cudaError_t launch_quantize_f16(const float* x, int64_t rows, int64_t cols, bool per_row, uint16_t* q,

@@ -92,3 +92,53 @@ def test_small_or_absent_workspace_takes_the_direct_path(q8):
     np.testing.assert_array_equal(y0.cpu().numpy().view(np.int32), y1.cpu().numpy().view(np.int32))
     # decode shapes take no workspace
     assert q8.q8_gemm_workspace(16, N, K) == 0
+
+
+@pytest.mark.parametrize("M,K,per_row,sym", [(300, 4096, True, True), (257, 1040, True, False), (64, 40000, True, True),
+                                             (100, 2048, False, True), (33, 64, True, False)])
+def test_dual_quantizer_writes_both_code_formats(q8, M, K, per_row, sym):
+    # one pass for rows of up to 32768 elements, the quantizer and the copy kernel beyond (K = 40000)
+    # and for per-tensor scales: the same codes, scales and zero points as the single-format calls
+    wl = workloads.WORKLOADS["relu4k" if not sym else "prefill2k"]
+    a = dev(workloads.make_activations(wl, M=M, K=K))
+    qa, qa16, s_a, z_a = q8.q8_quantize_act_dual(a, per_row=per_row, symmetric=sym)
+    qa_ref, s_ref, z_ref = q8.q8_quantize_act(a, per_row=per_row, symmetric=sym)
+    qa16_ref, _, _ = q8.q8_quantize_act_f16(a, per_row=per_row, symmetric=sym)
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    np.testing.assert_array_equal(qa.cpu().numpy(), qa_ref.cpu().numpy())
+    np.testing.assert_array_equal(qa16.view(torch.int16).cpu().numpy(), qa16_ref.view(torch.int16).cpu().numpy())
+    np.testing.assert_array_equal(s_a.cpu().numpy().view(np.int32), s_ref.cpu().numpy().view(np.int32))
+    if not sym:
+        np.testing.assert_array_equal(z_a.cpu().numpy(), z_ref.cpu().numpy())
+    ref = oracle.quantize_sym(a.cpu().numpy(), per_row=per_row)[0] if sym else \
+        oracle.quantize_asym(a.cpu().numpy(), per_row=per_row)[0]
+    np.testing.assert_array_equal(qa16.float().cpu().numpy().astype(np.int32), ref.astype(np.int32))
+
+
+@pytest.mark.parametrize("name,M,N,K,sym", [("prefill2k", 512, 2048, 2048, True), ("relu4k", 2048, 4096, 4096, False),
+                                            ("prefill2k", 333, 520, 1040, True), ("decode", 16, 1024, 4096, True)])
+def test_linear_with_workspace_equals_linear(q8, name, M, N, K, sym):
+    # the quantizer writes the fp16 copy itself and the pair kernel loads it; the decode shape
+    # takes no workspace (q8_linear itself)
+    wl = workloads.WORKLOADS[name]
+    a = dev(workloads.make_activations(wl, M=M, K=K))
+    w = dev(workloads.make_weights(wl, N=N, K=K))
+    qw, s_w = q8.q8_quantize_weight(w, per_row=True)
+    cs = None if sym else q8.q8_colsum(qw)
+    need = q8.q8_gemm_workspace(M, N, K)
+    ws = torch.full((max(need, 16),), 0x55, dtype=torch.uint8, device="cuda")
+    y_ref = q8.q8_linear(a, qw, s_w, cs, symmetric=sym)
+    qa = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    for _ in range(2):
+        y = q8.q8_linear(a, qw, s_w, cs, symmetric=sym, qa=qa, workspace=ws)
+        torch.cuda.synchronize()
+        assert q8.q8_device_error() == 0
+        np.testing.assert_array_equal(y.cpu().numpy().view(np.int32), y_ref.cpu().numpy().view(np.int32))
+    qa_ref, _, _ = q8.q8_quantize_act(a, symmetric=sym)
+    np.testing.assert_array_equal(qa.cpu().numpy(), qa_ref.cpu().numpy())
+    if need == 0:
+        assert bool((ws == 0x55).all())
+    else:
+        np.testing.assert_array_equal(ws.view(torch.float16)[:M * K].view(M, K).float().cpu().numpy().astype(np.int32),
+                                      qa_ref.cpu().numpy().astype(np.int32))
