@@ -48,9 +48,9 @@ L2_FLUSH_BYTES = 256 << 20
 # capture was taken on.
 MEASURED_TRAFFIC = {
     # the CTA-pair kernel loading the fp16 copy of the activation codes (the GEMM with a workspace)
-    "tcgen05_pair_f16a": {"bytes": 1_777_453_312 + 257_442_304,
+    "tcgen05_pair_f16a": {"bytes": 1_778_580_480 + 256_575_488,
                           "sources": ("q8_gemm_tc2.cu", "q8_tc_ptx.cuh", "q8_internal.h"),
-                          "sha256_16": "c7be40686a656454"},
+                          "sha256_16": "9d6b7a4e7fec3637"},
 }
 
 
@@ -1089,6 +1089,8 @@ def main():
                     help="only the W4A8 (int4 weight) measurements (one JSON object, for profiling)")
     ap.add_argument("--mx-only", action="store_true",
                     help="only the block-scaled weight measurements (one JSON object, for profiling)")
+    ap.add_argument("--rms-only", action="store_true",
+                    help="only the fused RMSNorm + quantize measurement (one JSON object, for profiling)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode-shaped workload (one JSON object, for profiling)")
     ap.add_argument("--f16a-only", action="store_true",
@@ -1113,7 +1115,8 @@ def main():
         a = torch.from_numpy(workloads.make_activations(wl)).to(device)
         qa, s_a, _ = q8.q8_quantize_act(a)
         del a
-        print(json.dumps(measure_w4a8(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K)))
+        ws = gemm_workspace(q8, wl.M, wl.N, wl.K, device)
+        print(json.dumps(measure_w4a8(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K, ws)))
         return
     if args.mx_only:
         import torch
@@ -1128,7 +1131,23 @@ def main():
         a = torch.from_numpy(workloads.make_activations(wl)).to(device)
         qa, s_a, _ = q8.q8_quantize_act(a)
         del a
-        print(json.dumps(measure_mx(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K)))
+        ws = gemm_workspace(q8, wl.M, wl.N, wl.K, device)
+        print(json.dumps(measure_mx(q8, device, qa, s_a, flush, args, peaks()[0], 2.0 * wl.M * wl.N * wl.K, ws)))
+        return
+    if args.rms_only:
+        import torch
+        import int8_quantized_gemm_gb300 as q8
+        from int8_quantized_gemm_gb300 import build
+        build.build()
+        q8.load()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        wl = workloads.WORKLOADS[HEADLINE]
+        a = torch.from_numpy(workloads.make_activations(wl)).to(device)
+        qa = torch.empty((wl.M, wl.K), dtype=torch.int8, device=device)
+        s_a = torch.empty(wl.M, dtype=torch.float32, device=device)
+        print(json.dumps(measure_rmsnorm_quantize(q8, a, qa, s_a, flush, args, peaks()[0])))
         return
     if args.decode_only:
         import torch

@@ -704,10 +704,14 @@ __device__ __forceinline__ void bulk_row_load(uint32_t dst, const float* src, ui
                  : "memory");
 }
 
-template <int VPT>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+// THREADS threads per CTA, VPT float4 per thread; FULL: every row is exactly VPT * THREADS float4
+// (no bounds checks). With THREADS <= 512 each thread keeps its gamma float4s in registers for all
+// its rows (the persistent grid gives a thread the same columns in every row).
+template <int VPT, int THREADS, bool FULL>
+__global__ void __launch_bounds__(THREADS, 1)
     rmsnorm_quantize_stream_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int64_t rows,
                                    int64_t cols, float eps, int8_t* __restrict__ q, float* __restrict__ s) {
+    constexpr bool kGammaRegs = THREADS <= 512 && VPT <= 8;
     extern __shared__ __align__(128) uint8_t rowbuf[];
     __shared__ __align__(8) uint64_t bar_cells[kStreamBufs];
     __shared__ float2 red[32];
@@ -715,9 +719,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     __shared__ float bc[4];
     __shared__ int abort_cell;
     const uint32_t bytes = (uint32_t)(cols * 4);
-    const int64_t n4 = cols / 4;
+    const int n4 = (int)(cols / 4);
     const float4* g4 = reinterpret_cast<const float4*>(gamma);
     volatile int* abort_flag = &abort_cell;
+    auto live = [&](int j) { return FULL || (int)threadIdx.x + j * THREADS < n4; };
+    float4 gv[kGammaRegs ? VPT : 1];
+    if constexpr (kGammaRegs) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            gv[j] = live(j) ? __ldg(g4 + threadIdx.x + j * THREADS) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     if (threadIdx.x == 0) {
         for (int b = 0; b < kStreamBufs; ++b) tc::mbar_init(tc::smem_u32(&bar_cells[b]), 1);
         abort_cell = 0;
@@ -745,9 +756,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         uint32_t tmin = 0xFFFFFFFFu;   // min over the thread's elements of 2 |x|bits - 2 (zeros: huge)
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
-            if (i < n4) {
-                const uint4 r = tc::lds128(buf + 16u * (uint32_t)i);
+            if (live(j)) {
+                const uint4 r = tc::lds128(buf + 16u * (threadIdx.x + (uint32_t)(j * THREADS)));
                 v[j] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
                 pair_add_square(hi, lo, v[j].x);
                 pair_add_square(hi, lo, v[j].y);
@@ -767,12 +777,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         const float rms = bc[0], rr = bc[1];
         const bool fast = rms >= 0x1p-60f && rms <= 0x1p60f && tmin >= 2u * kDivTinyBits - 2u;
         float amax = 0.0f;
+        auto gamma_of = [&](int j) { return kGammaRegs ? gv[kGammaRegs ? j : 0] : __ldg(g4 + threadIdx.x + j * THREADS); };
         if (fast) {
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
-                if (i < n4) {
-                    const float4 g = __ldg(g4 + i);
+                if (live(j)) {
+                    const float4 g = gamma_of(j);
                     v[j] = make_float4(__fmul_rn(div_markstein(v[j].x, rms, rr), g.x),
                                        __fmul_rn(div_markstein(v[j].y, rms, rr), g.y),
                                        __fmul_rn(div_markstein(v[j].z, rms, rr), g.z),
@@ -783,9 +793,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         } else {
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
-                if (i < n4) {
-                    const float4 g = __ldg(g4 + i);
+                if (live(j)) {
+                    const float4 g = gamma_of(j);
                     v[j] = make_float4(__fmul_rn(__fdiv_rn(v[j].x, rms), g.x), __fmul_rn(__fdiv_rn(v[j].y, rms), g.y),
                                        __fmul_rn(__fdiv_rn(v[j].z, rms), g.z), __fmul_rn(__fdiv_rn(v[j].w, rms), g.w));
                     amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
@@ -798,18 +807,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * cols);
         float dmax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
-            if (i < n4) qr[i] = sym_codes4_tracked(v[j], rc, dmax);
-        }
+        for (int j = 0; j < VPT; ++j)
+            if (live(j)) qr[threadIdx.x + j * THREADS] = sym_codes4_tracked(v[j], rc, dmax);
         if (dmax >= kNearHalf) {   // some quotient near a half-integer (rare): this thread's codes exactly
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int64_t i = threadIdx.x + (int64_t)j * kStreamThreads;
-                if (i < n4)
-                    qr[i] = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc), sym_code(v[j].z, sc, rc),
-                                  sym_code(v[j].w, sc, rc));
-            }
+            for (int j = 0; j < VPT; ++j)
+                if (live(j))
+                    qr[threadIdx.x + j * THREADS] = pack4(sym_code(v[j].x, sc, rc), sym_code(v[j].y, sc, rc),
+                                                          sym_code(v[j].z, sc, rc), sym_code(v[j].w, sc, rc));
         }
         // (the reductions' shared cells: red is written again by the next row before its first
         // barrier, after every thread has passed this row's second barrier, which follows the
@@ -821,16 +826,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 }
 
-template <int VPT>
+template <int VPT, int THREADS, bool FULL>
 cudaError_t launch_rms_stream(const float* x, const float* gamma, int64_t rows, int64_t cols, float eps, int8_t* q,
                               float* s, cudaStream_t st) {
     const int smem = (int)(cols * 4) * kStreamBufs;
-    cudaError_t e = cudaFuncSetAttribute(rmsnorm_quantize_stream_kernel<VPT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = rmsnorm_quantize_stream_kernel<VPT, THREADS, FULL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t cap = num_sms();
     const unsigned grid = (unsigned)(rows < cap ? rows : cap);
-    rmsnorm_quantize_stream_kernel<VPT><<<grid, kStreamThreads, smem, st>>>(x, gamma, rows, cols, eps, q, s);
+    kern<<<grid, THREADS, smem, st>>>(x, gamma, rows, cols, eps, q, s);
     note_launch();
     return cudaGetLastError();
 }
@@ -1086,8 +1091,12 @@ cudaError_t launch_rmsnorm_quantize(const float* x, const float* gamma, int64_t 
     if (n4 <= 256) return launch_rms_rows<1>(x, gamma, rows, cols, eps, threads_for(1), q, s, stream);
     // rows of 1024 .. 16384 elements with many rows: the streaming kernel (three rows in flight
     // per SM through shared memory)
-    if (n4 > 256 && n4 <= kStreamThreads * 4 && rows >= 2 * (int64_t)num_sms())
-        return launch_rms_stream<4>(x, gamma, rows, cols, eps, q, s, stream);
+    if (n4 > 256 && n4 <= kStreamThreads * 4 && rows >= 2 * (int64_t)num_sms()) {
+        // rows of exactly 16384 elements: 512 threads of eight float4 each, no bounds checks, gamma
+        // in registers (fewer warps per row: half the reduction work per element)
+        if (n4 == 512 * 8) return launch_rms_stream<8, 512, true>(x, gamma, rows, cols, eps, q, s, stream);
+        return launch_rms_stream<4, kStreamThreads, false>(x, gamma, rows, cols, eps, q, s, stream);
+    }
     if (n4 <= 1024 * 4) return launch_rms_rows<4>(x, gamma, rows, cols, eps, threads_for(4), q, s, stream);
     if (n4 <= 1024 * 8) return launch_rms_rows<8>(x, gamma, rows, cols, eps, threads_for(8), q, s, stream);
     rmsnorm_quantize_long_rows_kernel<<<(unsigned)rows, 1024, 0, stream>>>(x, gamma, cols, eps, q, s);

@@ -170,12 +170,13 @@ def test_rmsnorm_quotient_paths(q8):
         compare(host(qb), host(sb), ref)
 
 
-def test_streaming_kernel_rows_with_every_path(q8):
-    """Enough rows (>= two per SM) and a ragged K for the streaming kernel: random rows of several
-    workloads, zero rows, rows with tiny elements (IEEE path), huge-range rows and eps-dominated
-    rows, in an order that puts each kind into every shared-memory buffer slot."""
-    rng = np.random.default_rng(21)
-    M, K = 460, 4112
+@pytest.mark.parametrize("M,K", [(460, 4112), (320, 16384)])
+def test_streaming_kernel_rows_with_every_path(q8, M, K):
+    """Enough rows (>= two per SM) for the streaming kernel, with a ragged K (the general form) and
+    with K = 16384 (512 threads of eight float4, no bounds checks): random rows, zero rows, rows
+    with tiny elements (IEEE path), huge-range rows and eps-dominated rows, in an order that puts
+    each kind into every shared-memory buffer slot."""
+    rng = np.random.default_rng(21 + K)
     a = workloads.make_activations(workloads.WORKLOADS["prefill2k"], M=M, K=K)
     for r in range(0, M, 7):
         kind = (r // 7) % 5
