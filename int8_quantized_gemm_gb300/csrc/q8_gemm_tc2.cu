@@ -88,12 +88,14 @@ constexpr int kSfStage = BNH * 4;   // scale words of one stage's 128 weight row
 // Block-scaled weights enter the MMA as the fp16 values q * s (exact: s = 2^-24 .. 2^9), so the
 // products are no longer integers and TMEM accumulates the whole K in fp32 (one chunk).
 // Warp roles: warp 0 TMA, warp 1 MMA (even CTA) or relay (odd CTA), then kConvWarps converter
-// warps, then kDrainWarps drain warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..).
-// The int8 and int4 formats drain every exact chunk and take 6 converters and 8 drains; the
-// block-scaled format drains once per tile and takes 10 converters and 4 drains (each drain warp
-// then reads its 256 accumulator columns in two halves). Registers: the producer-side warps
-// shrink to kRegsLow, the drain warps grow to kRegsHigh; (2 + kConvWarps) * 32 * kRegsLow +
-// kDrainWarps * 32 * kRegsHigh <= 512 * 128, the registers the block is launched with.
+// warps, then (block-scaled weights with fp16 activations) two idle warps, then kDrainWarps drain
+// warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..). The int8 and int4 formats
+// drain every exact chunk and take 6 converters and 8 drains; the block-scaled formats drain once
+// per tile and take 4 drains (each drain warp then reads its 256 accumulator columns in two
+// halves) and 10 converters, or 8 with fp16 activations (two weight chunks per thread and stage).
+// Registers: warps [0, kDrain0) shrink to kRegsLow and the drain warps grow to kRegsHigh;
+// setmaxnreg acts on whole warpgroups, so kDrain0 is a multiple of 4, and kDrain0 * 32 *
+// kRegsLow + kDrainWarps * 32 * kRegsHigh <= 512 * 128, the registers the block is launched with.
 // Activation codes as fp16 values (kWA16, kW4A16, kWMxA16): TMA writes the A half of each fp16
 // operand stage directly (the 128-byte swizzle of a [128 x 64] fp16 box is the K-major layout of
 // the UMMA descriptors), the staging ring holds the weights only, and the converters convert W.
@@ -108,11 +110,17 @@ struct PairCfg {
     static constexpr bool A16 = WF == kWA16 || WF == kW4A16 || WF == kWMxA16;
     static constexpr int S16 = A16 ? 5 : 4;                   // fp16 operand stages (32 KB each)
     static constexpr int kOffStage8 = S16 * kStage16;
-    static constexpr int kConvWarps = MX ? 10 : 6;
-    static constexpr int kDrainWarps = 16 - 2 - kConvWarps;
+    // block-scaled weights with fp16 activations: eight converter warps (two weight chunks per
+    // thread and stage), then two idle warps, then the drains
+    static constexpr int kConvWarps = MX ? (A16 ? 8 : 10) : 6;
+    static constexpr int kDrainWarps = MX ? 4 : 8;
+    static constexpr int kDrain0 = 16 - kDrainWarps;                // first drain warp
     static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
     static constexpr int kRegsLow = MX ? 104 : 72, kRegsHigh = 184;
-    static_assert((2 + kConvWarps) * 32 * kRegsLow + kDrainWarps * 32 * kRegsHigh <= kThreads * 128,
+    static_assert(2 + kConvWarps <= kDrain0, "warp roles above the block");
+    // setmaxnreg acts on whole warpgroups: warps [0, kDrain0) shrink, warps [kDrain0, 16) grow
+    static_assert(kDrain0 % 4 == 0, "the register split must fall on a warpgroup boundary");
+    static_assert(kDrain0 * 32 * kRegsLow + kDrainWarps * 32 * kRegsHigh <= kThreads * 128,
                   "register split above the launch's registers");
     static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
@@ -233,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int my_full = cluster < n_full ? (n_full - 1 - cluster) / nclusters + 1 : 0;
     const int total_g = my_full * KB + (my_units - my_full) * un.kb_part;   // stages of this cluster
 
-    if (warp < 2 + kConvWarps) {
+    if (warp < C::kDrain0) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::kRegsLow));
       if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
@@ -333,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive_remote(mapa_shared(bar_full16 + 8 * s, 0));
             }
         }
-      } else {
+      } else if (warp < 2 + kConvWarps) {
         // ---------------------------------------------------------------- converters
         if constexpr (A16 && !W4 && !MX) {
             // W only: 512 16-byte int8 chunks per stage (128 rows x 4); thread ct takes idx = ct + T j
@@ -390,7 +398,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             constexpr int T = C::kConvT;
             constexpr int kIdx0 = A16 ? 512 : 0;                      // chunk index of staging byte 0
             constexpr int NJ = (1024 - kIdx0 + T - 1) / T;            // chunks per thread and stage
-            static_assert(!MX || T == 320, "the block-scaled slot map assumes 10 converter warps");
+            static_assert(!MX || T == 320 || (A16 && T == 256), "the block-scaled slot maps assume 10 converter "
+                                                                 "warps, or 8 with fp16 activations");
             const int ct = threadIdx.x - 64;
             const int r0 = (kIdx0 >> 2) + (ct >> 2), c0 = ct & 3;
             const uint32_t src0 = (uint32_t)(ct * 16);
@@ -399,8 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // Block-scaled weights (T = 320): the thread's weight chunks (512 <= idx < 1024; weight
             // row (idx - 512) / 4 of the CTA's half, K chunk c0 of the stage) are, with int8
             // activations, j = 2 (slot 1) and one of j = 1 (ct >= 192) or j = 3 (ct < 64) (slot 0);
-            // with fp16 activations j = 0 (slot 0) and j = 1 (slot 1, ct < 192). Their scale words are
-            // read from global memory (L2) kSfAhead stages ahead of use.
+            // with fp16 activations j = 0 (slot 0) and j = 1 (slot 1: ct < 192 with ten converter warps,
+            // every thread with eight). Their scale words arrive by TMA with the stage's weights or,
+            // where the scale array's layout does not allow that, from L2 kSfAhead stages ahead.
             auto slot_j = [&](int jw) { return A16 ? jw : (jw == 1 ? 2 : (ct < 64 ? 3 : 1)); };
             auto slot_of = [](int j) { return A16 ? (j & 1) : (j == 2 ? 1 : 0); };
             // A ring of kSfAhead prefetched stages: slot 0 is the stage being converted.
@@ -623,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 8 drain warps: warp pair (w, w + 4) takes accumulator columns [0, 128) and [128, 256);
         // 4 drain warps: each takes both halves, one after the other
         constexpr int kHalves = 8 / kDrainWarps;
-        const int col_half = kHalves == 1 ? (warp - 2 - kConvWarps) >> 2 : 0;
+        const int col_half = kHalves == 1 ? (warp - C::kDrain0) >> 2 : 0;
         int acc[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) acc[c] = 0;
@@ -732,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // at chunk c ^ (lane & 7)) and one TMA store, which writes whole lines and clips
                     // rows >= M and columns >= N. ESZ (bytes per output) is a compile-time constant
                     // so that acc[] stays in registers.
-                    const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - 2 - kConvWarps) * kEpiBytes);
+                    const uint32_t ebuf = sbase + kOffEpi + (uint32_t)((warp - C::kDrain0) * kEpiBytes);
                     auto blocks = [&](auto esz_tag) {
                         constexpr int ESZ = decltype(esz_tag)::value;
                         constexpr int BCOLS = 128 / ESZ;
