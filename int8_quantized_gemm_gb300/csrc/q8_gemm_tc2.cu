@@ -67,7 +67,6 @@ constexpr int BMH = 128;
 constexpr int BN = 256;             // columns of the pair tile (W rows; 128 per CTA)
 constexpr int BNH = 128;
 constexpr int BK = 64;
-constexpr int kConv = 192;          // converter threads of the int8 / int4 formats: warps 2..7
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;      // two 128 x 256 fp32 accumulator buffers per CTA
 
@@ -562,11 +561,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // int4 weights: A as above over its 512 chunks (j < 3, idx < 512; not with fp16 activations,
-            // which TMA has put in place); W's 256 packed chunks (128 rows x 2 chunks of 32 K) take
-            // idx = ct + 192 j (j < 2, idx < 256): row ct / 2 + 96 j, chunk ct % 2; each becomes four
+            // int4 weights: A as above over its 512 chunks (idx = ct + T j < 512; not with fp16
+            // activations, which TMA has put in place); W's 256 packed chunks (128 rows x 2 chunks of
+            // 32 K) take idx = ct + T j (idx < 256): row ct / 2 + (T / 2) j, chunk ct % 2; each becomes four
             // fp16 chunks 4 (ct % 2) + q of its row, word q of the packed chunk (8 K) giving fp16 chunk
             // q through two nibble pairs, in the pair order of cvt_word.
+            constexpr int T = C::kConvT;   // converter threads (a multiple of 32)
             const int ct = threadIdx.x - 64;
             const int ra = ct >> 2, ca = ct & 3;
             const uint32_t srcA = (uint32_t)(ct * 16);
@@ -581,39 +581,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar_full8 + 8 * s8, (uint32_t)((g / S8) & 1), abort_flag, kErrConvFull, &g_tc2_error))
                     break;
                 const uint32_t st8 = sbase + kOffStage8 + s8 * kStage8;
-                uint4 ia[3], iw[2];
+                constexpr int NA = (512 + T - 1) / T, NW = (256 + T - 1) / T;
+                uint4 ia[NA], iw[NW];
     #pragma unroll
-                for (int j = 0; j < 3; ++j)
-                    ia[j] = (!A16 && ct + kConv * j < 512) ? lds128(st8 + srcA + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < NA; ++j)
+                    ia[j] = (!A16 && ct + T * j < 512) ? lds128(st8 + srcA + T * 16 * j) : make_uint4(0, 0, 0, 0);
     #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    iw[j] = (ct + kConv * j < 256) ? lds128(st8 + srcW + kConv * 16 * j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < NW; ++j)
+                    iw[j] = (ct + T * j < 256) ? lds128(st8 + srcW + T * 16 * j) : make_uint4(0, 0, 0, 0);
                 if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrConvEmpty,
                                &g_tc2_error))
                     break;
                 const uint32_t st16 = sbase + s16 * kStage16;
     #pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    if (!A16 && ct + kConv * j < 512) {
+                for (int j = 0; j < NA; ++j) {
+                    if (!A16 && ct + T * j < 512) {
                         uint4 o0, o1;
                         cvt_word(ia[j].x, o0.x, o0.y);
                         cvt_word(ia[j].y, o0.z, o0.w);
                         cvt_word(ia[j].z, o1.x, o1.y);
                         cvt_word(ia[j].w, o1.z, o1.w);
-                        sts128(st16 + dA0 + 6144 * j, o0);
-                        sts128(st16 + dA1 + 6144 * j, o1);
+                        sts128(st16 + dA0 + 32 * T * j, o0);   // rows ra + (T / 4) j
+                        sts128(st16 + dA1 + 32 * T * j, o1);
                     }
                 }
     #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    if (ct + kConv * j < 256) {
+                for (int j = 0; j < NW; ++j) {
+                    if (ct + T * j < 256) {
                         const uint32_t wv[4] = {iw[j].x, iw[j].y, iw[j].z, iw[j].w};
     #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             uint4 o;
                             cvt_int4x4<0x4140u>(wv[q], o.x, o.y);
                             cvt_int4x4<0x4342u>(wv[q], o.z, o.w);
-                            sts128(st16 + dW[q] + 12288 * j, o);
+                            sts128(st16 + dW[q] + 64 * T * j, o);   // rows rw + (T / 2) j
                         }
                     }
                 }
