@@ -341,6 +341,48 @@ __global__ void __launch_bounds__(512) tensor_codes_kernel(const float* __restri
     }
 }
 
+// A small tensor (per-tensor granularity) in one CTA: the range over all elements (block maximum,
+// the same values as the grid-wide range kernel's), the scale (and zero point) computed by every
+// thread from it, then the codes with the tensor's second read served by L1 / L2. The same
+// operations as the three-kernel path, without its two memsets and three launches.
+template <bool ASYM, bool H>
+__global__ void __launch_bounds__(1024) tensor_small_kernel(const float* __restrict__ x, int64_t n4,
+                                                            float* __restrict__ s, int32_t* __restrict__ z,
+                                                            void* __restrict__ q) {
+    __shared__ float red[64];
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    float hi = 0.0f, nlo = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = x4[i];
+        if (ASYM) {
+            hi = fmaxf(hi, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            nlo = fmaxf(nlo, -fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+        } else {
+            hi = fmaxf(hi, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    }
+    block_max2<ASYM>(hi, nlo, red);
+    float sc;
+    int zp = 0;
+    if (ASYM) {
+        asym_params(-nlo, hi, &sc, &zp);
+    } else {
+        sc = sym_scale(hi);
+    }
+    if (threadIdx.x == 0) {
+        s[0] = sc;
+        if (ASYM) z[0] = zp;
+    }
+    const float rc = __fdiv_rn(1.0f, sc);
+    const int zoff = zp - (int)kMagicBits;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = x4[i];
+        float dmax = 0.0f;
+        store_codes4_tracked<ASYM, H>(q, i, v, rc, zoff, dmax);
+        if (dmax >= kNearHalf) store_codes4_exact<ASYM, H>(q, i, v, sc, rc, zoff);
+    }
+}
+
 // colsum[n] = sum_k qw[n][k]: one warp per weight row, 16-byte loads, dp4a
 // against ones (four signed bytes summed into an int32 per instruction).
 __global__ void __launch_bounds__(256) colsum_kernel(const int8_t* __restrict__ qw, int64_t N,
@@ -1033,6 +1075,11 @@ cudaError_t dispatch_rows(const float* x, int64_t rows, int64_t cols, void* q, f
 template <bool ASYM, bool H>
 cudaError_t dispatch_tensor(const float* x, int64_t n, void* q, float* s, int32_t* z, cudaStream_t st) {
     const int64_t n4 = n / 4;
+    if (n4 <= 8192) {   // up to 128 KB of fp32: one CTA, one launch
+        tensor_small_kernel<ASYM, H><<<1, 1024, 0, st>>>(x, n4, s, z, q);
+        note_launch();
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaMemsetAsync(s, 0, sizeof(float), st);
     if (e == cudaSuccess && ASYM) e = cudaMemsetAsync(z, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return e;

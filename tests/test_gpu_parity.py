@@ -62,9 +62,12 @@ QUANT_CASES = [
     (37, 528, True, False, "prefill2k"),       # ragged K per thread block
     (5, 40000, True, True, "prefill2k"),       # rows longer than the register budget
     (3, 40000, True, False, "relu4k"),
-    (300, 48, False, False, "relu4k"),         # per-tensor asymmetric
+    (300, 48, False, False, "relu4k"),         # per-tensor asymmetric (one-CTA kernel)
     (1, 16, True, True, "tiny"),
     (7, 1040, False, True, "prefill2k"),
+    (32, 1024, False, True, "prefill2k"),      # per-tensor, exactly 8192 float4: the one-CTA kernel
+    (33, 1008, False, True, "prefill2k"),      # per-tensor, 8316 float4: range, parameter and code kernels
+    (512, 2048, False, False, "relu4k"),       # per-tensor asymmetric over the grid
 ]
 
 
