@@ -4,7 +4,8 @@ Integer results (int8 and int4 weights) are compared with the oracle's int64 GEM
 bit; block-scaled results use codes in [-3, 3] and exponents within four binades of a row
 base, where every partial sum is exact in fp32, so they too must match the oracle's exactly
 rounded sum bit for bit. A kernel that does not take a shape rejects it (Q8Error) and is
-skipped for that shape; every shape runs on at least the CTA-pair kernel.
+skipped for that shape; every shape runs on at least the CTA-pair kernel. The workspace forms
+(the activation codes copied once as fp16 values for the pair kernel) run on the same shapes.
 """
 import numpy as np
 import pytest
@@ -69,6 +70,14 @@ def test_random_shapes_int8_and_int4_weights(q8, seed):
                            ("tcgen05_pair", "decode"))
         for k, acc in got4.items():
             np.testing.assert_array_equal(acc.astype(np.int64), want4, err_msg=f"int4 {k} {M}x{N}x{K}")
+        # the workspace forms with unit scales: y = fl(acc), rounded once like the oracle's int64 sums
+        ws = torch.empty(2 * M * K, dtype=torch.uint8, device="cuda")
+        ones_m, ones_n = dev(np.ones(M, np.float32)), dev(np.ones(N, np.float32))
+        y8 = q8.q8_gemm_dequant(dev(qa), ones_m, None, dev(qw), ones_n, workspace=ws).cpu().numpy()
+        y4 = q8.q8_gemm_w4a8(dev(qa), ones_m, None, packed, ones_n, workspace=ws).cpu().numpy()
+        assert q8.q8_device_error() == 0
+        np.testing.assert_array_equal(y8, want.astype(np.float32), err_msg=f"int8 workspace {M}x{N}x{K}")
+        np.testing.assert_array_equal(y4, want4.astype(np.float32), err_msg=f"int4 workspace {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("seed", [303])
@@ -87,6 +96,10 @@ def test_random_shapes_block_scaled_weights(q8, seed):
                                                        kernel=k).cpu().numpy(), ("tcgen05_pair", "decode"))
         for k, t in got.items():
             np.testing.assert_array_equal(t.view(np.int32), t_ref.view(np.int32), err_msg=f"mx {k} G{G} {M}x{N}x{K}")
+        ws = torch.empty(2 * M * K, dtype=torch.uint8, device="cuda")
+        t = q8.q8_gemm_mx(dev(qa), ones, dev(q), dev(sf.view(np.int32)), G, workspace=ws).cpu().numpy()
+        assert q8.q8_device_error() == 0
+        np.testing.assert_array_equal(t.view(np.int32), t_ref.view(np.int32), err_msg=f"mx workspace G{G} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("seed", [404])
@@ -104,3 +117,9 @@ def test_random_shapes_fp32_layer_with_the_default_kernel(q8, seed):
                                         threads=8)
         assert st == oracle.OK
         np.testing.assert_array_equal(y.view(np.int32), y_ref.view(np.int32), err_msg=f"{M}x{N}x{K}")
+        # the layer in one call with a workspace (quantizer writing the fp16 copy, pair kernel on it)
+        ws = torch.empty(max(16, q8.q8_gemm_workspace(M, N, K)), dtype=torch.uint8, device="cuda")
+        y_ws = q8.q8_linear(dev(a), dev(qw), dev(sw), q8.q8_colsum(dev(qw)), symmetric=False, workspace=ws)
+        assert q8.q8_device_error() == 0
+        np.testing.assert_array_equal(y_ws.cpu().numpy().view(np.int32), y_ref.view(np.int32),
+                                      err_msg=f"linear workspace {M}x{N}x{K}")
