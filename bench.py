@@ -41,6 +41,25 @@ HEADLINE = "prefill16k"
 DECODE = "decode"
 METRIC = "W8A8 GEMM TOPS (2MNK/s incl. act quantize)"
 L2_FLUSH_BYTES = 256 << 20
+HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal; every HBM fraction is also given against it
+
+
+def add_nominal_hbm(obj):
+    """Beside every HBM fraction of the measured copy bandwidth, the same rate against the
+    nominal HBM bandwidth (in place, recursively)."""
+    if isinstance(obj, dict):
+        if "frac_hbm" in obj and "GB/s" in obj:
+            obj["frac_hbm_nominal"] = round(obj["GB/s"] / HBM_NOMINAL_GBS, 4)
+        if "gemm_frac_hbm" in obj and "gemm_GB/s" in obj:
+            obj["gemm_frac_hbm_nominal"] = round(obj["gemm_GB/s"] / HBM_NOMINAL_GBS, 4)
+        if obj.get("bound") == "hbm" and obj.get("unit") == "GB/s" and "achieved" in obj:
+            obj["frac_nominal"] = round(obj["achieved"] / HBM_NOMINAL_GBS, 4)
+        for v in obj.values():
+            add_nominal_hbm(v)
+    elif isinstance(obj, list):
+        for v in obj:
+            add_nominal_hbm(v)
+    return obj
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # headline GEMM kernel on the headline workload, from the ncu capture of this kernel.
@@ -434,7 +453,7 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "wall_s_timed": round(wall1 - wall0, 3),
         }
-        print(json.dumps(line))
+        print(json.dumps(add_nominal_hbm(line)))
 
 
 def gemm_workspace(q8, M, N, K, device):
