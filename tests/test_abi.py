@@ -212,6 +212,29 @@ def test_gemm_workspace_sizes(lib):
     assert st == q8.Q8_ERR_INVALID_ARG
 
 
+def test_workspace_entries_reject_bad_arguments(lib):
+    import int8_quantized_gemm_gb300 as q8
+    f32 = ctypes.c_float(0.0)
+    big = 1 << 30
+    # int4 and block-scaled GEMMs with a misaligned workspace; a group size the format does not have
+    assert lib.q8_gemm_w4a8_ws(FAKE, FAKE, None, 1, FAKE, FAKE, None, None, 512, 512, 512, 0, FAKE, f32,
+                               MISALIGNED, big, None) == q8.Q8_ERR_INVALID_ARG
+    assert lib.q8_gemm_mx_ws(FAKE, FAKE, 1, FAKE, FAKE, 32, None, 512, 512, 512, 0, FAKE, f32,
+                             MISALIGNED, big, None) == q8.Q8_ERR_INVALID_ARG
+    assert lib.q8_gemm_mx_ws(FAKE, FAKE, 1, FAKE, FAKE, 64, None, 512, 512, 512, 0, FAKE, f32,
+                             FAKE, big, None) == q8.Q8_ERR_INVALID_ARG
+    # the layer with a workspace: a misaligned workspace, a symmetry that is not an enum value
+    assert lib.q8_linear_ws(FAKE, 512, 512, 1, 0, FAKE, FAKE, None, FAKE, FAKE, 1, None, 512, FAKE,
+                            MISALIGNED, big, None) == q8.Q8_ERR_INVALID_ARG
+    assert q8.q8_gemm_workspace(512, 512, 512) > 0
+    assert lib.q8_linear_ws(FAKE, 512, 512, 1, 7, FAKE, FAKE, None, FAKE, FAKE, 1, None, 512, FAKE,
+                            FAKE, big, None) == q8.Q8_ERR_INVALID_ARG
+    # the dual quantizer: no fp16 output, a misaligned one, a zero point without asymmetry
+    assert lib.q8_quantize_act_dual(FAKE, 8, 64, 1, 0, FAKE, None, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert lib.q8_quantize_act_dual(FAKE, 8, 64, 1, 0, FAKE, MISALIGNED, FAKE, None, None) == q8.Q8_ERR_INVALID_ARG
+    assert lib.q8_quantize_act_dual(FAKE, 8, 64, 1, 0, FAKE, FAKE, FAKE, FAKE, None) == q8.Q8_ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     import int8_quantized_gemm_gb300 as q8
