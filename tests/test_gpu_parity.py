@@ -297,8 +297,9 @@ def test_full_size_workload(q8, name):
     """The bench's launch configuration (kernel chosen by q8_gemm_pick, the layer's workspace where
     the shape takes one) at the workload's full size: every code, scale and zero point bit-exact;
     y and the INT32 accumulators compared with the threaded oracle at every output, except for the
-    large prefill (1.1e12 multiply-adds), where they are compared at sampled outputs; the layer
-    with and without the workspace bit-identical."""
+    large prefill (1.1e12 multiply-adds), where they are compared on 16 whole rows, 16 whole columns
+    and 3000 sampled outputs; the layer with and without the workspace bit-identical, and (the
+    bench's step) with the quantizer writing the codes' fp16 copy itself."""
     wl = workloads.WORKLOADS[name]
     a = workloads.make_activations(wl)
     w = workloads.make_weights(wl)
@@ -322,6 +323,15 @@ def test_full_size_workload(q8, name):
     assert_no_device_error(q8)
     assert torch.equal(y.view(torch.int32), y_direct.view(torch.int32))
     del y_direct
+    if ws is not None:   # the bench's step: the quantizer writes the fp16 copy, the pair kernel reads it
+        ws16 = ws.view(torch.float16)[:wl.M * wl.K].view(wl.M, wl.K)
+        ws.fill_(0x55)
+        qa2, _, s_a2, z_a2 = q8.q8_quantize_act_dual(a_d, per_row=apr, symmetric=wl.act_symmetric, qa16=ws16)
+        y_step = q8.q8_gemm_f16a(ws16, s_a2, z_a2, qw, s_w, cs)
+        assert_no_device_error(q8)
+        assert torch.equal(qa2, qa) and torch.equal(s_a2.view(torch.int32), s_a.view(torch.int32))
+        assert torch.equal(y_step.view(torch.int32), y.view(torch.int32))
+        del y_step, qa2
     np.testing.assert_array_equal(host(s_a), rsa)
     np.testing.assert_array_equal(host(qa), rqa)
     if rza is not None:
@@ -342,6 +352,20 @@ def test_full_size_workload(q8, name):
     yt, acct = torch.as_tensor(ms).cuda(), torch.as_tensor(ns).cuda()
     np.testing.assert_array_equal(host(acc[yt, acct]).astype(np.int64), racc)
     assert max_ulp(host(y[yt, acct]), ry) <= 2
+    # whole rows (every N-tile) and whole columns (every M-tile)
+    rng = np.random.default_rng(wl.seed + 17)
+    rows = np.unique(np.concatenate([rng.integers(0, wl.M, 14), [0, wl.M - 1]]))
+    cols = np.unique(np.concatenate([rng.integers(0, wl.N, 14), [0, wl.N - 1]]))
+    threads = oracle.max_threads()
+    ry_r, st = oracle.linear_codes(rqa[rows], rsa[rows] if apr else rsa, None, rqw, rsw, apr, wpr, threads=threads)
+    assert st == oracle.OK
+    yh, acch = host(y), host(acc)
+    assert max_ulp(yh[rows], ry_r) <= 2
+    np.testing.assert_array_equal(acch[rows].astype(np.int64), oracle.gemm_acc(rqa[rows], rqw, threads=threads))
+    ry_c, st = oracle.linear_codes(rqa, rsa, None, rqw[cols], rsw[cols] if wpr else rsw, apr, wpr, threads=threads)
+    assert st == oracle.OK
+    assert max_ulp(yh[:, cols], ry_c) <= 2
+    np.testing.assert_array_equal(acch[:, cols].astype(np.int64), oracle.gemm_acc(rqa, rqw[cols], threads=threads))
 
 
 @pytest.mark.slow
