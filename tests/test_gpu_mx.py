@@ -241,8 +241,13 @@ def test_full_size_sampled_outputs(q8):
     qw, sf = q8.q8_quantize_weight_mx(dev(w_np), G)
     y = q8.q8_gemm_mx(qa, sa, qw, sf, G)
     t = q8.q8_gemm_mx(qa, torch.ones(M, device="cuda"), qw, sf, G)
+    # the workspace form the bench also times: the same bits
+    t_ws = q8.q8_gemm_mx(qa, torch.ones(M, device="cuda"), qw, sf, G,
+                         workspace=torch.empty(2 * M * K, dtype=torch.uint8, device="cuda"))
     torch.cuda.synchronize()
     assert q8.q8_device_error() == 0
+    assert torch.equal(t_ws.view(torch.int32), t.view(torch.int32))
+    del t_ws
     rng = np.random.default_rng(0)
     ms = np.unique(np.concatenate([rng.integers(0, M, 40), [0, M - 1]]))
     ns = np.unique(np.concatenate([rng.integers(0, N, 40), [0, N - 1]]))

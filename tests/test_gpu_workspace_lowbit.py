@@ -201,3 +201,55 @@ def test_mx_scale_words_by_tma_and_by_loads_agree(q8, ws):
     np.testing.assert_array_equal(t1.view(np.int32), t2.view(np.int32))
     t_ref, absum = oracle.gemm_mx(qa, q, sf, G, threads=8)
     accumulation_gate(t1, t_ref, absum, qa, q, sf, G)
+
+
+def _ulp(a, b):
+    return int(gates.ulp_distance(a, b).max()) if a.size else 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["decode", "prefill16k"])
+def test_w4a8_full_size(q8, name):
+    """The measured int4 configurations at full size: the weights' codes and scales in full; the
+    decode layer at every output; the prefill layer (direct and with the workspace, bit-identical)
+    on 16 whole rows, 16 whole columns and 3000 sampled outputs."""
+    wl = workloads.WORKLOADS[name]
+    a = workloads.make_activations(wl)
+    w = workloads.make_weights(wl)
+    rq4, rs4 = oracle.quantize_int4(w)
+    qw4, s4 = q8.q8_quantize_weight_int4(dev(w))
+    del w
+    np.testing.assert_array_equal(host(qw4), oracle.pack_int4(rq4))
+    np.testing.assert_array_equal(host(s4), rs4)
+    rqa, rsa = oracle.quantize_sym(a, True)
+    qa, sa, _ = q8.q8_quantize_act(dev(a))
+    del a
+    np.testing.assert_array_equal(host(qa), rqa)
+    y = q8.q8_gemm_w4a8(qa, sa, None, qw4, s4)
+    threads = oracle.max_threads()
+    if name == "decode":
+        torch.cuda.synchronize()
+        assert q8.q8_device_error() == 0
+        ry, st = oracle.linear_codes(rqa, rsa, None, rq4, rs4, True, True, threads=threads)
+        assert st == oracle.OK
+        assert _ulp(host(y), ry) <= 2
+        return
+    y_ws = q8.q8_gemm_w4a8(qa, sa, None, qw4, s4, workspace=workspace(wl.M, wl.K))
+    torch.cuda.synchronize()
+    assert q8.q8_device_error() == 0
+    assert torch.equal(y_ws.view(torch.int32), y.view(torch.int32))
+    yh = host(y)
+    rng = np.random.default_rng(wl.seed + 23)
+    rows = np.unique(np.concatenate([rng.integers(0, wl.M, 14), [0, wl.M - 1]]))
+    cols = np.unique(np.concatenate([rng.integers(0, wl.N, 14), [0, wl.N - 1]]))
+    ry_r, st = oracle.linear_codes(rqa[rows], rsa[rows], None, rq4, rs4, True, True, threads=threads)
+    assert st == oracle.OK
+    assert _ulp(yh[rows], ry_r) <= 2
+    ry_c, st = oracle.linear_codes(rqa, rsa, None, rq4[cols], rs4[cols], True, True, threads=threads)
+    assert st == oracle.OK
+    assert _ulp(yh[:, cols], ry_c) <= 2
+    ms = rng.integers(0, wl.M, 3000)
+    ns = rng.integers(0, wl.N, 3000)
+    ry_s, _, st = oracle.linear_codes_at(rqa, rsa, None, rq4, rs4, ms, ns, True, True)
+    assert st == oracle.OK
+    assert _ulp(yh[ms, ns], ry_s) <= 2
