@@ -82,16 +82,15 @@ def test_rmsnorm_quantize_matches_oracle(q8, M, K, name):
     compare(host(qa), host(s_a), oracle.rmsnorm_quantize(a, gamma, EPS))
 
 
-def test_rmsnorm_quantize_full_size_sampled_rows(q8):
+def test_rmsnorm_quantize_full_size(q8):
+    # the measured configuration (the prefill16k activations, gamma seed 4, eps 1e-6): every row
     wl = workloads.WORKLOADS["prefill16k"]
     a = workloads.make_activations(wl)
     gamma = workloads.make_norm_weights(wl.K, seed=4)
     qa, s_a = q8.q8_rmsnorm_quantize_act(dev(a), dev(gamma), EPS)
     torch.cuda.synchronize()
-    rows = np.random.default_rng(0).choice(wl.M, size=256, replace=False)
-    rows.sort()
-    ref = oracle.rmsnorm_quantize(a[rows], gamma, EPS)
-    compare(host(qa)[rows], host(s_a)[rows], ref)
+    assert q8.q8_device_error() == 0
+    compare(host(qa), host(s_a), oracle.rmsnorm_quantize(a, gamma, EPS))
 
 
 def test_rmsnorm_constant_rows_exact(q8):
