@@ -87,8 +87,9 @@ constexpr int kSfStage = BNH * 4;   // scale words of one stage's 128 weight row
 // Block-scaled weights enter the MMA as the fp16 values q * s (exact: s = 2^-24 .. 2^9), so the
 // products are no longer integers and TMEM accumulates the whole K in fp32 (one chunk).
 // Warp roles: warp 0 TMA, warp 1 MMA (even CTA) or relay (odd CTA), then kConvWarps converter
-// warps, then (block-scaled weights with fp16 activations) two idle warps, then kDrainWarps drain
-// warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..). The int8 and int4 formats
+// warps, then (block-scaled weights with fp16 activations) a warp that issues the activation
+// loads and an idle warp, then kDrainWarps drain warps (a multiple of 4: warp w reads TMEM lanes
+// 32 (w % 4) ..). The int8 and int4 formats
 // drain every exact chunk and take 6 converters and 8 drains; the block-scaled formats drain once
 // per tile and take 4 drains (each drain warp then reads its 256 accumulator columns in two
 // halves) and 10 converters, or 8 with fp16 activations (two weight chunks per thread and stage).
@@ -110,7 +111,7 @@ struct PairCfg {
     static constexpr int S16 = A16 ? 5 : 4;                   // fp16 operand stages (32 KB each)
     static constexpr int kOffStage8 = S16 * kStage16;
     // block-scaled weights with fp16 activations: eight converter warps (two weight chunks per
-    // thread and stage), then two idle warps, then the drains
+    // thread and stage), then the warp that issues the activation loads, an idle warp, then the drains
     static constexpr int kConvWarps = MX ? (A16 ? 8 : 10) : 6;
     static constexpr int kDrainWarps = MX ? 4 : 8;
     static constexpr int kDrain0 = 16 - kDrainWarps;                // first drain warp
@@ -124,10 +125,10 @@ struct PairCfg {
     static_assert(kDrainWarps % 4 == 0 && (kConvT / 4) % 8 == 0, "drain warps cover whole TMEM lane quarters");
     static constexpr int kB8 = BNH * (W4 ? BK / 2 : BK);
     static constexpr int kStage8 = (A16 ? 0 : kA8) + kB8;     // 16 KB (int8), 12 KB (int4); fp16 A: 8 KB, 4 KB
-    static constexpr int S8 = W4 ? 5 : 4;                     // staging stages
+    static constexpr int S8 = (W4 || (MX && A16)) ? 5 : 4;    // staging stages
     static constexpr int KB_PER_CHUNK = W4 ? 256 : MX ? (1 << 30) : 16;
     static constexpr int kOffSf = kOffStage8 + S8 * kStage8;   // block-scaled: S8 x 128 scale words
-    static constexpr int kOffEpi = kOffSf + (MX ? S8 * kSfStage : 0);
+    static constexpr int kOffEpi = (kOffSf + (MX ? S8 * kSfStage : 0) + 1023) / 1024 * 1024;
     static constexpr int kOffBar = kOffEpi + kDrainWarps * kEpiBytes;
     static constexpr int kBarBytes = 8 * (2 * S8 + 3 * S16 + 4) + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
@@ -270,7 +271,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_2d(sdst, &tmap_sf, x0, wrow, bar_full8 + 8 * s);
                     tma_load_2d(sdst + kSfStage / 2, &tmap_sf, x0 + kSfStage / 2, wrow, bar_full8 + 8 * s);
                 }
-                if constexpr (A16) {
+                if constexpr (A16 && MX) {
+                    // the fp16 A codes are loaded by their own warp (below), so that this loop does not
+                    // wait for the MMA to release an operand stage before it stages the next weights
+                    tma_load_2d(dst, &tmap_w, kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
+                } else if constexpr (A16) {
                     tma_load_2d(dst, &tmap_w, W4 ? kx * (BK / 2) : kx * BK, n0 + (int)rank * BNH, bar_full8 + 8 * s);
                     // the fp16 A codes go straight into the operand stage once the MMA has released it;
                     // their bytes complete on the barrier the converters arrive on
@@ -338,6 +343,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar_conv16 + 8 * s, (uint32_t)((g / S16) & 1), abort_flag, kErrRelay, &g_tc2_error))
                     break;
                 mbar_arrive_remote(mapa_shared(bar_full16 + 8 * s, 0));
+            }
+        }
+      } else if (MX && A16 && warp == 2 + kConvWarps) {
+        // ---------------------------------------------------------------- activation loads
+        // (block-scaled weights with fp16 activations): the fp16 A codes go straight into each
+        // operand stage once the MMA has released it; their bytes complete on the barrier the
+        // converters arrive on
+        if (lane == 0) {
+            int i = 0, kb = 0, m0 = 0, n0 = 0, k0 = 0, kbn = 0;
+            for (int g = 0; g < total_g; ++g) {
+                if (kb == 0) {
+                    int tile;
+                    bool part;
+                    un.get(cluster + i * nclusters, tile, k0, kbn, part);
+                    pair_coords(tg, tile, m0, n0);
+                }
+                const int s16 = g % S16;
+                if (!mbar_wait(bar_empty16 + 8 * s16, (uint32_t)(((g / S16) & 1) ^ 1), abort_flag, kErrProducer,
+                               &g_tc2_error))
+                    break;
+                const uint32_t fb = (leader ? bar_full16 : bar_conv16) + 8 * s16;
+                mbar_expect_tx(fb, kA16);
+                tma_load_2d(sbase + s16 * kStage16, &tmap_a, (k0 + kb) * BK, m0 + (int)rank * BMH, fb);
+                if (++kb == kbn) { kb = 0; ++i; }
             }
         }
       } else if (warp < 2 + kConvWarps) {
