@@ -147,9 +147,13 @@ struct PairGeom {
     int num_m, num_n, tiles;
 };
 
-// Pair tiles in bands of 4 M-tiles (1024 rows), N swept inside a band.
+// Pair tiles in bands of 8 M-tiles (2048 rows), N swept inside a band. The clusters of one wave
+// run consecutive tiles at about the same K, so each A and W block a wave touches is read from
+// DRAM about once per wave: GM A blocks and (clusters / GM) W blocks. With A blocks of fp16 codes
+// twice the bytes of int8 W blocks, that is least near GM = 6-8 for 76 clusters; GM = 8 keeps the
+// bands aligned to the tile grid of power-of-two M.
 __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, int& n0) {
-    constexpr int GM = 4;
+    constexpr int GM = 8;
     const int band = t / (GM * tg.num_n);
     const int within = t - band * GM * tg.num_n;
     const int rows = min(GM, tg.num_m - band * GM);
