@@ -117,6 +117,9 @@ struct PairCfg {
     static constexpr int kDrain0 = 16 - kDrainWarps;                // first drain warp
     static constexpr int kConvT = 32 * kConvWarps;                  // converter threads
     static constexpr int kRegsLow = MX ? 104 : 72, kRegsHigh = 184;
+    // tile order: bands of 8 M-tiles with fp16 activation codes (an A block is twice the bytes of
+    // a W block, which favours taller bands), 4 with int8 codes (measured at prefill16k)
+    static constexpr int kBand = A16 ? 8 : 4;
     static_assert(2 + kConvWarps <= kDrain0, "warp roles above the block");
     // setmaxnreg acts on whole warpgroups: warps [0, kDrain0) shrink, warps [kDrain0, 16) grow
     static_assert(kDrain0 % 4 == 0, "the register split must fall on a warpgroup boundary");
@@ -144,16 +147,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 struct PairGeom {
-    int num_m, num_n, tiles;
+    int num_m, num_n, tiles, band;   // band: M-tiles per band of the tile order (pair_coords)
 };
 
-// Pair tiles in bands of 8 M-tiles (2048 rows), N swept inside a band. The clusters of one wave
-// run consecutive tiles at about the same K, so each A and W block a wave touches is read from
-// DRAM about once per wave: GM A blocks and (clusters / GM) W blocks. With A blocks of fp16 codes
-// twice the bytes of int8 W blocks, that is least near GM = 6-8 for 76 clusters; GM = 8 keeps the
-// bands aligned to the tile grid of power-of-two M.
+// Pair tiles in bands of tg.band M-tiles, N swept inside a band. The clusters of one wave run
+// consecutive tiles at about the same K, so each A and W block a wave touches is read from DRAM
+// about once per wave: band A blocks and (clusters / band) W blocks.
 __device__ __forceinline__ void pair_coords(const PairGeom& tg, int t, int& m0, int& n0) {
-    constexpr int GM = 8;
+    const int GM = tg.band;
     const int band = t / (GM * tg.num_n);
     const int within = t - band * GM * tg.num_n;
     const int rows = min(GM, tg.num_m - band * GM);
@@ -237,6 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tg.num_m = (M + BM - 1) / BM;
     tg.num_n = (N + BN - 1) / BN;
     tg.tiles = tg.num_m * tg.num_n;
+    tg.band = C::kBand;
     const int cluster = (int)(blockIdx.x >> 1), nclusters = (int)(gridDim.x >> 1);
     const int KB = (K + BK - 1) / BK;   // k-blocks of a whole tile
     const PairUnits un{n_full, ksplit, KB, KB / ksplit};
@@ -934,11 +936,12 @@ __global__ void __launch_bounds__(256) part_tiles_epilogue_kernel(Epilogue ep, i
     }
 }
 
-static PairGeom pair_geom(int64_t M, int64_t N) {
+static PairGeom pair_geom(int64_t M, int64_t N, int band) {
     PairGeom tg;
     tg.num_m = (int)((M + BM - 1) / BM);
     tg.num_n = (int)((N + BN - 1) / BN);
     tg.tiles = tg.num_m * tg.num_n;
+    tg.band = band;
     return tg;
 }
 
@@ -958,7 +961,7 @@ static cudaError_t launch_gemm_tc2_t(const void* qa, const void* qw, int64_t M, 
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    const PairGeom tg = pair_geom(M, N);
+    const PairGeom tg = pair_geom(M, N, PairCfg<WF>::kBand);
     const int64_t units = n_full + (int64_t)(tg.tiles - n_full) * ksplit;
     const int64_t pairs = resident_pairs<WF>();
     const int clusters = (int)(units < pairs ? units : pairs);
@@ -999,7 +1002,7 @@ static cudaError_t launch_gemm_tc2_t(const void* qa, const void* qw, int64_t M, 
 template <int WF>
 static void plan_split(int64_t M, int64_t N, int64_t K, const Epilogue& ep, int& n_full, int& ksplit,
                        int32_t*& acc) {
-    const PairGeom tg = pair_geom(M, N);
+    const PairGeom tg = pair_geom(M, N, PairCfg<WF>::kBand);
     n_full = tg.tiles;
     ksplit = 1;
     acc = nullptr;
@@ -1027,7 +1030,7 @@ static cudaError_t launch_gemm_tc2_split(const void* qa, const void* qw, int64_t
     int32_t* acc;
     plan_split<WF>(M, N, K, ep, n_full, ksplit, acc);
     if (ksplit == 1) return launch_gemm_tc2_t<WF>(qa, qw, M, N, K, ep, stream, n_full, 1, nullptr);
-    const PairGeom tg = pair_geom(M, N);
+    const PairGeom tg = pair_geom(M, N, PairCfg<WF>::kBand);
     const dim3 grid(16, (unsigned)(tg.tiles - n_full));
     part_tiles_zero_kernel<<<grid, 256, 0, stream>>>(acc, (int)M, (int)N, tg, n_full);
     note_launch();
@@ -1045,7 +1048,7 @@ cudaError_t launch_gemm_tc2(const void* qa, const void* qw, int64_t M, int64_t N
     if (wfmt == kWMx || wfmt == kWMxA16) {
         if (!ep.mx_sf || (ep.mx_group != 32 && ep.mx_group != 128) || K % ep.mx_group != 0 || ep.out_i32 || ep.z_a)
             return cudaErrorInvalidValue;
-        const int tiles = pair_geom(M, N).tiles;
+        const int tiles = pair_geom(M, N, 1).tiles;   // the tile count (the band does not change it)
         return wfmt == kWMx ? launch_gemm_tc2_t<kWMx>(qa, qw, M, N, K, ep, stream, tiles, 1, nullptr)
                             : launch_gemm_tc2_t<kWMxA16>(qa, qw, M, N, K, ep, stream, tiles, 1, nullptr);
     }
