@@ -31,10 +31,11 @@ def dev(x):
 CASES = [
     # name, M, N, K, act_per_row, act_symmetric, w_per_row
     ("prefill2k", 512, 2048, 2048, True, True, True),      # small grid: every tile in K slices
-    ("relu4k", 2048, 4096, 4096, True, False, True),       # zero points and column sums; last wave sliced
+    ("relu4k", 2048, 4096, 4096, True, False, True),       # zero points and column sums; two waves of whole tiles
     ("prefill2k", 333, 520, 1040, True, True, True),       # ragged M, N and K
     ("relu4k", 257, 2052, 1024, False, False, False),      # per-tensor scales, sliced
     ("prefill16k", 1024, 1024, 16384, True, True, True),
+    ("prefill2k", 2344, 2056, 2048, True, True, True),     # 90 ragged tiles: the last wave's 14 in 4 K slices
 ]
 
 

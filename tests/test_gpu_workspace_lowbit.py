@@ -52,9 +52,10 @@ def workspace(M, K):
 
 W4_CASES = [
     # M, N, K, symmetric activations
-    (200, 264, 1088, True),       # ragged M and N, few k-blocks: every tile in K slices
+    (200, 264, 1088, True),       # ragged M and N, 17 k-blocks (no even K split): whole tiles
     (513, 777, 3104, False),      # zero points and column sums, ragged everything
-    (2048, 2048, 4096, True),     # several waves, last wave sliced
+    (2048, 2048, 4096, True),     # one wave of 64 whole tiles
+    (2344, 2056, 2048, True),     # 90 ragged tiles: two waves, the last wave's 14 tiles in 4 K slices
     (256, 256, 32, True),         # one k-block
     (300, 520, 16416, False),     # K past one exact 16384-K chunk
 ]
@@ -129,7 +130,8 @@ def test_w4a8_workspace_too_small_or_decode_shape_is_not_used(q8):
     assert q8.q8_device_error() == 0
 
 
-MX_CASES = [(200, 264, 1088, 32), (513, 777, 4096, 128), (2048, 1024, 4096, 32), (300, 520, 512, 128)]
+MX_CASES = [(200, 264, 1088, 32), (513, 777, 4096, 128), (2048, 1024, 4096, 32), (300, 520, 512, 128),
+            (2344, 2056, 512, 32)]   # 90 ragged tiles: two waves (whole tiles)
 
 
 @pytest.mark.parametrize("M,N,K,G", MX_CASES)
